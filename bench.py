@@ -1,0 +1,452 @@
+"""Benchmark of the W4A16 linear layer on GB300 (one JSON line on stdout).
+
+Workload (default, one GPU): the Llama-2-7B decode layers (K, N) = (4096,
+12288) qkv, (4096, 4096) o_proj, (4096, 22016) gate_up, (11008, 4096) down,
+AWQ group-128 4-bit asymmetric weights, bf16 activations, M in {1, 4, 16}.
+One step runs the fused GEMM for every (layer, M) pair: 12 calls. Every call
+reads its own copy of the repacked weights (12 copies, about 315 MB, well
+above the 129 MB L2), so no call finds its weights in L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+value       = weight GB/s over the timed steps (algorithmic bytes: packed codes
+              K*N/2 + scales G*N*2 + zeros G*N/2 per call), all ranks together.
+tflops      = 2*M*N*K summed over the calls / time.
+e2e         = the same metric through the public Python/C-ABI path with x
+              copied from pinned host memory and y copied back inside the
+              timed region, eager launches.
+roofline    = the decode kernel's per-launch durations (CUDA events on the
+              launch stream, launches front-loaded behind a long device copy
+              so the host never starves the GPU), against the measured HBM
+              copy bandwidth.
+cpu_baseline = the CPU oracle (numpy: unpack, dequantise, fp64 matmul) on the
+              o_proj layer at M = 1, 4 and 16.
+--impl reference times that oracle as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = ("W4A16 GEMM TFLOP/s and weight GB/s vs M (1–4096), % of HBM / bf16 TC roofline")
+WORKLOAD = synth.WORKLOADS[1]          # Llama-2-7B decode layers
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes per launch of the decode kernel from ncu (dram__bytes_read.sum +
+# dram__bytes_write.sum), keyed by the sha1 of the kernel source they were
+# taken on; see profiles/. A changed kernel source reports null.
+TRAFFIC_RECORDS: dict = {}
+
+
+def alg_bytes(K: int, N: int, group: int = 128) -> int:
+    G = K // group
+    return K * N // 2 + G * N * 2 + G * N // 2
+
+
+def kernel_source_hash() -> str:
+    p = os.path.join(ROOT, "int4_weight_only_repack_gb300", "csrc", "decode_kernel.cu")
+    with open(p, "rb") as f:
+        return hashlib.sha1(f.read()).hexdigest()[:12]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# --------------------------------------------------------------------------- #
+# Clock sampling during the timed region                                       #
+# --------------------------------------------------------------------------- #
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+            time.sleep(0.15)
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- #
+# Our arm                                                                       #
+# --------------------------------------------------------------------------- #
+def setup_dist():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int, device) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def build_calls(w4, torch, device):
+    """Repack one weight copy per (layer, M) and allocate x / y for each call."""
+    calls = []
+    for li, (K, N, name) in enumerate(WORKLOAD.shapes):
+        L = synth.make_workload_layer(WORKLOAD.index, li)
+        qweight = torch.from_numpy(L.qweight).to(device)
+        qzeros = torch.from_numpy(L.qzeros).to(device)
+        scales = torch.from_numpy(L.scales.view(np.int16)).to(device).view(torch.bfloat16)
+        for M in WORKLOAD.ms:
+            layer = w4.repack_awq(qweight, qzeros, scales, K, N, WORKLOAD.group, torch.bfloat16)
+            x_bits = synth.make_workload_x(WORKLOAD.index, li, M)
+            x = torch.from_numpy(x_bits.view(np.int16)).to(device).view(torch.bfloat16)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+            calls.append(dict(name=name, K=K, N=N, M=M, layer=layer, x=x, y=y, x_bits=x_bits))
+        del qweight, qzeros, scales
+    torch.cuda.synchronize()
+    return calls
+
+
+def run_step(w4, calls):
+    for c in calls:
+        L = c["layer"]
+        w4.w4a16_gemm(c["x"], L.qw, L.scales, L.zeros, None, c["y"], c["M"], c["N"], c["K"],
+                      L.group, L.dtype)
+
+
+def per_launch_times(w4, torch, calls, reps: int, device):
+    """Average duration of each call's kernel, CUDA events on the launch stream.
+
+    A long device-side copy is enqueued first so that every launch and event
+    below is queued before the GPU reaches them: the events then bracket the
+    kernels alone, not host enqueue gaps.
+    """
+    stream = torch.cuda.current_stream()
+    big = torch.empty(1 << 30, dtype=torch.uint8, device=device)
+    big2 = torch.empty_like(big)
+    totals = [0.0] * len(calls)
+    for _ in range(reps):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in calls]
+        for _ in range(6):
+            big2.copy_(big)
+        for c, (e0, e1) in zip(calls, evs):
+            L = c["layer"]
+            e0.record(stream)
+            w4.w4a16_gemm(c["x"], L.qw, L.scales, L.zeros, None, c["y"], c["M"], c["N"], c["K"],
+                          L.group, L.dtype)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        for i, (e0, e1) in enumerate(evs):
+            totals[i] += e0.elapsed_time(e1) * 1e-3
+    del big, big2
+    return [t / reps for t in totals]
+
+
+def cpu_baseline_measure(min_seconds: float = 10.0):
+    """The oracle as it stands on this host: o_proj (4096 x 4096) at M = 1, 4, 16."""
+    import oracle
+    li = [s[2] for s in WORKLOAD.shapes].index("o_proj")
+    K, N, _ = WORKLOAD.shapes[li]
+    L = synth.make_workload_layer(WORKLOAD.index, li)
+    xs = {M: synth.make_workload_x(WORKLOAD.index, li, M) for M in WORKLOAD.ms}
+    t0 = time.perf_counter()
+    done_bytes = 0
+    calls = 0
+    while True:
+        for M in WORKLOAD.ms:
+            oracle.reference_y(xs[M], L.qweight, L.qzeros, L.scales, WORKLOAD.group, "bf16", "awq")
+            done_bytes += alg_bytes(K, N)
+            calls += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds:
+            break
+    return {"value": done_bytes / el / 1e9, "unit": "GB/s", "cores": blas_threads(),
+            "kind": "oracle",
+            "sample": f"o_proj K=4096 N=4096 at M=1,4,16: {calls} full oracle calls (AWQ unpack, "
+                      f"fp32 dequantise, fp64 matmul) in {el:.1f} s"}
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def ours(args):
+    import torch
+
+    import int4_weight_only_repack_gb300 as w4
+
+    world, rank, local = setup_dist()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    w4.lib()
+
+    calls = build_calls(w4, torch, device)
+    step_bytes = sum(alg_bytes(c["K"], c["N"]) for c in calls)
+    step_flops = sum(2 * c["M"] * c["N"] * c["K"] for c in calls)
+
+    # warm-up (eager), then capture one step as a CUDA graph
+    for _ in range(max(args.warmup, 3)):
+        run_step(w4, calls)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run_step(w4, calls)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region ----------------------------------------------------------
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    elapsed = max_over_ranks(e0.elapsed_time(e1) * 1e-3, world, device)
+
+    # ---- per-launch kernel durations (roofline) ---------------------------------
+    t_launch = per_launch_times(w4, torch, calls, reps=5, device=device)
+    kern_bytes = sum(alg_bytes(c["K"], c["N"]) for c in calls)
+    kern_time = sum(t_launch)
+    peak, peak_src = measured_peaks()
+    achieved = kern_bytes / kern_time / 1e9
+    per_call = [{"layer": c["name"], "M": c["M"], "us": round(t * 1e6, 2),
+                 "gbs": round(alg_bytes(c["K"], c["N"]) / t / 1e9, 1),
+                 "frac": round(alg_bytes(c["K"], c["N"]) / t / 1e9 / peak, 3)}
+                for c, t in zip(calls, t_launch)]
+    traffic = TRAFFIC_RECORDS.get(kernel_source_hash())
+
+    # ---- end to end through the public API, host buffers ------------------------
+    e2e_steps = min(args.steps, 200)
+    hx = [torch.from_numpy(c["x_bits"].view(np.int16)).view(torch.bfloat16).pin_memory()
+          for c in calls]
+    hy = [torch.empty((c["M"], c["N"]), dtype=torch.bfloat16).pin_memory() for c in calls]
+    h2d = sum(t.numel() * 2 for t in hx)
+    d2h = sum(t.numel() * 2 for t in hy)
+    for _ in range(2):
+        for c, a, b in zip(calls, hx, hy):
+            c["x"].copy_(a, non_blocking=True)
+            w4.linear(c["x"], c["layer"], y=c["y"])
+            b.copy_(c["y"], non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        for c, a, b in zip(calls, hx, hy):
+            c["x"].copy_(a, non_blocking=True)
+            w4.linear(c["x"], c["layer"], y=c["y"])
+            b.copy_(c["y"], non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_el = max_over_ranks(time.perf_counter() - t0, world, device)
+
+    cpu_base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu_base = cpu_baseline_measure(args.cpu_seconds)
+
+    if rank == 0:
+        value = step_bytes * args.steps * world / elapsed / 1e9
+        line = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(elapsed / args.steps * 1e3, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded N(0,0.02) weights quantised per group of 128, x ~ N(0,1))",
+            "config": {
+                "workload": "llama2_7b_decode: (K,N)=(4096,12288),(4096,4096),(4096,22016),"
+                            "(11008,4096); M in {1,4,16}; AWQ g128; bf16",
+                "calls_per_step": len(calls),
+                "weight_bytes_per_step": step_bytes,
+                "l2": "inputs larger than L2: 12 distinct weight copies (%.0f MB) per step"
+                      % (step_bytes / 1e6),
+                "timing": "CUDA graph of one step replayed; CUDA events on the launch stream",
+                "parallelism": "replicas" if world > 1 else "single GPU",
+            },
+            "tflops": round(step_flops * args.steps * world / elapsed / 1e12, 4),
+            "gpu_launches": len(calls) * args.steps,
+            "clocks": clocks,
+            "e2e": {"value": round(step_bytes * e2e_steps * world / e2e_el / 1e9, 2),
+                    "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": e2e_steps},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "traffic": traffic, "peak_source": peak_src,
+                         "kernel": "w4a16_decode_kernel",
+                         "per_launch": per_call},
+            "cpu_baseline": cpu_base,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------------- #
+# Reference arm: the CPU oracle                                                 #
+# --------------------------------------------------------------------------- #
+def reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    li = [s[2] for s in WORKLOAD.shapes].index("o_proj")
+    K, N, _ = WORKLOAD.shapes[li]
+    L = synth.make_workload_layer(WORKLOAD.index, li)
+    Ms = list(WORKLOAD.ms)
+    xs = {M: synth.make_workload_x(WORKLOAD.index, li, M) for M in Ms}
+
+    def step(i):
+        M = Ms[i % len(Ms)]
+        oracle.reference_y(xs[M], L.qweight, L.qzeros, L.scales, WORKLOAD.group, "bf16", "awq")
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    el = time.perf_counter() - t0
+    value = alg_bytes(K, N) * args.steps / el / 1e9
+    sample = (f"each step: one full oracle call (AWQ unpack, fp32 dequantise, fp64 matmul) on "
+              f"o_proj K=4096 N=4096, M cycling 1,4,16")
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": "llama2_7b_decode (o_proj sample of it on the host cores)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": blas_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        reference(args)
+    else:
+        ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,189 @@
+/*
+ * w4a16.h — C ABI of the GB300 (sm_103a) W4A16 linear-layer library (libw4a16.so).
+ *
+ * A W4A16 layer stores its weight W [K, N] (K = input features, N = output
+ * features) as 4-bit codes q with one 4-bit zero z and one scale s per group of
+ * `group` consecutive input rows and per output column:
+ *
+ *     W[k, n] = (q[k, n] - z[g(k), n]) * s[g(k), n],   g(k) = k / group
+ *
+ * ("vLLM AWQ 4-bit 量化实践：AutoAWQ 模型加载、推理配置与内核调度原理", §5.3:
+ * b = (b - zeros) * scales), and the forward pass is y = x · W with x [M, K] and
+ * y [M, N] in the activation dtype (fp16 or bf16), accumulated in fp32.
+ *
+ * The library has the three hooks of the layer life cycle that
+ * "量化层加载:AWQ / GPTQ / Marlin / fp8" (职责) describes:
+ *   create_weights                 -> w4_repack_sizes (the caller allocates)
+ *   process_weights_after_loading  -> w4_repack_awq / w4_repack_gptq (one-time repack)
+ *   apply                          -> w4a16_gemm
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers unless stated; the caller owns every buffer.
+ *     The library allocates no device memory and keeps no pointer after a call
+ *     returns.
+ *   - All work is enqueued asynchronously on `stream` (a cudaStream_t; NULL =
+ *     the legacy default stream). No call synchronises the host.
+ *   - Arguments are validated on the host before anything is launched. On any
+ *     error the call returns a non-zero w4_status and launches nothing.
+ *     Validation needs no GPU: bad arguments are reported even where no CUDA
+ *     device exists.
+ *   - Half-precision arrays (x, y, scales) hold fp16 or bf16 as selected by
+ *     `dtype`; scales share the activation dtype ("量化层加载" 数据流: scales
+ *     are created in params_dtype).
+ *   - Every pointer must be 16-byte aligned.
+ *   - Shapes are int; 1 <= K, N <= 2^20 and 0 <= M <= 2^20. M == 0 is a no-op.
+ *   - group is 32, 64, 128 or -1 (one group spanning all of K), the sizes
+ *     "vLLM AWQ 4-bit 量化实践" §5.3 lists; K % group == 0.
+ *
+ * Layouts (int32 words; a code is 4 bits):
+ *   AWQ checkpoint ("量化层加载" 数据流; "vLLM AWQ 4-bit 量化实践" §5.1):
+ *     qweight [K][N/8], packed along N; column 8c+j of word (k, c) sits at
+ *     nibble REV[j], REV = {0,4,1,5,2,6,3,7} (_REVERSE_AWQ_PACK_ORDER).
+ *     qzeros [G][N/8] packed the same way, scales [G][N], G = K / group.
+ *   W4_LAYOUT_STD (the standard GPTQ-like layout, "量化层加载" 设计动机,
+ *     "vLLM AWQ 4-bit 量化实践" §5.1): qweight [K/8][N], row 8r+i of word (r, n)
+ *     at bits 4i..4i+3. Zeros [G][N/8] with column 8c+i at bits 4i..4i+3.
+ *     Needs K % 8 == 0 and N % 8 == 0.
+ *   W4_LAYOUT_TILE (this library's kernel layout, the role Marlin's repacked
+ *     layout plays in "量化层加载" 关键文件): needs K % 64 == 0, N % 16 == 0.
+ *     The words form atoms of 64 rows x 16 columns, 128 words each, stored
+ *     column-tile-major: atom a = (n/16) * (K/64) + k/64. Inside an atom, word
+ *     4*lane + j (lane = 4*gg + t) holds column n = 16*(n/16) + gg + 8*(j & 1)
+ *     and rows k = 64*(k/64) + 32*(j >> 1) + 8*t + e, e = 0..7, row offset e at
+ *     nibble position P[e], P = {0,4,1,5,2,6,3,7}. The zeros and scales of the
+ *     TILE layout are the STD zeros [G][N/8] and scales [G][N].
+ *     One 16-byte load per lane is then exactly the A-fragment set of four
+ *     m16n8k16 MMAs, and one word expands to one 16-byte run of 8 consecutive
+ *     rows of a K-major operand tile.
+ *
+ * GPTQ act-order ("量化层加载" 设计动机: desc_act creates g_idx): row k belongs
+ * to group g_idx[k]. w4_repack_gptq sorts the rows by group (stable: ties keep
+ * ascending k) into perm, stores the sorted rows, and w4a16_gemm then reads x
+ * column perm[j] for stored row j, whose group is j / group. g_idx must give
+ * every group exactly `group` rows (what desc_act checkpoints carry).
+ */
+#ifndef W4A16_H
+#define W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define W4_API __attribute__((visibility("default")))
+#else
+#define W4_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int w4_status;
+
+enum {
+    W4_OK = 0,
+    W4_ERR_NULL = 1,       /* a required pointer is NULL                              */
+    W4_ERR_SHAPE = 2,      /* M, K or N out of range or not a multiple the layout needs */
+    W4_ERR_GROUP = 3,      /* group not in {32, 64, 128, -1}, or K % group != 0         */
+    W4_ERR_ALIGN = 4,      /* a pointer is not 16-byte aligned                          */
+    W4_ERR_DTYPE = 5,      /* dtype not W4_F16 / W4_BF16                                */
+    W4_ERR_LAYOUT = 6,     /* layout not W4_LAYOUT_STD / W4_LAYOUT_TILE                 */
+    W4_ERR_ALIAS = 7,      /* an output buffer overlaps an input buffer                 */
+    W4_ERR_ARCH = 8,       /* the current CUDA device is not compute capability 10.3    */
+    W4_ERR_CUDA = 9,       /* a CUDA runtime call or kernel launch failed               */
+    W4_ERR_WORKSPACE = 10, /* workspace NULL or smaller than w4a16_gemm_workspace_size  */
+    W4_ERR_GIDX = 11       /* (written to *status_out by the device) g_idx irregular    */
+};
+
+enum { W4_F16 = 0, W4_BF16 = 1 };
+enum { W4_LAYOUT_STD = 0, W4_LAYOUT_TILE = 1 };
+
+/* Human-readable name of a status code (static string, never NULL). */
+W4_API const char* w4_status_string(w4_status status);
+
+/* ABI version of this library (increments on incompatible changes). */
+W4_API int w4_abi_version(void);
+
+/*
+ * Byte sizes of the repacked buffers for a K x N layer ("create_weights").
+ *   qw_bytes     = K*N/2 for both layouts,
+ *   zeros_bytes  = G*N/2 (standard-order zeros [G][N/8]),
+ *   scales_bytes = G*N*2 (scales [G][N]).
+ * Any output pointer may be NULL. Returns a validation status.
+ */
+W4_API w4_status w4_repack_sizes(int K, int N, int group, int layout,
+                          size_t* qw_bytes, size_t* zeros_bytes, size_t* scales_bytes);
+
+/*
+ * One-time repack of an AWQ checkpoint ("process_weights_after_loading";
+ * "量化层加载" 设计动机 and 关键文件: _convert_awq_to_standard_format, then the
+ * kernel's own repack; "vLLM AWQ 4-bit 量化实践" §5.1).
+ *   qweight  [K][N/8] int32 (AWQ order), qzeros [G][N/8] int32 (AWQ order),
+ *   scales   [G][N] (dtype).
+ *   qw_out   layout STD: [K/8][N]; layout TILE: K*N/8 words as described above.
+ *   zeros_out [G][N/8] standard order; scales_out [G][N] (a copy).
+ * Inputs are never modified; outputs must not overlap inputs (W4_ERR_ALIAS).
+ * Deterministic and re-runnable on new weights.
+ */
+W4_API w4_status w4_repack_awq(const int32_t* qweight, const int32_t* qzeros, const void* scales,
+                        int K, int N, int group, int dtype, int layout,
+                        int32_t* qw_out, int32_t* zeros_out, void* scales_out,
+                        void* stream);
+
+/*
+ * One-time repack of a GPTQ checkpoint (standard packing), with optional
+ * act-order ("量化层加载" 设计动机: desc_act / g_idx).
+ *   qweight [K/8][N] int32, qzeros [G][N/8] int32 (standard order), scales [G][N].
+ *   g_idx   [K] int32 or NULL. When given, rows are stored sorted by group and
+ *           perm_out [K] (required) receives the row order: stored row j is
+ *           input row perm_out[j]. *status_out (required, one int32) receives
+ *           W4_OK, or W4_ERR_GIDX if some g_idx value is outside [0, G) or some
+ *           group does not own exactly `group` rows; perm_out is then the
+ *           identity and the stored rows are unsorted. Both are written on the
+ *           device, in stream order.
+ *   qw_out / zeros_out / scales_out as for w4_repack_awq.
+ */
+W4_API w4_status w4_repack_gptq(const int32_t* qweight, const int32_t* qzeros, const void* scales,
+                         const int32_t* g_idx, int K, int N, int group, int dtype, int layout,
+                         int32_t* qw_out, int32_t* zeros_out, void* scales_out,
+                         int32_t* perm_out, int32_t* status_out, void* stream);
+
+/*
+ * Workspace bytes w4a16_gemm needs for this call shape (0 = none). Act-order
+ * calls above the small-M range stage the gathered activations x[:, perm] there.
+ */
+W4_API size_t w4a16_gemm_workspace_size(int M, int N, int K, int group, int dtype, int has_perm);
+
+/*
+ * The forward pass ("apply"): y[M][N] = x[M][K] · W, W dequantised from the
+ * TILE layout inside the kernel ("vLLM AWQ 4-bit 量化实践" §5.3: the fused
+ * kernel avoids materialising W; "vLLM 学习手册 01. 量化" §5.3: dequantisation
+ * fused with the multiply in registers).
+ *   x      [M][K] dtype, row-major.
+ *   qw     TILE layout words from w4_repack_*; zeros [G][N/8]; scales [G][N].
+ *   perm   [K] from w4_repack_gptq for act-order layers, else NULL.
+ *   y      [M][N] dtype, row-major; must not overlap any input.
+ *   workspace / workspace_bytes: device scratch of at least
+ *          w4a16_gemm_workspace_size(...) bytes (may be NULL when that is 0).
+ * Accumulation is fp32; the result is rounded once to dtype. Deterministic:
+ * the same inputs give the same bits.
+ */
+W4_API w4_status w4a16_gemm(const void* x, const int32_t* qw, const void* scales, const int32_t* zeros,
+                     const int32_t* perm, void* y, int M, int N, int K, int group, int dtype,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Dequantise a repacked layer to a dense W [K][N] (row-major): fp32 when out_f32
+ * is non-zero (exact), else dtype (one rounding of the exact value). Rows follow
+ * the stored order (sorted rows for act-order layers). Used by the tests and by
+ * the dequantise-then-GEMM comparison.
+ */
+W4_API w4_status w4_dequant(const int32_t* qw, const void* scales, const int32_t* zeros,
+                     int K, int N, int group, int dtype, int layout, int out_f32,
+                     void* w_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H */

@@ -1,0 +1,209 @@
+"""Python binding of libw4a16.so, the GB300 W4A16 linear-layer library.
+
+Argument marshalling only: every entry point below forwards device pointers,
+sizes and the current CUDA stream to the C ABI declared in include/w4a16.h and
+raises W4Error on a non-zero status. All computation runs in the library's CUDA
+kernels; there is no fallback path. If the shared library has not been built
+the first call raises, naming the build step.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "W4_F16", "W4_BF16", "W4_LAYOUT_STD", "W4_LAYOUT_TILE", "W4Error", "lib", "library_path",
+    "dtype_code", "w4_status_string", "w4_abi_version", "w4_repack_sizes", "w4_repack_awq",
+    "w4_repack_gptq", "w4a16_gemm_workspace_size", "w4a16_gemm", "w4_dequant",
+    "RepackedLayer", "repack_awq", "repack_gptq", "linear",
+]
+
+W4_F16, W4_BF16 = 0, 1
+W4_LAYOUT_STD, W4_LAYOUT_TILE = 0, 1
+W4_OK = 0
+W4_ERR_GIDX = 11
+
+_PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_PKG_DIR, "libw4a16.so")
+_LIB: Optional[ctypes.CDLL] = None
+
+_c_int, _c_size, _c_void_p = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+_SIGNATURES = {
+    "w4_status_string": (ctypes.c_char_p, [_c_int]),
+    "w4_abi_version": (_c_int, []),
+    "w4_repack_sizes": (_c_int, [_c_int, _c_int, _c_int, _c_int, ctypes.POINTER(_c_size),
+                                 ctypes.POINTER(_c_size), ctypes.POINTER(_c_size)]),
+    "w4_repack_awq": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int,
+                               _c_int, _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
+    "w4_repack_gptq": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_int, _c_int,
+                                _c_int, _c_int, _c_int, _c_void_p, _c_void_p, _c_void_p,
+                                _c_void_p, _c_void_p, _c_void_p]),
+    "w4a16_gemm_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "w4a16_gemm": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                            _c_int, _c_int, _c_int, _c_int, _c_int, _c_void_p, _c_size,
+                            _c_void_p]),
+    "w4_dequant": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int,
+                            _c_int, _c_int, _c_void_p, _c_void_p]),
+}
+
+
+class W4Error(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """Load libw4a16.so (built in-tree); raise if it is missing."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(library_path):
+            raise RuntimeError(
+                f"{library_path} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(library_path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+def w4_status_string(status: int) -> str:
+    return lib().w4_status_string(status).decode()
+
+
+def w4_abi_version() -> int:
+    return lib().w4_abi_version()
+
+
+def _check(status: int):
+    if status != W4_OK:
+        raise W4Error(status, w4_status_string(status))
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def dtype_code(dtype) -> int:
+    if dtype in (W4_F16, W4_BF16):
+        return dtype
+    if dtype in (torch.float16, "fp16", "float16"):
+        return W4_F16
+    if dtype in (torch.bfloat16, "bf16", "bfloat16"):
+        return W4_BF16
+    raise ValueError(f"unsupported activation dtype {dtype}")
+
+
+# --------------------------------------------------------------------------- #
+# Raw entry points (same names and argument order as the C ABI)                 #
+# --------------------------------------------------------------------------- #
+def w4_repack_sizes(K: int, N: int, group: int, layout: int):
+    a, b, c = _c_size(), _c_size(), _c_size()
+    _check(lib().w4_repack_sizes(K, N, group, layout, ctypes.byref(a), ctypes.byref(b),
+                                 ctypes.byref(c)))
+    return a.value, b.value, c.value
+
+
+def w4_repack_awq(qweight, qzeros, scales, K, N, group, dtype, layout, qw_out, zeros_out,
+                  scales_out, stream=None):
+    _check(lib().w4_repack_awq(_ptr(qweight), _ptr(qzeros), _ptr(scales), K, N, group,
+                               dtype_code(dtype), layout, _ptr(qw_out), _ptr(zeros_out),
+                               _ptr(scales_out), _stream(stream)))
+
+
+def w4_repack_gptq(qweight, qzeros, scales, g_idx, K, N, group, dtype, layout, qw_out, zeros_out,
+                   scales_out, perm_out=None, status_out=None, stream=None):
+    _check(lib().w4_repack_gptq(_ptr(qweight), _ptr(qzeros), _ptr(scales), _ptr(g_idx), K, N,
+                                group, dtype_code(dtype), layout, _ptr(qw_out), _ptr(zeros_out),
+                                _ptr(scales_out), _ptr(perm_out), _ptr(status_out),
+                                _stream(stream)))
+
+
+def w4a16_gemm_workspace_size(M, N, K, group, dtype, has_perm) -> int:
+    return lib().w4a16_gemm_workspace_size(M, N, K, group, dtype_code(dtype), int(bool(has_perm)))
+
+
+def w4a16_gemm(x, qw, scales, zeros, perm, y, M, N, K, group, dtype, workspace=None,
+               workspace_bytes=None, stream=None):
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().w4a16_gemm(_ptr(x), _ptr(qw), _ptr(scales), _ptr(zeros), _ptr(perm), _ptr(y),
+                            M, N, K, group, dtype_code(dtype), _ptr(workspace), workspace_bytes,
+                            _stream(stream)))
+
+
+def w4_dequant(qw, scales, zeros, K, N, group, dtype, layout, out_f32, w_out, stream=None):
+    _check(lib().w4_dequant(_ptr(qw), _ptr(scales), _ptr(zeros), K, N, group, dtype_code(dtype),
+                            layout, int(bool(out_f32)), _ptr(w_out), _stream(stream)))
+
+
+# --------------------------------------------------------------------------- #
+# Convenience: allocate outputs with torch, then call the entry points          #
+# --------------------------------------------------------------------------- #
+class RepackedLayer:
+    """Device buffers of one repacked layer (what the GEMM reads)."""
+
+    def __init__(self, K, N, group, dtype, layout, qw, zeros, scales, perm=None, status=None):
+        self.K, self.N, self.group, self.dtype, self.layout = K, N, group, dtype, layout
+        self.qw, self.zeros, self.scales, self.perm, self.status = qw, zeros, scales, perm, status
+
+
+def _half_dtype(dtype) -> torch.dtype:
+    return torch.bfloat16 if dtype_code(dtype) == W4_BF16 else torch.float16
+
+
+def _alloc_repacked(K, N, group, dtype, layout, device):
+    qw_b, z_b, s_b = w4_repack_sizes(K, N, group, layout)
+    qw = torch.empty(qw_b // 4, dtype=torch.int32, device=device)
+    zeros = torch.empty(z_b // 4, dtype=torch.int32, device=device)
+    scales = torch.empty(s_b // 2, dtype=_half_dtype(dtype), device=device)
+    return qw, zeros, scales
+
+
+def repack_awq(qweight, qzeros, scales, K, N, group, dtype, layout=W4_LAYOUT_TILE, stream=None):
+    qw, zeros, sc = _alloc_repacked(K, N, group, dtype, layout, qweight.device)
+    w4_repack_awq(qweight, qzeros, scales, K, N, group, dtype, layout, qw, zeros, sc, stream)
+    return RepackedLayer(K, N, group, dtype, layout, qw, zeros, sc)
+
+
+def repack_gptq(qweight, qzeros, scales, g_idx, K, N, group, dtype, layout=W4_LAYOUT_TILE,
+                stream=None):
+    qw, zeros, sc = _alloc_repacked(K, N, group, dtype, layout, qweight.device)
+    perm = status = None
+    if g_idx is not None:
+        perm = torch.empty(K, dtype=torch.int32, device=qweight.device)
+        status = torch.full((4,), -1, dtype=torch.int32, device=qweight.device)
+    w4_repack_gptq(qweight, qzeros, scales, g_idx, K, N, group, dtype, layout, qw, zeros, sc,
+                   perm, status, stream)
+    return RepackedLayer(K, N, group, dtype, layout, qw, zeros, sc, perm, status)
+
+
+def linear(x, layer: RepackedLayer, y=None, workspace=None, stream=None):
+    """y = x · W for a TILE-layout layer; x is [M, K] fp16/bf16 on the device."""
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, layer.N), dtype=x.dtype, device=x.device)
+    need = w4a16_gemm_workspace_size(M, layer.N, layer.K, layer.group, layer.dtype,
+                                     layer.perm is not None)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    w4a16_gemm(x, layer.qw, layer.scales, layer.zeros, layer.perm, y, M, layer.N, layer.K,
+               layer.group, layer.dtype, workspace, None, stream)
+    return y

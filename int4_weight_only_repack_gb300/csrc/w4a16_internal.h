@@ -1,0 +1,51 @@
+// Internal declarations shared by the library's translation units (host side).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/w4a16.h"
+
+namespace w4 {
+
+// Launchers. Arguments are validated by the C-ABI layer before these run.
+cudaError_t launch_awq_to_std(const int32_t* qweight, int32_t* qw_out, int K, int N,
+                              cudaStream_t s);
+cudaError_t launch_to_tile(const int32_t* src, int src_is_awq, const int32_t* perm,
+                           int32_t* qw_out, int K, int N, cudaStream_t s);
+cudaError_t launch_std_rows_permuted(const int32_t* src, const int32_t* perm, int32_t* qw_out,
+                                     int K, int N, cudaStream_t s);
+cudaError_t launch_meta(const int32_t* qzeros, int zeros_are_awq, const void* scales,
+                        int32_t* zeros_out, void* scales_out, int G, int N, cudaStream_t s);
+cudaError_t launch_act_order_perm(const int32_t* g_idx, int K, int group, int32_t* perm_out,
+                                  int32_t* status_out, cudaStream_t s);
+cudaError_t launch_dequant(const int32_t* qw, const void* scales, const int32_t* zeros, int K,
+                           int N, int group, int bf16, int layout, int out_f32, void* w_out,
+                           cudaStream_t s);
+
+struct GemmArgs {
+  const void* x;
+  const uint32_t* qw;
+  const void* scales;
+  const uint32_t* zeros;
+  const int32_t* perm;
+  void* y;
+  int M, N, K, group;
+  int bf16;
+  void* workspace;
+  size_t workspace_bytes;
+};
+
+// Small-M kernel: M rows processed in chunks of up to 64.
+cudaError_t launch_decode(const GemmArgs& a, cudaStream_t s);
+
+// Device properties cached per device.
+struct DeviceInfo {
+  int sm_count;
+  int major, minor;
+  int max_smem_optin;
+};
+cudaError_t device_info(DeviceInfo* out);
+
+}  // namespace w4

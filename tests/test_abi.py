@@ -1,0 +1,137 @@
+"""Host-side checks of the C ABI: the library loads, exports every declared
+symbol, and rejects bad arguments with the documented status before touching
+the GPU (these run on a machine without one)."""
+import ctypes
+
+import pytest
+
+from libutil import declared_symbols, ensure_built
+
+W4_OK, W4_ERR_NULL, W4_ERR_SHAPE, W4_ERR_GROUP, W4_ERR_ALIGN = 0, 1, 2, 3, 4
+W4_ERR_DTYPE, W4_ERR_LAYOUT, W4_ERR_ALIAS, W4_ERR_WORKSPACE = 5, 6, 7, 10
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return ensure_built()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert set(names) >= {"w4_repack_awq", "w4_repack_gptq", "w4a16_gemm", "w4_dequant",
+                          "w4_repack_sizes", "w4a16_gemm_workspace_size", "w4_status_string",
+                          "w4_abi_version"}
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_no_internal_symbols_leak(lib):
+    # the library hides everything but the C ABI
+    for name in ("launch_decode", "_ZN2w413launch_decodeERKNS_8GemmArgsEP11CUstream_st"):
+        with pytest.raises(AttributeError):
+            getattr(lib, name)
+
+
+def test_status_strings_and_version():
+    import int4_weight_only_repack_gb300 as w4
+    ensure_built()
+    assert w4.w4_abi_version() == 1
+    for st in range(12):
+        assert w4.w4_status_string(st)
+    assert "unknown" in w4.w4_status_string(99)
+
+
+def test_repack_sizes():
+    import int4_weight_only_repack_gb300 as w4
+    ensure_built()
+    # tiny layer: K=256, N=256, group 128 -> 32 KB codes, 2 groups
+    assert w4.w4_repack_sizes(256, 256, 128, w4.W4_LAYOUT_STD) == (256 * 256 // 2, 2 * 256 // 2,
+                                                                    2 * 256 * 2)
+    assert w4.w4_repack_sizes(4096, 22016, 128, w4.W4_LAYOUT_TILE) == (4096 * 22016 // 2,
+                                                                        32 * 22016 // 2,
+                                                                        32 * 22016 * 2)
+    assert w4.w4_repack_sizes(256, 64, -1, w4.W4_LAYOUT_TILE)[1] == 64 // 2
+
+
+FAKE = 0x10000  # a 16-byte aligned non-null address; never dereferenced
+
+
+@pytest.mark.parametrize("args,status", [
+    ((0, 256, 128, 0), W4_ERR_SHAPE),
+    ((256, 0, 128, 0), W4_ERR_SHAPE),
+    ((256, 256, 96, 0), W4_ERR_GROUP),
+    ((200, 256, 128, 0), W4_ERR_GROUP),
+    ((256, 260, 128, 0), W4_ERR_SHAPE),
+    ((256, 264, 128, 1), W4_ERR_SHAPE),     # TILE needs N % 16
+    ((288, 256, 32, 1), W4_ERR_SHAPE),      # TILE needs K % 64
+    ((256, 256, 128, 7), W4_ERR_LAYOUT),
+    ((1 << 21, 256, 128, 0), W4_ERR_SHAPE),
+])
+def test_repack_sizes_rejects(lib, args, status):
+    a = ctypes.c_size_t()
+    assert lib.w4_repack_sizes(*args, ctypes.byref(a), None, None) == status
+
+
+def _gemm(lib, x=FAKE, qw=FAKE * 2, sc=FAKE * 3, z=FAKE * 4, perm=None, y=FAKE * 5, M=4, N=256,
+          K=256, group=128, dtype=1, ws=None, ws_b=0):
+    return lib.w4a16_gemm(x, qw, sc, z, perm, y, M, N, K, group, dtype, ws, ws_b, None)
+
+
+def test_gemm_rejects_bad_arguments(lib):
+    assert _gemm(lib, x=None) == W4_ERR_NULL
+    assert _gemm(lib, y=None) == W4_ERR_NULL
+    assert _gemm(lib, qw=None) == W4_ERR_NULL
+    assert _gemm(lib, x=FAKE + 2) == W4_ERR_ALIGN
+    assert _gemm(lib, y=FAKE * 5 + 8) == W4_ERR_ALIGN
+    assert _gemm(lib, N=264) == W4_ERR_SHAPE
+    assert _gemm(lib, K=288, group=32) == W4_ERR_SHAPE
+    assert _gemm(lib, M=-1) == W4_ERR_SHAPE
+    assert _gemm(lib, group=16) == W4_ERR_GROUP
+    assert _gemm(lib, dtype=2) == W4_ERR_DTYPE
+    # y overlapping x
+    assert _gemm(lib, y=FAKE + 256) == W4_ERR_ALIAS
+    # M == 0 is a no-op that succeeds without touching the device
+    assert _gemm(lib, M=0) == W4_OK
+
+
+def test_repack_rejects_bad_arguments(lib):
+    f = lib.w4_repack_awq
+    ok = dict(qweight=FAKE, qzeros=FAKE * 3, scales=FAKE * 5, K=256, N=256, group=128, dtype=0,
+              layout=1, qw_out=FAKE * 7, zeros_out=FAKE * 9, scales_out=FAKE * 11, stream=None)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return f(*a.values())
+
+    assert call(qweight=None) == W4_ERR_NULL
+    assert call(scales_out=None) == W4_ERR_NULL
+    assert call(qw_out=FAKE * 7 + 4) == W4_ERR_ALIGN
+    assert call(qw_out=FAKE) == W4_ERR_ALIAS          # output over the input
+    assert call(zeros_out=FAKE * 7) == W4_ERR_ALIAS   # two outputs overlap
+    assert call(layout=2) == W4_ERR_LAYOUT
+    assert call(dtype=-1) == W4_ERR_DTYPE
+    g = lib.w4_repack_gptq
+    # act-order needs perm_out and status_out
+    assert g(FAKE, FAKE * 3, FAKE * 5, FAKE * 13, 256, 256, 128, 0, 1, FAKE * 7, FAKE * 9,
+             FAKE * 11, None, None, None) == W4_ERR_NULL
+    # too many groups for the act-order sort
+    assert g(FAKE, FAKE * 3, FAKE * 5, FAKE * 13, 1 << 19, 256, 32, 0, 1, FAKE * 7 * 1024,
+             FAKE * 9 * 1024, FAKE * 11 * 1024, FAKE * 15 * 1024, FAKE * 17 * 1024,
+             None) == W4_ERR_SHAPE
+
+
+def test_dequant_rejects_bad_arguments(lib):
+    d = lib.w4_dequant
+    assert d(None, FAKE, FAKE * 2, 256, 256, 128, 0, 1, 1, FAKE * 3, None) == W4_ERR_NULL
+    assert d(FAKE, FAKE * 2, FAKE * 3, 256, 256, 128, 0, 1, 1, FAKE, None) == W4_ERR_ALIAS
+    assert d(FAKE, FAKE * 2, FAKE * 3, 256, 256, 128, 0, 3, 1, FAKE * 9, None) == W4_ERR_LAYOUT
+
+
+def test_binding_raises_on_error():
+    import int4_weight_only_repack_gb300 as w4
+    ensure_built()
+    with pytest.raises(w4.W4Error) as e:
+        w4.w4a16_gemm(FAKE, FAKE * 2, FAKE * 3, FAKE * 4, None, FAKE * 5, 4, 264, 256, 128,
+                      "bf16", stream=0)
+    assert e.value.status == W4_ERR_SHAPE

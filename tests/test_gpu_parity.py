@@ -1,0 +1,286 @@
+"""GPU parity: every kernel against the CPU oracle on the same seeded inputs.
+
+Repacked tensors and dequantised weights must match bit for bit; the GEMM must
+satisfy max|y - y_ref| / max|y_ref| <= 4e-3 (fp32 accumulation, fp16/bf16
+output). Shapes span several tiles and end on ragged tiles; canaries around
+every output buffer catch writes out of bounds.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from libutil import ensure_built, half_from_dev, half_to_dev, to_dev
+
+pytestmark = pytest.mark.gpu
+
+TOL = 4e-3
+GUARD = 64
+CANARY = 0x5A5A5A5A
+
+
+@pytest.fixture(scope="module")
+def w4():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ensure_built()
+    import int4_weight_only_repack_gb300 as mod
+    return mod
+
+
+def guarded(n, dtype, device="cuda"):
+    """A buffer of n elements with canary guard bands on both sides."""
+    import torch
+    itemsize = torch.empty((), dtype=dtype).element_size()
+    raw = torch.empty(((n + 2 * GUARD) * itemsize + 3) // 4, dtype=torch.int32, device=device)
+    raw.fill_(CANARY)
+    body = raw.view(torch.uint8)[GUARD * itemsize:(GUARD + n) * itemsize].view(dtype)
+    return raw, body
+
+
+def check_guards(raw, n, itemsize):
+    b = raw.cpu().view(-1).numpy().view(np.uint8)
+    head = b[:GUARD * itemsize]
+    tail = b[(GUARD + n) * itemsize:]
+    # every canary byte is 0x5A
+    assert np.all(head == 0x5A), "write before the buffer"
+    assert np.all(tail == 0x5A), "write after the buffer"
+
+
+def hdt(dtype):
+    import torch
+    return torch.bfloat16 if dtype == "bf16" else torch.float16
+
+
+def repack(w4, L, layout, device="cuda"):
+    """Repack a synth layer on the GPU; returns (qw, zeros, scales, perm, status) tensors."""
+    import torch
+    K, N, g = L.K, L.N, L.group
+    qw_b, z_b, s_b = w4.w4_repack_sizes(K, N, g, layout)
+    qw_raw, qw = guarded(qw_b // 4, torch.int32)
+    z_raw, zeros = guarded(z_b // 4, torch.int32)
+    s_raw, scales = guarded(s_b // 2, hdt(L.dtype))
+    qweight, qzeros = to_dev(L.qweight), to_dev(L.qzeros)
+    sc_in = half_to_dev(L.scales, L.dtype)
+    perm = status = None
+    if L.fmt == "awq":
+        w4.w4_repack_awq(qweight, qzeros, sc_in, K, N, g, L.dtype, layout, qw, zeros, scales)
+    else:
+        gi = to_dev(L.g_idx) if L.g_idx is not None else None
+        if gi is not None:
+            perm = torch.empty(K, dtype=torch.int32, device=device)
+            status = torch.full((4,), -7, dtype=torch.int32, device=device)
+        w4.w4_repack_gptq(qweight, qzeros, sc_in, gi, K, N, g, L.dtype, layout, qw, zeros,
+                          scales, perm, status)
+    torch.cuda.synchronize()
+    check_guards(qw_raw, qw_b // 4, 4)
+    check_guards(z_raw, z_b // 4, 4)
+    check_guards(s_raw, s_b // 2, 2)
+    return qw, zeros, scales, perm, status
+
+
+def oracle_codes(L):
+    q, z, s = oracle.layer_codes(L.qweight, L.qzeros, L.scales, L.dtype, L.fmt)
+    return q, z, s
+
+
+REPACK_SHAPES = [
+    # K, N, group, dtype
+    (256, 256, 128, "fp16"),   # the tiny workload's shape
+    (320, 272, 64, "bf16"),    # 5 atom rows, 17 column tiles: ragged 128-column block
+    (128, 16, 32, "fp16"),     # one column tile
+    (512, 400, -1, "bf16"),    # per-channel group
+    (1024, 2064, 128, "bf16"),
+]
+
+
+@pytest.mark.parametrize("K,N,group,dtype", REPACK_SHAPES)
+def test_repack_awq_bitexact(w4, K, N, group, dtype):
+    L = synth.make_custom_layer([100, K, N], K, N, group=K if group == -1 else group, dtype=dtype)
+    L.group = group if group != -1 else K
+    grp = group
+    q, z, _ = oracle_codes(L)
+    qw_std_ref, z_std_ref = oracle.repack_awq_to_std(L.qweight, L.qzeros)
+    for layout in (w4.W4_LAYOUT_STD, w4.W4_LAYOUT_TILE):
+        qw, zeros, scales, _, _ = repack_layer_group(w4, L, layout, grp)
+        got = qw.cpu().numpy()
+        if layout == w4.W4_LAYOUT_TILE:
+            assert np.array_equal(got, oracle.tile_pack(q))
+        else:
+            assert np.array_equal(got.reshape(K // 8, N), qw_std_ref)
+        assert np.array_equal(zeros.cpu().numpy().reshape(z_std_ref.shape), z_std_ref)
+        assert np.array_equal(half_from_dev(scales).reshape(L.scales.shape), L.scales)
+
+
+def repack_layer_group(w4, L, layout, group):
+    """repack() with the ABI's group argument (-1 allowed) instead of L.group."""
+    saved = L.group
+    L.group = group
+    try:
+        return repack(w4, L, layout)
+    finally:
+        L.group = saved
+
+
+@pytest.mark.parametrize("K,N,group,act_order", [
+    (512, 272, 128, True), (768, 48, 64, True), (256, 32, 32, True), (384, 144, 128, False),
+])
+def test_repack_gptq_bitexact(w4, K, N, group, act_order):
+    L = synth.make_custom_layer([101, K, N], K, N, group=group, dtype="fp16", fmt="gptq",
+                                act_order=act_order)
+    q, z, _ = oracle_codes(L)
+    perm_ref = oracle.act_order_perm(L.g_idx) if act_order else np.arange(K)
+    for layout in (w4.W4_LAYOUT_STD, w4.W4_LAYOUT_TILE):
+        qw, zeros, scales, perm, status = repack(w4, L, layout)
+        if act_order:
+            assert status.cpu().numpy()[0] == 0
+            assert np.array_equal(perm.cpu().numpy(), perm_ref)
+        got = qw.cpu().numpy()
+        if layout == w4.W4_LAYOUT_TILE:
+            assert np.array_equal(got, oracle.tile_pack(q[perm_ref]))
+        else:
+            assert np.array_equal(got.reshape(K // 8, N), oracle.pack_rows_std(q[perm_ref]))
+        assert np.array_equal(zeros.cpu().numpy().reshape(L.qzeros.shape), L.qzeros)
+
+
+def test_gidx_irregular_reports_status(w4):
+    import torch
+    K, N, group = 256, 32, 64
+    L = synth.make_custom_layer([102], K, N, group=group, dtype="bf16", fmt="gptq", act_order=True)
+    for bad in ("range", "count"):
+        gi = L.g_idx.copy()
+        if bad == "range":
+            gi[5] = K // group          # one past the last group
+        else:
+            first0 = int(np.flatnonzero(gi == 0)[0])
+            gi[first0] = 1              # group 0 one short, group 1 one long
+        L2 = synth.Layer(L.K, L.N, L.group, L.dtype, L.fmt, L.qweight, L.qzeros, L.scales, gi)
+        _, _, _, perm, status = repack(w4, L2, w4.W4_LAYOUT_TILE)
+        assert status.cpu().numpy()[0] == 11  # W4_ERR_GIDX
+        assert np.array_equal(perm.cpu().numpy(), np.arange(K))
+
+
+@pytest.mark.parametrize("K,N,group,dtype", [(256, 256, 128, "fp16"), (320, 272, 64, "bf16"),
+                                             (512, 48, 32, "bf16"), (256, 400, 128, "fp16")])
+def test_dequant_bitexact(w4, K, N, group, dtype):
+    import torch
+    L = synth.make_custom_layer([103, K, N], K, N, group=group, dtype=dtype)
+    q, z, s = oracle_codes(L)
+    W_ref = oracle.dequant(q, z, s, oracle.group_of_rows(K, group))
+    for layout in (w4.W4_LAYOUT_STD, w4.W4_LAYOUT_TILE):
+        qw, zeros, scales, _, _ = repack(w4, L, layout)
+        raw, w32 = guarded(K * N, torch.float32)
+        w4.w4_dequant(qw, scales, zeros, K, N, group, dtype, layout, 1, w32)
+        raw_h, wh = guarded(K * N, hdt(dtype))
+        w4.w4_dequant(qw, scales, zeros, K, N, group, dtype, layout, 0, wh)
+        torch.cuda.synchronize()
+        check_guards(raw, K * N, 4)
+        check_guards(raw_h, K * N, 2)
+        assert np.array_equal(w32.cpu().numpy().reshape(K, N), W_ref)
+        assert np.array_equal(half_from_dev(wh).reshape(K, N),
+                              oracle.round_f64_to_half_bits(W_ref, dtype))
+
+
+def run_gemm(w4, L, x_bits, layout_parts, M, group=None):
+    import torch
+    qw, zeros, scales, perm, _ = layout_parts
+    K, N = L.K, L.N
+    g = L.group if group is None else group
+    xd = half_to_dev(x_bits, L.dtype) if M > 0 else torch.empty(0, dtype=hdt(L.dtype), device="cuda")
+    raw, y = guarded(M * N, hdt(L.dtype))
+    need = w4.w4a16_gemm_workspace_size(M, N, K, g, L.dtype, perm is not None)
+    ws = torch.zeros(max(need, 16), dtype=torch.uint8, device="cuda") if need else None
+    w4.w4a16_gemm(xd, qw, scales, zeros, perm, y, M, N, K, g, L.dtype, ws)
+    torch.cuda.synchronize()
+    check_guards(raw, M * N, 2)
+    return half_from_dev(y).reshape(M, N)
+
+
+def ulp_error(y_bits, y_ref, dtype):
+    """max over elements of |y - y_ref| / (ulp(y_ref) + 1e-5 * max|y_ref|).
+
+    The absolute 1e-5 * max|y_ref| term absorbs the fp32 accumulation error on
+    outputs that cancel to near zero, where one output ulp is tiny.
+    """
+    y = oracle.half_bits_to_f64(y_bits, dtype)
+    if y.size == 0:
+        return 0.0
+    mant = 11 if dtype == "fp16" else 8
+    e = np.floor(np.log2(np.maximum(np.abs(y_ref), 1e-30)))
+    if dtype == "fp16":
+        e = np.maximum(e, -14)
+    ulp = np.exp2(e - (mant - 1))
+    slack = 1e-5 * np.max(np.abs(y_ref))
+    return float(np.max(np.abs(y - y_ref) / (ulp + slack)))
+
+
+GEMM_CASES = [
+    # K, N, group, dtype, Ms
+    (256, 256, 128, "fp16", (4, 1, 0)),
+    (320, 272, 64, "bf16", (1, 2, 3, 7, 8, 9, 15, 16, 17)),
+    (1024, 2064, 128, "bf16", (1, 5, 16, 31, 33, 64, 65, 100)),
+    (2048, 512, 32, "fp16", (1, 16, 48)),
+    (768, 1040, -1, "bf16", (3, 24)),
+    (4096, 160, 128, "bf16", (1, 12)),
+]
+
+
+@pytest.mark.parametrize("K,N,group,dtype,Ms", GEMM_CASES)
+def test_gemm_vs_oracle(w4, K, N, group, dtype, Ms):
+    g = K if group == -1 else group
+    L = synth.make_custom_layer([104, K, N], K, N, group=g, dtype=dtype)
+    parts = repack_layer_group(w4, L, w4.W4_LAYOUT_TILE, group)
+    for M in Ms:
+        x = synth.make_custom_x([105, K, M], M, K, dtype)
+        y = run_gemm(w4, L, x, parts, M, group=group)
+        if M == 0:
+            continue
+        y_ref = oracle.reference_y(x, L.qweight, L.qzeros, L.scales, g, dtype, "awq")
+        err = oracle.rel_err(oracle.half_bits_to_f64(y, dtype), y_ref)
+        assert err <= TOL, (M, err)
+        # the small-M kernel multiplies exact (q - z) and scales in fp32:
+        # only the final rounding separates it from the exact result
+        assert ulp_error(y, y_ref, dtype) <= 1.0, (M, ulp_error(y, y_ref, dtype))
+
+
+@pytest.mark.parametrize("K,N,group,Ms", [(512, 272, 128, (1, 4, 16, 40)),
+                                          (1536, 64, 64, (1, 9)), (1024, 96, 32, (2, 17))])
+def test_gemm_act_order_vs_oracle(w4, K, N, group, Ms):
+    L = synth.make_custom_layer([106, K, N], K, N, group=group, dtype="fp16", fmt="gptq",
+                                act_order=True)
+    parts = repack(w4, L, w4.W4_LAYOUT_TILE)
+    for M in Ms:
+        x = synth.make_custom_x([107, K, M], M, K, "fp16")
+        y = run_gemm(w4, L, x, parts, M)
+        y_ref = oracle.reference_y(x, L.qweight, L.qzeros, L.scales, group, "fp16", "gptq",
+                                   g_idx=L.g_idx)
+        err = oracle.rel_err(oracle.half_bits_to_f64(y, "fp16"), y_ref)
+        assert err <= TOL, (M, err)
+        assert ulp_error(y, y_ref, "fp16") <= 1.0
+
+
+def test_gemm_is_deterministic(w4):
+    K, N, M = 2048, 1024, 16
+    L = synth.make_custom_layer([108], K, N, group=128, dtype="bf16")
+    parts = repack(w4, L, w4.W4_LAYOUT_TILE)
+    x = synth.make_custom_x([109], M, K, "bf16")
+    y1 = run_gemm(w4, L, x, parts, M)
+    y2 = run_gemm(w4, L, x, parts, M)
+    assert np.array_equal(y1, y2)
+
+
+def test_gemm_one_hot_rows_exact(w4):
+    """x = e_k picks row k of W: y must be RN(W[k, :]) exactly."""
+    K, N = 512, 272
+    L = synth.make_custom_layer([110], K, N, group=64, dtype="bf16")
+    parts = repack(w4, L, w4.W4_LAYOUT_TILE)
+    q, z, s = oracle_codes(L)
+    W = oracle.dequant(q, z, s, oracle.group_of_rows(K, 64))
+    ks = [0, 1, 63, 64, 300, 511]
+    x = np.zeros((len(ks), K), np.uint16)
+    for i, k in enumerate(ks):
+        x[i, k] = 0x3F80
+    y = run_gemm(w4, L, x, parts, len(ks))
+    for i, k in enumerate(ks):
+        assert np.array_equal(y[i], oracle.round_f64_to_half_bits(W[k], "bf16"))
