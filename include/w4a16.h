@@ -92,7 +92,8 @@ enum {
     W4_ERR_ARCH = 8,       /* the current CUDA device is not compute capability 10.3    */
     W4_ERR_CUDA = 9,       /* a CUDA runtime call or kernel launch failed               */
     W4_ERR_WORKSPACE = 10, /* workspace NULL or smaller than w4a16_gemm_workspace_size  */
-    W4_ERR_GIDX = 11       /* (written to *status_out by the device) g_idx irregular    */
+    W4_ERR_GIDX = 11,      /* (written to *status_out by the device) g_idx irregular    */
+    W4_ERR_TIMEOUT = 12    /* (device status word) a kernel gave up on a pipeline wait  */
 };
 
 enum { W4_F16 = 0, W4_BF16 = 1 };
@@ -150,7 +151,8 @@ W4_API w4_status w4_repack_gptq(const int32_t* qweight, const int32_t* qzeros, c
 
 /*
  * Workspace bytes w4a16_gemm needs for this call shape (0 = none). Act-order
- * calls above the small-M range stage the gathered activations x[:, perm] there.
+ * calls with M > 64 stage the gathered activations x[:, perm] there
+ * (M*K*2 bytes, rounded up to 256). The contents need no initialisation.
  */
 W4_API size_t w4a16_gemm_workspace_size(int M, int N, int K, int group, int dtype, int has_perm);
 
@@ -166,11 +168,23 @@ W4_API size_t w4a16_gemm_workspace_size(int M, int N, int K, int group, int dtyp
  *   workspace / workspace_bytes: device scratch of at least
  *          w4a16_gemm_workspace_size(...) bytes (may be NULL when that is 0).
  * Accumulation is fp32; the result is rounded once to dtype. Deterministic:
- * the same inputs give the same bits.
+ * the same inputs give the same bits. M <= 64 (or N % 32 != 0) runs the
+ * small-M kernel (CUDA-core dequantisation into exact (q - z) operands,
+ * mma.sync, per-group fp32 scaling); larger M runs the tcgen05 kernel, whose
+ * B operand is the dequantised weight rounded once to dtype.
  */
 W4_API w4_status w4a16_gemm(const void* x, const int32_t* qw, const void* scales, const int32_t* zeros,
                      const int32_t* perm, void* y, int M, int N, int K, int group, int dtype,
                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Read the library's device status word: W4_OK, or W4_ERR_TIMEOUT once some
+ * kernel of this library gave up on an internal pipeline wait (every such wait
+ * is bounded at one second; the kernel then drains its own copies, frees its
+ * tensor memory and exits, leaving its output incomplete). With clear != 0 the
+ * word is reset to W4_OK. Synchronous: it waits for the device.
+ */
+W4_API w4_status w4_device_status(int32_t* status_out, int clear);
 
 /*
  * Dequantise a repacked layer to a dense W [K][N] (row-major): fp32 when out_f32

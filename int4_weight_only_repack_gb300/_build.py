@@ -19,7 +19,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_NAME = "libw4a16.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 
-SOURCES = ("w4a16_api.cu", "repack_kernels.cu", "decode_kernel.cu")
+SOURCES = ("w4a16_api.cu", "repack_kernels.cu", "decode_kernel.cu", "prefill_kernel.cu")
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CXX_FLAGS = [
@@ -41,33 +41,35 @@ def _run(cmd):
     return proc.returncode, proc.stdout
 
 
-def build(verbose: bool = False, ptxas_info: bool = False) -> str:
+def build(verbose: bool = False, ptxas_info: bool = False, csrc: str = CSRC,
+          out: str = LIB_PATH, build_dir: str = BUILD_DIR, defines=()) -> str:
     """Compile every CUDA source and link libw4a16.so; returns the library path."""
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    extra += [f"-D{d}" for d in defines]
     jobs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         jobs.append((src, obj, [cc, *ARCH_FLAGS, *CXX_FLAGS, *extra, "-c",
-                                os.path.join(CSRC, src), "-o", obj]))
+                                os.path.join(csrc, src), "-o", obj]))
     with ThreadPoolExecutor(max_workers=len(jobs)) as ex:
         results = list(ex.map(lambda j: (j[0], *_run(j[2])), jobs))
     failed = False
-    for src, rc, out in results:
+    for src, rc, log in results:
         if verbose or rc != 0 or ptxas_info:
-            sys.stdout.write(f"--- {src} (rc={rc})\n{out}")
+            sys.stdout.write(f"--- {src} (rc={rc})\n{log}")
         failed |= rc != 0
     if failed:
         raise RuntimeError("nvcc compilation failed")
-    tmp = LIB_PATH + ".tmp"
-    rc, out = _run([cc, *ARCH_FLAGS, "-shared", "-o", tmp, *[j[1] for j in jobs],
+    tmp = out + ".tmp"
+    rc, log = _run([cc, *ARCH_FLAGS, "-shared", "-o", tmp, *[j[1] for j in jobs],
                     "-Xcompiler", "-fvisibility=hidden"])
     if rc != 0:
-        sys.stdout.write(out)
+        sys.stdout.write(log)
         raise RuntimeError("nvcc link failed")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

@@ -5,238 +5,368 @@
 // the kernel is organised around the weight stream:
 //
 //  * Each warp owns one 16-column tile and a contiguous run of 64-row TILE
-//    atoms. One 16-byte load per lane fetches a whole atom (512 B per warp,
-//    fully coalesced); the four words a lane receives are exactly the A
-//    fragments of four m16n8k16 MMAs in the swapped form y^T = W^T · x^T (the
-//    weight columns fill the MMA's 16 rows, the tokens its 8 columns). Loads
-//    are issued PIPE atoms ahead of use to keep enough bytes in flight.
+//    atoms (512 bytes each, contiguous in memory). Lane 0 streams the run into
+//    a private shared-memory ring with bulk asynchronous copies
+//    (cp.async.bulk, completion counted on one mbarrier per stage), so many
+//    kilobytes per warp are in flight without holding registers. Each lane
+//    then reads its 16 bytes of an atom: exactly the A fragments of four
+//    m16n8k16 MMAs in the swapped form y^T = W^T · x^T (the weight columns
+//    fill the MMA's 16 rows, the tokens its 8 columns).
 //  * Dequantisation ("vLLM AWQ 4-bit 量化实践" §5.3: (b - zeros) * scales) is
 //    split: the MMA consumes (q - z), which is exact in fp16/bf16, and the
-//    per-(group, column) scale is applied to the fp32 partial sum of each
-//    group. One LOP3 turns a nibble pair into MAGIC + q halves and one packed
-//    subtraction of MAGIC + z leaves q - z.
-//  * The CTA stages its slice of x in shared memory once (gathering x[:, perm]
-//    for act-order layers), padded so fragment loads are free of bank conflicts.
+//    per-(group, column) scale multiplies the fp32 partial sum of each group.
+//    One LOP3 turns a nibble pair into MAGIC + q halves and one packed
+//    subtraction of MAGIC + z leaves q - z. A warp's scales and zeros are
+//    staged once in shared memory.
+//  * The CTA stages its slice of x in shared memory (gathering x[:, perm] for
+//    act-order layers), padded so fragment loads are free of bank conflicts.
 //  * Split-K across the CTAs of a thread-block cluster (up to 8 along K): each
 //    CTA leaves its fp32 partial tile in its own shared memory, and after a
 //    cluster barrier every CTA sums a slice of the outputs over all peers
 //    through distributed shared memory, in a fixed order (deterministic, no
-//    global workspace, no atomics, no spin waits: "vLLM AWQ 4-bit 量化实践"
-//    §5.3 names split-K for the fused kernel).
+//    global workspace, no atomics: "vLLM AWQ 4-bit 量化实践" §5.3 names
+//    split-K for the fused kernel).
+//  * Waits on the ring's mbarriers are bounded (one second); on a timeout the
+//    warp records W4_ERR_TIMEOUT in the device status word, lets its copies in
+//    flight land (bounded again) and stops computing.
 #include <cooperative_groups.h>
 
 #include <algorithm>
 #include <mutex>
 #include <unordered_map>
 
+#include "sm100_ptx.cuh"
 #include "w4a16_device.cuh"
 #include "w4a16_internal.h"
 
 namespace cg = cooperative_groups;
 
 namespace w4 {
+
+extern __device__ int g_device_status;
+
 namespace {
+
+using namespace sm100;
 
 constexpr int DEC_THREADS = 256;
 constexpr int DEC_WARPS = DEC_THREADS / 32;
 constexpr int ATOM_K = 64;
 constexpr int ATOM_WORDS = 128;
+constexpr int ATOM_BYTES = 512;
 constexpr int MAX_SPLIT = 8;
+constexpr int RING = 4;              // stages per warp
+constexpr int STAGE_ATOMS = 2;       // atoms per stage (1 KB)
+constexpr int X_BUDGET = 32 * 1024;  // bytes of staged x per CTA
+constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
 
 struct DecodeParams {
-  const uint16_t* x;      // [M][K]
-  const uint32_t* qw;     // TILE words
-  const uint16_t* scales; // [G][N]
-  const uint32_t* zeros;  // [G][N/8] standard order
-  const int32_t* perm;    // [K] or nullptr
-  uint16_t* y;            // [M][N]
-  int M, N, K, group;
-  int A;                  // K / 64
-  int WN;                 // warps along N per CTA (WK = 8 / WN along K)
-  int chunk_atoms;        // atoms of x staged in shared memory at a time
-  int x_stride;           // shared x row stride in halves
+  const uint16_t* x;       // [M][K]
+  const uint32_t* qw;      // TILE words
+  const uint16_t* scales;  // [G][N]
+  const uint32_t* zeros;   // [G][N/8] standard order
+  const int32_t* perm;     // [K] or nullptr
+  uint16_t* y;             // [M][N]
+  int M, N, K;
+  int gshift;              // group = 1 << gshift; 31 = one group over all of K
+  int A;                   // K / 64
+  int WN;                  // warps along N per CTA (WK = 8 / WN along K)
+  int chunk_atoms;         // atoms of x staged in shared memory at a time
+  int x_stride;            // shared x row stride in halves
+  int maxg;                // group slots of the per-warp scale / zero stage
+  int xp_stride;           // row length of the x prefix sums (2 * chunk_atoms + 1)
 };
 
-template <int MT>
-struct Pipe {
-  static constexpr int depth = MT <= 2 ? 8 : (MT == 4 ? 4 : 2);
+struct SmemLayout {
+  int xs, ring, bars, meta_s, meta_z, xpre, red, total;
 };
 
-// Scale pair (rows gg and gg+8 of the tile) and the tile's 16 zeros for one group.
-struct Meta {
-  uint32_t s;    // lo 16 bits: scale of column gg, hi: column gg+8
-  uint2 z;       // zeros words for columns [16nt, 16nt+8) and [16nt+8, 16nt+16)
-};
-
-__device__ __forceinline__ Meta load_meta(const DecodeParams& p, int gi, int nt, int gg) {
-  Meta m;
-  const uint16_t* sp = p.scales + (size_t)gi * p.N + nt * 16 + gg;
-  const uint32_t lo = __ldg(sp), hi = __ldg(sp + 8);
-  m.s = lo | (hi << 16);
-  m.z = __ldg(reinterpret_cast<const uint2*>(p.zeros + (size_t)gi * (p.N / 8) + nt * 2));
-  return m;
+__host__ __device__ inline SmemLayout smem_layout(int MT, int m_rows, int x_stride, int maxg,
+                                                  int xp_stride) {
+  SmemLayout L;
+  L.xs = 0;
+  L.ring = ((m_rows * x_stride * 2) + 1023) & ~1023;
+  L.bars = L.ring + DEC_WARPS * RING * STAGE_ATOMS * ATOM_BYTES;
+  L.meta_s = L.bars + DEC_WARPS * RING * 8;
+  L.meta_z = L.meta_s + DEC_WARPS * maxg * 32;
+  L.xpre = (L.meta_z + DEC_WARPS * maxg * 8 + 15) & ~15;
+  L.red = (L.xpre + 8 * MT * xp_stride * 4 + 15) & ~15;
+  L.total = L.red + DEC_WARPS * 16 * 8 * MT * 4;
+  return L;
 }
 
-template <int MT, bool BF16, bool G32>
-__global__ void __launch_bounds__(DEC_THREADS, 2) w4a16_decode_kernel(const DecodeParams p) {
-  constexpr int PIPE = Pipe<MT>::depth;
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// MT: token tiles of 8 (M <= 8 * MT). G64: every 64-row atom lies in one group.
+// With bf16 the MMA consumes the codes as 128 + q (exact in bf16) and each
+// group's partial sum is corrected by (128 + z) * sum(x) before scaling; with
+// fp16 the operand is q - z (exact) and needs no correction.
+template <int MT, bool BF16, bool G64>
+__global__ void __launch_bounds__(DEC_THREADS, MT <= 2 ? 3 : 2) w4a16_decode_kernel(const DecodeParams p) {
   constexpr uint32_t MAGIC = Magic<BF16>::pair;
-  extern __shared__ __align__(16) uint8_t smem[];
+  constexpr bool BIAS = BF16;
+  extern __shared__ __align__(1024) uint8_t smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gg = lane >> 2, t = lane & 3;
   const int S = gridDim.y;          // split-K factor == cluster size along y
   const int srank = blockIdx.y;     // rank inside the cluster
   const int WN = p.WN, WK = DEC_WARPS / WN;
+  const int MR = 8 * MT;
+  const SmemLayout L = smem_layout(MT, p.M, p.x_stride, p.maxg, p.xp_stride);
 
-  // CTA K range in atoms.
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem + L.xs);
+  uint8_t* ring = smem + L.ring + warp * (RING * STAGE_ATOMS * ATOM_BYTES);
+  const uint32_t ring_s = smem_addr(ring);
+  const uint32_t bar0 = smem_addr(smem + L.bars + warp * RING * 8);
+  uint16_t* meta_s = reinterpret_cast<uint16_t*>(smem + L.meta_s) + warp * p.maxg * 16;
+  uint2* meta_z = reinterpret_cast<uint2*>(smem + L.meta_z) + warp * p.maxg;
+  float* xpre = reinterpret_cast<float*>(smem + L.xpre);
+  float* red = reinterpret_cast<float*>(smem + L.red);
+  const int NCOL = 16 * WN;
+
+  // CTA K range in atoms
   const int ka0 = (int)((long long)srank * p.A / S);
   const int ka1 = (int)((long long)(srank + 1) * p.A / S);
 
-  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
-  float* red = reinterpret_cast<float*>(smem + (size_t)8 * MT * p.x_stride * 2);
-  const int NCOL = 16 * WN;     // columns per CTA
-  const int MR = 8 * MT;        // padded rows
-
   const int wn = warp % WN, wk = warp / WN;
   const int nt = blockIdx.x * WN + wn;
-  const int NT = p.N / 16;
-  const bool warp_has_cols = nt < NT;
-  const uint32_t* wbase = p.qw + (size_t)nt * p.A * ATOM_WORDS + lane * 4;
-  const int group = p.group;
+  const bool has_cols = nt < p.N / 16;
+  const uint32_t* wsrc = p.qw + (size_t)nt * p.A * ATOM_WORDS;  // this tile's atom run
+
+  if (lane == 0) {
+    for (int s = 0; s < RING; ++s) mbar_init(bar0 + 8 * s, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
 
   float acc[MT][4], tot[MT][4];
 #pragma unroll
   for (int i = 0; i < MT; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = tot[i][j] = 0.f;
-  int cur_g = -1;
-  float s_lo = 0.f, s_hi = 0.f;
+  int cur_g = -1;       // group being accumulated in acc (-1: none)
+  int hs = 0;           // chunk-relative half-atom index where it started
+  float s_lo = 0.f, s_hi = 0.f, zlf = 0.f, zhf = 0.f;
   uint32_t zl = 0, zh = 0;
+  uint32_t it = 0;      // stages consumed by this warp (ring position and phase)
+  bool alive = true;    // false once a wait gave up
 
-  // The CTA range is walked in chunks whose x slice fits the shared buffer.
+  // tot += s * (acc - (MAGIC + z) * sum of x over halves [h0, h1)); acc = 0
+  auto flush = [&](int h0, int h1) {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      float c0 = 0.f, c1 = 0.f;
+      if constexpr (BIAS) {
+        const float* xp = xpre + (8 * mt + 2 * t) * p.xp_stride;
+        c0 = xp[h1] - xp[h0];
+        c1 = xp[p.xp_stride + h1] - xp[p.xp_stride + h0];
+      }
+      tot[mt][0] = fmaf(s_lo, fmaf(-zlf, c0, acc[mt][0]), tot[mt][0]);
+      tot[mt][1] = fmaf(s_lo, fmaf(-zlf, c1, acc[mt][1]), tot[mt][1]);
+      tot[mt][2] = fmaf(s_hi, fmaf(-zhf, c0, acc[mt][2]), tot[mt][2]);
+      tot[mt][3] = fmaf(s_hi, fmaf(-zhf, c1, acc[mt][3]), tot[mt][3]);
+      acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+    }
+  };
+
   for (int c0 = ka0; c0 < ka1; c0 += p.chunk_atoms) {
     const int c1 = min(ka1, c0 + p.chunk_atoms);
     const int kx0 = c0 * ATOM_K;
     const int KC = (c1 - c0) * ATOM_K;
+    const int wa0 = c0 + (int)((long long)wk * (c1 - c0) / WK);
+    const int wa1 = c0 + (int)((long long)(wk + 1) * (c1 - c0) / WK);
+    const int n_atoms = (has_cols && alive) ? wa1 - wa0 : 0;
+    const int n_stages = (n_atoms + STAGE_ATOMS - 1) / STAGE_ATOMS;
 
-    // ---- stage x[:, kx0:kx0+KC] (gathered through perm) ------------------------
+    // Stage j of this chunk goes to ring slot (it + j) % RING, where `it` is
+    // the warp's consumed-stage count when the chunk starts.
+    auto issue = [&](int j, uint32_t slot) {
+      const int a = wa0 + j * STAGE_ATOMS;
+      const uint32_t bytes = (uint32_t)min(STAGE_ATOMS, wa1 - a) * ATOM_BYTES;
+      mbar_arrive_expect_tx(bar0 + 8 * slot, bytes);
+      bulk_copy(ring_s + slot * (STAGE_ATOMS * ATOM_BYTES), wsrc + (size_t)a * ATOM_WORDS, bytes,
+                bar0 + 8 * slot);
+    };
+
+    // 1) start the weight stream first: it has the longest latency
+    if (lane == 0 && n_stages > 0) {
+      fence_proxy_async_smem();  // earlier reads of the ring precede these copies
+      for (int j = 0; j < min(RING, n_stages); ++j) issue(j, (it + j) % RING);
+    }
+
+    // 2) stage x[:M, kx0:kx0+KC] (gathered through perm)
     {
       const int chunks = KC / 8;
-      for (int i = tid; i < MR * chunks; i += DEC_THREADS) {
-        const int m = i / chunks, c = i % chunks;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (m < p.M) {
-          const uint16_t* xr = p.x + (size_t)m * p.K;
-          if (p.perm == nullptr) {
-            v = __ldg(reinterpret_cast<const uint4*>(xr + kx0 + 8 * c));
-          } else {
-            uint16_t h[8];
+      for (int i = tid; i < p.M * chunks; i += DEC_THREADS) {
+        const int m = i / chunks, c = i - m * chunks;
+        const uint16_t* xr = p.x + (size_t)m * p.K;
+        uint4 v;
+        if (p.perm == nullptr) {
+          v = __ldg(reinterpret_cast<const uint4*>(xr + kx0 + 8 * c));
+        } else {
+          uint16_t h[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) h[e] = __ldg(xr + __ldg(p.perm + kx0 + 8 * c + e));
-            v.x = h[0] | ((uint32_t)h[1] << 16);
-            v.y = h[2] | ((uint32_t)h[3] << 16);
-            v.z = h[4] | ((uint32_t)h[5] << 16);
-            v.w = h[6] | ((uint32_t)h[7] << 16);
-          }
+          for (int e = 0; e < 8; ++e) h[e] = __ldg(xr + __ldg(p.perm + kx0 + 8 * c + e));
+          v.x = h[0] | ((uint32_t)h[1] << 16);
+          v.y = h[2] | ((uint32_t)h[3] << 16);
+          v.z = h[4] | ((uint32_t)h[5] << 16);
+          v.w = h[6] | ((uint32_t)h[7] << 16);
         }
         *reinterpret_cast<uint4*>(xs + (size_t)m * p.x_stride + 8 * c) = v;
       }
     }
+
+    // 3) this warp's scales and zeros for the groups its atoms touch
+    const int g_first = (wa0 * ATOM_K) >> p.gshift;
+    if (n_atoms > 0) {
+      const int g_last = (wa1 * ATOM_K - 1) >> p.gshift;
+      for (int gl = lane; gl <= g_last - g_first; gl += 32) {
+        const int gi = g_first + gl;
+        const uint4* sp = reinterpret_cast<const uint4*>(p.scales + (size_t)gi * p.N + nt * 16);
+        uint4* sd = reinterpret_cast<uint4*>(meta_s + gl * 16);
+        sd[0] = __ldg(sp);
+        sd[1] = __ldg(sp + 1);
+        meta_z[gl] = __ldg(reinterpret_cast<const uint2*>(p.zeros + (size_t)gi * (p.N / 8) + nt * 2));
+      }
+    }
     __syncthreads();
 
-    // ---- per-warp weight stream ------------------------------------------------
-    const int wa0 = c0 + (int)((long long)wk * (c1 - c0) / WK);
-    const int wa1 = c0 + (int)((long long)(wk + 1) * (c1 - c0) / WK);
-    if (warp_has_cols && wa1 > wa0) {
-      const int n_atoms = wa1 - wa0;
-      uint4 wb[PIPE];
-      Meta mb[PIPE][G32 ? 2 : 1];
-
-      auto fetch = [&](int slot, int a) {
-        wb[slot] = ldg_stream_v4(wbase + (size_t)a * ATOM_WORDS);
-        mb[slot][0] = load_meta(p, (a * ATOM_K) / group, nt, gg);
-        if constexpr (G32) mb[slot][1] = load_meta(p, (a * ATOM_K + 32) / group, nt, gg);
-      };
-
+    // 4) prefix sums of x over 32-row halves (the zero correction of bf16)
+    const int n32 = KC / 32;
+    if constexpr (BIAS) {
+      for (int i = tid; i < MR * n32; i += DEC_THREADS) {
+        const int m = i / n32, hh = i - m * n32;
+        float sum = 0.f;
+        if (m < p.M) {
+          const uint4* xr = reinterpret_cast<const uint4*>(xs + (size_t)m * p.x_stride + 32 * hh);
 #pragma unroll
-      for (int i = 0; i < PIPE; ++i)
-        if (i < n_atoms) fetch(i, wa0 + i);
-
-      for (int base = 0; base < n_atoms; base += PIPE) {
+          for (int q = 0; q < 4; ++q) {
+            const uint4 v = xr[q];
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int i = 0; i < PIPE; ++i) {
-          const int ai = base + i;
-          if (ai < n_atoms) {
-            const int a = wa0 + ai;
-            const uint4 w = wb[i];
-            Meta mh[G32 ? 2 : 1];
-            mh[0] = mb[i][0];
-            if constexpr (G32) mh[1] = mb[i][1];
-            if (ai + PIPE < n_atoms) fetch(i, a + PIPE);
+            for (int e = 0; e < 4; ++e)
+              sum += __uint_as_float(wv[e] << 16) + __uint_as_float(wv[e] & 0xFFFF0000u);
+          }
+        }
+        xpre[m * p.xp_stride + hh + 1] = sum;
+      }
+      __syncthreads();
+      for (int m = tid; m < MR; m += DEC_THREADS) {
+        float run = 0.f;
+        xpre[m * p.xp_stride] = 0.f;
+        for (int hh = 1; hh <= n32; ++hh) {
+          run += xpre[m * p.xp_stride + hh];
+          xpre[m * p.xp_stride + hh] = run;
+        }
+      }
+      __syncthreads();
+    }
 
+    // 5) consume the ring
+    hs = 2 * (wa0 - c0);
+    for (int j = 0; j < n_stages; ++j) {
+      const uint32_t slot = it % RING;
+      const uint32_t parity = (it / RING) & 1;
+      bool ready = mbar_try_wait(bar0 + 8 * slot, parity);
+      if (!ready) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!(ready = mbar_try_wait(bar0 + 8 * slot, parity)))
+          if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) break;
+      }
+      if (!ready) {
+        // give up: record it, let the copies in flight land, stop streaming
+        if (lane == 0) atomicExch(&g_device_status, W4_ERR_TIMEOUT);
+        const int in_flight = min(RING, n_stages - j);
+        for (int q = 0; q < in_flight; ++q) {
+          const uint32_t sl = (it + q) % RING;
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(bar0 + 8 * sl, ((it + q) / RING) & 1))
+            if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) break;
+        }
+        alive = false;
+        break;
+      }
+      const uint8_t* stage = ring + slot * (STAGE_ATOMS * ATOM_BYTES);
+      const int a_base = wa0 + j * STAGE_ATOMS;
+      const int cnt = min(STAGE_ATOMS, wa1 - a_base);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int gi = (a * ATOM_K + 32 * h) / group;
+      for (int u = 0; u < STAGE_ATOMS; ++u) {
+        if (u < cnt) {
+          const int a = a_base + u;
+          const uint4 w = *reinterpret_cast<const uint4*>(stage + u * ATOM_BYTES + lane * 16);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (!G64 || h == 0) {
+              const int gi = (a * ATOM_K + 32 * h) >> p.gshift;
               if (gi != cur_g) {
-                if (cur_g >= 0) {
-#pragma unroll
-                  for (int mt = 0; mt < MT; ++mt) {
-                    tot[mt][0] = fmaf(s_lo, acc[mt][0], tot[mt][0]);
-                    tot[mt][1] = fmaf(s_lo, acc[mt][1], tot[mt][1]);
-                    tot[mt][2] = fmaf(s_hi, acc[mt][2], tot[mt][2]);
-                    tot[mt][3] = fmaf(s_hi, acc[mt][3], tot[mt][3]);
-                    acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
-                  }
-                }
+                const int hcur = 2 * (a - c0) + h;
+                if (cur_g >= 0) flush(hs, hcur);
+                hs = hcur;
                 cur_g = gi;
-                const Meta& m = mh[G32 ? h : 0];
-                s_lo = half_bits_to_float<BF16>((uint16_t)(m.s & 0xFFFF));
-                s_hi = half_bits_to_float<BF16>((uint16_t)(m.s >> 16));
-                const uint32_t z0 = (m.z.x >> (4 * gg)) & 0xF;
-                const uint32_t z1 = (m.z.y >> (4 * gg)) & 0xF;
+                const int gl = gi - g_first;
+                s_lo = half_bits_to_float<BF16>(meta_s[gl * 16 + gg]);
+                s_hi = half_bits_to_float<BF16>(meta_s[gl * 16 + gg + 8]);
+                const uint2 zw = meta_z[gl];
+                const uint32_t z0 = (zw.x >> (4 * gg)) & 0xF;
+                const uint32_t z1 = (zw.y >> (4 * gg)) & 0xF;
                 zl = MAGIC | z0 | (z0 << 16);
                 zh = MAGIC | z1 | (z1 << 16);
+                zlf = BIAS ? (float)(128 + z0) : 0.f;
+                zhf = BIAS ? (float)(128 + z1) : 0.f;
               }
-              const uint32_t wlo = h ? w.z : w.x;  // column gg
-              const uint32_t whi = h ? w.w : w.y;  // column gg + 8
-
-              // x fragments for this 32-row block: rows 8t..8t+7 of token row 8mt+gg
-              uint4 xf[MT];
-              const int kl = a * ATOM_K + 32 * h - kx0 + 8 * t;
+            }
+            const uint32_t wlo = h ? w.z : w.x;  // column gg
+            const uint32_t whi = h ? w.w : w.y;  // column gg + 8
+            const int kl = a * ATOM_K + 32 * h - kx0 + 8 * t;
+            uint4 xf[MT];
 #pragma unroll
-              for (int mt = 0; mt < MT; ++mt)
-                xf[mt] = *reinterpret_cast<const uint4*>(xs + (size_t)(8 * mt + gg) * p.x_stride + kl);
-
+            for (int mt = 0; mt < MT; ++mt) {
+              const int row = 8 * mt + gg;
+              xf[mt] = row < p.M ? *reinterpret_cast<const uint4*>(xs + (size_t)row * p.x_stride + kl)
+                                 : make_uint4(0, 0, 0, 0);
+            }
 #pragma unroll
-              for (int step = 0; step < 2; ++step) {
-                const int sh = 8 * step;
-                const uint32_t a0 = sub_x2<BF16>(lop3_and_or(wlo >> sh, 0x000F000Fu, MAGIC), zl);
-                const uint32_t a2 = sub_x2<BF16>(lop3_and_or(wlo >> (sh + 4), 0x000F000Fu, MAGIC), zl);
-                const uint32_t a1 = sub_x2<BF16>(lop3_and_or(whi >> sh, 0x000F000Fu, MAGIC), zh);
-                const uint32_t a3 = sub_x2<BF16>(lop3_and_or(whi >> (sh + 4), 0x000F000Fu, MAGIC), zh);
+            for (int step = 0; step < 2; ++step) {
+              const int sh = 8 * step;
+              uint32_t a0 = lop3_and_or(wlo >> sh, 0x000F000Fu, MAGIC);
+              uint32_t a2 = lop3_and_or(wlo >> (sh + 4), 0x000F000Fu, MAGIC);
+              uint32_t a1 = lop3_and_or(whi >> sh, 0x000F000Fu, MAGIC);
+              uint32_t a3 = lop3_and_or(whi >> (sh + 4), 0x000F000Fu, MAGIC);
+              if constexpr (!BIAS) {
+                a0 = sub_x2<BF16>(a0, zl);
+                a2 = sub_x2<BF16>(a2, zl);
+                a1 = sub_x2<BF16>(a1, zh);
+                a3 = sub_x2<BF16>(a3, zh);
+              }
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                  const uint32_t b0 = step ? xf[mt].z : xf[mt].x;
-                  const uint32_t b1 = step ? xf[mt].w : xf[mt].y;
-                  mma_16816<BF16>(acc[mt], a0, a1, a2, a3, b0, b1);
-                }
+              for (int mt = 0; mt < MT; ++mt) {
+                const uint32_t b0 = step ? xf[mt].z : xf[mt].x;
+                const uint32_t b1 = step ? xf[mt].w : xf[mt].y;
+                mma_16816<BF16>(acc[mt], a0, a1, a2, a3, b0, b1);
               }
             }
           }
         }
       }
+      __syncwarp();
+      if (lane == 0 && j + RING < n_stages) {
+        fence_proxy_async_smem();  // the reads of this slot precede the next copy into it
+        issue(j + RING, slot);     // slot == (it_at_chunk_start + j + RING) % RING
+      }
+      ++it;
     }
-    __syncthreads();  // the next chunk overwrites xs
-  }
-  if (cur_g >= 0) {
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      tot[mt][0] = fmaf(s_lo, acc[mt][0], tot[mt][0]);
-      tot[mt][1] = fmaf(s_lo, acc[mt][1], tot[mt][1]);
-      tot[mt][2] = fmaf(s_hi, acc[mt][2], tot[mt][2]);
-      tot[mt][3] = fmaf(s_hi, acc[mt][3], tot[mt][3]);
-    }
+    // the prefix sums and the scale / zero stage belong to this chunk: close the group
+    if (cur_g >= 0) flush(hs, 2 * (wa1 - c0));
+    cur_g = -1;
+    __syncthreads();  // the next chunk overwrites xs, xpre and the scale / zero stage
   }
 
   // ---- partial tile to shared memory: red[wk][col][m] --------------------------
@@ -259,7 +389,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 2) w4a16_decode_kernel(const Deco
     const int o0 = (int)((long long)srank * total / S);
     const int o1 = (int)((long long)(srank + 1) * total / S);
     for (int o = o0 + tid; o < o1; o += DEC_THREADS) {
-      const int m = o / NCOL, col = o % NCOL;
+      const int m = o / NCOL, col = o - m * NCOL;
       const int n = blockIdx.x * NCOL + col;
       if (n >= p.N) continue;
       float sum = 0.f;
@@ -273,30 +403,25 @@ __global__ void __launch_bounds__(DEC_THREADS, 2) w4a16_decode_kernel(const Deco
   cluster.sync();
 }
 
-template <int MT, bool BF16, bool G32>
+template <int MT, bool BF16, bool G64>
 void* kernel_ptr() {
-  return reinterpret_cast<void*>(&w4a16_decode_kernel<MT, BF16, G32>);
+  return reinterpret_cast<void*>(&w4a16_decode_kernel<MT, BF16, G64>);
 }
 
-void* pick_kernel(int MT, bool bf16, bool g32) {
-#define W4_PICK(mt)                                                                     \
-  if (MT == mt) {                                                                       \
-    if (bf16) return g32 ? kernel_ptr<mt, true, true>() : kernel_ptr<mt, true, false>(); \
-    return g32 ? kernel_ptr<mt, false, true>() : kernel_ptr<mt, false, false>();        \
+template <int MT>
+void* pick_mt(bool bf16, bool g64) {
+  if (bf16) return g64 ? kernel_ptr<MT, true, true>() : kernel_ptr<MT, true, false>();
+  return g64 ? kernel_ptr<MT, false, true>() : kernel_ptr<MT, false, false>();
+}
+
+void* pick_kernel(int MT, bool bf16, bool g64) {
+  switch (MT) {
+    case 1: return pick_mt<1>(bf16, g64);
+    case 2: return pick_mt<2>(bf16, g64);
+    case 4: return pick_mt<4>(bf16, g64);
+    case 8: return pick_mt<8>(bf16, g64);
+    default: return nullptr;
   }
-  W4_PICK(1)
-  W4_PICK(2)
-  W4_PICK(4)
-  W4_PICK(8)
-#undef W4_PICK
-  return nullptr;
-}
-
-// Largest per-CTA K range (rows) whose x slice fits the shared-memory budget.
-int max_rows_per_cta(int MT) {
-  const int budget = 96 * 1024;  // x slice bytes; leaves room for 2 CTAs per SM
-  int rows = budget / (8 * MT * 2);
-  return std::max(ATOM_K, (rows / ATOM_K) * ATOM_K);
 }
 
 // Raise a kernel's dynamic shared-memory limit once per (kernel, device); the
@@ -316,39 +441,71 @@ cudaError_t ensure_smem(void* fn, size_t bytes) {
   return e;
 }
 
+// Rows of x (per token) a CTA stages at a time.
+int max_rows_per_chunk(int M) {
+  const int rows = X_BUDGET / (M * 2);
+  return std::max(ATOM_K, (rows / ATOM_K) * ATOM_K);
+}
+
 struct DecodePlan {
   int WN, S;
+  int chunk_atoms, x_stride, maxg, xp_stride;
+  SmemLayout L;
 };
 
-// Choose warps-along-N and the split-K factor: fill the GPU's CTA slots as
-// evenly as possible while keeping each warp's run long enough to pipeline.
-DecodePlan plan_decode(int N, int K, int MT, int sm_count) {
+// Shared-memory plan of one launch shape.
+DecodePlan shape_plan(int WN, int S, int A, int Mc, int MT, int gshift) {
+  DecodePlan d;
+  d.WN = WN;
+  d.S = S;
+  const int cta_atoms = (A + S - 1) / S;
+  d.chunk_atoms = std::min(cta_atoms, max_rows_per_chunk(Mc) / ATOM_K);
+  d.x_stride = d.chunk_atoms * ATOM_K + 32;  // halves; row stride = 64 mod 128 bytes
+  const int WK = DEC_WARPS / WN;
+  const int warp_atoms = (d.chunk_atoms + WK - 1) / WK;
+  d.maxg = (gshift == 31) ? 1 : (warp_atoms * ATOM_K >> gshift) + 2;
+  d.xp_stride = 2 * d.chunk_atoms + 1;
+  d.L = smem_layout(MT, Mc, d.x_stride, d.maxg, d.xp_stride);
+  return d;
+}
+
+// Choose warps-along-N and the split-K factor: fill the GPU's CTA slots (as
+// many as registers and shared memory allow per SM) as evenly as possible while
+// keeping each warp's run long enough to stream.
+DecodePlan plan_decode(int N, int K, int Mc, int MT, int gshift, const DeviceInfo& info) {
   const int NT = N / 16, A = K / ATOM_K;
-  const int slots = 2 * sm_count;
-  DecodePlan best{8, 1};
+  const int reg_ctas = MT <= 2 ? 3 : 2;
+  DecodePlan best = shape_plan(8, 1, A, Mc, MT, gshift);
   double best_score = -1.0;
   for (int WN = 8; WN >= 1; WN >>= 1) {
     const int WK = DEC_WARPS / WN;
     const int cols = (NT + WN - 1) / WN;
-    for (int S = 1; S <= MAX_SPLIT; ++S) {
-      if (S > A) break;
+    for (int S = 1; S <= MAX_SPLIT && S <= A; ++S) {
+      const double per_warp = (double)A / (S * WK);
+      if (per_warp < 1.0) continue;
+      const DecodePlan d = shape_plan(WN, S, A, Mc, MT, gshift);
+      const int smem_ctas = info.smem_per_sm / (d.L.total + 1024);
+      const int per_sm = std::max(1, std::min(reg_ctas, smem_ctas));
+      const long long slots = (long long)per_sm * info.sm_count;
       const long long ctas = (long long)cols * S;
-      const int per_warp = A / (S * WK);
-      if (per_warp < 1) continue;
       const long long waves = (ctas + slots - 1) / slots;
       double eff = (double)ctas / (double)(waves * slots);
-      // idle warps when the column count does not fill WN
-      eff *= (double)NT / (double)(cols * WN);
-      // short runs cannot keep enough loads in flight
-      const double pipe = std::min(1.0, per_warp / 6.0);
-      const double score = eff * (0.5 + 0.5 * pipe) - 0.002 * S - 0.001 * (8 / WN);
+      eff *= (double)NT / (double)(cols * WN);  // idle warps in the last column block
+      const double stream = std::min(1.0, per_warp / 8.0);  // short runs stream poorly
+      const double score = eff * (0.6 + 0.4 * stream) - 0.004 * S - 0.002 * (8 / WN);
       if (score > best_score) {
         best_score = score;
-        best = {WN, S};
+        best = d;
       }
     }
   }
   return best;
+}
+
+int log2_exact(int v) {
+  int s = 0;
+  while ((1 << s) < v) ++s;
+  return (1 << s) == v ? s : -1;
 }
 
 }  // namespace
@@ -357,19 +514,16 @@ cudaError_t launch_decode(const GemmArgs& a, cudaStream_t stream) {
   DeviceInfo info;
   cudaError_t err = device_info(&info);
   if (err != cudaSuccess) return err;
-  const bool g32 = (a.group % 64) != 0;
-  for (int r0 = 0; r0 < a.M; r0 += 64) {
-    const int Mc = std::min(64, a.M - r0);
+  int gshift = log2_exact(a.group);
+  if (a.group == a.K || gshift < 0) gshift = 31;  // one group over all of K
+  const int A = a.K / ATOM_K;
+  const bool g64 = gshift >= 6;  // groups of 64 or more: one group per atom
+  for (int r0 = 0; r0 < a.M; r0 += DECODE_MAX_M) {
+    const int Mc = std::min(DECODE_MAX_M, a.M - r0);
     const int MT = Mc <= 8 ? 1 : Mc <= 16 ? 2 : Mc <= 32 ? 4 : 8;
-    const DecodePlan plan = plan_decode(a.N, a.K, MT, info.sm_count);
-    const int A = a.K / ATOM_K;
-    const int cta_atoms = (A + plan.S - 1) / plan.S;
-    const int chunk_atoms = std::min(cta_atoms, max_rows_per_cta(MT) / ATOM_K);
-    const int x_stride = chunk_atoms * ATOM_K + 32;  // halves; row stride = 64 mod 128 bytes
-    const size_t smem = (size_t)8 * MT * x_stride * 2 + (size_t)DEC_WARPS * 16 * 8 * MT * 4;
-    void* fn = pick_kernel(MT, a.bf16 != 0, g32);
-    err = ensure_smem(fn, smem);
-    if (err != cudaSuccess) return err;
+    const DecodePlan plan = plan_decode(a.N, a.K, Mc, MT, gshift, info);
+    void* fn = pick_kernel(MT, a.bf16 != 0, g64);
+    if ((err = ensure_smem(fn, plan.L.total)) != cudaSuccess) return err;
 
     DecodeParams p;
     p.x = static_cast<const uint16_t*>(a.x) + (size_t)r0 * a.K;
@@ -381,16 +535,18 @@ cudaError_t launch_decode(const GemmArgs& a, cudaStream_t stream) {
     p.M = Mc;
     p.N = a.N;
     p.K = a.K;
-    p.group = a.group;
+    p.gshift = gshift;
     p.A = A;
     p.WN = plan.WN;
-    p.chunk_atoms = chunk_atoms;
-    p.x_stride = x_stride;
+    p.chunk_atoms = plan.chunk_atoms;
+    p.x_stride = plan.x_stride;
+    p.maxg = plan.maxg;
+    p.xp_stride = plan.xp_stride;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((a.N / 16 + plan.WN - 1) / plan.WN, plan.S, 1);
     cfg.blockDim = dim3(DEC_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = plan.L.total;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -400,8 +556,7 @@ cudaError_t launch_decode(const GemmArgs& a, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     void* args[] = {&p};
-    err = cudaLaunchKernelExC(&cfg, fn, args);
-    if (err != cudaSuccess) return err;
+    if ((err = cudaLaunchKernelExC(&cfg, fn, args)) != cudaSuccess) return err;
   }
   return cudaSuccess;
 }

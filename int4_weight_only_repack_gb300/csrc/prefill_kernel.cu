@@ -1,0 +1,463 @@
+// Large-M (prefill) W4A16 GEMM on the 5th-generation tensor cores (tcgen05).
+//
+// Prefill is bound by tensor-core throughput ("vLLM 学习手册 01. 量化" §1:
+// the prefill phase is compute-bound), so the weight stream is turned into
+// UMMA operands as fast as the tensor cores consume them ("vLLM 学习手册 01.
+// 量化" §5.3: dequantisation fused with the multiply; "vLLM AWQ 4-bit 量化实践"
+// §5.3: W = (b - zeros) * scales):
+//
+//  * Persistent kernel, one CTA per SM, CTA tile 128 (M) x 256 (N), K blocks of
+//    64. Tiles are walked with M fastest so neighbouring CTAs share a weight
+//    column block in L2.
+//  * Warp roles (16 warps): warp 0 issues TMA copies (x tile with the 128-byte
+//    swizzle, the packed weight atoms, scales and zeros) into a 3-stage ring;
+//    warps 8-15 dequantise the packed atoms into the bf16/fp16 B operand,
+//    written directly in the K-major 128-byte-swizzled layout UMMA reads (one
+//    16-byte store per packed word); warp 1 issues the UMMAs from one thread
+//    into a TMEM accumulator; warps 4-7 drain the accumulator (tcgen05.ld),
+//    round to the activation dtype and store y. Warp 2 owns the TMEM
+//    allocation. The accumulator is double-buffered (2 x 256 TMEM columns) so
+//    the epilogue of one tile overlaps the main loop of the next.
+//  * Every wait on an mbarrier is bounded: after one second the CTA raises an
+//    abort flag, records W4_ERR_TIMEOUT in the library's device status word,
+//    lets its copies and UMMAs drain (again bounded), frees TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "sm100_ptx.cuh"
+#include "w4a16_device.cuh"
+#include "w4a16_internal.h"
+
+namespace w4 {
+
+// Non-zero once a kernel of this library gave up on a wait (see w4_device_status).
+__device__ int g_device_status = 0;
+
+namespace {
+
+using namespace sm100;
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 3;
+constexpr int THREADS = 512;
+constexpr int DEQ_THREADS = 256;  // warps 8-15
+constexpr int EPI_THREADS = 128;  // warps 4-7
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int P_BYTES = BN * BK / 2;
+constexpr int S_BYTES = 2 * BN * 2;   // two group rows of scales
+constexpr int Z_BYTES = 2 * BN / 2;   // two group rows of zeros
+constexpr int Z_SLOT = 1024;
+constexpr uint32_t STAGE_TX = A_BYTES + P_BYTES + S_BYTES + Z_BYTES;
+constexpr int TMEM_COLS = 512;        // two 128 x 256 fp32 accumulators
+
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+constexpr int OFF_P = OFF_B + STAGES * B_BYTES;
+constexpr int OFF_S = OFF_P + STAGES * P_BYTES;
+constexpr int OFF_Z = OFF_S + STAGES * S_BYTES;
+constexpr int OFF_BAR = OFF_Z + STAGES * Z_SLOT;
+constexpr int NUM_BARS = 3 * STAGES + 4 + 1;
+constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
+constexpr int SMEM_USED = OFF_MISC + 16;
+constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base to 1024
+
+constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;  // 1 s per wait
+
+struct PrefillParams {
+  CUtensorMap tm_a;  // x [M][K], box 64 x 128, 128-byte swizzle
+  CUtensorMap tm_p;  // TILE words as [N/16][K/64 * 128], box 128 x 16
+  CUtensorMap tm_s;  // scales [G][N], box 256 x 2
+  CUtensorMap tm_z;  // zeros [G][N/8], box 32 x 2
+  uint16_t* y;
+  int M, N, K, group;
+  int m_blocks, num_tiles, k_blocks;
+};
+
+struct Bars {
+  uint32_t base;
+  __device__ uint32_t full(int s) const { return base + 8 * s; }
+  __device__ uint32_t bfull(int s) const { return base + 8 * (STAGES + s); }
+  __device__ uint32_t empty(int s) const { return base + 8 * (2 * STAGES + s); }
+  __device__ uint32_t accfull(int b) const { return base + 8 * (3 * STAGES + b); }
+  __device__ uint32_t accempty(int b) const { return base + 8 * (3 * STAGES + 2 + b); }
+  __device__ uint32_t mmadone() const { return base + 8 * (3 * STAGES + 4); }
+};
+
+// Wait for an mbarrier phase. Returns false when this CTA is aborting: either
+// another role raised the flag, or this wait ran past the limit (then it
+// raises the flag and records the timeout).
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+      *abort_flag = 1;
+      atomicExch(&g_device_status, W4_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Bounded drain wait used on the abort path only.
+__device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) return;
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi, bool bf16) {
+  uint32_t d;
+  if (bf16) {
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  } else {
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  }
+  return d;
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_constant__ PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_addr(smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const Bars bars{sbase + OFF_BAR};
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bars.full(s), 1);
+      mbar_init(bars.bfull(s), DEQ_THREADS);
+      mbar_init(bars.empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bars.accfull(b), 1);
+      mbar_init(bars.accempty(b), EPI_THREADS);
+    }
+    mbar_init(bars.mmadone(), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_addr(tmem_holder), TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&p.tm_a);
+    prefetch_tmap(&p.tm_p);
+    prefetch_tmap(&p.tm_s);
+    prefetch_tmap(&p.tm_z);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const int KB = p.k_blocks;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      int it = 0;
+      int last_armed[STAGES];
+      for (int s = 0; s < STAGES; ++s) last_armed[s] = -1;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        const int m_blk = tile % p.m_blocks, n_blk = tile / p.m_blocks;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!wait_phase(bars.empty(s), ph ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bars.full(s), STAGE_TX);
+          last_armed[s] = it;
+          const int gi = (kb * BK) / p.group;
+          tma_load_2d(sbase + OFF_A + s * A_BYTES, &p.tm_a, bars.full(s), kb * BK, m_blk * BM);
+          tma_load_2d(sbase + OFF_P + s * P_BYTES, &p.tm_p, bars.full(s), kb * 128, n_blk * (BN / 16));
+          tma_load_2d(sbase + OFF_S + s * S_BYTES, &p.tm_s, bars.full(s), n_blk * BN, gi);
+          tma_load_2d(sbase + OFF_Z + s * Z_SLOT, &p.tm_z, bars.full(s), n_blk * (BN / 8), gi);
+        }
+      }
+      if (!ok) {
+        // let the copies already issued land before the CTA can exit
+        for (int s = 0; s < STAGES; ++s)
+          if (last_armed[s] >= 0) drain_phase(bars.full(s), (last_armed[s] / STAGES) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- UMMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC = idesc_f16(BF16 ? 1 : 0, BM, BN);
+      int it = 0, lt = 0;
+      bool ok = true;
+      bool issued = false;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++lt) {
+        const int buf = lt & 1;
+        const uint32_t aph = (lt >> 1) & 1;
+        if (!wait_phase(bars.accempty(buf), aph ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + buf * BN;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!wait_phase(bars.full(s), ph, abort_flag) || !wait_phase(bars.bfull(s), ph, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = smem_desc_k128(sbase + OFF_A + s * A_BYTES);
+          const uint64_t bdesc = smem_desc_k128(sbase + OFF_B + s * B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            // advance 16 elements (32 bytes) along K inside the swizzled rows
+            umma_f16(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb | k) != 0);
+          }
+          issued = true;
+          umma_commit(bars.empty(s));
+        }
+        if (ok) umma_commit(bars.accfull(buf));
+      }
+      if (!ok && issued) {
+        umma_commit(bars.mmadone());
+        drain_phase(bars.mmadone(), 0);
+      }
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ---------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    const int row = quarter * 32 + lane;
+    int lt = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++lt) {
+      const int m_blk = tile % p.m_blocks, n_blk = tile / p.m_blocks;
+      const int buf = lt & 1;
+      const uint32_t aph = (lt >> 1) & 1;
+      if (!wait_phase(bars.accfull(buf), aph, abort_flag)) break;
+      tc_fence_after();
+      const int m = m_blk * BM + row;
+      uint16_t* yrow = p.y + (size_t)m * p.N;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + buf * BN + c0, r);
+        tmem_ld_wait();
+        const int n = n_blk * BN + c0;
+        if (m < p.M) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (n + 8 * i < p.N) {
+              uint4 v;
+              v.x = pack_half2(__uint_as_float(r[8 * i + 0]), __uint_as_float(r[8 * i + 1]), BF16);
+              v.y = pack_half2(__uint_as_float(r[8 * i + 2]), __uint_as_float(r[8 * i + 3]), BF16);
+              v.z = pack_half2(__uint_as_float(r[8 * i + 4]), __uint_as_float(r[8 * i + 5]), BF16);
+              v.w = pack_half2(__uint_as_float(r[8 * i + 6]), __uint_as_float(r[8 * i + 7]), BF16);
+              *reinterpret_cast<uint4*>(yrow + n + 8 * i) = v;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bars.accempty(buf));
+    }
+  } else if (warp >= 8) {
+    // ---------------------------------------------------------------- dequantise
+    constexpr uint32_t MAGIC = Magic<BF16>::pair;
+    const int wd = warp - 8;
+    const int gg = lane >> 2, t = lane & 3;
+    const bool two_groups = p.group < BK;  // group 32: each K half has its own group row
+    int it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        if (!wait_phase(bars.full(s), ph, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint16_t* sS = reinterpret_cast<const uint16_t*>(smem + OFF_S + s * S_BYTES);
+        const uint32_t* sZ = reinterpret_cast<const uint32_t*>(smem + OFF_Z + s * Z_SLOT);
+        const uint8_t* sP = smem + OFF_P + s * P_BYTES;
+        uint8_t* sB = smem + OFF_B + s * B_BYTES;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int at = wd + 8 * r;  // atom (16-column tile) inside the block
+          const uint4 w = *reinterpret_cast<const uint4*>(sP + (at * 128 + 4 * lane) * 4);
+          const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            // odd gg store the other K half first: the 8 lanes of each store
+            // phase then hit 8 distinct 16-byte bank groups
+            const int j = jj ^ ((gg & 1) << 1);
+            const uint32_t word = wv[j];
+            const int n_loc = at * 16 + gg + 8 * (j & 1);
+            const int h = j >> 1;
+            const int grow = two_groups ? h : 0;
+            const uint32_t sb = sS[grow * BN + n_loc];
+            const uint32_t z = (sZ[grow * (BN / 8) + (n_loc >> 3)] >> (4 * (n_loc & 7))) & 0xF;
+            const uint32_t zz = MAGIC | z | (z << 16);
+            const uint32_t ss = sb | (sb << 16);
+            uint4 o;
+            o.x = mul_x2<BF16>(sub_x2<BF16>(lop3_and_or(word, 0x000F000Fu, MAGIC), zz), ss);
+            o.y = mul_x2<BF16>(sub_x2<BF16>(lop3_and_or(word >> 4, 0x000F000Fu, MAGIC), zz), ss);
+            o.z = mul_x2<BF16>(sub_x2<BF16>(lop3_and_or(word >> 8, 0x000F000Fu, MAGIC), zz), ss);
+            o.w = mul_x2<BF16>(sub_x2<BF16>(lop3_and_or(word >> 12, 0x000F000Fu, MAGIC), zz), ss);
+            const int c = 4 * h + t;  // 16-byte chunk along K inside the 128-byte row
+            const int off = (n_loc >> 3) * 1024 + (n_loc & 7) * 128 + ((c ^ (n_loc & 7)) << 4);
+            *reinterpret_cast<uint4*>(sB + off) = o;
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bars.bfull(s));
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ---- act-order: x'[m][j] = x[m][perm[j]] --------------------------------------
+__global__ void __launch_bounds__(256) gather_columns_kernel(const uint16_t* __restrict__ x,
+                                                             const int32_t* __restrict__ perm,
+                                                             uint16_t* __restrict__ xg, int M, int K) {
+  const size_t total = (size_t)M * K;
+  for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < total; i += (size_t)gridDim.x * 256) {
+    const size_t m = i / K;
+    const int j = (int)(i - m * K);
+    xg[i] = x[m * K + perm[j]];
+  }
+}
+
+// ---- host side ------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::mutex mu;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+               uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swz) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t ensure_prefill_smem(void* fn) {
+  static std::mutex mu;
+  static bool done[64][2] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int which = fn == reinterpret_cast<void*>(&w4a16_prefill_kernel<true>) ? 1 : 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 64 && done[dev][which]) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e == cudaSuccess && dev < 64) done[dev][which] = true;
+  return e;
+}
+
+}  // namespace
+
+size_t prefill_workspace_bytes(int M, int K, bool has_perm) {
+  if (!has_perm) return 0;
+  return ((size_t)M * K * 2 + 255) & ~(size_t)255;
+}
+
+bool prefill_supported(int M, int N, int K) {
+  return M > 0 && N % 32 == 0 && K % BK == 0;
+}
+
+cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
+  DeviceInfo info;
+  cudaError_t err = device_info(&info);
+  if (err != cudaSuccess) return err;
+  const void* x = a.x;
+  if (a.perm) {
+    uint16_t* xg = static_cast<uint16_t*>(a.workspace);
+    const size_t total = (size_t)a.M * a.K;
+    const unsigned g = (unsigned)std::min<size_t>((total + 255) / 256, (size_t)info.sm_count * 16);
+    gather_columns_kernel<<<g, 256, 0, stream>>>(static_cast<const uint16_t*>(a.x), a.perm, xg,
+                                                  a.M, a.K);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    x = xg;
+  }
+  PrefillParams p;
+  const int G = a.K / a.group;
+  const CUtensorMapDataType act = a.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  bool ok = encode_2d(&p.tm_a, act, x, a.K, a.M, (uint64_t)a.K * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && encode_2d(&p.tm_p, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.qw, (uint64_t)(a.K / 64) * 128,
+                       a.N / 16, (uint64_t)(a.K / 64) * 512, 128, BN / 16,
+                       CU_TENSOR_MAP_SWIZZLE_NONE);
+  ok = ok && encode_2d(&p.tm_s, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.scales, a.N, G, (uint64_t)a.N * 2,
+                       BN, 2, CU_TENSOR_MAP_SWIZZLE_NONE);
+  ok = ok && encode_2d(&p.tm_z, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.zeros, a.N / 8, G,
+                       (uint64_t)a.N / 2, BN / 8, 2, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (!ok) return cudaErrorInvalidValue;
+  p.y = static_cast<uint16_t*>(a.y);
+  p.M = a.M;
+  p.N = a.N;
+  p.K = a.K;
+  p.group = a.group;
+  p.m_blocks = (a.M + BM - 1) / BM;
+  const int n_blocks = (a.N + BN - 1) / BN;
+  p.num_tiles = p.m_blocks * n_blocks;
+  p.k_blocks = a.K / BK;
+
+  void* fn = a.bf16 ? reinterpret_cast<void*>(&w4a16_prefill_kernel<true>)
+                    : reinterpret_cast<void*>(&w4a16_prefill_kernel<false>);
+  if ((err = ensure_prefill_smem(fn)) != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(std::min(p.num_tiles, info.sm_count), 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
+  void* args[] = {&p};
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+cudaError_t read_device_status(int* out, int clear) {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int));
+  if (e != cudaSuccess) return e;
+  *out = v;
+  if (clear && v != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int));
+  }
+  return e;
+}
+
+}  // namespace w4

@@ -82,6 +82,9 @@ cudaError_t device_info(DeviceInfo* out) {
     if ((e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
                                     dev)) != cudaSuccess)
       return e;
+    if ((e = cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                                    dev)) != cudaSuccess)
+      return e;
     g_info[dev].info = d;
     g_info[dev].valid = true;
   }
@@ -109,6 +112,7 @@ const char* w4_status_string(w4_status s) {
     case W4_ERR_CUDA: return "W4_ERR_CUDA: a CUDA call or kernel launch failed";
     case W4_ERR_WORKSPACE: return "W4_ERR_WORKSPACE: workspace missing or too small";
     case W4_ERR_GIDX: return "W4_ERR_GIDX: g_idx out of range or groups not of equal size";
+    case W4_ERR_TIMEOUT: return "W4_ERR_TIMEOUT: a kernel gave up on a pipeline wait";
     default: return "unknown w4_status";
   }
 }
@@ -201,13 +205,18 @@ w4_status w4_repack_gptq(const int32_t* qweight, const int32_t* qzeros, const vo
 }
 
 size_t w4a16_gemm_workspace_size(int M, int N, int K, int group, int dtype, int has_perm) {
-  (void)M;
-  (void)N;
-  (void)K;
   (void)group;
   (void)dtype;
-  (void)has_perm;
-  return 0;
+  if (M <= DECODE_MAX_M || !prefill_supported(M, N, K)) return 0;
+  return prefill_workspace_bytes(M, K, has_perm != 0);
+}
+
+w4_status w4_device_status(int32_t* status_out, int clear) {
+  if (!status_out) return W4_ERR_NULL;
+  int v = 0;
+  if (read_device_status(&v, clear) != cudaSuccess) return W4_ERR_CUDA;
+  *status_out = v;
+  return W4_OK;
 }
 
 w4_status w4a16_gemm(const void* x, const int32_t* qw, const void* scales, const int32_t* zeros,
@@ -248,6 +257,8 @@ w4_status w4a16_gemm(const void* x, const int32_t* qw, const void* scales, const
   a.bf16 = dtype == W4_BF16;
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
+  if (M > DECODE_MAX_M && prefill_supported(M, N, K))
+    return from_cuda(launch_prefill(a, static_cast<cudaStream_t>(stream)));
   return from_cuda(launch_decode(a, static_cast<cudaStream_t>(stream)));
 }
 

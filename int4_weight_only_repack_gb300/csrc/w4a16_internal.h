@@ -38,13 +38,24 @@ struct GemmArgs {
 };
 
 // Small-M kernel: M rows processed in chunks of up to 64.
+constexpr int DECODE_MAX_M = 64;
 cudaError_t launch_decode(const GemmArgs& a, cudaStream_t s);
+
+// Large-M tcgen05 kernel (M > DECODE_MAX_M, N % 32 == 0). Act-order calls
+// gather x[:, perm] into the workspace first.
+bool prefill_supported(int M, int N, int K);
+size_t prefill_workspace_bytes(int M, int K, bool has_perm);
+cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t s);
+
+// The device status word the kernels raise on a timed-out wait.
+cudaError_t read_device_status(int* out, int clear);
 
 // Device properties cached per device.
 struct DeviceInfo {
   int sm_count;
   int major, minor;
   int max_smem_optin;
+  int smem_per_sm;
 };
 cudaError_t device_info(DeviceInfo* out);
 

@@ -284,3 +284,98 @@ def test_gemm_one_hot_rows_exact(w4):
     y = run_gemm(w4, L, x, parts, len(ks))
     for i, k in enumerate(ks):
         assert np.array_equal(y[i], oracle.round_f64_to_half_bits(W[k], "bf16"))
+
+
+# --------------------------------------------------------------------------- #
+# Large-M (tcgen05) path                                                        #
+# --------------------------------------------------------------------------- #
+def rounded_w_reference(x_bits, L, group, fmt="awq"):
+    """fp64 y with the weight rounded once to the activation dtype (the large-M
+    kernel's B operand): a composition of oracle steps, used for a tight check."""
+    q, z, s = oracle.layer_codes(L.qweight, L.qzeros, L.scales, L.dtype, fmt)
+    K = q.shape[0]
+    W = oracle.dequant(q, z, s, oracle.group_of_rows(K, group, L.g_idx))
+    Wr = oracle.half_bits_to_f64(oracle.round_f64_to_half_bits(W, L.dtype), L.dtype)
+    return oracle.gemm(oracle.half_bits_to_f64(x_bits, L.dtype), Wr)
+
+
+PREFILL_CASES = [
+    # K, N, group, dtype, Ms
+    (256, 256, 128, "bf16", (65, 128, 130)),
+    (512, 288, 64, "fp16", (100, 257)),          # ragged last column block (32 of 256)
+    (1024, 512, 32, "bf16", (192,)),
+    (768, 1024, -1, "fp16", (129,)),
+    (4096, 512, 128, "bf16", (256,)),
+    (256, 4096, 128, "bf16", (2048,)),           # 256 tiles: several per CTA
+]
+
+
+@pytest.mark.parametrize("K,N,group,dtype,Ms", PREFILL_CASES)
+def test_gemm_large_m_vs_oracle(w4, K, N, group, dtype, Ms):
+    g = K if group == -1 else group
+    L = synth.make_custom_layer([111, K, N], K, N, group=g, dtype=dtype)
+    parts = repack_layer_group(w4, L, w4.W4_LAYOUT_TILE, group)
+    for M in Ms:
+        x = synth.make_custom_x([112, K, M], M, K, dtype)
+        y = run_gemm(w4, L, x, parts, M, group=group)
+        yv = oracle.half_bits_to_f64(y, dtype)
+        y_ref = oracle.reference_y(x, L.qweight, L.qzeros, L.scales, g, dtype, "awq")
+        err = oracle.rel_err(yv, y_ref)
+        assert err <= TOL, (M, err)
+        # against x . RN(W): only fp32 accumulation and the final rounding remain
+        y_rw = rounded_w_reference(x, L, g)
+        assert ulp_error(y, y_rw, dtype) <= 1.0, (M, ulp_error(y, y_rw, dtype))
+    assert w4.w4_device_status() == 0
+
+
+@pytest.mark.parametrize("K,N,group,Ms", [(512, 256, 128, (65, 200)), (1024, 320, 64, (96,))])
+def test_gemm_large_m_act_order(w4, K, N, group, Ms):
+    L = synth.make_custom_layer([113, K, N], K, N, group=group, dtype="fp16", fmt="gptq",
+                                act_order=True)
+    parts = repack(w4, L, w4.W4_LAYOUT_TILE)
+    for M in Ms:
+        x = synth.make_custom_x([114, K, M], M, K, "fp16")
+        assert w4.w4a16_gemm_workspace_size(M, N, K, group, "fp16", True) >= M * K * 2
+        y = run_gemm(w4, L, x, parts, M)
+        y_ref = oracle.reference_y(x, L.qweight, L.qzeros, L.scales, group, "fp16", "gptq",
+                                   g_idx=L.g_idx)
+        err = oracle.rel_err(oracle.half_bits_to_f64(y, "fp16"), y_ref)
+        assert err <= TOL, (M, err)
+        y_rw = rounded_w_reference(x, L, group, fmt="gptq")
+        assert ulp_error(y, y_rw, "fp16") <= 1.0
+
+
+def test_gemm_large_m_workspace_checked(w4):
+    import torch
+    K, N, M = 256, 256, 100
+    L = synth.make_custom_layer([115], K, N, group=128, dtype="fp16", fmt="gptq", act_order=True)
+    qw, zeros, scales, perm, _ = repack(w4, L, w4.W4_LAYOUT_TILE)
+    x = half_to_dev(synth.make_custom_x([116], M, K, "fp16"), "fp16")
+    y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    with pytest.raises(w4.W4Error) as e:
+        w4.w4a16_gemm(x, qw, scales, zeros, perm, y, M, N, K, 128, "fp16", None)
+    assert e.value.status == 10  # W4_ERR_WORKSPACE
+    small = torch.empty(M * K * 2 - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(w4.W4Error):
+        w4.w4a16_gemm(x, qw, scales, zeros, perm, y, M, N, K, 128, "fp16", small)
+
+
+def test_gemm_large_m_non_multiple_of_32_columns(w4):
+    """N % 32 != 0 stays on the small-M kernel in chunks of 64 rows."""
+    K, N, M = 256, 272, 150
+    L = synth.make_custom_layer([117], K, N, group=64, dtype="bf16")
+    parts = repack(w4, L, w4.W4_LAYOUT_TILE)
+    x = synth.make_custom_x([118], M, K, "bf16")
+    assert w4.w4a16_gemm_workspace_size(M, N, K, 64, "bf16", False) == 0
+    y = run_gemm(w4, L, x, parts, M)
+    y_ref = oracle.reference_y(x, L.qweight, L.qzeros, L.scales, 64, "bf16", "awq")
+    assert oracle.rel_err(oracle.half_bits_to_f64(y, "bf16"), y_ref) <= TOL
+    assert ulp_error(y, y_ref, "bf16") <= 1.0
+
+
+def test_gemm_large_m_deterministic(w4):
+    K, N, M = 1024, 1024, 512
+    L = synth.make_custom_layer([119], K, N, group=128, dtype="bf16")
+    parts = repack(w4, L, w4.W4_LAYOUT_TILE)
+    x = synth.make_custom_x([120], M, K, "bf16")
+    assert np.array_equal(run_gemm(w4, L, x, parts, M), run_gemm(w4, L, x, parts, M))

@@ -67,7 +67,8 @@ def check_layer(w4, cfg, li):
         assert np.array_equal(layer.perm.cpu().numpy(), perm)
     # repack: sampled atoms, bit-exact
     A, NT = K // 64, N // 16
-    atoms = np.unique(np.concatenate([[0, NT * A - 1], rng.choice(NT * A, 254, replace=False)]))
+    n_pick = min(NT * A, 254)
+    atoms = np.unique(np.concatenate([[0, NT * A - 1], rng.choice(NT * A, n_pick, replace=False)]))
     words = layer.qw.view(-1)
     idx = torch.from_numpy((atoms[:, None] * 128 + np.arange(128)[None, :]).reshape(-1)).to(words.device)
     got = words[idx].cpu().numpy().reshape(len(atoms), 128)
