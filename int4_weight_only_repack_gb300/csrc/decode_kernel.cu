@@ -21,11 +21,14 @@
 //  * The CTA stages its slice of x in shared memory (gathering x[:, perm] for
 //    act-order layers), padded so fragment loads are free of bank conflicts.
 //  * Split-K across the CTAs of a thread-block cluster (up to 8 along K): each
-//    CTA leaves its fp32 partial tile in its own shared memory, and after a
-//    cluster barrier every CTA sums a slice of the outputs over all peers
-//    through distributed shared memory, in a fixed order (deterministic, no
-//    global workspace, no atomics: "vLLM AWQ 4-bit 量化实践" §5.3 names
-//    split-K for the fused kernel).
+//    CTA pushes its fp32 partial sums into the shared memory of the CTA that
+//    owns those output columns (distributed shared memory stores), one
+//    cluster barrier later every owner sums its slice over the peers in a
+//    fixed order (deterministic, no global workspace, no atomics:
+//    "vLLM AWQ 4-bit 量化实践" §5.3 names split-K for the fused kernel).
+//  * Launch order inside a CTA: the small loads that gate the first MMA (x,
+//    scales, zeros) are issued before the weight stream, so they are not
+//    queued behind it.
 //  * Waits on the ring's mbarriers are bounded (one second); on a timeout the
 //    warp records W4_ERR_TIMEOUT in the device status word, lets its copies in
 //    flight land (bounded again) and stops computing.
@@ -55,9 +58,9 @@ constexpr int ATOM_K = 64;
 constexpr int ATOM_WORDS = 128;
 constexpr int ATOM_BYTES = 512;
 constexpr int MAX_SPLIT = 8;
-constexpr int RING = 4;              // stages per warp
-constexpr int STAGE_ATOMS = 2;       // atoms per stage (1 KB)
-constexpr int X_BUDGET = 32 * 1024;  // bytes of staged x per CTA
+constexpr int STAGE_ATOMS = 4;       // atoms per ring stage (2 KB)
+constexpr int MAX_RING = 8;          // stages per warp, upper bound
+constexpr int X_BUDGET = 48 * 1024;  // bytes of staged x per CTA
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
 
 struct DecodeParams {
@@ -71,27 +74,34 @@ struct DecodeParams {
   int gshift;              // group = 1 << gshift; 31 = one group over all of K
   int A;                   // K / 64
   int WN;                  // warps along N per CTA (WK = 8 / WN along K)
+  int ring;                // stages per warp
   int chunk_atoms;         // atoms of x staged in shared memory at a time
   int x_stride;            // shared x row stride in halves
   int maxg;                // group slots of the per-warp scale / zero stage
   int xp_stride;           // row length of the x prefix sums (2 * chunk_atoms + 1)
+  int slice;               // output columns owned by each CTA of a cluster
 };
 
 struct SmemLayout {
-  int xs, ring, bars, meta_s, meta_z, xpre, red, total;
+  int xs, ring, bars, meta_s, meta_z, xpre, red, recv, total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int MT, int m_rows, int x_stride, int maxg,
-                                                  int xp_stride) {
+// x keeps M token rows plus one row of zeros (read by the MMA lanes whose
+// token row is beyond M).
+__host__ __device__ inline SmemLayout smem_layout(int MT, int m_rows, int x_stride, int ring,
+                                                  int maxg, int xp_stride, int WN, int S,
+                                                  int slice) {
   SmemLayout L;
   L.xs = 0;
-  L.ring = ((m_rows * x_stride * 2) + 1023) & ~1023;
-  L.bars = L.ring + DEC_WARPS * RING * STAGE_ATOMS * ATOM_BYTES;
-  L.meta_s = L.bars + DEC_WARPS * RING * 8;
+  L.ring = (((m_rows + 1) * x_stride * 2) + 1023) & ~1023;
+  L.bars = L.ring + DEC_WARPS * ring * STAGE_ATOMS * ATOM_BYTES;
+  L.meta_s = (L.bars + (DEC_WARPS * ring + 1) * 8 + 15) & ~15;
   L.meta_z = L.meta_s + DEC_WARPS * maxg * 32;
   L.xpre = (L.meta_z + DEC_WARPS * maxg * 8 + 15) & ~15;
   L.red = (L.xpre + 8 * MT * xp_stride * 4 + 15) & ~15;
-  L.total = L.red + DEC_WARPS * 16 * 8 * MT * 4;
+  const int red_bytes = WN < DEC_WARPS ? DEC_WARPS * 16 * 8 * MT * 4 : 0;
+  L.recv = (L.red + red_bytes + 15) & ~15;
+  L.total = L.recv + S * slice * 8 * MT * 4;
   return L;
 }
 
@@ -104,6 +114,33 @@ __device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// Bounded wait; false when the limit ran out (the caller records the timeout).
+__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) return false;
+  return true;
+}
+
+// D += A * B for one m16n8k16 tile, fp32 accumulate (non-volatile: the
+// compiler may schedule it freely; its outputs keep it alive).
+template <bool BF16>
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  if constexpr (BF16) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+
 // MT: token tiles of 8 (M <= 8 * MT). G64: every 64-row atom lies in one group.
 // With bf16 the MMA consumes the codes as 128 + q (exact in bf16) and each
 // group's partial sum is corrected by (128 + z) * sum(x) before scaling; with
@@ -112,6 +149,7 @@ template <int MT, bool BF16, bool G64>
 __global__ void __launch_bounds__(DEC_THREADS, MT <= 2 ? 3 : 2) w4a16_decode_kernel(const DecodeParams p) {
   constexpr uint32_t MAGIC = Magic<BF16>::pair;
   constexpr bool BIAS = BF16;
+  constexpr int SLOT = STAGE_ATOMS * ATOM_BYTES;
   extern __shared__ __align__(1024) uint8_t smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -120,17 +158,21 @@ __global__ void __launch_bounds__(DEC_THREADS, MT <= 2 ? 3 : 2) w4a16_decode_ker
   const int srank = blockIdx.y;     // rank inside the cluster
   const int WN = p.WN, WK = DEC_WARPS / WN;
   const int MR = 8 * MT;
-  const SmemLayout L = smem_layout(MT, p.M, p.x_stride, p.maxg, p.xp_stride);
+  const int RINGN = p.ring;
+  const SmemLayout L = smem_layout(MT, p.M, p.x_stride, RINGN, p.maxg, p.xp_stride, WN, S, p.slice);
 
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem + L.xs);
-  uint8_t* ring = smem + L.ring + warp * (RING * STAGE_ATOMS * ATOM_BYTES);
+  uint8_t* ring = smem + L.ring + warp * (RINGN * SLOT);
   const uint32_t ring_s = smem_addr(ring);
-  const uint32_t bar0 = smem_addr(smem + L.bars + warp * RING * 8);
+  const uint32_t bar0 = smem_addr(smem + L.bars + warp * RINGN * 8);
+  const uint32_t xbar = smem_addr(smem + L.bars + DEC_WARPS * RINGN * 8);
   uint16_t* meta_s = reinterpret_cast<uint16_t*>(smem + L.meta_s) + warp * p.maxg * 16;
   uint2* meta_z = reinterpret_cast<uint2*>(smem + L.meta_z) + warp * p.maxg;
   float* xpre = reinterpret_cast<float*>(smem + L.xpre);
   float* red = reinterpret_cast<float*>(smem + L.red);
+  float* recv = reinterpret_cast<float*>(smem + L.recv);
   const int NCOL = 16 * WN;
+  const uint32_t gmask = p.gshift >= 31 ? 0x7FFFFFFFu : ((1u << p.gshift) - 1u);
 
   // CTA K range in atoms
   const int ka0 = (int)((long long)srank * p.A / S);
@@ -140,23 +182,28 @@ __global__ void __launch_bounds__(DEC_THREADS, MT <= 2 ? 3 : 2) w4a16_decode_ker
   const int nt = blockIdx.x * WN + wn;
   const bool has_cols = nt < p.N / 16;
   const uint32_t* wsrc = p.qw + (size_t)nt * p.A * ATOM_WORDS;  // this tile's atom run
+  uint16_t* xzero = xs + (size_t)p.M * p.x_stride;              // the zero row
 
   if (lane == 0) {
-    for (int s = 0; s < RING; ++s) mbar_init(bar0 + 8 * s, 1);
+    for (int s = 0; s < RINGN; ++s) mbar_init(bar0 + 8 * s, 1);
+    if (warp == 0) mbar_init(xbar, 1);
     fence_mbar_init();
   }
-  __syncwarp();
+  for (int i = tid; i < p.x_stride / 8; i += DEC_THREADS)
+    reinterpret_cast<uint4*>(xzero)[i] = make_uint4(0, 0, 0, 0);
+  __syncthreads();
 
   float acc[MT][4], tot[MT][4];
 #pragma unroll
   for (int i = 0; i < MT; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = tot[i][j] = 0.f;
-  int cur_g = -1;       // group being accumulated in acc (-1: none)
-  int hs = 0;           // chunk-relative half-atom index where it started
+  int hs = 0;           // chunk-relative half-atom index where the open group started
+  int g_first = 0;      // first group of this warp's run in the chunk
   float s_lo = 0.f, s_hi = 0.f, zlf = 0.f, zhf = 0.f;
   uint32_t zl = 0, zh = 0;
   uint32_t it = 0;      // stages consumed by this warp (ring position and phase)
+  uint32_t xphase = 0;  // phase of the x barrier
   bool alive = true;    // false once a wait gave up
 
   // tot += s * (acc - (MAGIC + z) * sum of x over halves [h0, h1)); acc = 0
@@ -176,6 +223,19 @@ __global__ void __launch_bounds__(DEC_THREADS, MT <= 2 ? 3 : 2) w4a16_decode_ker
       acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
     }
   };
+  // scale / zero registers for group gi (staged in shared memory)
+  auto open_group = [&](int gi) {
+    const int gl = gi - g_first;
+    s_lo = half_bits_to_float<BF16>(meta_s[gl * 16 + gg]);
+    s_hi = half_bits_to_float<BF16>(meta_s[gl * 16 + gg + 8]);
+    const uint2 zw = meta_z[gl];
+    const uint32_t z0 = (zw.x >> (4 * gg)) & 0xF;
+    const uint32_t z1 = (zw.y >> (4 * gg)) & 0xF;
+    zl = MAGIC | z0 | (z0 << 16);
+    zh = MAGIC | z1 | (z1 << 16);
+    zlf = BIAS ? (float)(128 + z0) : 0.f;
+    zhf = BIAS ? (float)(128 + z1) : 0.f;
+  };
 
   for (int c0 = ka0; c0 < ka1; c0 += p.chunk_atoms) {
     const int c1 = min(ka1, c0 + p.chunk_atoms);
@@ -185,222 +245,256 @@ __global__ void __launch_bounds__(DEC_THREADS, MT <= 2 ? 3 : 2) w4a16_decode_ker
     const int wa1 = c0 + (int)((long long)(wk + 1) * (c1 - c0) / WK);
     const int n_atoms = (has_cols && alive) ? wa1 - wa0 : 0;
     const int n_stages = (n_atoms + STAGE_ATOMS - 1) / STAGE_ATOMS;
+    const bool x_async = p.perm == nullptr;
 
-    // Stage j of this chunk goes to ring slot (it + j) % RING, where `it` is
+    // Stage j of this chunk goes to ring slot (it + j) % RINGN, where `it` is
     // the warp's consumed-stage count when the chunk starts.
     auto issue = [&](int j, uint32_t slot) {
       const int a = wa0 + j * STAGE_ATOMS;
       const uint32_t bytes = (uint32_t)min(STAGE_ATOMS, wa1 - a) * ATOM_BYTES;
       mbar_arrive_expect_tx(bar0 + 8 * slot, bytes);
-      bulk_copy(ring_s + slot * (STAGE_ATOMS * ATOM_BYTES), wsrc + (size_t)a * ATOM_WORDS, bytes,
-                bar0 + 8 * slot);
+      bulk_copy(ring_s + slot * SLOT, wsrc + (size_t)a * ATOM_WORDS, bytes, bar0 + 8 * slot);
     };
 
-    // 1) start the weight stream first: it has the longest latency
+    // 1) the loads that gate the first MMA go first: x, then scales / zeros
+    if (x_async && tid == 0) {
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(xbar, (uint32_t)(p.M * KC * 2));
+      for (int m = 0; m < p.M; ++m)
+        bulk_copy(smem_addr(xs + (size_t)m * p.x_stride), p.x + (size_t)m * p.K + kx0,
+                  (uint32_t)(KC * 2), xbar);
+    }
+    g_first = (wa0 * ATOM_K) >> p.gshift;
+    const int ng = n_atoms > 0 ? ((wa1 * ATOM_K - 1) >> p.gshift) - g_first + 1 : 0;
+    uint4 ms0 = make_uint4(0, 0, 0, 0), ms1 = ms0;
+    uint2 mz = make_uint2(0, 0);
+    if (lane < ng) {
+      const int gi = g_first + lane;
+      const uint4* sp = reinterpret_cast<const uint4*>(p.scales + (size_t)gi * p.N + nt * 16);
+      ms0 = __ldg(sp);
+      ms1 = __ldg(sp + 1);
+      mz = __ldg(reinterpret_cast<const uint2*>(p.zeros + (size_t)gi * (p.N / 8) + nt * 2));
+    }
+    // 2) then the weight stream
     if (lane == 0 && n_stages > 0) {
       fence_proxy_async_smem();  // earlier reads of the ring precede these copies
-      for (int j = 0; j < min(RING, n_stages); ++j) issue(j, (it + j) % RING);
+      for (int j = 0; j < min(RINGN, n_stages); ++j) issue(j, (it + j) % RINGN);
     }
-
-    // 2) stage x[:M, kx0:kx0+KC] (gathered through perm)
-    {
+    // 3) scales / zeros to shared memory (groups beyond 32 per warp: direct)
+    if (lane < ng) {
+      uint4* sd = reinterpret_cast<uint4*>(meta_s + lane * 16);
+      sd[0] = ms0;
+      sd[1] = ms1;
+      meta_z[lane] = mz;
+    }
+    for (int gl = lane + 32; gl < ng; gl += 32) {
+      const int gi = g_first + gl;
+      const uint4* sp = reinterpret_cast<const uint4*>(p.scales + (size_t)gi * p.N + nt * 16);
+      uint4* sd = reinterpret_cast<uint4*>(meta_s + gl * 16);
+      sd[0] = __ldg(sp);
+      sd[1] = __ldg(sp + 1);
+      meta_z[gl] = __ldg(reinterpret_cast<const uint2*>(p.zeros + (size_t)gi * (p.N / 8) + nt * 2));
+    }
+    if (!x_async) {
+      // act-order: gather x[:, perm] with plain loads
       const int chunks = KC / 8;
       for (int i = tid; i < p.M * chunks; i += DEC_THREADS) {
         const int m = i / chunks, c = i - m * chunks;
         const uint16_t* xr = p.x + (size_t)m * p.K;
-        uint4 v;
-        if (p.perm == nullptr) {
-          v = __ldg(reinterpret_cast<const uint4*>(xr + kx0 + 8 * c));
-        } else {
-          uint16_t h[8];
+        uint16_t h[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) h[e] = __ldg(xr + __ldg(p.perm + kx0 + 8 * c + e));
-          v.x = h[0] | ((uint32_t)h[1] << 16);
-          v.y = h[2] | ((uint32_t)h[3] << 16);
-          v.z = h[4] | ((uint32_t)h[5] << 16);
-          v.w = h[6] | ((uint32_t)h[7] << 16);
-        }
+        for (int e = 0; e < 8; ++e) h[e] = __ldg(xr + __ldg(p.perm + kx0 + 8 * c + e));
+        uint4 v;
+        v.x = h[0] | ((uint32_t)h[1] << 16);
+        v.y = h[2] | ((uint32_t)h[3] << 16);
+        v.z = h[4] | ((uint32_t)h[5] << 16);
+        v.w = h[6] | ((uint32_t)h[7] << 16);
         *reinterpret_cast<uint4*>(xs + (size_t)m * p.x_stride + 8 * c) = v;
       }
-    }
-
-    // 3) this warp's scales and zeros for the groups its atoms touch
-    const int g_first = (wa0 * ATOM_K) >> p.gshift;
-    if (n_atoms > 0) {
-      const int g_last = (wa1 * ATOM_K - 1) >> p.gshift;
-      for (int gl = lane; gl <= g_last - g_first; gl += 32) {
-        const int gi = g_first + gl;
-        const uint4* sp = reinterpret_cast<const uint4*>(p.scales + (size_t)gi * p.N + nt * 16);
-        uint4* sd = reinterpret_cast<uint4*>(meta_s + gl * 16);
-        sd[0] = __ldg(sp);
-        sd[1] = __ldg(sp + 1);
-        meta_z[gl] = __ldg(reinterpret_cast<const uint2*>(p.zeros + (size_t)gi * (p.N / 8) + nt * 2));
+      __syncthreads();
+    } else {
+      if (!bounded_wait(xbar, xphase & 1)) {
+        if (tid == 0) atomicExch(&g_device_status, W4_ERR_TIMEOUT);
+        alive = false;
       }
+      ++xphase;
     }
-    __syncthreads();
 
-    // 4) prefix sums of x over 32-row halves (the zero correction of bf16)
+    // 4) prefix sums of x over 32-row halves (bf16 zero correction), one token
+    //    row per warp at a time, lanes over halves
     const int n32 = KC / 32;
     if constexpr (BIAS) {
-      for (int i = tid; i < MR * n32; i += DEC_THREADS) {
-        const int m = i / n32, hh = i - m * n32;
-        float sum = 0.f;
-        if (m < p.M) {
-          const uint4* xr = reinterpret_cast<const uint4*>(xs + (size_t)m * p.x_stride + 32 * hh);
+      for (int m = warp; m < MR; m += DEC_WARPS) {
+        float* xp = xpre + m * p.xp_stride;
+        float carry = 0.f;
+        if (lane == 0) xp[0] = 0.f;
+        for (int h0 = 0; h0 < n32; h0 += 32) {
+          const int hh = h0 + lane;
+          float sum = 0.f;
+          if (m < p.M && hh < n32) {
+            const uint4* xr = reinterpret_cast<const uint4*>(xs + (size_t)m * p.x_stride + 32 * hh);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint4 v = xr[q];
-            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+            for (int q = 0; q < 4; ++q) {
+              const uint4 v = xr[q];
+              const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              sum += __uint_as_float(wv[e] << 16) + __uint_as_float(wv[e] & 0xFFFF0000u);
+              for (int e = 0; e < 4; ++e)
+                sum += __uint_as_float(wv[e] << 16) + __uint_as_float(wv[e] & 0xFFFF0000u);
+            }
           }
-        }
-        xpre[m * p.xp_stride + hh + 1] = sum;
-      }
-      __syncthreads();
-      for (int m = tid; m < MR; m += DEC_THREADS) {
-        float run = 0.f;
-        xpre[m * p.xp_stride] = 0.f;
-        for (int hh = 1; hh <= n32; ++hh) {
-          run += xpre[m * p.xp_stride + hh];
-          xpre[m * p.xp_stride + hh] = run;
+#pragma unroll
+          for (int d = 1; d < 32; d <<= 1) {
+            const float v = __shfl_up_sync(0xFFFFFFFFu, sum, d);
+            if (lane >= d) sum += v;
+          }
+          if (hh < n32) xp[hh + 1] = carry + sum;
+          carry += __shfl_sync(0xFFFFFFFFu, sum, 31);
         }
       }
-      __syncthreads();
     }
+    __syncthreads();  // x prefix sums and every warp's scale / zero stage are ready
 
     // 5) consume the ring
+    const uint16_t* xrow[MT];  // this lane's token row (or the zero row), column 8t - kx0
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      const int row = 8 * mt + gg;
+      xrow[mt] = (row < p.M ? xs + (size_t)row * p.x_stride : xzero) + 8 * t - kx0;
+    }
     hs = 2 * (wa0 - c0);
-    for (int j = 0; j < n_stages; ++j) {
-      const uint32_t slot = it % RING;
-      const uint32_t parity = (it / RING) & 1;
-      bool ready = mbar_try_wait(bar0 + 8 * slot, parity);
-      if (!ready) {
-        const uint64_t t0 = globaltimer_ns();
-        while (!(ready = mbar_try_wait(bar0 + 8 * slot, parity)))
-          if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) break;
+    if (n_atoms > 0) open_group((wa0 * ATOM_K) >> p.gshift);
+
+    auto atom = [&](int a, const uint4 w) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (!G64 || h == 0) {
+          const uint32_t kabs = (uint32_t)(a * ATOM_K + 32 * h);
+          if ((kabs & gmask) == 0) {  // a group starts here
+            const int hcur = 2 * (a - c0) + h;
+            flush(hs, hcur);
+            hs = hcur;
+            open_group((int)(kabs >> p.gshift));
+          }
+        }
+        const uint32_t wlo = h ? w.z : w.x;  // column gg
+        const uint32_t whi = h ? w.w : w.y;  // column gg + 8
+        uint4 xf[MT];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+          xf[mt] = *reinterpret_cast<const uint4*>(xrow[mt] + a * ATOM_K + 32 * h);
+#pragma unroll
+        for (int step = 0; step < 2; ++step) {
+          const int sh = 8 * step;
+          uint32_t a0 = lop3_and_or(wlo >> sh, 0x000F000Fu, MAGIC);
+          uint32_t a2 = lop3_and_or(wlo >> (sh + 4), 0x000F000Fu, MAGIC);
+          uint32_t a1 = lop3_and_or(whi >> sh, 0x000F000Fu, MAGIC);
+          uint32_t a3 = lop3_and_or(whi >> (sh + 4), 0x000F000Fu, MAGIC);
+          if constexpr (!BIAS) {
+            a0 = sub_x2<BF16>(a0, zl);
+            a2 = sub_x2<BF16>(a2, zl);
+            a1 = sub_x2<BF16>(a1, zh);
+            a3 = sub_x2<BF16>(a3, zh);
+          }
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            const uint32_t b0 = step ? xf[mt].z : xf[mt].x;
+            const uint32_t b1 = step ? xf[mt].w : xf[mt].y;
+            mma16816<BF16>(acc[mt], a0, a1, a2, a3, b0, b1);
+          }
+        }
       }
-      if (!ready) {
+    };
+
+    for (int j = 0; j < n_stages; ++j) {
+      const uint32_t slot = it % RINGN;
+      if (!bounded_wait(bar0 + 8 * slot, (it / RINGN) & 1)) {
         // give up: record it, let the copies in flight land, stop streaming
         if (lane == 0) atomicExch(&g_device_status, W4_ERR_TIMEOUT);
-        const int in_flight = min(RING, n_stages - j);
-        for (int q = 0; q < in_flight; ++q) {
-          const uint32_t sl = (it + q) % RING;
-          const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(bar0 + 8 * sl, ((it + q) / RING) & 1))
-            if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) break;
-        }
+        const int in_flight = min(RINGN, n_stages - j);
+        for (int q = 0; q < in_flight; ++q)
+          bounded_wait(bar0 + 8 * ((it + q) % RINGN), ((it + q) / RINGN) & 1);
         alive = false;
         break;
       }
-      const uint8_t* stage = ring + slot * (STAGE_ATOMS * ATOM_BYTES);
+      const uint8_t* stage = ring + slot * SLOT + lane * 16;
       const int a_base = wa0 + j * STAGE_ATOMS;
-      const int cnt = min(STAGE_ATOMS, wa1 - a_base);
+      if (a_base + STAGE_ATOMS <= wa1) {
+        uint4 w[STAGE_ATOMS];
 #pragma unroll
-      for (int u = 0; u < STAGE_ATOMS; ++u) {
-        if (u < cnt) {
-          const int a = a_base + u;
-          const uint4 w = *reinterpret_cast<const uint4*>(stage + u * ATOM_BYTES + lane * 16);
+        for (int u = 0; u < STAGE_ATOMS; ++u) w[u] = *reinterpret_cast<const uint4*>(stage + u * ATOM_BYTES);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            if (!G64 || h == 0) {
-              const int gi = (a * ATOM_K + 32 * h) >> p.gshift;
-              if (gi != cur_g) {
-                const int hcur = 2 * (a - c0) + h;
-                if (cur_g >= 0) flush(hs, hcur);
-                hs = hcur;
-                cur_g = gi;
-                const int gl = gi - g_first;
-                s_lo = half_bits_to_float<BF16>(meta_s[gl * 16 + gg]);
-                s_hi = half_bits_to_float<BF16>(meta_s[gl * 16 + gg + 8]);
-                const uint2 zw = meta_z[gl];
-                const uint32_t z0 = (zw.x >> (4 * gg)) & 0xF;
-                const uint32_t z1 = (zw.y >> (4 * gg)) & 0xF;
-                zl = MAGIC | z0 | (z0 << 16);
-                zh = MAGIC | z1 | (z1 << 16);
-                zlf = BIAS ? (float)(128 + z0) : 0.f;
-                zhf = BIAS ? (float)(128 + z1) : 0.f;
-              }
-            }
-            const uint32_t wlo = h ? w.z : w.x;  // column gg
-            const uint32_t whi = h ? w.w : w.y;  // column gg + 8
-            const int kl = a * ATOM_K + 32 * h - kx0 + 8 * t;
-            uint4 xf[MT];
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-              const int row = 8 * mt + gg;
-              xf[mt] = row < p.M ? *reinterpret_cast<const uint4*>(xs + (size_t)row * p.x_stride + kl)
-                                 : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int step = 0; step < 2; ++step) {
-              const int sh = 8 * step;
-              uint32_t a0 = lop3_and_or(wlo >> sh, 0x000F000Fu, MAGIC);
-              uint32_t a2 = lop3_and_or(wlo >> (sh + 4), 0x000F000Fu, MAGIC);
-              uint32_t a1 = lop3_and_or(whi >> sh, 0x000F000Fu, MAGIC);
-              uint32_t a3 = lop3_and_or(whi >> (sh + 4), 0x000F000Fu, MAGIC);
-              if constexpr (!BIAS) {
-                a0 = sub_x2<BF16>(a0, zl);
-                a2 = sub_x2<BF16>(a2, zl);
-                a1 = sub_x2<BF16>(a1, zh);
-                a3 = sub_x2<BF16>(a3, zh);
-              }
-#pragma unroll
-              for (int mt = 0; mt < MT; ++mt) {
-                const uint32_t b0 = step ? xf[mt].z : xf[mt].x;
-                const uint32_t b1 = step ? xf[mt].w : xf[mt].y;
-                mma_16816<BF16>(acc[mt], a0, a1, a2, a3, b0, b1);
-              }
-            }
-          }
-        }
+        for (int u = 0; u < STAGE_ATOMS; ++u) atom(a_base + u, w[u]);
+      } else {
+        for (int u = 0; u < wa1 - a_base; ++u)
+          atom(a_base + u, *reinterpret_cast<const uint4*>(stage + u * ATOM_BYTES));
       }
       __syncwarp();
-      if (lane == 0 && j + RING < n_stages) {
+      if (lane == 0 && j + RINGN < n_stages) {
         fence_proxy_async_smem();  // the reads of this slot precede the next copy into it
-        issue(j + RING, slot);     // slot == (it_at_chunk_start + j + RING) % RING
+        issue(j + RINGN, slot);    // slot == (it_at_chunk_start + j + RINGN) % RINGN
       }
       ++it;
     }
     // the prefix sums and the scale / zero stage belong to this chunk: close the group
-    if (cur_g >= 0) flush(hs, 2 * (wa1 - c0));
-    cur_g = -1;
+    if (n_atoms > 0) flush(hs, 2 * (wa1 - c0));
     __syncthreads();  // the next chunk overwrites xs, xpre and the scale / zero stage
   }
 
-  // ---- partial tile to shared memory: red[wk][col][m] --------------------------
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
-    const int m0 = 8 * mt + 2 * t;
-    float* r0 = red + ((size_t)wk * NCOL + wn * 16 + gg) * MR;
-    float* r1 = red + ((size_t)wk * NCOL + wn * 16 + gg + 8) * MR;
-    r0[m0] = tot[mt][0];
-    r0[m0 + 1] = tot[mt][1];
-    r1[m0] = tot[mt][2];
-    r1[m0 + 1] = tot[mt][3];
-  }
-
-  // ---- cluster reduction over the S CTAs that share this column block ----------
+  // ---- split-K: push partial sums to the CTA that owns each output column -------
   cg::cluster_group cluster = cg::this_cluster();
-  cluster.sync();
-  {
-    const int total = p.M * NCOL;
-    const int o0 = (int)((long long)srank * total / S);
-    const int o1 = (int)((long long)(srank + 1) * total / S);
-    for (int o = o0 + tid; o < o1; o += DEC_THREADS) {
-      const int m = o / NCOL, col = o - m * NCOL;
-      const int n = blockIdx.x * NCOL + col;
-      if (n >= p.N) continue;
-      float sum = 0.f;
-      for (int r = 0; r < S; ++r) {
-        const float* peer = cluster.map_shared_rank(red, r);
-        for (int q = 0; q < WK; ++q) sum += peer[((size_t)q * NCOL + col) * MR + m];
+  const int SL = p.slice;
+  auto push = [&](int col, int m, float v) {
+    const int owner = col / SL;
+    float* dst = cluster.map_shared_rank(recv, owner);
+    dst[((size_t)srank * SL + (col - owner * SL)) * MR + m] = v;
+  };
+  if (WK == 1) {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      const int m0 = 8 * mt + 2 * t;
+      const int ca = wn * 16 + gg, cb = ca + 8;
+      if (m0 < p.M) {
+        push(ca, m0, tot[mt][0]);
+        push(cb, m0, tot[mt][2]);
       }
-      p.y[(size_t)m * p.N + n] = float_to_half_bits<BF16>(sum);
+      if (m0 + 1 < p.M) {
+        push(ca, m0 + 1, tot[mt][1]);
+        push(cb, m0 + 1, tot[mt][3]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      const int m0 = 8 * mt + 2 * t;
+      float* r0 = red + ((size_t)wk * NCOL + wn * 16 + gg) * MR;
+      float* r1 = red + ((size_t)wk * NCOL + wn * 16 + gg + 8) * MR;
+      r0[m0] = tot[mt][0];
+      r0[m0 + 1] = tot[mt][1];
+      r1[m0] = tot[mt][2];
+      r1[m0 + 1] = tot[mt][3];
+    }
+    __syncthreads();
+    for (int o = tid; o < NCOL * p.M; o += DEC_THREADS) {
+      const int col = o / p.M, m = o - col * p.M;
+      float v = 0.f;
+      for (int q = 0; q < WK; ++q) v += red[((size_t)q * NCOL + col) * MR + m];
+      push(col, m, v);
     }
   }
   cluster.sync();
+  {
+    const int c_lo = srank * SL;
+    const int c_hi = min(NCOL, c_lo + SL);
+    const int width = c_hi - c_lo;
+    for (int o = tid; o < width * p.M; o += DEC_THREADS) {
+      const int m = o / width, cl = o - m * width;
+      const int n = blockIdx.x * NCOL + c_lo + cl;
+      if (n >= p.N) continue;
+      float sum = 0.f;
+      for (int r = 0; r < S; ++r) sum += recv[((size_t)r * SL + cl) * MR + m];
+      p.y[(size_t)m * p.N + n] = float_to_half_bits<BF16>(sum);
+    }
+  }
 }
 
 template <int MT, bool BF16, bool G64>
@@ -449,15 +543,16 @@ int max_rows_per_chunk(int M) {
 
 struct DecodePlan {
   int WN, S;
-  int chunk_atoms, x_stride, maxg, xp_stride;
+  int ring, chunk_atoms, x_stride, maxg, xp_stride, slice;
   SmemLayout L;
 };
 
 // Shared-memory plan of one launch shape.
-DecodePlan shape_plan(int WN, int S, int A, int Mc, int MT, int gshift) {
+DecodePlan shape_plan(int WN, int S, int A, int Mc, int MT, int gshift, int ring) {
   DecodePlan d;
   d.WN = WN;
   d.S = S;
+  d.ring = ring;
   const int cta_atoms = (A + S - 1) / S;
   d.chunk_atoms = std::min(cta_atoms, max_rows_per_chunk(Mc) / ATOM_K);
   d.x_stride = d.chunk_atoms * ATOM_K + 32;  // halves; row stride = 64 mod 128 bytes
@@ -465,36 +560,59 @@ DecodePlan shape_plan(int WN, int S, int A, int Mc, int MT, int gshift) {
   const int warp_atoms = (d.chunk_atoms + WK - 1) / WK;
   d.maxg = (gshift == 31) ? 1 : (warp_atoms * ATOM_K >> gshift) + 2;
   d.xp_stride = 2 * d.chunk_atoms + 1;
-  d.L = smem_layout(MT, Mc, d.x_stride, d.maxg, d.xp_stride);
+  d.slice = (16 * WN + S - 1) / S;
+  d.L = smem_layout(MT, Mc, d.x_stride, ring, d.maxg, d.xp_stride, WN, S, d.slice);
   return d;
 }
 
-// Choose warps-along-N and the split-K factor: fill the GPU's CTA slots (as
-// many as registers and shared memory allow per SM) as evenly as possible while
-// keeping each warp's run long enough to stream.
+// Deepest ring (2..MAX_RING stages, no deeper than the warp's run) that keeps
+// `per_sm` CTAs resident.
+DecodePlan fit_ring(int WN, int S, int A, int Mc, int MT, int gshift, int per_sm, int smem_per_sm) {
+  const int WK = DEC_WARPS / WN;
+  const int warp_atoms = ((A + S - 1) / S + WK - 1) / WK;
+  const int need = std::max(2, std::min(MAX_RING, (warp_atoms + STAGE_ATOMS - 1) / STAGE_ATOMS));
+  DecodePlan d = shape_plan(WN, S, A, Mc, MT, gshift, 2);
+  for (int r = need; r >= 2; --r) {
+    d = shape_plan(WN, S, A, Mc, MT, gshift, r);
+    if ((d.L.total + 1024) * per_sm <= smem_per_sm) break;
+  }
+  return d;
+}
+
+// Choose warps-along-N and the split-K factor with a small time model. A
+// wave of CTAs shares the HBM bandwidth among its members and pays a fixed
+// start-up / drain cost; a CTA streams at most ~1/16 of an SM's share alone
+// per warp, so fewer than two resident CTAs per SM leave bandwidth unused.
 DecodePlan plan_decode(int N, int K, int Mc, int MT, int gshift, const DeviceInfo& info) {
   const int NT = N / 16, A = K / ATOM_K;
   const int reg_ctas = MT <= 2 ? 3 : 2;
-  DecodePlan best = shape_plan(8, 1, A, Mc, MT, gshift);
-  double best_score = -1.0;
+  const double overhead = 2.5e-6, bw = 6.5e12;
+  const double sm_bw = bw / info.sm_count;
+  DecodePlan best = shape_plan(8, 1, A, Mc, MT, gshift, 2);
+  double best_t = 1e30;
   for (int WN = 8; WN >= 1; WN >>= 1) {
     const int WK = DEC_WARPS / WN;
     const int cols = (NT + WN - 1) / WN;
     for (int S = 1; S <= MAX_SPLIT && S <= A; ++S) {
-      const double per_warp = (double)A / (S * WK);
-      if (per_warp < 1.0) continue;
-      const DecodePlan d = shape_plan(WN, S, A, Mc, MT, gshift);
+      if ((double)A / (S * WK) < 1.0) continue;
+      const DecodePlan d = fit_ring(WN, S, A, Mc, MT, gshift, 2, info.smem_per_sm);
       const int smem_ctas = info.smem_per_sm / (d.L.total + 1024);
       const int per_sm = std::max(1, std::min(reg_ctas, smem_ctas));
       const long long slots = (long long)per_sm * info.sm_count;
-      const long long ctas = (long long)cols * S;
-      const long long waves = (ctas + slots - 1) / slots;
-      double eff = (double)ctas / (double)(waves * slots);
-      eff *= (double)NT / (double)(cols * WN);  // idle warps in the last column block
-      const double stream = std::min(1.0, per_warp / 8.0);  // short runs stream poorly
-      const double score = eff * (0.6 + 0.4 * stream) - 0.004 * S - 0.002 * (8 / WN);
-      if (score > best_score) {
-        best_score = score;
+      long long left = (long long)cols * S;
+      const double cta_bytes = (double)(16 * WN) * ((double)A / S) * 32.0;  // 64 rows x 16 cols / 2
+      double t = 0.0;
+      while (left > 0) {
+        const long long now = std::min(left, slots);
+        const double per_sm_ctas = (double)now / info.sm_count;
+        // an SM streams at its share of HBM once it holds two CTAs
+        const double rate = sm_bw * std::min(1.0, per_sm_ctas / 2.0) / std::max(1.0, per_sm_ctas);
+        t += overhead + cta_bytes / rate;
+        left -= now;
+      }
+      t += 0.05e-6 * S;
+      if (t < best_t) {
+        best_t = t;
         best = d;
       }
     }
@@ -538,10 +656,12 @@ cudaError_t launch_decode(const GemmArgs& a, cudaStream_t stream) {
     p.gshift = gshift;
     p.A = A;
     p.WN = plan.WN;
+    p.ring = plan.ring;
     p.chunk_atoms = plan.chunk_atoms;
     p.x_stride = plan.x_stride;
     p.maxg = plan.maxg;
     p.xp_stride = plan.xp_stride;
+    p.slice = plan.slice;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((a.N / 16 + plan.WN - 1) / plan.WN, plan.S, 1);

@@ -40,29 +40,38 @@ namespace {
 
 using namespace sm100;
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 3;
+// NACC accumulators of 128 rows share each dequantised B tile: the CTA tile is
+// (128 * NACC) x 256. NACC = 1 double-buffers the accumulator in TMEM (epilogue
+// overlaps the next tile); NACC = 2 fills TMEM with the two accumulators and
+// halves the dequantisation work per MMA.
+constexpr int BN = 256, BK = 64, STAGES = 3;
 constexpr int THREADS = 512;
 constexpr int DEQ_THREADS = 256;  // warps 8-15
 constexpr int EPI_THREADS = 128;  // warps 4-7
-constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int P_BYTES = BN * BK / 2;
 constexpr int S_BYTES = 2 * BN * 2;   // two group rows of scales
 constexpr int Z_BYTES = 2 * BN / 2;   // two group rows of zeros
 constexpr int Z_SLOT = 1024;
-constexpr uint32_t STAGE_TX = A_BYTES + P_BYTES + S_BYTES + Z_BYTES;
-constexpr int TMEM_COLS = 512;        // two 128 x 256 fp32 accumulators
+constexpr int TMEM_COLS = 512;
 
-constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-constexpr int OFF_P = OFF_B + STAGES * B_BYTES;
-constexpr int OFF_S = OFF_P + STAGES * P_BYTES;
-constexpr int OFF_Z = OFF_S + STAGES * S_BYTES;
-constexpr int OFF_BAR = OFF_Z + STAGES * Z_SLOT;
-constexpr int NUM_BARS = 3 * STAGES + 4 + 1;
-constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
-constexpr int SMEM_USED = OFF_MISC + 16;
-constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base to 1024
+template <int NACC>
+struct Cfg {
+  static constexpr int BM = 128 * NACC;
+  static constexpr int NBUF = NACC == 1 ? 2 : 1;  // accumulator buffers in TMEM
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr uint32_t STAGE_TX = A_BYTES + P_BYTES + S_BYTES + Z_BYTES;
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+  static constexpr int OFF_P = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_S = OFF_P + STAGES * P_BYTES;
+  static constexpr int OFF_Z = OFF_S + STAGES * S_BYTES;
+  static constexpr int OFF_BAR = OFF_Z + STAGES * Z_SLOT;
+  static constexpr int NUM_BARS = 3 * STAGES + 2 * NBUF + 1;
+  static constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
+  static constexpr int SMEM_USED = OFF_MISC + 16;
+  static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base to 1024
+};
 
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;  // 1 s per wait
 
@@ -76,14 +85,15 @@ struct PrefillParams {
   int m_blocks, num_tiles, k_blocks;
 };
 
+template <int NBUF>
 struct Bars {
   uint32_t base;
   __device__ uint32_t full(int s) const { return base + 8 * s; }
   __device__ uint32_t bfull(int s) const { return base + 8 * (STAGES + s); }
   __device__ uint32_t empty(int s) const { return base + 8 * (2 * STAGES + s); }
   __device__ uint32_t accfull(int b) const { return base + 8 * (3 * STAGES + b); }
-  __device__ uint32_t accempty(int b) const { return base + 8 * (3 * STAGES + 2 + b); }
-  __device__ uint32_t mmadone() const { return base + 8 * (3 * STAGES + 4); }
+  __device__ uint32_t accempty(int b) const { return base + 8 * (3 * STAGES + NBUF + b); }
+  __device__ uint32_t mmadone() const { return base + 8 * (3 * STAGES + 2 * NBUF); }
 };
 
 // Wait for an mbarrier phase. Returns false when this CTA is aborting: either
@@ -121,13 +131,18 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi, bool bf16) {
   return d;
 }
 
-template <bool BF16>
+template <bool BF16, int NACC>
 __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_constant__ PrefillParams p) {
+  using C = Cfg<NACC>;
+  constexpr int BM = C::BM, NBUF = C::NBUF, A_BYTES = C::A_BYTES;
+  constexpr int OFF_A = C::OFF_A, OFF_B = C::OFF_B, OFF_P = C::OFF_P, OFF_S = C::OFF_S;
+  constexpr int OFF_Z = C::OFF_Z, OFF_BAR = C::OFF_BAR, OFF_MISC = C::OFF_MISC;
+  constexpr uint32_t STAGE_TX = C::STAGE_TX;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_addr(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const Bars bars{sbase + OFF_BAR};
+  const Bars<NBUF> bars{sbase + OFF_BAR};
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
@@ -137,7 +152,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
       mbar_init(bars.bfull(s), DEQ_THREADS);
       mbar_init(bars.empty(s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NBUF; ++b) {
       mbar_init(bars.accfull(b), 1);
       mbar_init(bars.accempty(b), EPI_THREADS);
     }
@@ -195,19 +210,19 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
   } else if (warp == 1) {
     // ---------------------------------------------------------------- UMMA issuer
     if (lane == 0) {
-      constexpr uint32_t IDESC = idesc_f16(BF16 ? 1 : 0, BM, BN);
+      constexpr uint32_t IDESC = idesc_f16(BF16 ? 1 : 0, 128, BN);
       int it = 0, lt = 0;
       bool ok = true;
       bool issued = false;
       for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++lt) {
-        const int buf = lt & 1;
-        const uint32_t aph = (lt >> 1) & 1;
+        const int buf = lt % NBUF;
+        const uint32_t aph = (lt / NBUF) & 1;
         if (!wait_phase(bars.accempty(buf), aph ^ 1, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem + buf * BN;
+        const uint32_t d_tmem = tmem + buf * (BN * NACC);
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
@@ -216,12 +231,16 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
             break;
           }
           tc_fence_after();
-          const uint64_t adesc = smem_desc_k128(sbase + OFF_A + s * A_BYTES);
           const uint64_t bdesc = smem_desc_k128(sbase + OFF_B + s * B_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
-            // advance 16 elements (32 bytes) along K inside the swizzled rows
-            umma_f16(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb | k) != 0);
+#pragma unroll
+            for (int i = 0; i < NACC; ++i) {
+              // accumulator i: rows 128 i .. 128 i + 127 of the A tile; advance
+              // 16 elements (32 bytes) along K inside the swizzled rows
+              const uint64_t adesc = smem_desc_k128(sbase + OFF_A + s * A_BYTES + i * (128 * BK * 2));
+              umma_f16(d_tmem + i * BN, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb | k) != 0);
+            }
           }
           issued = true;
           umma_commit(bars.empty(s));
@@ -236,32 +255,34 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
   } else if (warp >= 4 && warp < 8) {
     // ---------------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
-    const int row = quarter * 32 + lane;
     int lt = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++lt) {
       const int m_blk = tile % p.m_blocks, n_blk = tile / p.m_blocks;
-      const int buf = lt & 1;
-      const uint32_t aph = (lt >> 1) & 1;
+      const int buf = lt % NBUF;
+      const uint32_t aph = (lt / NBUF) & 1;
       if (!wait_phase(bars.accfull(buf), aph, abort_flag)) break;
       tc_fence_after();
-      const int m = m_blk * BM + row;
-      uint16_t* yrow = p.y + (size_t)m * p.N;
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + buf * BN + c0, r);
-        tmem_ld_wait();
-        const int n = n_blk * BN + c0;
-        if (m < p.M) {
+      for (int i = 0; i < NACC; ++i) {
+        const int m = m_blk * BM + i * 128 + quarter * 32 + lane;
+        uint16_t* yrow = p.y + (size_t)m * p.N;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + buf * (BN * NACC) + i * BN + c0, r);
+          tmem_ld_wait();
+          const int n = n_blk * BN + c0;
+          if (m < p.M) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            if (n + 8 * i < p.N) {
-              uint4 v;
-              v.x = pack_half2(__uint_as_float(r[8 * i + 0]), __uint_as_float(r[8 * i + 1]), BF16);
-              v.y = pack_half2(__uint_as_float(r[8 * i + 2]), __uint_as_float(r[8 * i + 3]), BF16);
-              v.z = pack_half2(__uint_as_float(r[8 * i + 4]), __uint_as_float(r[8 * i + 5]), BF16);
-              v.w = pack_half2(__uint_as_float(r[8 * i + 6]), __uint_as_float(r[8 * i + 7]), BF16);
-              *reinterpret_cast<uint4*>(yrow + n + 8 * i) = v;
+            for (int q = 0; q < 4; ++q) {
+              if (n + 8 * q < p.N) {
+                uint4 v;
+                v.x = pack_half2(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1]), BF16);
+                v.y = pack_half2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3]), BF16);
+                v.z = pack_half2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5]), BF16);
+                v.w = pack_half2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7]), BF16);
+                *reinterpret_cast<uint4*>(yrow + n + 8 * q) = v;
+              }
             }
           }
         }
@@ -373,16 +394,15 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint6
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cudaError_t ensure_prefill_smem(void* fn) {
+cudaError_t ensure_prefill_smem(void* fn, int which, int bytes) {
   static std::mutex mu;
-  static bool done[64][2] = {};
+  static bool done[64][4] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const int which = fn == reinterpret_cast<void*>(&w4a16_prefill_kernel<true>) ? 1 : 0;
   std::lock_guard<std::mutex> lock(mu);
   if (dev < 64 && done[dev][which]) return cudaSuccess;
-  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess && dev < 64) done[dev][which] = true;
   return e;
 }
@@ -412,6 +432,10 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     x = xg;
   }
+  // Two accumulators per CTA (256-row tiles) once they still give every SM a tile.
+  const int n_blocks = (a.N + BN - 1) / BN;
+  const int nacc = ((long long)((a.M + 255) / 256) * n_blocks >= info.sm_count) ? 2 : 1;
+  const int BM = 128 * nacc;
   PrefillParams p;
   const int G = a.K / a.group;
   const CUtensorMapDataType act = a.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -430,17 +454,26 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
   p.K = a.K;
   p.group = a.group;
   p.m_blocks = (a.M + BM - 1) / BM;
-  const int n_blocks = (a.N + BN - 1) / BN;
   p.num_tiles = p.m_blocks * n_blocks;
   p.k_blocks = a.K / BK;
 
-  void* fn = a.bf16 ? reinterpret_cast<void*>(&w4a16_prefill_kernel<true>)
-                    : reinterpret_cast<void*>(&w4a16_prefill_kernel<false>);
-  if ((err = ensure_prefill_smem(fn)) != cudaSuccess) return err;
+  void* fn;
+  int smem_bytes;
+  if (nacc == 2) {
+    fn = a.bf16 ? reinterpret_cast<void*>(&w4a16_prefill_kernel<true, 2>)
+                : reinterpret_cast<void*>(&w4a16_prefill_kernel<false, 2>);
+    smem_bytes = Cfg<2>::SMEM_BYTES;
+  } else {
+    fn = a.bf16 ? reinterpret_cast<void*>(&w4a16_prefill_kernel<true, 1>)
+                : reinterpret_cast<void*>(&w4a16_prefill_kernel<false, 1>);
+    smem_bytes = Cfg<1>::SMEM_BYTES;
+  }
+  if ((err = ensure_prefill_smem(fn, (a.bf16 ? 1 : 0) + 2 * (nacc - 1), smem_bytes)) != cudaSuccess)
+    return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(std::min(p.num_tiles, info.sm_count), 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = stream;
   cfg.attrs = nullptr;
   cfg.numAttrs = 0;

@@ -307,6 +307,8 @@ PREFILL_CASES = [
     (768, 1024, -1, "fp16", (129,)),
     (4096, 512, 128, "bf16", (256,)),
     (256, 4096, 128, "bf16", (2048,)),           # 256 tiles: several per CTA
+    (128, 4128, 128, "bf16", (2600,)),           # 256-row tiles, ragged in M and N
+    (256, 4096, 32, "fp16", (2560,)),            # 256-row tiles, group 32
 ]
 
 
