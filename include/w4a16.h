@@ -178,6 +178,37 @@ W4_API w4_status w4a16_gemm(const void* x, const int32_t* qw, const void* scales
                      void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Size of the static device scratch array that w4a16_gemm_noalloc uses (32 MiB).
+ */
+#define W4_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/*
+ * w4a16_gemm without a caller-provided workspace. (This entry point has no
+ * counterpart in the pages: it serves callers of this library that cannot
+ * allocate device memory at call time, such as code running inside a
+ * CUDA-graph capture where cudaMalloc is not allowed, or a host that embeds
+ * the library behind an interface with no allocator.)
+ *
+ * Same arguments, layouts, results and error statuses as w4a16_gemm, minus
+ * workspace / workspace_bytes. Where w4a16_gemm would need a workspace
+ * (act-order calls with M > 64), this call stages x[:, perm] in one static
+ * device array of W4_NOALLOC_SCRATCH_BYTES that the library holds on every
+ * GPU that loads it, until the process exits; calls whose staging would
+ * exceed it (M * K * 2 bytes) return W4_ERR_WORKSPACE and launch nothing.
+ * It never allocates or frees device memory.
+ *   - Set-up: the first call on each device looks up the array's device
+ *     address (cudaGetSymbolAddress) with that device current. Make that first
+ *     call before any stream capture on the device.
+ *   - All calls share the one array: calls that may overlap on the GPU (on
+ *     different streams, or from different host threads) race on it and must
+ *     be ordered by the caller. The array is fully overwritten before it is
+ *     read, so nothing needs clearing between calls.
+ */
+W4_API w4_status w4a16_gemm_noalloc(const void* x, const int32_t* qw, const void* scales,
+                                    const int32_t* zeros, const int32_t* perm, void* y, int M,
+                                    int N, int K, int group, int dtype, void* stream);
+
+/*
  * Read the library's device status word: W4_OK, or W4_ERR_TIMEOUT once some
  * kernel of this library gave up on an internal pipeline wait (every such wait
  * is bounded at one second; the kernel then drains its own copies, frees its

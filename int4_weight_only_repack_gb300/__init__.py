@@ -17,7 +17,8 @@ import torch
 __all__ = [
     "W4_F16", "W4_BF16", "W4_LAYOUT_STD", "W4_LAYOUT_TILE", "W4Error", "lib", "library_path",
     "dtype_code", "w4_status_string", "w4_abi_version", "w4_repack_sizes", "w4_repack_awq",
-    "w4_repack_gptq", "w4a16_gemm_workspace_size", "w4a16_gemm", "w4_dequant", "w4_device_status",
+    "w4_repack_gptq", "w4a16_gemm_workspace_size", "w4a16_gemm", "w4a16_gemm_noalloc", "w4_dequant",
+    "w4_device_status",
     "RepackedLayer", "repack_awq", "repack_gptq", "linear",
 ]
 
@@ -48,6 +49,9 @@ _SIGNATURES = {
     "w4_dequant": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int,
                             _c_int, _c_int, _c_void_p, _c_void_p]),
     "w4_device_status": (_c_int, [ctypes.POINTER(ctypes.c_int32), _c_int]),
+    "w4a16_gemm_noalloc": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                    _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                    _c_void_p]),
 }
 
 
@@ -148,6 +152,13 @@ def w4a16_gemm(x, qw, scales, zeros, perm, y, M, N, K, group, dtype, workspace=N
     _check(lib().w4a16_gemm(_ptr(x), _ptr(qw), _ptr(scales), _ptr(zeros), _ptr(perm), _ptr(y),
                             M, N, K, group, dtype_code(dtype), _ptr(workspace), workspace_bytes,
                             _stream(stream)))
+
+
+def w4a16_gemm_noalloc(x, qw, scales, zeros, perm, y, M, N, K, group, dtype, stream=None):
+    """w4a16_gemm for callers that cannot allocate device memory: act-order
+    staging goes to the library's static device array instead of a workspace."""
+    _check(lib().w4a16_gemm_noalloc(_ptr(x), _ptr(qw), _ptr(scales), _ptr(zeros), _ptr(perm),
+                                    _ptr(y), M, N, K, group, dtype_code(dtype), _stream(stream)))
 
 
 def w4_device_status(clear: bool = False) -> int:

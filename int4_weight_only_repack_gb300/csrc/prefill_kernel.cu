@@ -481,6 +481,30 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
+// ---- static scratch for w4a16_gemm_noalloc ------------------------------------
+// One array per GPU that loads the library, held until exit. Host code must
+// not pass the symbol itself to a kernel (it names a host-side stand-in): the
+// device address comes from cudaGetSymbolAddress, once per device.
+__device__ __align__(256) uint8_t g_noalloc_scratch[W4_NOALLOC_SCRATCH_BYTES];
+
+cudaError_t noalloc_scratch(void** out, size_t* bytes) {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_noalloc_scratch)) != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  *bytes = W4_NOALLOC_SCRATCH_BYTES;
+  return cudaSuccess;
+}
+
 cudaError_t read_device_status(int* out, int clear) {
   int v = 0;
   cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int));

@@ -262,6 +262,31 @@ w4_status w4a16_gemm(const void* x, const int32_t* qw, const void* scales, const
   return from_cuda(launch_decode(a, static_cast<cudaStream_t>(stream)));
 }
 
+w4_status w4a16_gemm_noalloc(const void* x, const int32_t* qw, const void* scales,
+                             const int32_t* zeros, const int32_t* perm, void* y, int M, int N,
+                             int K, int group, int dtype, void* stream) {
+  w4_status st = check_dims(K, N, group, dtype);
+  if (st) return st;
+  if (M < 0 || M > MAX_DIM) return W4_ERR_SHAPE;
+  if ((st = check_layout_dims(K, N, W4_LAYOUT_TILE))) return st;
+  const size_t need = w4a16_gemm_workspace_size(M, N, K, group, dtype, perm != nullptr);
+  if (need > W4_NOALLOC_SCRATCH_BYTES) return W4_ERR_WORKSPACE;
+  if (need == 0 || M == 0) {
+    // nothing to stage: the call is w4a16_gemm without a workspace
+    return w4a16_gemm(x, qw, scales, zeros, perm, y, M, N, K, group, dtype, nullptr, 0, stream);
+  }
+  // validate everything the scratch does not decide before touching the device
+  st = w4a16_gemm(x, qw, scales, zeros, perm, y, 0, N, K, group, dtype, nullptr, 0, stream);
+  if (st) return st;
+  if (!x || !y) return W4_ERR_NULL;
+  if ((st = check_arch())) return st;
+  void* scratch = nullptr;
+  size_t scratch_bytes = 0;
+  if (noalloc_scratch(&scratch, &scratch_bytes) != cudaSuccess) return W4_ERR_CUDA;
+  return w4a16_gemm(x, qw, scales, zeros, perm, y, M, N, K, group, dtype, scratch, scratch_bytes,
+                    stream);
+}
+
 w4_status w4_dequant(const int32_t* qw, const void* scales, const int32_t* zeros, int K, int N,
                      int group, int dtype, int layout, int out_f32, void* w_out, void* stream) {
   w4_status st = check_dims(K, N, group, dtype);

@@ -47,6 +47,10 @@ bool prefill_supported(int M, int N, int K);
 size_t prefill_workspace_bytes(int M, int K, bool has_perm);
 cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t s);
 
+// Device address and size of the static scratch array of w4a16_gemm_noalloc
+// (looked up once per device, with that device current).
+cudaError_t noalloc_scratch(void** out, size_t* bytes);
+
 // The device status word the kernels raise on a timed-out wait.
 cudaError_t read_device_status(int* out, int clear);
 
