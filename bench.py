@@ -50,7 +50,9 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes per launch of the decode kernel from ncu (dram__bytes_read.sum +
 # dram__bytes_write.sum), keyed by the sha1 of the kernel source they were
 # taken on; see profiles/. A changed kernel source reports null.
-TRAFFIC_RECORDS: dict = {}
+TRAFFIC_RECORDS: dict = {
+    "54c0d3eb0b98": 26502293,   # mean of the 12 launches of one step
+}
 
 
 def alg_bytes(K: int, N: int, group: int = 128) -> int:
@@ -433,6 +435,36 @@ def reference(args):
     print(json.dumps(line), flush=True)
 
 
+def single(args):
+    """One GEMM call shape repeated `--steps` times (for profiler captures)."""
+    import torch
+
+    import int4_weight_only_repack_gb300 as w4
+
+    parts = args.single.split(",")
+    K, N, M = int(parts[0]), int(parts[1]), int(parts[2])
+    dtype = parts[3] if len(parts) > 3 else "bf16"
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+    dev = torch.device("cuda")
+    L = synth.make_custom_layer([5, K, N], K, N, group=128, dtype=dtype)
+    layer = w4.repack_awq(torch.from_numpy(L.qweight).to(dev), torch.from_numpy(L.qzeros).to(dev),
+                          torch.from_numpy(L.scales.view(np.int16)).to(dev).view(tdt), K, N, 128, tdt)
+    x = torch.from_numpy(synth.make_custom_x([6, M, K], M, K, dtype).view(np.int16)).to(dev).view(tdt)
+    y = torch.empty((M, N), dtype=tdt, device=dev)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        w4.linear(x, layer, y=y)
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) * 1e-3 / max(1, args.steps)
+    print(json.dumps({"single": [K, N, M, dtype], "us_per_call": round(t * 1e6, 2),
+                      "weight_gbs": round(alg_bytes(K, N) / t / 1e9, 1),
+                      "tflops": round(2.0 * M * N * K / t / 1e12, 2),
+                      "device_status": w4.w4_device_status()}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -441,8 +473,12 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--single", default=None,
+                    help="K,N,M[,dtype]: time one layer shape only (profiling aid)")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.single:
+        single(args)
+    elif args.impl == "reference":
         reference(args)
     else:
         ours(args)

@@ -28,7 +28,9 @@
 //    "vLLM AWQ 4-bit 量化实践" §5.3 names split-K for the fused kernel).
 //  * Launch order inside a CTA: the small loads that gate the first MMA (x,
 //    scales, zeros) are issued before the weight stream, so they are not
-//    queued behind it.
+//    queued behind it; the weight stream is marked evict-first in L2. Launches
+//    use programmatic stream serialization: a CTA may become resident while
+//    the previous kernel drains, and waits for it before touching memory.
 //  * Waits on the ring's mbarriers are bounded (one second); on a timeout the
 //    warp records W4_ERR_TIMEOUT in the device status word, lets its copies in
 //    flight land (bounded again) and stops computing.
@@ -83,7 +85,7 @@ struct DecodeParams {
 };
 
 struct SmemLayout {
-  int xs, ring, bars, meta_s, meta_z, xpre, red, recv, total;
+  int xs, ring, bars, meta_s, meta_z, meta_f, xpre, red, recv, total;
 };
 
 // x keeps M token rows plus one row of zeros (read by the MMA lanes whose
@@ -97,7 +99,8 @@ __host__ __device__ inline SmemLayout smem_layout(int MT, int m_rows, int x_stri
   L.bars = L.ring + DEC_WARPS * ring * STAGE_ATOMS * ATOM_BYTES;
   L.meta_s = (L.bars + (DEC_WARPS * ring + 1) * 8 + 15) & ~15;
   L.meta_z = L.meta_s + DEC_WARPS * maxg * 32;
-  L.xpre = (L.meta_z + DEC_WARPS * maxg * 8 + 15) & ~15;
+  L.meta_f = (L.meta_z + DEC_WARPS * maxg * 8 + 15) & ~15;
+  L.xpre = (L.meta_f + DEC_WARPS * maxg * 16 * 8 + 15) & ~15;
   L.red = (L.xpre + 8 * MT * xp_stride * 4 + 15) & ~15;
   const int red_bytes = WN < DEC_WARPS ? DEC_WARPS * 16 * 8 * MT * 4 : 0;
   L.recv = (L.red + red_bytes + 15) & ~15;
@@ -112,6 +115,32 @@ __device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_
           dst),
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
+}
+
+// Weight-stream copy: the weights are read once per call, so they are marked
+// evict-first in L2, which keeps x, scales and zeros resident.
+__device__ __forceinline__ void bulk_copy_stream(uint32_t dst, const void* src, uint32_t bytes,
+                                                 uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 16-byte shared-memory load from a 32-bit shared-window address.
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
 }
 
 // Bounded wait; false when the limit ran out (the caller records the timeout).
@@ -145,8 +174,12 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 // With bf16 the MMA consumes the codes as 128 + q (exact in bf16) and each
 // group's partial sum is corrected by (128 + z) * sum(x) before scaling; with
 // fp16 the operand is q - z (exact) and needs no correction.
+#ifndef W4_DECODE_MIN_CTAS
+#define W4_DECODE_MIN_CTAS 3  // resident CTAs per SM the register budget is sized for (M <= 16)
+#endif
+
 template <int MT, bool BF16, bool G64>
-__global__ void __launch_bounds__(DEC_THREADS, MT <= 2 ? 3 : 2) w4a16_decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(DEC_THREADS, MT <= 2 ? W4_DECODE_MIN_CTAS : 2) w4a16_decode_kernel(const DecodeParams p) {
   constexpr uint32_t MAGIC = Magic<BF16>::pair;
   constexpr bool BIAS = BF16;
   constexpr int SLOT = STAGE_ATOMS * ATOM_BYTES;
@@ -168,6 +201,9 @@ __global__ void __launch_bounds__(DEC_THREADS, MT <= 2 ? 3 : 2) w4a16_decode_ker
   const uint32_t xbar = smem_addr(smem + L.bars + DEC_WARPS * RINGN * 8);
   uint16_t* meta_s = reinterpret_cast<uint16_t*>(smem + L.meta_s) + warp * p.maxg * 16;
   uint2* meta_z = reinterpret_cast<uint2*>(smem + L.meta_z) + warp * p.maxg;
+  // per (group, column): {scale, (128 + zero) * scale} in fp32, the two factors
+  // of the bf16 group correction
+  float2* meta_f = reinterpret_cast<float2*>(smem + L.meta_f) + warp * p.maxg * 16;
   float* xpre = reinterpret_cast<float*>(smem + L.xpre);
   float* red = reinterpret_cast<float*>(smem + L.red);
   float* recv = reinterpret_cast<float*>(smem + L.recv);
@@ -183,6 +219,14 @@ __global__ void __launch_bounds__(DEC_THREADS, MT <= 2 ? 3 : 2) w4a16_decode_ker
   const bool has_cols = nt < p.N / 16;
   const uint32_t* wsrc = p.qw + (size_t)nt * p.A * ATOM_WORDS;  // this tile's atom run
   uint16_t* xzero = xs + (size_t)p.M * p.x_stride;              // the zero row
+
+  // Launched with programmatic stream serialization: the CTA may become
+  // resident while the previous kernel in the stream drains. It waits for that
+  // kernel (griddepcontrol.wait) before touching global memory, then lets the
+  // next kernel in the stream start its own launch.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+  const uint64_t stream_policy = evict_first_policy();
 
   if (lane == 0) {
     for (int s = 0; s < RINGN; ++s) mbar_init(bar0 + 8 * s, 1);
@@ -200,41 +244,62 @@ __global__ void __launch_bounds__(DEC_THREADS, MT <= 2 ? 3 : 2) w4a16_decode_ker
     for (int j = 0; j < 4; ++j) acc[i][j] = tot[i][j] = 0.f;
   int hs = 0;           // chunk-relative half-atom index where the open group started
   int g_first = 0;      // first group of this warp's run in the chunk
-  float s_lo = 0.f, s_hi = 0.f, zlf = 0.f, zhf = 0.f;
+  float s_lo = 0.f, s_hi = 0.f, zs_lo = 0.f, zs_hi = 0.f;
   uint32_t zl = 0, zh = 0;
-  uint32_t it = 0;      // stages consumed by this warp (ring position and phase)
+  uint32_t it = 0;      // stages consumed by this warp
+  uint32_t rslot = 0;   // ring slot of the next stage to consume (== it % RINGN)
+  uint32_t rphase = 0;  // its mbarrier phase parity (== (it / RINGN) & 1)
   uint32_t xphase = 0;  // phase of the x barrier
   bool alive = true;    // false once a wait gave up
 
-  // tot += s * (acc - (MAGIC + z) * sum of x over halves [h0, h1)); acc = 0
+  // tot += s * acc - (MAGIC + z) * s * (sum of x over halves [h0, h1)); acc = 0
+  // ((MAGIC + z) * s is exact in fp32: two 8-bit significands)
   auto flush = [&](int h0, int h1) {
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
-      float c0 = 0.f, c1 = 0.f;
       if constexpr (BIAS) {
         const float* xp = xpre + (8 * mt + 2 * t) * p.xp_stride;
-        c0 = xp[h1] - xp[h0];
-        c1 = xp[p.xp_stride + h1] - xp[p.xp_stride + h0];
+        const float c0 = xp[h1] - xp[h0];
+        const float c1 = xp[p.xp_stride + h1] - xp[p.xp_stride + h0];
+        tot[mt][0] = fmaf(s_lo, acc[mt][0], fmaf(-zs_lo, c0, tot[mt][0]));
+        tot[mt][1] = fmaf(s_lo, acc[mt][1], fmaf(-zs_lo, c1, tot[mt][1]));
+        tot[mt][2] = fmaf(s_hi, acc[mt][2], fmaf(-zs_hi, c0, tot[mt][2]));
+        tot[mt][3] = fmaf(s_hi, acc[mt][3], fmaf(-zs_hi, c1, tot[mt][3]));
+      } else {
+        tot[mt][0] = fmaf(s_lo, acc[mt][0], tot[mt][0]);
+        tot[mt][1] = fmaf(s_lo, acc[mt][1], tot[mt][1]);
+        tot[mt][2] = fmaf(s_hi, acc[mt][2], tot[mt][2]);
+        tot[mt][3] = fmaf(s_hi, acc[mt][3], tot[mt][3]);
       }
-      tot[mt][0] = fmaf(s_lo, fmaf(-zlf, c0, acc[mt][0]), tot[mt][0]);
-      tot[mt][1] = fmaf(s_lo, fmaf(-zlf, c1, acc[mt][1]), tot[mt][1]);
-      tot[mt][2] = fmaf(s_hi, fmaf(-zhf, c0, acc[mt][2]), tot[mt][2]);
-      tot[mt][3] = fmaf(s_hi, fmaf(-zhf, c1, acc[mt][3]), tot[mt][3]);
       acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
     }
   };
   // scale / zero registers for group gi (staged in shared memory)
   auto open_group = [&](int gi) {
     const int gl = gi - g_first;
-    s_lo = half_bits_to_float<BF16>(meta_s[gl * 16 + gg]);
-    s_hi = half_bits_to_float<BF16>(meta_s[gl * 16 + gg + 8]);
-    const uint2 zw = meta_z[gl];
-    const uint32_t z0 = (zw.x >> (4 * gg)) & 0xF;
-    const uint32_t z1 = (zw.y >> (4 * gg)) & 0xF;
-    zl = MAGIC | z0 | (z0 << 16);
-    zh = MAGIC | z1 | (z1 << 16);
-    zlf = BIAS ? (float)(128 + z0) : 0.f;
-    zhf = BIAS ? (float)(128 + z1) : 0.f;
+    const float2 f_lo = meta_f[gl * 16 + gg], f_hi = meta_f[gl * 16 + gg + 8];
+    s_lo = f_lo.x;
+    zs_lo = f_lo.y;
+    s_hi = f_hi.x;
+    zs_hi = f_hi.y;
+    if constexpr (!BIAS) {
+      const uint2 zw = meta_z[gl];
+      const uint32_t z0 = (zw.x >> (4 * gg)) & 0xF;
+      const uint32_t z1 = (zw.y >> (4 * gg)) & 0xF;
+      zl = MAGIC | z0 | (z0 << 16);
+      zh = MAGIC | z1 | (z1 << 16);
+    }
+  };
+  // expand one group's 16 scales and 16 zeros into meta_f
+  auto stage_group_f = [&](int gl, const uint4 a, const uint4 b, const uint2 z) {
+    const uint32_t sv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const uint16_t sb = (uint16_t)(sv[c >> 1] >> (16 * (c & 1)));
+      const float sf = half_bits_to_float<BF16>(sb);
+      const uint32_t zc = ((c < 8 ? z.x : z.y) >> (4 * (c & 7))) & 0xF;
+      meta_f[gl * 16 + c] = make_float2(sf, (float)(128 + zc) * sf);
+    }
   };
 
   for (int c0 = ka0; c0 < ka1; c0 += p.chunk_atoms) {
@@ -253,7 +318,8 @@ __global__ void __launch_bounds__(DEC_THREADS, MT <= 2 ? 3 : 2) w4a16_decode_ker
       const int a = wa0 + j * STAGE_ATOMS;
       const uint32_t bytes = (uint32_t)min(STAGE_ATOMS, wa1 - a) * ATOM_BYTES;
       mbar_arrive_expect_tx(bar0 + 8 * slot, bytes);
-      bulk_copy(ring_s + slot * SLOT, wsrc + (size_t)a * ATOM_WORDS, bytes, bar0 + 8 * slot);
+      bulk_copy_stream(ring_s + slot * SLOT, wsrc + (size_t)a * ATOM_WORDS, bytes, bar0 + 8 * slot,
+                       stream_policy);
     };
 
     // 1) the loads that gate the first MMA go first: x, then scales / zeros
@@ -278,7 +344,11 @@ __global__ void __launch_bounds__(DEC_THREADS, MT <= 2 ? 3 : 2) w4a16_decode_ker
     // 2) then the weight stream
     if (lane == 0 && n_stages > 0) {
       fence_proxy_async_smem();  // earlier reads of the ring precede these copies
-      for (int j = 0; j < min(RINGN, n_stages); ++j) issue(j, (it + j) % RINGN);
+      uint32_t sl = rslot;
+      for (int j = 0; j < min(RINGN, n_stages); ++j) {
+        issue(j, sl);
+        sl = (sl + 1 == (uint32_t)RINGN) ? 0u : sl + 1;
+      }
     }
     // 3) scales / zeros to shared memory (groups beyond 32 per warp: direct)
     if (lane < ng) {
@@ -286,14 +356,18 @@ __global__ void __launch_bounds__(DEC_THREADS, MT <= 2 ? 3 : 2) w4a16_decode_ker
       sd[0] = ms0;
       sd[1] = ms1;
       meta_z[lane] = mz;
+      stage_group_f(lane, ms0, ms1, mz);
     }
     for (int gl = lane + 32; gl < ng; gl += 32) {
       const int gi = g_first + gl;
       const uint4* sp = reinterpret_cast<const uint4*>(p.scales + (size_t)gi * p.N + nt * 16);
       uint4* sd = reinterpret_cast<uint4*>(meta_s + gl * 16);
-      sd[0] = __ldg(sp);
-      sd[1] = __ldg(sp + 1);
-      meta_z[gl] = __ldg(reinterpret_cast<const uint2*>(p.zeros + (size_t)gi * (p.N / 8) + nt * 2));
+      const uint4 a = __ldg(sp), b = __ldg(sp + 1);
+      const uint2 z = __ldg(reinterpret_cast<const uint2*>(p.zeros + (size_t)gi * (p.N / 8) + nt * 2));
+      sd[0] = a;
+      sd[1] = b;
+      meta_z[gl] = z;
+      stage_group_f(gl, a, b, z);
     }
     if (!x_async) {
       // act-order: gather x[:, perm] with plain loads
@@ -354,22 +428,38 @@ __global__ void __launch_bounds__(DEC_THREADS, MT <= 2 ? 3 : 2) w4a16_decode_ker
     }
     __syncthreads();  // x prefix sums and every warp's scale / zero stage are ready
 
-    // 5) consume the ring
-    const uint16_t* xrow[MT];  // this lane's token row (or the zero row), column 8t - kx0
+    // 5) consume the ring. Shared-memory operands are addressed with 32-bit
+    //    shared-window addresses: per stage one base for the weights and one per
+    //    token tile for x, with constant offsets inside the stage.
+    uint32_t xa[MT];  // this lane's x row (or the zero row) at the warp's first atom, column 8t
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
       const int row = 8 * mt + gg;
-      xrow[mt] = (row < p.M ? xs + (size_t)row * p.x_stride : xzero) + 8 * t - kx0;
+      xa[mt] = smem_addr(row < p.M ? xs + (size_t)row * p.x_stride : xzero) +
+               2u * (uint32_t)(8 * t + (wa0 - c0) * ATOM_K);
     }
     hs = 2 * (wa0 - c0);
+    // atoms left before the next group boundary (groups of 64 rows or more)
+    const int apg = G64 ? (p.gshift >= 31 ? (1 << 30) : (1 << (p.gshift - 6))) : 1;
+    int gleft = G64 ? apg - (wa0 & (apg - 1)) : 0;
     if (n_atoms > 0) open_group((wa0 * ATOM_K) >> p.gshift);
 
-    auto atom = [&](int a, const uint4 w) {
+    // one atom: 64 rows x 16 columns, four m16n8k16 MMAs per token tile;
+    // xo = byte offset of the atom's x columns from xa
+    auto atom = [&](int a, const uint4 w, const uint32_t xo) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        if (!G64 || h == 0) {
+        if constexpr (G64) {
+          if (h == 0 && gleft == 0) {  // a group starts at this atom
+            const int hcur = 2 * (a - c0);
+            flush(hs, hcur);
+            hs = hcur;
+            open_group((a * ATOM_K) >> p.gshift);
+            gleft = apg;
+          }
+        } else {
           const uint32_t kabs = (uint32_t)(a * ATOM_K + 32 * h);
-          if ((kabs & gmask) == 0) {  // a group starts here
+          if ((kabs & gmask) == 0) {
             const int hcur = 2 * (a - c0) + h;
             flush(hs, hcur);
             hs = hcur;
@@ -380,8 +470,7 @@ __global__ void __launch_bounds__(DEC_THREADS, MT <= 2 ? 3 : 2) w4a16_decode_ker
         const uint32_t whi = h ? w.w : w.y;  // column gg + 8
         uint4 xf[MT];
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-          xf[mt] = *reinterpret_cast<const uint4*>(xrow[mt] + a * ATOM_K + 32 * h);
+        for (int mt = 0; mt < MT; ++mt) xf[mt] = lds128(xa[mt] + xo + 64u * h);
 #pragma unroll
         for (int step = 0; step < 2; ++step) {
           const int sh = 8 * step;
@@ -403,11 +492,13 @@ __global__ void __launch_bounds__(DEC_THREADS, MT <= 2 ? 3 : 2) w4a16_decode_ker
           }
         }
       }
+      if constexpr (G64) --gleft;
     };
 
+    const uint32_t wlane = ring_s + (uint32_t)lane * 16u;
     for (int j = 0; j < n_stages; ++j) {
-      const uint32_t slot = it % RINGN;
-      if (!bounded_wait(bar0 + 8 * slot, (it / RINGN) & 1)) {
+      const uint32_t slot = rslot;
+      if (!bounded_wait(bar0 + 8 * slot, rphase)) {
         // give up: record it, let the copies in flight land, stop streaming
         if (lane == 0) atomicExch(&g_device_status, W4_ERR_TIMEOUT);
         const int in_flight = min(RINGN, n_stages - j);
@@ -416,17 +507,18 @@ __global__ void __launch_bounds__(DEC_THREADS, MT <= 2 ? 3 : 2) w4a16_decode_ker
         alive = false;
         break;
       }
-      const uint8_t* stage = ring + slot * SLOT + lane * 16;
+      const uint32_t st = wlane + slot * SLOT;
       const int a_base = wa0 + j * STAGE_ATOMS;
+      const uint32_t xo = (uint32_t)j * (STAGE_ATOMS * ATOM_K * 2);
       if (a_base + STAGE_ATOMS <= wa1) {
         uint4 w[STAGE_ATOMS];
 #pragma unroll
-        for (int u = 0; u < STAGE_ATOMS; ++u) w[u] = *reinterpret_cast<const uint4*>(stage + u * ATOM_BYTES);
+        for (int u = 0; u < STAGE_ATOMS; ++u) w[u] = lds128(st + u * ATOM_BYTES);
 #pragma unroll
-        for (int u = 0; u < STAGE_ATOMS; ++u) atom(a_base + u, w[u]);
+        for (int u = 0; u < STAGE_ATOMS; ++u) atom(a_base + u, w[u], xo + u * (ATOM_K * 2));
       } else {
         for (int u = 0; u < wa1 - a_base; ++u)
-          atom(a_base + u, *reinterpret_cast<const uint4*>(stage + u * ATOM_BYTES));
+          atom(a_base + u, lds128(st + u * ATOM_BYTES), xo + u * (ATOM_K * 2));
       }
       __syncwarp();
       if (lane == 0 && j + RINGN < n_stages) {
@@ -434,6 +526,10 @@ __global__ void __launch_bounds__(DEC_THREADS, MT <= 2 ? 3 : 2) w4a16_decode_ker
         issue(j + RINGN, slot);    // slot == (it_at_chunk_start + j + RINGN) % RINGN
       }
       ++it;
+      if (++rslot == (uint32_t)RINGN) {
+        rslot = 0;
+        rphase ^= 1u;
+      }
     }
     // the prefix sums and the scale / zero stage belong to this chunk: close the group
     if (n_atoms > 0) flush(hs, 2 * (wa1 - c0));
@@ -585,7 +681,7 @@ DecodePlan fit_ring(int WN, int S, int A, int Mc, int MT, int gshift, int per_sm
 // per warp, so fewer than two resident CTAs per SM leave bandwidth unused.
 DecodePlan plan_decode(int N, int K, int Mc, int MT, int gshift, const DeviceInfo& info) {
   const int NT = N / 16, A = K / ATOM_K;
-  const int reg_ctas = MT <= 2 ? 3 : 2;
+  const int reg_ctas = MT <= 2 ? W4_DECODE_MIN_CTAS : 2;
   const double overhead = 2.5e-6, bw = 6.5e12;
   const double sm_bw = bw / info.sm_count;
   DecodePlan best = shape_plan(8, 1, A, Mc, MT, gshift, 2);
@@ -595,7 +691,13 @@ DecodePlan plan_decode(int N, int K, int Mc, int MT, int gshift, const DeviceInf
     const int cols = (NT + WN - 1) / WN;
     for (int S = 1; S <= MAX_SPLIT && S <= A; ++S) {
       if ((double)A / (S * WK) < 1.0) continue;
-      const DecodePlan d = fit_ring(WN, S, A, Mc, MT, gshift, 2, info.smem_per_sm);
+      // three resident CTAs per SM (more warps to hide latency) when registers
+      // allow it and a ring of at least three stages still fits; else two
+      DecodePlan d = fit_ring(WN, S, A, Mc, MT, gshift, 2, info.smem_per_sm);
+      if (reg_ctas >= 3) {
+        const DecodePlan d3 = fit_ring(WN, S, A, Mc, MT, gshift, 3, info.smem_per_sm);
+        if (d3.ring >= 3 && (d3.L.total + 1024) * 3 <= info.smem_per_sm) d = d3;
+      }
       const int smem_ctas = info.smem_per_sm / (d.L.total + 1024);
       const int per_sm = std::max(1, std::min(reg_ctas, smem_ctas));
       const long long slots = (long long)per_sm * info.sm_count;
@@ -668,13 +770,15 @@ cudaError_t launch_decode(const GemmArgs& a, cudaStream_t stream) {
     cfg.blockDim = dim3(DEC_THREADS, 1, 1);
     cfg.dynamicSmemBytes = plan.L.total;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = plan.S;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     void* args[] = {&p};
     if ((err = cudaLaunchKernelExC(&cfg, fn, args)) != cudaSuccess) return err;
   }

@@ -146,6 +146,12 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
+  // Launched with programmatic stream serialization: wait for the previous
+  // kernel in the stream before touching global memory, then let the next one
+  // start its launch.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bars.full(s), 1);
@@ -434,7 +440,14 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
   }
   // Two accumulators per CTA (256-row tiles) once they still give every SM a tile.
   const int n_blocks = (a.N + BN - 1) / BN;
-  const int nacc = ((long long)((a.M + 255) / 256) * n_blocks >= info.sm_count) ? 2 : 1;
+  // A 256-row tile does the MMA work of two 128-row tiles in ~1.25x the time
+  // (it dequantises each B tile once for both). Pick the tiling with fewer
+  // estimated wave-times.
+  const long long t128 = (long long)((a.M + 127) / 128) * n_blocks;
+  const long long t256 = (long long)((a.M + 255) / 256) * n_blocks;
+  const double w128 = (double)((t128 + info.sm_count - 1) / info.sm_count);
+  const double w256 = 1.25 * (double)((t256 + info.sm_count - 1) / info.sm_count);
+  const int nacc = w256 < w128 ? 2 : 1;
   const int BM = 128 * nacc;
   PrefillParams p;
   const int G = a.K / a.group;
@@ -475,8 +488,11 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
   cfg.blockDim = dim3(THREADS, 1, 1);
   cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = stream;
-  cfg.attrs = nullptr;
-  cfg.numAttrs = 0;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   void* args[] = {&p};
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
