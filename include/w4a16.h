@@ -46,8 +46,14 @@
  *     Needs K % 8 == 0 and N % 8 == 0.
  *   W4_LAYOUT_TILE (this library's kernel layout, the role Marlin's repacked
  *     layout plays in "量化层加载" 关键文件): needs K % 64 == 0, N % 16 == 0.
- *     The words form atoms of 64 rows x 16 columns, 128 words each, stored
- *     column-tile-major: atom a = (n/16) * (K/64) + k/64. Inside an atom, word
+ *     The words form atoms of 64 rows x 16 columns, 128 words each. Columns
+ *     are taken in groups of eight 16-column tiles (128 columns; a partial last
+ *     group is padded with zero atoms, so the buffer holds K * ceil(N/128) * 64
+ *     bytes), and atom (k/64, n/16) sits at index
+ *     a = ((n/128) * (K/64) + k/64) * 8 + (n/16) % 8: the eight tiles of a
+ *     group at one k-atom are adjacent (4 KB) and a group's whole K range is
+ *     one contiguous run, which the kernels stream in large copies. Inside an
+ *     atom, word
  *     4*lane + j (lane = 4*gg + t) holds column n = 16*(n/16) + gg + 8*(j & 1)
  *     and rows k = 64*(k/64) + 32*(j >> 1) + 8*t + e, e = 0..7, row offset e at
  *     nibble position P[e], P = {0,4,1,5,2,6,3,7}. The zeros and scales of the
@@ -107,7 +113,8 @@ W4_API int w4_abi_version(void);
 
 /*
  * Byte sizes of the repacked buffers for a K x N layer ("create_weights").
- *   qw_bytes     = K*N/2 for both layouts,
+ *   qw_bytes     = K*N/2 for W4_LAYOUT_STD, K*ceil(N/128)*128/2 for
+ *                  W4_LAYOUT_TILE (whole 128-column groups),
  *   zeros_bytes  = G*N/2 (standard-order zeros [G][N/8]),
  *   scales_bytes = G*N*2 (scales [G][N]).
  * Any output pointer may be NULL. Returns a validation status.

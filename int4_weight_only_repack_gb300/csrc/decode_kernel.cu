@@ -4,40 +4,50 @@
 // 量化" §1: decode has FLOPs/Bytes ~ 1 and moving the weights dominates), so
 // the kernel is organised around the weight stream:
 //
-//  * Each warp owns one 16-column tile and a contiguous run of 64-row TILE
-//    atoms (512 bytes each, contiguous in memory). Lane 0 streams the run into
-//    a private shared-memory ring with bulk asynchronous copies
-//    (cp.async.bulk, completion counted on one mbarrier per stage), so many
-//    kilobytes per warp are in flight without holding registers. Each lane
-//    then reads its 16 bytes of an atom: exactly the A fragments of four
-//    m16n8k16 MMAs in the swapped form y^T = W^T · x^T (the weight columns
-//    fill the MMA's 16 rows, the tokens its 8 columns).
+//  * A CTA owns one 128-column group (eight 16-column tiles, one warp each)
+//    and a K range. In the TILE layout that group's atoms are one contiguous
+//    run along K (the eight tiles of a k-atom are adjacent, 4 KB), so the CTA
+//    reads its weights as a single sequential stream: bulk asynchronous copies
+//    (cp.async.bulk) of several k-atoms at a time into a CTA-wide ring, each
+//    completion counted on one mbarrier per stage. Every warp reads its tile's
+//    atom of each k-atom; the last warp to finish a stage refills its slot
+//    with the stage one ring-length ahead. The CTA's first stages are also
+//    prefetched into L2 before the kernel waits for its predecessor in the
+//    stream (L2 is the device's point of coherence, so this never reads stale
+//    data), and the stream keeps a prefetch a few stages ahead of the ring.
+//  * One 16-byte shared-memory load per lane is exactly the A-fragment set of
+//    four m16n8k16 MMAs in the swapped form y^T = W^T · x^T (the weight
+//    columns fill the MMA's 16 rows, the tokens its 8 columns).
 //  * Dequantisation ("vLLM AWQ 4-bit 量化实践" §5.3: (b - zeros) * scales) is
-//    split: the MMA consumes (q - z), which is exact in fp16/bf16, and the
+//    split: one LOP3 turns a nibble pair into MAGIC + q halves and the
 //    per-(group, column) scale multiplies the fp32 partial sum of each group.
-//    One LOP3 turns a nibble pair into MAGIC + q halves and one packed
-//    subtraction of MAGIC + z leaves q - z. A warp's scales and zeros are
-//    staged once in shared memory.
+//    With bf16 and M <= 16 the MMA consumes MAGIC + q = 128 + q directly and
+//    the group sum is corrected by (128 + z) * s * sum(x); the per-group sums
+//    of x are computed once per CTA (MMAs against an all-ones operand) before
+//    the weight loop. Otherwise one packed subtraction per register forms
+//    q - z, exact in both types.
 //  * The CTA stages its slice of x in shared memory (gathering x[:, perm] for
-//    act-order layers), padded so fragment loads are free of bank conflicts.
-//  * Split-K across the CTAs of a thread-block cluster (up to 8 along K): each
+//    act-order layers), padded so fragment loads are free of bank conflicts;
+//    when it does not fit, x is staged in double-buffered chunks while the
+//    weight stream runs on across chunk boundaries.
+//  * Split-K across the CTAs of a thread-block cluster (up to 16 along K): each
 //    CTA pushes its fp32 partial sums into the shared memory of the CTA that
 //    owns those output columns (distributed shared memory stores), one
 //    cluster barrier later every owner sums its slice over the peers in a
 //    fixed order (deterministic, no global workspace, no atomics:
 //    "vLLM AWQ 4-bit 量化实践" §5.3 names split-K for the fused kernel).
-//  * Launch order inside a CTA: the small loads that gate the first MMA (x,
-//    scales, zeros) are issued before the weight stream, so they are not
-//    queued behind it; the weight stream is marked evict-first in L2. Launches
-//    use programmatic stream serialization: a CTA may become resident while
-//    the previous kernel drains, and waits for it before touching memory.
-//  * Waits on the ring's mbarriers are bounded (one second); on a timeout the
-//    warp records W4_ERR_TIMEOUT in the device status word, lets its copies in
-//    flight land (bounded again) and stops computing.
+//  * Launches use programmatic stream serialization: a CTA may become resident
+//    while the previous kernel drains; it waits for it (griddepcontrol.wait)
+//    before reading x or staging anything from global memory.
+//  * Every wait is bounded (one second). A timed-out wait records
+//    W4_ERR_TIMEOUT in the device status word and raises a CTA abort flag that
+//    ends every other wait at once; the CTA lets its copies in flight land
+//    (bounded again) before it exits.
 #include <cooperative_groups.h>
 
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 #include <unordered_map>
 
 #include "sm100_ptx.cuh"
@@ -54,15 +64,22 @@ namespace {
 
 using namespace sm100;
 
-constexpr int DEC_THREADS = 256;
-constexpr int DEC_WARPS = DEC_THREADS / 32;
+constexpr int DEC_WARPS = 8;                  // one warp per tile of a 128-column group
+constexpr int DEC_THREADS = DEC_WARPS * 32;
 constexpr int ATOM_K = 64;
-constexpr int ATOM_WORDS = 128;
 constexpr int ATOM_BYTES = 512;
-constexpr int MAX_SPLIT = 8;
-constexpr int STAGE_ATOMS = 4;       // atoms per ring stage (2 KB)
-constexpr int MAX_RING = 8;          // stages per warp, upper bound
-constexpr int X_BUDGET = 48 * 1024;  // bytes of staged x per CTA
+constexpr int KROW_BYTES = DEC_WARPS * ATOM_BYTES;  // a column group's atoms at one k-atom
+constexpr int MAX_SPLIT = 16;                // cluster size (above 8: non-portable)
+#ifndef W4_DECODE_SA
+#define W4_DECODE_SA 4  // k-atoms per ring stage
+#endif
+constexpr int SA = W4_DECODE_SA;
+constexpr int STAGE_BYTES = SA * KROW_BYTES;  // 16 KB
+constexpr int MAX_RING = 8;
+constexpr int X_BUDGET = 48 * 1024;           // bytes of staged x per CTA
+#ifndef W4_DECODE_PF
+#define W4_DECODE_PF 2  // stages prefetched into L2 beyond the ring
+#endif
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
 
 struct DecodeParams {
@@ -75,35 +92,35 @@ struct DecodeParams {
   int M, N, K;
   int gshift;              // group = 1 << gshift; 31 = one group over all of K
   int A;                   // K / 64
-  int WN;                  // warps along N per CTA (WK = 8 / WN along K)
-  int ring;                // stages per warp
-  int chunk_atoms;         // atoms of x staged in shared memory at a time
+  int ring;                // stages of the CTA's ring
+  int pf;                  // stages prefetched into L2 beyond the ring
+  int chunk_atoms;         // k-atoms of x staged at a time (a multiple of SA when chunked)
+  int nbuf;                // x chunk buffers: 2 when the CTA's K range spans several chunks
   int x_stride;            // shared x row stride in halves
-  int maxg;                // group slots of the per-warp scale / zero stage
-  int xp_stride;           // row length of the x prefix sums (2 * chunk_atoms + 1)
+  int maxg;                // group slots per chunk
   int slice;               // output columns owned by each CTA of a cluster
 };
 
 struct SmemLayout {
-  int xs, ring, bars, meta_s, meta_z, meta_f, xpre, red, recv, total;
+  int xs, ring, bars, cnt, meta, xsum, recv, total;
 };
 
-// x keeps M token rows plus one row of zeros (read by the MMA lanes whose
-// token row is beyond M).
-__host__ __device__ inline SmemLayout smem_layout(int MT, int m_rows, int x_stride, int ring,
-                                                  int maxg, int xp_stride, int WN, int S,
-                                                  int slice) {
+// xs: nbuf buffers of M token rows, then one row of zeros (read by the MMA
+// lanes whose token row is beyond M). bars: ring mbarriers, then one per x
+// buffer. cnt: per slot the count of warps done with it (monotonic), per slot
+// the last stage copied into it, per x buffer the last chunk copied into it,
+// and the abort flag. meta: per warp and group slot, one float4 per lane group.
+// xsum: per group slot, the sum of x over the group's rows for each token.
+__host__ __device__ inline SmemLayout smem_layout(int MT, int m_rows, int x_stride, int nbuf,
+                                                  int ring, int maxg, int S, int slice) {
   SmemLayout L;
   L.xs = 0;
-  L.ring = (((m_rows + 1) * x_stride * 2) + 1023) & ~1023;
-  L.bars = L.ring + DEC_WARPS * ring * STAGE_ATOMS * ATOM_BYTES;
-  L.meta_s = (L.bars + (DEC_WARPS * ring + 1) * 8 + 15) & ~15;
-  L.meta_z = L.meta_s + DEC_WARPS * maxg * 32;
-  L.meta_f = (L.meta_z + DEC_WARPS * maxg * 8 + 15) & ~15;
-  L.xpre = (L.meta_f + DEC_WARPS * maxg * 16 * 8 + 15) & ~15;
-  L.red = (L.xpre + 8 * MT * xp_stride * 4 + 15) & ~15;
-  const int red_bytes = WN < DEC_WARPS ? DEC_WARPS * 16 * 8 * MT * 4 : 0;
-  L.recv = (L.red + red_bytes + 15) & ~15;
+  L.ring = (((nbuf * m_rows + 1) * x_stride * 2) + 1023) & ~1023;
+  L.bars = L.ring + ring * STAGE_BYTES;
+  L.cnt = L.bars + (ring + 2) * 8;
+  L.meta = (L.cnt + (2 * ring + 2 + 1) * 4 + 15) & ~15;
+  L.xsum = L.meta + DEC_WARPS * maxg * 8 * 16;
+  L.recv = L.xsum + maxg * 8 * MT * 4;
   L.total = L.recv + S * slice * 8 * MT * 4;
   return L;
 }
@@ -128,6 +145,11 @@ __device__ __forceinline__ void bulk_copy_stream(uint32_t dst, const void* src, 
       : "memory");
 }
 
+// Bring [src, src + bytes) into L2 (16-byte aligned, a multiple of 16 bytes).
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ uint64_t evict_first_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -143,13 +165,28 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
-// Bounded wait; false when the limit ran out (the caller records the timeout).
-__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity) {
+// Bounded wait that also gives up at once when the CTA's abort flag is up;
+// false when it gave up (a timeout raises the flag and records the status).
+__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity,
+                                             volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) return false;
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+      *abort_flag = 1;
+      atomicExch(&g_device_status, W4_ERR_TIMEOUT);
+      return false;
+    }
+  }
   return true;
+}
+
+// Bounded wait used only while draining after an abort.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) return;
 }
 
 // D += A * B for one m16n8k16 tile, fp32 accumulate (non-volatile: the
@@ -171,208 +208,230 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 }
 
 // MT: token tiles of 8 (M <= 8 * MT). G64: every 64-row atom lies in one group.
-// With bf16 the MMA consumes the codes as 128 + q (exact in bf16) and each
-// group's partial sum is corrected by (128 + z) * sum(x) before scaling; with
-// fp16 the operand is q - z (exact) and needs no correction.
 #ifndef W4_DECODE_MIN_CTAS
-#define W4_DECODE_MIN_CTAS 3  // resident CTAs per SM the register budget is sized for (M <= 16)
+#define W4_DECODE_MIN_CTAS 3  // resident CTAs per SM the M <= 8 register budget is sized for
 #endif
+constexpr int decode_min_ctas(int MT) { return MT == 1 ? W4_DECODE_MIN_CTAS : 2; }
 
 template <int MT, bool BF16, bool G64>
-__global__ void __launch_bounds__(DEC_THREADS, MT <= 2 ? W4_DECODE_MIN_CTAS : 2) w4a16_decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
+    w4a16_decode_kernel(const DecodeParams p) {
   constexpr uint32_t MAGIC = Magic<BF16>::pair;
-  constexpr bool BIAS = BF16;
-  constexpr int SLOT = STAGE_ATOMS * ATOM_BYTES;
+  constexpr bool BIAS = BF16 && MT <= 2;             // 128 + q operand, group-sum correction
+  constexpr uint32_t ONES = BF16 ? 0x3F803F80u : 0x3C003C00u;  // 1.0 in both halves
   extern __shared__ __align__(1024) uint8_t smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gg = lane >> 2, t = lane & 3;
   const int S = gridDim.y;          // split-K factor == cluster size along y
   const int srank = blockIdx.y;     // rank inside the cluster
-  const int WN = p.WN, WK = DEC_WARPS / WN;
   const int MR = 8 * MT;
-  const int RINGN = p.ring;
-  const SmemLayout L = smem_layout(MT, p.M, p.x_stride, RINGN, p.maxg, p.xp_stride, WN, S, p.slice);
+  const int D = p.ring;
+  const int NB = p.nbuf;
+  const SmemLayout L = smem_layout(MT, p.M, p.x_stride, NB, D, p.maxg, S, p.slice);
 
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem + L.xs);
-  uint8_t* ring = smem + L.ring + warp * (RINGN * SLOT);
-  const uint32_t ring_s = smem_addr(ring);
-  const uint32_t bar0 = smem_addr(smem + L.bars + warp * RINGN * 8);
-  const uint32_t xbar = smem_addr(smem + L.bars + DEC_WARPS * RINGN * 8);
-  uint16_t* meta_s = reinterpret_cast<uint16_t*>(smem + L.meta_s) + warp * p.maxg * 16;
-  uint2* meta_z = reinterpret_cast<uint2*>(smem + L.meta_z) + warp * p.maxg;
-  // per (group, column): {scale, (128 + zero) * scale} in fp32, the two factors
-  // of the bf16 group correction
-  float2* meta_f = reinterpret_cast<float2*>(smem + L.meta_f) + warp * p.maxg * 16;
-  float* xpre = reinterpret_cast<float*>(smem + L.xpre);
-  float* red = reinterpret_cast<float*>(smem + L.red);
+  uint16_t* xzero = xs + (size_t)NB * p.M * p.x_stride;  // the zero row
+  const uint32_t ring_s = smem_addr(smem + L.ring);
+  const uint32_t full0 = smem_addr(smem + L.bars);       // + 8 * slot
+  const uint32_t xbar0 = full0 + 8 * D;                   // + 8 * buffer
+  int* cnt = reinterpret_cast<int*>(smem + L.cnt);        // [D] warps done with each slot
+  int* last_stage = cnt + D;                              // [D] last stage copied into each slot
+  int* last_chunk = last_stage + D;                       // [2] last x chunk copied into each buffer
+  volatile int* abort_flag = last_chunk + 2;
+  // per (group slot, lane group gg): {s, c, s', c'} for columns gg and gg + 8 of
+  // the warp's tile; c = (128 + z) * s with the bias operand, else the packed
+  // MAGIC + z halves (as bits)
+  float4* meta = reinterpret_cast<float4*>(smem + L.meta) + warp * p.maxg * 8;
+  float* xsum = reinterpret_cast<float*>(smem + L.xsum);  // [maxg][MR]
   float* recv = reinterpret_cast<float*>(smem + L.recv);
-  const int NCOL = 16 * WN;
-  const uint32_t gmask = p.gshift >= 31 ? 0x7FFFFFFFu : ((1u << p.gshift) - 1u);
+  constexpr int NCOL = 16 * DEC_WARPS;
 
-  // CTA K range in atoms
-  const int ka0 = (int)((long long)srank * p.A / S);
-  const int ka1 = (int)((long long)(srank + 1) * p.A / S);
+  // CTA K range: whole stages of SA k-atoms (the last one may be partial), so
+  // stage starts are aligned to SA k-atoms and a group of 128 rows or fewer
+  // never straddles a stage
+  const int nst_all = (p.A + SA - 1) / SA;
+  const int ka0 = min(p.A, (int)((long long)srank * nst_all / S) * SA);
+  const int ka1 = min(p.A, (int)((long long)(srank + 1) * nst_all / S) * SA);
+  const int NS = (ka1 - ka0 + SA - 1) / SA;
+  const int nchunks = (ka1 - ka0 + p.chunk_atoms - 1) / p.chunk_atoms;
 
-  const int wn = warp % WN, wk = warp / WN;
-  const int nt = blockIdx.x * WN + wn;
+  const int cgi = blockIdx.x;  // column group
+  const int nt = cgi * DEC_WARPS + warp;
   const bool has_cols = nt < p.N / 16;
-  const uint32_t* wsrc = p.qw + (size_t)nt * p.A * ATOM_WORDS;  // this tile's atom run
-  uint16_t* xzero = xs + (size_t)p.M * p.x_stride;              // the zero row
-
-  // Launched with programmatic stream serialization: the CTA may become
-  // resident while the previous kernel in the stream drains. It waits for that
-  // kernel (griddepcontrol.wait) before touching global memory, then lets the
-  // next kernel in the stream start its own launch.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;");
+  // the column group's run: k-atom a at byte offset a * KROW_BYTES
+  const uint8_t* gsrc = reinterpret_cast<const uint8_t*>(p.qw) + (size_t)cgi * p.A * KROW_BYTES;
   const uint64_t stream_policy = evict_first_policy();
+  const bool x_async = p.perm == nullptr;
 
-  if (lane == 0) {
-    for (int s = 0; s < RINGN; ++s) mbar_init(bar0 + 8 * s, 1);
-    if (warp == 0) mbar_init(xbar, 1);
-    fence_mbar_init();
-  }
-  for (int i = tid; i < p.x_stride / 8; i += DEC_THREADS)
-    reinterpret_cast<uint4*>(xzero)[i] = make_uint4(0, 0, 0, 0);
-  __syncthreads();
-
-  float acc[MT][4], tot[MT][4];
-#pragma unroll
-  for (int i = 0; i < MT; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = tot[i][j] = 0.f;
-  int hs = 0;           // chunk-relative half-atom index where the open group started
-  int g_first = 0;      // first group of this warp's run in the chunk
-  float s_lo = 0.f, s_hi = 0.f, zs_lo = 0.f, zs_hi = 0.f;
-  uint32_t zl = 0, zh = 0;
-  uint32_t it = 0;      // stages consumed by this warp
-  uint32_t rslot = 0;   // ring slot of the next stage to consume (== it % RINGN)
-  uint32_t rphase = 0;  // its mbarrier phase parity (== (it / RINGN) & 1)
-  uint32_t xphase = 0;  // phase of the x barrier
-  bool alive = true;    // false once a wait gave up
-
-  // tot += s * acc - (MAGIC + z) * s * (sum of x over halves [h0, h1)); acc = 0
-  // ((MAGIC + z) * s is exact in fp32: two 8-bit significands)
-  auto flush = [&](int h0, int h1) {
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      if constexpr (BIAS) {
-        const float* xp = xpre + (8 * mt + 2 * t) * p.xp_stride;
-        const float c0 = xp[h1] - xp[h0];
-        const float c1 = xp[p.xp_stride + h1] - xp[p.xp_stride + h0];
-        tot[mt][0] = fmaf(s_lo, acc[mt][0], fmaf(-zs_lo, c0, tot[mt][0]));
-        tot[mt][1] = fmaf(s_lo, acc[mt][1], fmaf(-zs_lo, c1, tot[mt][1]));
-        tot[mt][2] = fmaf(s_hi, acc[mt][2], fmaf(-zs_hi, c0, tot[mt][2]));
-        tot[mt][3] = fmaf(s_hi, acc[mt][3], fmaf(-zs_hi, c1, tot[mt][3]));
-      } else {
-        tot[mt][0] = fmaf(s_lo, acc[mt][0], tot[mt][0]);
-        tot[mt][1] = fmaf(s_lo, acc[mt][1], tot[mt][1]);
-        tot[mt][2] = fmaf(s_hi, acc[mt][2], tot[mt][2]);
-        tot[mt][3] = fmaf(s_hi, acc[mt][3], tot[mt][3]);
-      }
-      acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
-    }
+  // x of chunk ci into buffer ci % NB, completion on that buffer's barrier (tid 0)
+  auto issue_x = [&](int ci) {
+    const int c0 = ka0 + ci * p.chunk_atoms;
+    const int KC = (min(ka1, c0 + p.chunk_atoms) - c0) * ATOM_K;
+    const int b = NB == 2 ? (ci & 1) : 0;
+    uint16_t* dst = xs + (size_t)b * p.M * p.x_stride;
+    last_chunk[b] = ci;
+    mbar_arrive_expect_tx(xbar0 + 8 * b, (uint32_t)(p.M * KC * 2));
+    for (int m = 0; m < p.M; ++m)
+      bulk_copy(smem_addr(dst + (size_t)m * p.x_stride), p.x + (size_t)m * p.K + c0 * ATOM_K,
+                (uint32_t)(KC * 2), xbar0 + 8 * b);
   };
-  // scale / zero registers for group gi (staged in shared memory)
-  auto open_group = [&](int gi) {
-    const int gl = gi - g_first;
-    const float2 f_lo = meta_f[gl * 16 + gg], f_hi = meta_f[gl * 16 + gg + 8];
-    s_lo = f_lo.x;
-    zs_lo = f_lo.y;
-    s_hi = f_hi.x;
-    zs_hi = f_hi.y;
-    if constexpr (!BIAS) {
-      const uint2 zw = meta_z[gl];
-      const uint32_t z0 = (zw.x >> (4 * gg)) & 0xF;
-      const uint32_t z1 = (zw.y >> (4 * gg)) & 0xF;
-      zl = MAGIC | z0 | (z0 << 16);
-      zh = MAGIC | z1 | (z1 << 16);
-    }
+  // stage j (k-atoms [ka0 + j*SA, ...)) into ring slot j % D (one thread)
+  auto issue_stage = [&](int j) {
+    const int a = ka0 + j * SA;
+    const uint32_t bytes = (uint32_t)min(SA, ka1 - a) * KROW_BYTES;
+    const int slot = j % D;
+    last_stage[slot] = j;
+    mbar_arrive_expect_tx(full0 + 8 * slot, bytes);
+    bulk_copy_stream(ring_s + slot * STAGE_BYTES, gsrc + (size_t)a * KROW_BYTES, bytes,
+                     full0 + 8 * slot, stream_policy);
+    // stage j + pf into L2 (stages below D + pf were prefetched at the start)
+    const int pa = a + p.pf * SA;
+    if (p.pf > 0 && pa < ka1 && j >= D)
+      prefetch_l2(gsrc + (size_t)pa * KROW_BYTES, (uint32_t)min(SA, ka1 - pa) * KROW_BYTES);
   };
-  // expand one group's 16 scales and 16 zeros into meta_f
-  auto stage_group_f = [&](int gl, const uint4 a, const uint4 b, const uint2 z) {
+  // one group's 16 scales and 16 zeros (of this warp's tile) into its 8 meta entries
+  auto stage_meta = [&](int gl, const uint4 a, const uint4 b, const uint2 z) {
     const uint32_t sv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const uint16_t sb = (uint16_t)(sv[c >> 1] >> (16 * (c & 1)));
-      const float sf = half_bits_to_float<BF16>(sb);
-      const uint32_t zc = ((c < 8 ? z.x : z.y) >> (4 * (c & 7))) & 0xF;
-      meta_f[gl * 16 + c] = make_float2(sf, (float)(128 + zc) * sf);
+    for (int c = 0; c < 8; ++c) {
+      const float s_lo = half_bits_to_float<BF16>((uint16_t)(sv[c >> 1] >> (16 * (c & 1))));
+      const float s_hi = half_bits_to_float<BF16>((uint16_t)(sv[4 + (c >> 1)] >> (16 * (c & 1))));
+      const uint32_t z_lo = (z.x >> (4 * c)) & 0xF;
+      const uint32_t z_hi = (z.y >> (4 * c)) & 0xF;
+      float4 e;
+      e.x = s_lo;
+      e.z = s_hi;
+      if constexpr (BIAS) {
+        e.y = (float)(128 + z_lo) * s_lo;
+        e.w = (float)(128 + z_hi) * s_hi;
+      } else {
+        e.y = __uint_as_float(MAGIC | z_lo | (z_lo << 16));
+        e.w = __uint_as_float(MAGIC | z_hi | (z_hi << 16));
+      }
+      meta[gl * 8 + c] = e;
     }
   };
-
-  for (int c0 = ka0; c0 < ka1; c0 += p.chunk_atoms) {
+  // scales / zeros of the groups of chunk ci for this warp's tile; in the first
+  // chunk the ring fill waits until every warp has issued these loads, so they
+  // are not queued behind the weight stream
+  auto stage_chunk_meta = [&](int ci) {
+    const int c0 = ka0 + ci * p.chunk_atoms;
     const int c1 = min(ka1, c0 + p.chunk_atoms);
-    const int kx0 = c0 * ATOM_K;
-    const int KC = (c1 - c0) * ATOM_K;
-    const int wa0 = c0 + (int)((long long)wk * (c1 - c0) / WK);
-    const int wa1 = c0 + (int)((long long)(wk + 1) * (c1 - c0) / WK);
-    const int n_atoms = (has_cols && alive) ? wa1 - wa0 : 0;
-    const int n_stages = (n_atoms + STAGE_ATOMS - 1) / STAGE_ATOMS;
-    const bool x_async = p.perm == nullptr;
-
-    // Stage j of this chunk goes to ring slot (it + j) % RINGN, where `it` is
-    // the warp's consumed-stage count when the chunk starts.
-    auto issue = [&](int j, uint32_t slot) {
-      const int a = wa0 + j * STAGE_ATOMS;
-      const uint32_t bytes = (uint32_t)min(STAGE_ATOMS, wa1 - a) * ATOM_BYTES;
-      mbar_arrive_expect_tx(bar0 + 8 * slot, bytes);
-      bulk_copy_stream(ring_s + slot * SLOT, wsrc + (size_t)a * ATOM_WORDS, bytes, bar0 + 8 * slot,
-                       stream_policy);
-    };
-
-    // 1) the loads that gate the first MMA go first: x, then scales / zeros
-    if (x_async && tid == 0) {
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(xbar, (uint32_t)(p.M * KC * 2));
-      for (int m = 0; m < p.M; ++m)
-        bulk_copy(smem_addr(xs + (size_t)m * p.x_stride), p.x + (size_t)m * p.K + kx0,
-                  (uint32_t)(KC * 2), xbar);
-    }
-    g_first = (wa0 * ATOM_K) >> p.gshift;
-    const int ng = n_atoms > 0 ? ((wa1 * ATOM_K - 1) >> p.gshift) - g_first + 1 : 0;
+    const int g_first = (c0 * ATOM_K) >> p.gshift;
+    const int ng = ((c1 * ATOM_K - 1) >> p.gshift) - g_first + 1;
     uint4 ms0 = make_uint4(0, 0, 0, 0), ms1 = ms0;
     uint2 mz = make_uint2(0, 0);
-    if (lane < ng) {
+    const bool mine = has_cols && lane < ng;
+    if (mine) {
       const int gi = g_first + lane;
       const uint4* sp = reinterpret_cast<const uint4*>(p.scales + (size_t)gi * p.N + nt * 16);
       ms0 = __ldg(sp);
       ms1 = __ldg(sp + 1);
       mz = __ldg(reinterpret_cast<const uint2*>(p.zeros + (size_t)gi * (p.N / 8) + nt * 2));
     }
-    // 2) then the weight stream
-    if (lane == 0 && n_stages > 0) {
-      fence_proxy_async_smem();  // earlier reads of the ring precede these copies
-      uint32_t sl = rslot;
-      for (int j = 0; j < min(RINGN, n_stages); ++j) {
-        issue(j, sl);
-        sl = (sl + 1 == (uint32_t)RINGN) ? 0u : sl + 1;
+    if (ci == 0) {
+      __syncthreads();  // every warp has issued its gating loads
+      if (tid == 0) {
+        for (int j = 0; j < min(D, NS); ++j) issue_stage(j);
+        // and the pf stages beyond the ring into L2
+        const int a0 = ka0 + min(D, NS) * SA, a1 = min(ka1, ka0 + (D + p.pf) * SA);
+        if (a1 > a0)
+          prefetch_l2(gsrc + (size_t)a0 * KROW_BYTES, (uint32_t)(a1 - a0) * KROW_BYTES);
       }
     }
-    // 3) scales / zeros to shared memory (groups beyond 32 per warp: direct)
-    if (lane < ng) {
-      uint4* sd = reinterpret_cast<uint4*>(meta_s + lane * 16);
-      sd[0] = ms0;
-      sd[1] = ms1;
-      meta_z[lane] = mz;
-      stage_group_f(lane, ms0, ms1, mz);
-    }
-    for (int gl = lane + 32; gl < ng; gl += 32) {
+    if (mine) stage_meta(lane, ms0, ms1, mz);
+    for (int gl = lane + 32; has_cols && gl < ng; gl += 32) {
       const int gi = g_first + gl;
       const uint4* sp = reinterpret_cast<const uint4*>(p.scales + (size_t)gi * p.N + nt * 16);
-      uint4* sd = reinterpret_cast<uint4*>(meta_s + gl * 16);
-      const uint4 a = __ldg(sp), b = __ldg(sp + 1);
-      const uint2 z = __ldg(reinterpret_cast<const uint2*>(p.zeros + (size_t)gi * (p.N / 8) + nt * 2));
-      sd[0] = a;
-      sd[1] = b;
-      meta_z[gl] = z;
-      stage_group_f(gl, a, b, z);
+      const uint4 a = __ldg(sp), bb = __ldg(sp + 1);
+      const uint2 z =
+          __ldg(reinterpret_cast<const uint2*>(p.zeros + (size_t)gi * (p.N / 8) + nt * 2));
+      stage_meta(gl, a, bb, z);
     }
+  };
+
+  // ---- before the dependency wait: everything that does not read x ------------
+  // The weights, scales and zeros are read here, before the kernel waits for its
+  // predecessor on the stream: the library's contract is that they are not
+  // written by the kernel launched just before the GEMM (the repack entry points
+  // end with an empty kernel for that reason).
+  if (tid == 0) {
+    for (int s = 0; s < D; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      cnt[s] = 0;
+      last_stage[s] = -1;
+    }
+    for (int b = 0; b < NB; ++b) mbar_init(xbar0 + 8 * b, 1);
+    last_chunk[0] = last_chunk[1] = -1;
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  for (int i = tid; i < p.x_stride / 8; i += DEC_THREADS)
+    reinterpret_cast<uint4*>(xzero)[i] = make_uint4(0, 0, 0, 0);
+  __syncthreads();  // barrier initialisation, counters and the zero row
+  if (nchunks > 0) stage_chunk_meta(0);
+
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (tid == 0 && x_async && nchunks > 0) {
+    issue_x(0);
+    if (NB == 2 && nchunks > 1) issue_x(1);
+  }
+
+  float acc[MT][4], tot[MT][4];
+#pragma unroll
+  for (int i = 0; i < MT; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = tot[i][j] = 0.f;
+  float4 gf = make_float4(0.f, 0.f, 0.f, 0.f);  // factors of the open group
+  int gslot = -1;                               // its slot in meta / xsum (-1: none open)
+  uint32_t rslot = 0, rphase = 0;               // ring slot of the next stage, its parity
+
+  // tot += s * acc - (128 + z) * s * sum(x) with the bias operand, else s * acc; acc = 0
+  // ((128 + z) * s is exact in fp32: two 8-bit significands)
+  auto flush = [&]() {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      if constexpr (BIAS) {
+        const float2 xg = *reinterpret_cast<const float2*>(xsum + gslot * MR + 8 * mt + 2 * t);
+        tot[mt][0] = fmaf(gf.x, acc[mt][0], fmaf(-gf.y, xg.x, tot[mt][0]));
+        tot[mt][1] = fmaf(gf.x, acc[mt][1], fmaf(-gf.y, xg.y, tot[mt][1]));
+        tot[mt][2] = fmaf(gf.z, acc[mt][2], fmaf(-gf.w, xg.x, tot[mt][2]));
+        tot[mt][3] = fmaf(gf.z, acc[mt][3], fmaf(-gf.w, xg.y, tot[mt][3]));
+      } else {
+        tot[mt][0] = fmaf(gf.x, acc[mt][0], tot[mt][0]);
+        tot[mt][1] = fmaf(gf.x, acc[mt][1], tot[mt][1]);
+        tot[mt][2] = fmaf(gf.z, acc[mt][2], tot[mt][2]);
+        tot[mt][3] = fmaf(gf.z, acc[mt][3], tot[mt][3]);
+      }
+      acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+    }
+  };
+  // close the open group (if any) and open the next one
+  auto next_group = [&]() {
+    if (gslot >= 0) flush();
+    ++gslot;
+    gf = meta[gslot * 8 + gg];
+  };
+
+  for (int ci = 0; ci < nchunks; ++ci) {
+    const int c0 = ka0 + ci * p.chunk_atoms;
+    const int c1 = min(ka1, c0 + p.chunk_atoms);
+    const int KC = (c1 - c0) * ATOM_K;
+    const int b = NB == 2 ? (ci & 1) : 0;
+    const int g_first = (c0 * ATOM_K) >> p.gshift;
+    const int ng = ((c1 * ATOM_K - 1) >> p.gshift) - g_first + 1;
+    const bool live = !*abort_flag;
+
+    // 1) scales / zeros (the first chunk's were staged before the wait)
+    if (ci > 0 && live) stage_chunk_meta(ci);
+    // 2) x of this chunk
+    uint16_t* xb = xs + (size_t)b * p.M * p.x_stride;
     if (!x_async) {
       // act-order: gather x[:, perm] with plain loads
       const int chunks = KC / 8;
-      for (int i = tid; i < p.M * chunks; i += DEC_THREADS) {
+      const int kx0 = c0 * ATOM_K;
+      for (int i = tid; live && i < p.M * chunks; i += DEC_THREADS) {
         const int m = i / chunks, c = i - m * chunks;
         const uint16_t* xr = p.x + (size_t)m * p.K;
         uint16_t h[8];
@@ -383,157 +442,180 @@ __global__ void __launch_bounds__(DEC_THREADS, MT <= 2 ? W4_DECODE_MIN_CTAS : 2)
         v.y = h[2] | ((uint32_t)h[3] << 16);
         v.z = h[4] | ((uint32_t)h[5] << 16);
         v.w = h[6] | ((uint32_t)h[7] << 16);
-        *reinterpret_cast<uint4*>(xs + (size_t)m * p.x_stride + 8 * c) = v;
+        *reinterpret_cast<uint4*>(xb + (size_t)m * p.x_stride + 8 * c) = v;
       }
-      __syncthreads();
-    } else {
-      if (!bounded_wait(xbar, xphase & 1)) {
-        if (tid == 0) atomicExch(&g_device_status, W4_ERR_TIMEOUT);
-        alive = false;
-      }
-      ++xphase;
+      if constexpr (BIAS) __syncthreads();  // the sums below read every warp's rows
+    } else if (live) {
+      bounded_wait(xbar0 + 8 * b, (uint32_t)((NB == 2 ? ci >> 1 : ci) & 1), abort_flag);
     }
-
-    // 4) prefix sums of x over 32-row halves (bf16 zero correction), one token
-    //    row per warp at a time, lanes over halves
-    const int n32 = KC / 32;
+    // 3) per-group sums of x (bias operand): warp w takes group slots w, w + 8, ...
+    //    and runs the 32-row halves of the group's part of this chunk through MMAs
+    //    whose A operand is all ones (four independent accumulator chains)
     if constexpr (BIAS) {
-      for (int m = warp; m < MR; m += DEC_WARPS) {
-        float* xp = xpre + m * p.xp_stride;
-        float carry = 0.f;
-        if (lane == 0) xp[0] = 0.f;
-        for (int h0 = 0; h0 < n32; h0 += 32) {
-          const int hh = h0 + lane;
-          float sum = 0.f;
-          if (m < p.M && hh < n32) {
-            const uint4* xr = reinterpret_cast<const uint4*>(xs + (size_t)m * p.x_stride + 32 * hh);
+      for (int gl = warp; gl < ng; gl += DEC_WARPS) {
+        const int gi = g_first + gl;
+        const int r0 = max(c0 * ATOM_K, p.gshift >= 31 ? 0 : gi << p.gshift);
+        const int r1 = min(c1 * ATOM_K, p.gshift >= 31 ? p.K : (gi + 1) << p.gshift);
+        float sacc[4][MT][4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const uint4 v = xr[q];
-              const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                sum += __uint_as_float(wv[e] << 16) + __uint_as_float(wv[e] & 0xFFFF0000u);
+          for (int mt = 0; mt < MT; ++mt)
+            sacc[c][mt][0] = sacc[c][mt][1] = sacc[c][mt][2] = sacc[c][mt][3] = 0.f;
+        for (int r = r0; r < r1; r += 128) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            if (r + 32 * c < r1) {
+#pragma unroll
+              for (int mt = 0; mt < MT; ++mt) {
+                const int row = 8 * mt + gg;
+                const uint16_t* xr = row < p.M ? xb + (size_t)row * p.x_stride : xzero;
+                const uint4 xf =
+                    *reinterpret_cast<const uint4*>(xr + (r + 32 * c - c0 * ATOM_K) + 8 * t);
+                mma16816<BF16>(sacc[c][mt], ONES, ONES, ONES, ONES, xf.x, xf.y);
+                mma16816<BF16>(sacc[c][mt], ONES, ONES, ONES, ONES, xf.z, xf.w);
+              }
             }
           }
+        }
+        if (gg == 0) {
 #pragma unroll
-          for (int d = 1; d < 32; d <<= 1) {
-            const float v = __shfl_up_sync(0xFFFFFFFFu, sum, d);
-            if (lane >= d) sum += v;
-          }
-          if (hh < n32) xp[hh + 1] = carry + sum;
-          carry += __shfl_sync(0xFFFFFFFFu, sum, 31);
+          for (int mt = 0; mt < MT; ++mt)
+            *reinterpret_cast<float2*>(xsum + gl * MR + 8 * mt + 2 * t) =
+                make_float2((sacc[0][mt][0] + sacc[1][mt][0]) + (sacc[2][mt][0] + sacc[3][mt][0]),
+                            (sacc[0][mt][1] + sacc[1][mt][1]) + (sacc[2][mt][1] + sacc[3][mt][1]));
         }
       }
     }
-    __syncthreads();  // x prefix sums and every warp's scale / zero stage are ready
+    __syncthreads();  // x, the group sums and every warp's scale / zero stage are ready
 
-    // 5) consume the ring. Shared-memory operands are addressed with 32-bit
-    //    shared-window addresses: per stage one base for the weights and one per
-    //    token tile for x, with constant offsets inside the stage.
-    uint32_t xa[MT];  // this lane's x row (or the zero row) at the warp's first atom, column 8t
+    // 4) consume this chunk's stages. Shared-memory operands are addressed with
+    //    32-bit shared-window addresses with constant offsets inside a stage.
+    uint32_t xa[MT];  // this lane's x row (or the zero row) at the chunk's first atom, column 8t
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
       const int row = 8 * mt + gg;
-      xa[mt] = smem_addr(row < p.M ? xs + (size_t)row * p.x_stride : xzero) +
-               2u * (uint32_t)(8 * t + (wa0 - c0) * ATOM_K);
+      xa[mt] = smem_addr(row < p.M ? xb + (size_t)row * p.x_stride : xzero) + 16u * (uint32_t)t;
     }
-    hs = 2 * (wa0 - c0);
-    // atoms left before the next group boundary (groups of 64 rows or more)
+    // k-atoms per group (groups of 64 rows or more); a chunk that starts inside
+    // a group (only possible for groups longer than a stage) opens it at once
     const int apg = G64 ? (p.gshift >= 31 ? (1 << 30) : (1 << (p.gshift - 6))) : 1;
-    int gleft = G64 ? apg - (wa0 & (apg - 1)) : 0;
-    if (n_atoms > 0) open_group((wa0 * ATOM_K) >> p.gshift);
+    gslot = -1;
+    if (has_cols && G64 && (c0 & (apg - 1)) != 0) next_group();
 
-    // one atom: 64 rows x 16 columns, four m16n8k16 MMAs per token tile;
-    // xo = byte offset of the atom's x columns from xa
-    auto atom = [&](int a, const uint4 w, const uint32_t xo) {
+    // one half atom (32 rows x 16 columns): two k-steps, one x load and two MMAs
+    // per token tile; xo = byte offset of the atom's x columns from xa
+    auto half_atom = [&](const uint32_t wlo, const uint32_t whi, const uint32_t xo) {
+      uint32_t af[2][4];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if constexpr (G64) {
-          if (h == 0 && gleft == 0) {  // a group starts at this atom
-            const int hcur = 2 * (a - c0);
-            flush(hs, hcur);
-            hs = hcur;
-            open_group((a * ATOM_K) >> p.gshift);
-            gleft = apg;
-          }
-        } else {
-          const uint32_t kabs = (uint32_t)(a * ATOM_K + 32 * h);
-          if ((kabs & gmask) == 0) {
-            const int hcur = 2 * (a - c0) + h;
-            flush(hs, hcur);
-            hs = hcur;
-            open_group((int)(kabs >> p.gshift));
-          }
-        }
-        const uint32_t wlo = h ? w.z : w.x;  // column gg
-        const uint32_t whi = h ? w.w : w.y;  // column gg + 8
-        uint4 xf[MT];
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) xf[mt] = lds128(xa[mt] + xo + 64u * h);
-#pragma unroll
-        for (int step = 0; step < 2; ++step) {
-          const int sh = 8 * step;
-          uint32_t a0 = lop3_and_or(wlo >> sh, 0x000F000Fu, MAGIC);
-          uint32_t a2 = lop3_and_or(wlo >> (sh + 4), 0x000F000Fu, MAGIC);
-          uint32_t a1 = lop3_and_or(whi >> sh, 0x000F000Fu, MAGIC);
-          uint32_t a3 = lop3_and_or(whi >> (sh + 4), 0x000F000Fu, MAGIC);
-          if constexpr (!BIAS) {
-            a0 = sub_x2<BF16>(a0, zl);
-            a2 = sub_x2<BF16>(a2, zl);
-            a1 = sub_x2<BF16>(a1, zh);
-            a3 = sub_x2<BF16>(a3, zh);
-          }
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            const uint32_t b0 = step ? xf[mt].z : xf[mt].x;
-            const uint32_t b1 = step ? xf[mt].w : xf[mt].y;
-            mma16816<BF16>(acc[mt], a0, a1, a2, a3, b0, b1);
-          }
+      for (int step = 0; step < 2; ++step) {
+        const int sh = 8 * step;
+        af[step][0] = lop3_and_or(wlo >> sh, 0x000F000Fu, MAGIC);
+        af[step][2] = lop3_and_or(wlo >> (sh + 4), 0x000F000Fu, MAGIC);
+        af[step][1] = lop3_and_or(whi >> sh, 0x000F000Fu, MAGIC);
+        af[step][3] = lop3_and_or(whi >> (sh + 4), 0x000F000Fu, MAGIC);
+        if constexpr (!BIAS) {
+          const uint32_t zl = __float_as_uint(gf.y), zh = __float_as_uint(gf.w);
+          af[step][0] = sub_x2<BF16>(af[step][0], zl);
+          af[step][2] = sub_x2<BF16>(af[step][2], zl);
+          af[step][1] = sub_x2<BF16>(af[step][1], zh);
+          af[step][3] = sub_x2<BF16>(af[step][3], zh);
         }
       }
-      if constexpr (G64) --gleft;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const uint4 xf = lds128(xa[mt] + xo);
+        mma16816<BF16>(acc[mt], af[0][0], af[0][1], af[0][2], af[0][3], xf.x, xf.y);
+        mma16816<BF16>(acc[mt], af[1][0], af[1][1], af[1][2], af[1][3], xf.z, xf.w);
+      }
+    };
+    // one atom (64 rows x 16 columns); `start` says whether a group starts here
+    auto atom = [&](const uint4 w, const uint32_t xo, const bool start) {
+      if constexpr (G64) {
+        if (start) next_group();
+        half_atom(w.x, w.y, xo);
+        half_atom(w.z, w.w, xo + 64u);
+      } else {  // groups of 32 rows: each half atom is a group
+        next_group();
+        half_atom(w.x, w.y, xo);
+        next_group();
+        half_atom(w.z, w.w, xo + 64u);
+      }
+    };
+    // a full stage with group starts at compile-time positions: every P-th atom
+    // (P = 1, 2), or (P = 0) at most one, at the first atom
+    auto full_stage = [&](const uint32_t st, const uint32_t xo, const int a_base, auto P) {
+      constexpr int PP = decltype(P)::value;
+      const bool first = (a_base & (apg - 1)) == 0;
+#pragma unroll
+      for (int u = 0; u < SA; ++u) {
+        const bool start = PP == 0 ? (u == 0 && first) : (u % PP == 0);
+        atom(lds128(st + u * KROW_BYTES), xo + u * (ATOM_K * 2), start);
+      }
     };
 
-    const uint32_t wlane = ring_s + (uint32_t)lane * 16u;
-    for (int j = 0; j < n_stages; ++j) {
-      const uint32_t slot = rslot;
-      if (!bounded_wait(bar0 + 8 * slot, rphase)) {
-        // give up: record it, let the copies in flight land, stop streaming
-        if (lane == 0) atomicExch(&g_device_status, W4_ERR_TIMEOUT);
-        const int in_flight = min(RINGN, n_stages - j);
-        for (int q = 0; q < in_flight; ++q)
-          bounded_wait(bar0 + 8 * ((it + q) % RINGN), ((it + q) / RINGN) & 1);
-        alive = false;
-        break;
-      }
-      const uint32_t st = wlane + slot * SLOT;
-      const int a_base = wa0 + j * STAGE_ATOMS;
-      const uint32_t xo = (uint32_t)j * (STAGE_ATOMS * ATOM_K * 2);
-      if (a_base + STAGE_ATOMS <= wa1) {
-        uint4 w[STAGE_ATOMS];
-#pragma unroll
-        for (int u = 0; u < STAGE_ATOMS; ++u) w[u] = lds128(st + u * ATOM_BYTES);
-#pragma unroll
-        for (int u = 0; u < STAGE_ATOMS; ++u) atom(a_base + u, w[u], xo + u * (ATOM_K * 2));
-      } else {
-        for (int u = 0; u < wa1 - a_base; ++u)
-          atom(a_base + u, lds128(st + u * ATOM_BYTES), xo + u * (ATOM_K * 2));
+    const int j0 = (c0 - ka0) / SA;
+    const int j1 = min(NS, (c1 - ka0 + SA - 1) / SA);
+    const uint32_t wbase = ring_s + (uint32_t)warp * ATOM_BYTES + (uint32_t)lane * 16u;
+    for (int j = j0; j < j1; ++j) {
+      const bool ready = live && bounded_wait(full0 + 8 * rslot, rphase, abort_flag);
+      if (ready && has_cols) {
+        const int a_base = ka0 + j * SA;
+        const uint32_t st = wbase + rslot * STAGE_BYTES;
+        const uint32_t xo = (uint32_t)(a_base - c0) * (ATOM_K * 2);
+        if (a_base + SA <= c1) {
+          if (!G64 || apg >= SA)
+            full_stage(st, xo, a_base, std::integral_constant<int, 0>());
+          else if (apg == 2)
+            full_stage(st, xo, a_base, std::integral_constant<int, 2>());
+          else if (apg == 1)
+            full_stage(st, xo, a_base, std::integral_constant<int, 1>());
+          else
+            full_stage(st, xo, a_base, std::integral_constant<int, 4>());
+        } else {
+          for (int u = 0; u < c1 - a_base; ++u)
+            atom(lds128(st + u * KROW_BYTES), xo + u * (ATOM_K * 2),
+                 ((a_base + u) & (apg - 1)) == 0);
+        }
       }
       __syncwarp();
-      if (lane == 0 && j + RINGN < n_stages) {
-        fence_proxy_async_smem();  // the reads of this slot precede the next copy into it
-        issue(j + RINGN, slot);    // slot == (it_at_chunk_start + j + RINGN) % RINGN
+      // release the slot; the last of the eight warps refills it with stage j + D
+      if (lane == 0 && ready) {
+        __threadfence_block();  // this warp's reads of the slot precede its count
+        const int old = atomicAdd(&cnt[rslot], 1);
+        if ((old & (DEC_WARPS - 1)) == DEC_WARPS - 1 && j + D < NS) {
+          __threadfence_block();     // every warp's reads precede the refill
+          fence_proxy_async_smem();  // ... which the async proxy performs
+          issue_stage(j + D);
+        }
       }
-      ++it;
-      if (++rslot == (uint32_t)RINGN) {
+      if (++rslot == (uint32_t)D) {
         rslot = 0;
         rphase ^= 1u;
       }
     }
-    // the prefix sums and the scale / zero stage belong to this chunk: close the group
-    if (n_atoms > 0) flush(hs, 2 * (wa1 - c0));
-    __syncthreads();  // the next chunk overwrites xs, xpre and the scale / zero stage
+    // the scale / zero stage and the sums belong to this chunk: close the group
+    if (has_cols && gslot >= 0) flush();
+    __syncthreads();  // the chunk's x buffer, sums and scale / zero stage are free again
+    if (x_async && tid == 0 && NB == 2 && ci + 2 < nchunks && !*abort_flag) {
+      fence_proxy_async_smem();  // the reads of the buffer precede the copy into it
+      issue_x(ci + 2);
+    }
+  }
+  // the weight stream is done: the next kernel on the stream may start launching
+  asm volatile("griddepcontrol.launch_dependents;");
+
+  // ---- after an abort: let every copy in flight land before the CTA exits ------
+  if (*abort_flag) {
+    __syncthreads();
+    if (tid == 0) {
+      for (int s = 0; s < D; ++s)
+        if (last_stage[s] >= 0) drain_wait(full0 + 8 * s, (uint32_t)((last_stage[s] / D) & 1));
+      for (int bb = 0; bb < NB; ++bb)
+        if (last_chunk[bb] >= 0)
+          drain_wait(xbar0 + 8 * bb,
+                     (uint32_t)((NB == 2 ? last_chunk[bb] >> 1 : last_chunk[bb]) & 1));
+    }
   }
 
   // ---- split-K: push partial sums to the CTA that owns each output column -------
@@ -544,11 +626,11 @@ __global__ void __launch_bounds__(DEC_THREADS, MT <= 2 ? W4_DECODE_MIN_CTAS : 2)
     float* dst = cluster.map_shared_rank(recv, owner);
     dst[((size_t)srank * SL + (col - owner * SL)) * MR + m] = v;
   };
-  if (WK == 1) {
+  if (has_cols) {
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
       const int m0 = 8 * mt + 2 * t;
-      const int ca = wn * 16 + gg, cb = ca + 8;
+      const int ca = warp * 16 + gg, cb = ca + 8;
       if (m0 < p.M) {
         push(ca, m0, tot[mt][0]);
         push(cb, m0, tot[mt][2]);
@@ -558,24 +640,6 @@ __global__ void __launch_bounds__(DEC_THREADS, MT <= 2 ? W4_DECODE_MIN_CTAS : 2)
         push(cb, m0 + 1, tot[mt][3]);
       }
     }
-  } else {
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      const int m0 = 8 * mt + 2 * t;
-      float* r0 = red + ((size_t)wk * NCOL + wn * 16 + gg) * MR;
-      float* r1 = red + ((size_t)wk * NCOL + wn * 16 + gg + 8) * MR;
-      r0[m0] = tot[mt][0];
-      r0[m0 + 1] = tot[mt][1];
-      r1[m0] = tot[mt][2];
-      r1[m0 + 1] = tot[mt][3];
-    }
-    __syncthreads();
-    for (int o = tid; o < NCOL * p.M; o += DEC_THREADS) {
-      const int col = o / p.M, m = o - col * p.M;
-      float v = 0.f;
-      for (int q = 0; q < WK; ++q) v += red[((size_t)q * NCOL + col) * MR + m];
-      push(col, m, v);
-    }
   }
   cluster.sync();
   {
@@ -584,7 +648,7 @@ __global__ void __launch_bounds__(DEC_THREADS, MT <= 2 ? W4_DECODE_MIN_CTAS : 2)
     const int width = c_hi - c_lo;
     for (int o = tid; o < width * p.M; o += DEC_THREADS) {
       const int m = o / width, cl = o - m * width;
-      const int n = blockIdx.x * NCOL + c_lo + cl;
+      const int n = cgi * NCOL + c_lo + cl;
       if (n >= p.N) continue;
       float sum = 0.f;
       for (int r = 0; r < S; ++r) sum += recv[((size_t)r * SL + cl) * MR + m];
@@ -614,8 +678,9 @@ void* pick_kernel(int MT, bool bf16, bool g64) {
   }
 }
 
-// Raise a kernel's dynamic shared-memory limit once per (kernel, device); the
-// attribute call is then kept out of the launch path (and out of graph capture).
+// Raise a kernel's dynamic shared-memory limit (and allow clusters above the
+// portable size of 8) once per (kernel, device); the attribute calls are then
+// kept out of the launch path (and out of graph capture).
 cudaError_t ensure_smem(void* fn, size_t bytes) {
   static std::mutex mu;
   static std::unordered_map<uint64_t, size_t> done;
@@ -627,99 +692,136 @@ cudaError_t ensure_smem(void* fn, size_t bytes) {
   auto it = done.find(key);
   if (it != done.end() && it->second >= bytes) return cudaSuccess;
   e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e == cudaSuccess) done[key] = bytes;
   return e;
 }
 
-// Rows of x (per token) a CTA stages at a time.
-int max_rows_per_chunk(int M) {
-  const int rows = X_BUDGET / (M * 2);
-  return std::max(ATOM_K, (rows / ATOM_K) * ATOM_K);
-}
-
 struct DecodePlan {
-  int WN, S;
-  int ring, chunk_atoms, x_stride, maxg, xp_stride, slice;
+  int S;
+  int ring, pf, chunk_atoms, nbuf, x_stride, maxg, slice;
   SmemLayout L;
 };
 
-// Shared-memory plan of one launch shape.
-DecodePlan shape_plan(int WN, int S, int A, int Mc, int MT, int gshift, int ring) {
+// Shared-memory plan of one launch shape. x of the CTA's whole K range is
+// staged at once when it fits X_BUDGET; otherwise in chunks of a multiple of
+// SA k-atoms, double-buffered so the next chunk's x lands while the current
+// one is consumed.
+DecodePlan shape_plan(int S, int A, int Mc, int MT, int gshift, int ring) {
   DecodePlan d;
-  d.WN = WN;
   d.S = S;
   d.ring = ring;
-  const int cta_atoms = (A + S - 1) / S;
-  d.chunk_atoms = std::min(cta_atoms, max_rows_per_chunk(Mc) / ATOM_K);
+  d.pf = W4_DECODE_PF;
+  const int cta_atoms = ((A + SA - 1) / SA + S - 1) / S * SA;  // whole stages
+  if (cta_atoms * ATOM_K * Mc * 2 <= X_BUDGET) {
+    d.nbuf = 1;
+    d.chunk_atoms = cta_atoms;
+  } else {
+    d.nbuf = 2;
+    d.chunk_atoms = std::max(SA, X_BUDGET / 2 / (Mc * 2) / ATOM_K / SA * SA);
+  }
   d.x_stride = d.chunk_atoms * ATOM_K + 32;  // halves; row stride = 64 mod 128 bytes
-  const int WK = DEC_WARPS / WN;
-  const int warp_atoms = (d.chunk_atoms + WK - 1) / WK;
-  d.maxg = (gshift == 31) ? 1 : (warp_atoms * ATOM_K >> gshift) + 2;
-  d.xp_stride = 2 * d.chunk_atoms + 1;
-  d.slice = (16 * WN + S - 1) / S;
-  d.L = smem_layout(MT, Mc, d.x_stride, ring, d.maxg, d.xp_stride, WN, S, d.slice);
+  d.maxg = (gshift == 31) ? 1 : (d.chunk_atoms * ATOM_K >> gshift) + 2;
+  d.slice = (16 * DEC_WARPS + S - 1) / S;
+  d.L = smem_layout(MT, Mc, d.x_stride, d.nbuf, ring, d.maxg, S, d.slice);
   return d;
 }
 
-// Deepest ring (2..MAX_RING stages, no deeper than the warp's run) that keeps
-// `per_sm` CTAs resident.
-DecodePlan fit_ring(int WN, int S, int A, int Mc, int MT, int gshift, int per_sm, int smem_per_sm) {
-  const int WK = DEC_WARPS / WN;
-  const int warp_atoms = ((A + S - 1) / S + WK - 1) / WK;
-  const int need = std::max(2, std::min(MAX_RING, (warp_atoms + STAGE_ATOMS - 1) / STAGE_ATOMS));
-  DecodePlan d = shape_plan(WN, S, A, Mc, MT, gshift, 2);
+// Deepest ring (2..MAX_RING stages, no deeper than the CTA's stage count) that
+// keeps `per_sm` CTAs resident.
+DecodePlan fit_ring(int S, int A, int Mc, int MT, int gshift, int per_sm, int smem_per_sm) {
+  const int stages = ((A + SA - 1) / SA + S - 1) / S;
+  const int need = std::max(2, std::min(MAX_RING, stages));
+  DecodePlan d = shape_plan(S, A, Mc, MT, gshift, 2);
   for (int r = need; r >= 2; --r) {
-    d = shape_plan(WN, S, A, Mc, MT, gshift, r);
+    d = shape_plan(S, A, Mc, MT, gshift, r);
     if ((d.L.total + 1024) * per_sm <= smem_per_sm) break;
   }
   return d;
 }
 
-// Choose warps-along-N and the split-K factor with a small time model. A
-// wave of CTAs shares the HBM bandwidth among its members and pays a fixed
-// start-up / drain cost; a CTA streams at most ~1/16 of an SM's share alone
-// per warp, so fewer than two resident CTAs per SM leave bandwidth unused.
+// Choose the split-K factor (and with it the ring) with a small time model.
+// CTAs run in waves; each wave pays a fixed start-up / drain cost plus the
+// longer of its weight stream and its instruction stream. A CTA streams at
+// most the bytes it keeps in flight (its ring) per memory latency, and the
+// CTAs of an SM share that SM's part of the HBM bandwidth. Chunked x staging
+// adds a barrier per extra chunk.
 DecodePlan plan_decode(int N, int K, int Mc, int MT, int gshift, const DeviceInfo& info) {
-  const int NT = N / 16, A = K / ATOM_K;
-  const int reg_ctas = MT <= 2 ? W4_DECODE_MIN_CTAS : 2;
-  const double overhead = 2.5e-6, bw = 6.5e12;
+  const int NG = (N / 16 + DEC_WARPS - 1) / DEC_WARPS, A = K / ATOM_K;
+  const int reg_ctas = decode_min_ctas(MT);
+  const double overhead = 2.0e-6, bw = 6.6e12, lat = 1.5e-6, chunk_cost = 0.5e-6;
+  const double issue_rate = 4.0 * 1.9e9 * 0.6;         // warp instructions per second per SM
+  const double inst_per_atom = 40.0 + 10.0 * MT;
   const double sm_bw = bw / info.sm_count;
-  DecodePlan best = shape_plan(8, 1, A, Mc, MT, gshift, 2);
+  DecodePlan best = shape_plan(1, A, Mc, MT, gshift, 2);
   double best_t = 1e30;
-  for (int WN = 8; WN >= 1; WN >>= 1) {
-    const int WK = DEC_WARPS / WN;
-    const int cols = (NT + WN - 1) / WN;
-    for (int S = 1; S <= MAX_SPLIT && S <= A; ++S) {
-      if ((double)A / (S * WK) < 1.0) continue;
-      // three resident CTAs per SM (more warps to hide latency) when registers
-      // allow it and a ring of at least three stages still fits; else two
-      DecodePlan d = fit_ring(WN, S, A, Mc, MT, gshift, 2, info.smem_per_sm);
-      if (reg_ctas >= 3) {
-        const DecodePlan d3 = fit_ring(WN, S, A, Mc, MT, gshift, 3, info.smem_per_sm);
-        if (d3.ring >= 3 && (d3.L.total + 1024) * 3 <= info.smem_per_sm) d = d3;
-      }
-      const int smem_ctas = info.smem_per_sm / (d.L.total + 1024);
-      const int per_sm = std::max(1, std::min(reg_ctas, smem_ctas));
-      const long long slots = (long long)per_sm * info.sm_count;
-      long long left = (long long)cols * S;
-      const double cta_bytes = (double)(16 * WN) * ((double)A / S) * 32.0;  // 64 rows x 16 cols / 2
-      double t = 0.0;
-      while (left > 0) {
-        const long long now = std::min(left, slots);
-        const double per_sm_ctas = (double)now / info.sm_count;
-        // an SM streams at its share of HBM once it holds two CTAs
-        const double rate = sm_bw * std::min(1.0, per_sm_ctas / 2.0) / std::max(1.0, per_sm_ctas);
-        t += overhead + cta_bytes / rate;
-        left -= now;
-      }
-      t += 0.05e-6 * S;
-      if (t < best_t) {
-        best_t = t;
-        best = d;
-      }
+  const int nst_all = (A + SA - 1) / SA;
+  for (int S = 1; S <= MAX_SPLIT && S <= nst_all; ++S) {
+    DecodePlan d = fit_ring(S, A, Mc, MT, gshift, 2, info.smem_per_sm);
+    if (reg_ctas >= 3) {
+      const DecodePlan d3 = fit_ring(S, A, Mc, MT, gshift, 3, info.smem_per_sm);
+      if (d3.ring >= 3 && (d3.L.total + 1024) * 3 <= info.smem_per_sm) d = d3;
+    }
+    const int smem_ctas = info.smem_per_sm / (d.L.total + 1024);
+    const int per_sm = std::max(1, std::min(reg_ctas, smem_ctas));
+    const long long slots = (long long)per_sm * info.sm_count;
+    long long left = (long long)NG * S;
+    const double cta_atoms = (double)A / S;
+    const double cta_bytes = cta_atoms * KROW_BYTES;
+    const double cta_inflight = (double)d.ring * STAGE_BYTES;
+    const int nchunks = (int)((cta_atoms + d.chunk_atoms - 1) / d.chunk_atoms);
+    const double cta_inst = (double)DEC_WARPS * cta_atoms * inst_per_atom;
+    double t = 0.0;
+    while (left > 0) {
+      const long long now = std::min(left, slots);
+      const double c = std::max(1.0, (double)now / info.sm_count);  // CTAs sharing an SM
+      const double rate = std::min(sm_bw / c, cta_inflight / lat);
+      const double t_mem = cta_bytes / rate;
+      const double t_issue = cta_inst * c / issue_rate;
+      t += overhead + std::max(t_mem, t_issue) + (nchunks - 1) * chunk_cost;
+      left -= now;
+    }
+    t += 0.05e-6 * S;
+    if (t < best_t) {
+      best_t = t;
+      best = d;
     }
   }
   return best;
+}
+
+// Plans are cached per (device, shape): planning costs tens of microseconds of
+// host time, more than a decode launch.
+struct PlanKey {
+  int dev, N, K, Mc, gshift;
+  bool operator==(const PlanKey& o) const {
+    return dev == o.dev && N == o.N && K == o.K && Mc == o.Mc && gshift == o.gshift;
+  }
+};
+struct PlanKeyHash {
+  size_t operator()(const PlanKey& k) const {
+    uint64_t h = (uint64_t)k.dev * 0x9E3779B97F4A7C15ull;
+    h ^= (uint64_t)k.N + 0x7F4A7C15ull + (h << 6) + (h >> 2);
+    h ^= (uint64_t)k.K + 0x7F4A7C15ull + (h << 6) + (h >> 2);
+    h ^= (uint64_t)k.Mc + 0x7F4A7C15ull + (h << 6) + (h >> 2);
+    h ^= (uint64_t)k.gshift + 0x7F4A7C15ull + (h << 6) + (h >> 2);
+    return (size_t)h;
+  }
+};
+
+cudaError_t cached_plan(int N, int K, int Mc, int MT, int gshift, const DeviceInfo& info,
+                        DecodePlan* out) {
+  static std::mutex mu;
+  static std::unordered_map<PlanKey, DecodePlan, PlanKeyHash> plans;
+  int dev = 0;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const PlanKey key{dev, N, K, Mc, gshift};
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = plans.find(key);
+  if (it == plans.end()) it = plans.emplace(key, plan_decode(N, K, Mc, MT, gshift, info)).first;
+  *out = it->second;
+  return cudaSuccess;
 }
 
 int log2_exact(int v) {
@@ -741,7 +843,8 @@ cudaError_t launch_decode(const GemmArgs& a, cudaStream_t stream) {
   for (int r0 = 0; r0 < a.M; r0 += DECODE_MAX_M) {
     const int Mc = std::min(DECODE_MAX_M, a.M - r0);
     const int MT = Mc <= 8 ? 1 : Mc <= 16 ? 2 : Mc <= 32 ? 4 : 8;
-    const DecodePlan plan = plan_decode(a.N, a.K, Mc, MT, gshift, info);
+    DecodePlan plan;
+    if ((err = cached_plan(a.N, a.K, Mc, MT, gshift, info, &plan)) != cudaSuccess) return err;
     void* fn = pick_kernel(MT, a.bf16 != 0, g64);
     if ((err = ensure_smem(fn, plan.L.total)) != cudaSuccess) return err;
 
@@ -757,16 +860,16 @@ cudaError_t launch_decode(const GemmArgs& a, cudaStream_t stream) {
     p.K = a.K;
     p.gshift = gshift;
     p.A = A;
-    p.WN = plan.WN;
     p.ring = plan.ring;
+    p.pf = plan.pf;
     p.chunk_atoms = plan.chunk_atoms;
+    p.nbuf = plan.nbuf;
     p.x_stride = plan.x_stride;
     p.maxg = plan.maxg;
-    p.xp_stride = plan.xp_stride;
     p.slice = plan.slice;
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((a.N / 16 + plan.WN - 1) / plan.WN, plan.S, 1);
+    cfg.gridDim = dim3((a.N / 16 + DEC_WARPS - 1) / DEC_WARPS, plan.S, 1);
     cfg.blockDim = dim3(DEC_THREADS, 1, 1);
     cfg.dynamicSmemBytes = plan.L.total;
     cfg.stream = stream;

@@ -77,7 +77,7 @@ constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;  // 1 s per wait
 
 struct PrefillParams {
   CUtensorMap tm_a;  // x [M][K], box 64 x 128, 128-byte swizzle
-  CUtensorMap tm_p;  // TILE words as [N/16][K/64 * 128], box 128 x 16
+  CUtensorMap tm_p;  // TILE words as [N/128][K/64][8][128], box 128 x 8 x 1 x 2
   CUtensorMap tm_s;  // scales [G][N], box 256 x 2
   CUtensorMap tm_z;  // zeros [G][N/8], box 32 x 2
   uint16_t* y;
@@ -202,7 +202,8 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
           last_armed[s] = it;
           const int gi = (kb * BK) / p.group;
           tma_load_2d(sbase + OFF_A + s * A_BYTES, &p.tm_a, bars.full(s), kb * BK, m_blk * BM);
-          tma_load_2d(sbase + OFF_P + s * P_BYTES, &p.tm_p, bars.full(s), kb * 128, n_blk * (BN / 16));
+          // the 16 atoms (two column groups) of this N block at k-atom kb
+          tma_load_4d(sbase + OFF_P + s * P_BYTES, &p.tm_p, bars.full(s), 0, 0, kb, n_blk * (BN / 128));
           tma_load_2d(sbase + OFF_S + s * S_BYTES, &p.tm_s, bars.full(s), n_blk * BN, gi);
           tma_load_2d(sbase + OFF_Z + s * Z_SLOT, &p.tm_z, bars.full(s), n_blk * (BN / 8), gi);
         }
@@ -400,6 +401,21 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint6
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// TILE words viewed as [column group][k-atom][tile in group][word]: one box is
+// the 8 atoms of `box_groups` consecutive column groups at one k-atom.
+bool encode_tile_4d(CUtensorMap* map, const void* qw, int K, int N, uint32_t box_groups) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t A = (cuuint64_t)K / 64, NG = ((cuuint64_t)N + 127) / 128;
+  const cuuint64_t dims[4] = {128, 8, A, NG};
+  const cuuint64_t strides[3] = {512, 8 * 512, A * 8 * 512};
+  const cuuint32_t box[4] = {128, 8, 1, box_groups};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, const_cast<void*>(qw), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t ensure_prefill_smem(void* fn, int which, int bytes) {
   static std::mutex mu;
   static bool done[64][4] = {};
@@ -453,9 +469,7 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
   const int G = a.K / a.group;
   const CUtensorMapDataType act = a.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   bool ok = encode_2d(&p.tm_a, act, x, a.K, a.M, (uint64_t)a.K * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && encode_2d(&p.tm_p, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.qw, (uint64_t)(a.K / 64) * 128,
-                       a.N / 16, (uint64_t)(a.K / 64) * 512, 128, BN / 16,
-                       CU_TENSOR_MAP_SWIZZLE_NONE);
+  ok = ok && encode_tile_4d(&p.tm_p, a.qw, a.K, a.N, BN / 128);
   ok = ok && encode_2d(&p.tm_s, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.scales, a.N, G, (uint64_t)a.N * 2,
                        BN, 2, CU_TENSOR_MAP_SWIZZLE_NONE);
   ok = ok && encode_2d(&p.tm_z, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.zeros, a.N / 8, G,

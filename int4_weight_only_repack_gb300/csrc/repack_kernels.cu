@@ -49,9 +49,10 @@ __device__ void load_block_codes(int kind, const uint32_t* __restrict__ src,
       codes[kk][col] = (w >> (4 * (ks & 7))) & 0xF;
     }
   } else {
-    // TILE: eight atoms (n0/16 + i, k0/64), 128 words each
+    // TILE: the eight atoms of column group n0/128 at k-atom k0/64 are adjacent
     const int A = K / BK;
     const int kb = k0 / BK;
+    const uint32_t* grp = src + ((size_t)(n0 / BN) * A + kb) * 8 * 128;
     for (int i = tid; i < 8 * 128; i += BLOCK_THREADS) {
       const int at = i >> 7, wl = i & 127;
       if (at * 16 >= ncols) continue;
@@ -59,14 +60,16 @@ __device__ void load_block_codes(int kind, const uint32_t* __restrict__ src,
       const int gg = lane >> 2, t = lane & 3;
       const int col = at * 16 + gg + 8 * (j & 1);
       const int kk0 = 32 * (j >> 1) + 8 * t;
-      const uint32_t w = src[((size_t)(n0 / 16 + at) * A + kb) * 128 + wl];
+      const uint32_t w = grp[at * 128 + wl];
 #pragma unroll
       for (int e = 0; e < 8; ++e) codes[kk0 + e][col] = (w >> (4 * tile_nibble_pos(e))) & 0xF;
     }
   }
 }
 
-// Repack any source into the TILE layout. grid = (ceil(N/128), K/64).
+// Repack any source into the TILE layout. grid = (ceil(N/128), K/64): one block
+// writes the eight adjacent atoms of its column group at its k-atom (the atoms
+// of a partial last group beyond N are written as zeros).
 __global__ void __launch_bounds__(BLOCK_THREADS) to_tile_kernel(
     const uint32_t* __restrict__ src, int kind, const int32_t* __restrict__ perm,
     uint32_t* __restrict__ out, int K, int N) {
@@ -77,9 +80,13 @@ __global__ void __launch_bounds__(BLOCK_THREADS) to_tile_kernel(
   __syncthreads();
   const int A = K / BK;
   const int kb = blockIdx.y;
+  uint32_t* grp = out + ((size_t)blockIdx.x * A + kb) * 8 * 128;
   for (int i = threadIdx.x; i < 8 * 128; i += BLOCK_THREADS) {
     const int at = i >> 7, wl = i & 127;
-    if (at * 16 >= ncols) continue;
+    if (at * 16 >= ncols) {
+      grp[i] = 0u;
+      continue;
+    }
     const int lane = wl >> 2, j = wl & 3;
     const int gg = lane >> 2, t = lane & 3;
     const int col = at * 16 + gg + 8 * (j & 1);
@@ -87,7 +94,7 @@ __global__ void __launch_bounds__(BLOCK_THREADS) to_tile_kernel(
     uint32_t w = 0;
 #pragma unroll
     for (int e = 0; e < 8; ++e) w |= (uint32_t)codes[kk0 + e][col] << (4 * tile_nibble_pos(e));
-    out[((size_t)(n0 / 16 + at) * A + kb) * 128 + wl] = w;
+    grp[i] = w;
   }
 }
 
@@ -241,11 +248,18 @@ __global__ void __launch_bounds__(BLOCK_THREADS) dequant_kernel(
   }
 }
 
+__global__ void stream_fence_kernel() {}
+
 inline unsigned blocks_for(size_t n, int per = BLOCK_THREADS) {
   return (unsigned)((n + per - 1) / per);
 }
 
 }  // namespace
+
+cudaError_t launch_stream_fence(cudaStream_t s) {
+  stream_fence_kernel<<<1, 32, 0, s>>>();
+  return cudaGetLastError();
+}
 
 cudaError_t launch_awq_to_std(const int32_t* qweight, int32_t* qw_out, int K, int N,
                               cudaStream_t s) {

@@ -117,7 +117,7 @@ const char* w4_status_string(w4_status s) {
   }
 }
 
-int w4_abi_version(void) { return 1; }
+int w4_abi_version(void) { return 2; }
 
 w4_status w4_repack_sizes(int K, int N, int group, int layout, size_t* qw_bytes,
                           size_t* zeros_bytes, size_t* scales_bytes) {
@@ -125,7 +125,9 @@ w4_status w4_repack_sizes(int K, int N, int group, int layout, size_t* qw_bytes,
   if (st) return st;
   if ((st = check_layout_dims(K, N, layout))) return st;
   const size_t G = (size_t)K / resolve_group(group, K);
-  if (qw_bytes) *qw_bytes = (size_t)K * N / 2;
+  // TILE pads N to whole 128-column groups
+  const size_t n_store = layout == W4_LAYOUT_TILE ? ((size_t)N + 127) / 128 * 128 : (size_t)N;
+  if (qw_bytes) *qw_bytes = (size_t)K * n_store / 2;
   if (zeros_bytes) *zeros_bytes = G * N / 2;
   if (scales_bytes) *scales_bytes = G * N * 2;
   return W4_OK;
@@ -144,10 +146,12 @@ w4_status w4_repack_awq(const int32_t* qweight, const int32_t* qzeros, const voi
   const int g = resolve_group(group, K);
   const size_t G = (size_t)K / g;
   const size_t qw_b = (size_t)K * N / 2, z_b = G * N / 2, s_b = G * N * 2;
+  size_t qw_out_b = 0;
+  w4_repack_sizes(K, N, group, layout, &qw_out_b, nullptr, nullptr);
   const void* ins[3] = {qweight, qzeros, scales};
   const size_t in_b[3] = {qw_b, z_b, s_b};
   const void* outs[3] = {qw_out, zeros_out, scales_out};
-  const size_t out_b[3] = {qw_b, z_b, s_b};
+  const size_t out_b[3] = {qw_out_b, z_b, s_b};
   for (int i = 0; i < 3; ++i)
     for (int j = 0; j < 3; ++j)
       if (overlaps(outs[i], out_b[i], ins[j], in_b[j]) || (i != j && overlaps(outs[i], out_b[i], outs[j], out_b[j])))
@@ -157,7 +161,9 @@ w4_status w4_repack_awq(const int32_t* qweight, const int32_t* qzeros, const voi
   cudaError_t e = layout == W4_LAYOUT_STD ? launch_awq_to_std(qweight, qw_out, K, N, s)
                                           : launch_to_tile(qweight, 1, nullptr, qw_out, K, N, s);
   if (e != cudaSuccess) return W4_ERR_CUDA;
-  return from_cuda(launch_meta(qzeros, 1, scales, zeros_out, scales_out, (int)G, N, s));
+  if (launch_meta(qzeros, 1, scales, zeros_out, scales_out, (int)G, N, s) != cudaSuccess)
+    return W4_ERR_CUDA;
+  return from_cuda(launch_stream_fence(s));
 }
 
 w4_status w4_repack_gptq(const int32_t* qweight, const int32_t* qzeros, const void* scales,
@@ -177,12 +183,14 @@ w4_status w4_repack_gptq(const int32_t* qweight, const int32_t* qzeros, const vo
   const size_t G = (size_t)K / g;
   if (g_idx && G > (size_t)MAX_ACT_ORDER_GROUPS) return W4_ERR_SHAPE;
   const size_t qw_b = (size_t)K * N / 2, z_b = G * N / 2, s_b = G * N * 2;
+  size_t qw_out_b = 0;
+  w4_repack_sizes(K, N, group, layout, &qw_out_b, nullptr, nullptr);
   const size_t gi_b = g_idx ? (size_t)K * 4 : 0;
   const void* ins[4] = {qweight, qzeros, scales, g_idx};
   const size_t in_b[4] = {qw_b, z_b, s_b, gi_b};
   const void* outs[5] = {qw_out, zeros_out, scales_out, g_idx ? perm_out : nullptr,
                          g_idx ? status_out : nullptr};
-  const size_t out_b[5] = {qw_b, z_b, s_b, gi_b, g_idx ? (size_t)4 : 0};
+  const size_t out_b[5] = {qw_out_b, z_b, s_b, gi_b, g_idx ? (size_t)4 : 0};
   for (int i = 0; i < 5; ++i) {
     for (int j = 0; j < 4; ++j)
       if (overlaps(outs[i], out_b[i], ins[j], in_b[j])) return W4_ERR_ALIAS;
@@ -201,7 +209,9 @@ w4_status w4_repack_gptq(const int32_t* qweight, const int32_t* qzeros, const vo
                       ? launch_std_rows_permuted(qweight, perm, qw_out, K, N, s)
                       : launch_to_tile(qweight, 0, perm, qw_out, K, N, s);
   if (e != cudaSuccess) return W4_ERR_CUDA;
-  return from_cuda(launch_meta(qzeros, 0, scales, zeros_out, scales_out, (int)G, N, s));
+  if (launch_meta(qzeros, 0, scales, zeros_out, scales_out, (int)G, N, s) != cudaSuccess)
+    return W4_ERR_CUDA;
+  return from_cuda(launch_stream_fence(s));
 }
 
 size_t w4a16_gemm_workspace_size(int M, int N, int K, int group, int dtype, int has_perm) {

@@ -20,6 +20,11 @@ cudaError_t launch_meta(const int32_t* qzeros, int zeros_are_awq, const void* sc
                         int32_t* zeros_out, void* scales_out, int G, int N, cudaStream_t s);
 cudaError_t launch_act_order_perm(const int32_t* g_idx, int K, int group, int32_t* perm_out,
                                   int32_t* status_out, cudaStream_t s);
+// An empty kernel launched in full stream order after the repack kernels: the
+// GEMM kernels may read their weights before the kernel just before them on the
+// stream has finished (programmatic dependent launch), and this keeps that
+// kernel from being one that writes weights.
+cudaError_t launch_stream_fence(cudaStream_t s);
 cudaError_t launch_dequant(const int32_t* qw, const void* scales, const int32_t* zeros, int K,
                            int N, int group, int bf16, int layout, int out_f32, void* w_out,
                            cudaStream_t s);

@@ -179,21 +179,37 @@ TILE_NIBBLE_ROW = (0, 2, 4, 6, 1, 3, 5, 7)
 TILE_ATOM_K = 64
 TILE_ATOM_N = 16
 TILE_ATOM_WORDS = 128
+TILE_GROUP_TILES = 8          # 16-column tiles per column group (128 columns)
+
+
+def tile_words(K: int, N: int) -> int:
+    """Number of TILE words of a K x N layer: N is padded to whole 128-column groups."""
+    return K * (-(-N // (TILE_ATOM_N * TILE_GROUP_TILES)) * TILE_ATOM_N * TILE_GROUP_TILES) // 8
+
+
+def tile_atom(kb: int, nt: int, K: int) -> int:
+    """Index of atom (k-atom kb, column tile nt): column group outermost, then k, then the tile."""
+    A = K // TILE_ATOM_K
+    return ((nt // TILE_GROUP_TILES) * A + kb) * TILE_GROUP_TILES + nt % TILE_GROUP_TILES
 
 
 def tile_pos(k: int, n: int, K: int, N: int):
     """(word index, nibble position) of code (k, n) in the TILE layout.
 
     The layout (also written out in include/w4a16.h):
-      * atoms of 16 columns x 64 rows, 128 words each, stored column-tile-major:
-        atom index a = (n // 16) * (K // 64) + k // 64;
+      * atoms of 16 columns x 64 rows, 128 words each; columns are taken in
+        groups of 8 tiles (128 columns, the last group padded with zero atoms)
+        and atom (kb, nt) sits at index
+        ((nt // 8) * (K // 64) + kb) * 8 + nt % 8, kb = k // 64, nt = n // 16,
+        so one group's atoms at one k-atom are 8 consecutive atoms and a group's
+        whole K range is one contiguous run;
       * inside an atom, word 4*lane + j with lane = 4*gg + t, where
         gg = n % 8, t = (k % 32) // 8, j = 2 * ((k % 64) // 32) + (n % 16) // 8;
       * the word holds rows 8t..8t+7 (plus the atom/half offsets) of column n,
         row offset TILE_NIBBLE_ROW[p] at nibble position p.
     """
     assert K % TILE_ATOM_K == 0 and N % TILE_ATOM_N == 0
-    a = (n // TILE_ATOM_N) * (K // TILE_ATOM_K) + k // TILE_ATOM_K
+    a = tile_atom(k // TILE_ATOM_K, n // TILE_ATOM_N, K)
     kk = k % TILE_ATOM_K
     nn = n % TILE_ATOM_N
     gg = nn % 8
@@ -206,19 +222,22 @@ def tile_pos(k: int, n: int, K: int, N: int):
 
 
 def tile_pack(codes: np.ndarray) -> np.ndarray:
-    """[K, N] codes -> TILE words (int32, K*N/8 of them), per `tile_pos`.
+    """[K, N] codes -> TILE words (int32, `tile_words(K, N)` of them), per `tile_pos`.
 
-    Vectorised form of `tile_pos`: code (k, n) with
-      k = 64*kb + 32*jh + 8*t + e,  n = 16*nt + 8*jl + gg
-    goes to word ((nt*(K/64) + kb)*128 + 4*(4*gg + t) + 2*jh + jl), nibble
-    position TILE_NIBBLE_ROW.index(e).
+    Vectorised form of `tile_pos`: with N padded by zero codes to Np (a
+    multiple of 128), code (k, n) with
+      k = 64*kb + 32*jh + 8*t + e,  n = 128*cg + 16*w + 8*jl + gg
+    goes to word (((cg*(K/64) + kb)*8 + w)*128 + 4*(4*gg + t) + 2*jh + jl),
+    nibble position TILE_NIBBLE_ROW.index(e).
     """
     K, N = codes.shape
-    c = np.asarray(codes).astype(np.uint32)
-    # axes: kb, jh, t, e, nt, jl, gg
-    c = c.reshape(K // 64, 2, 4, 8, N // 16, 2, 8)
-    # -> nt, kb, gg, t, jh, jl, e
-    c = c.transpose(4, 0, 6, 2, 1, 5, 3)
+    Np = tile_words(K, N) * 8 // K
+    c = np.zeros((K, Np), dtype=np.uint32)
+    c[:, :N] = np.asarray(codes).astype(np.uint32)
+    # axes: kb, jh, t, e, cg, w, jl, gg
+    c = c.reshape(K // 64, 2, 4, 8, Np // 128, 8, 2, 8)
+    # -> cg, kb, w, gg, t, jh, jl, e
+    c = c.transpose(4, 0, 5, 7, 2, 1, 6, 3)
     words = np.zeros(c.shape[:-1], dtype=np.uint32)
     for p, e in enumerate(TILE_NIBBLE_ROW):
         words |= c[..., e] << np.uint32(4 * p)
@@ -226,14 +245,15 @@ def tile_pack(codes: np.ndarray) -> np.ndarray:
 
 
 def tile_unpack(words: np.ndarray, K: int, N: int) -> np.ndarray:
-    """Inverse of `tile_pack`: TILE words -> [K, N] codes."""
-    u = np.asarray(words).view(np.uint32).reshape(N // 16, K // 64, 8, 4, 2, 2)
+    """Inverse of `tile_pack`: TILE words -> [K, N] codes (the padding dropped)."""
+    Np = tile_words(K, N) * 8 // K
+    u = np.asarray(words).view(np.uint32).reshape(Np // 128, K // 64, 8, 8, 4, 2, 2)
     c = np.empty(u.shape + (8,), dtype=np.uint8)
     for p, e in enumerate(TILE_NIBBLE_ROW):
         c[..., e] = (u >> np.uint32(4 * p)) & 0xF
-    # nt, kb, gg, t, jh, jl, e -> kb, jh, t, e, nt, jl, gg
-    c = c.transpose(1, 4, 3, 6, 0, 5, 2)
-    return np.ascontiguousarray(c).reshape(K, N)
+    # cg, kb, w, gg, t, jh, jl, e -> kb, jh, t, e, cg, w, jl, gg
+    c = c.transpose(1, 5, 4, 7, 0, 2, 6, 3)
+    return np.ascontiguousarray(c).reshape(K, Np)[:, :N]
 
 
 # --------------------------------------------------------------------------- #

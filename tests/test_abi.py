@@ -35,7 +35,7 @@ def test_no_internal_symbols_leak(lib):
 def test_status_strings_and_version():
     import int4_weight_only_repack_gb300 as w4
     ensure_built()
-    assert w4.w4_abi_version() == 1
+    assert w4.w4_abi_version() == 2
     for st in range(12):
         assert w4.w4_status_string(st)
     assert "unknown" in w4.w4_status_string(99)
@@ -51,6 +51,9 @@ def test_repack_sizes():
                                                                         32 * 22016 // 2,
                                                                         32 * 22016 * 2)
     assert w4.w4_repack_sizes(256, 64, -1, w4.W4_LAYOUT_TILE)[1] == 64 // 2
+    # TILE pads N to whole 128-column groups; STD does not
+    assert w4.w4_repack_sizes(256, 272, 128, w4.W4_LAYOUT_TILE)[0] == 256 * 384 // 2
+    assert w4.w4_repack_sizes(256, 272, 128, w4.W4_LAYOUT_STD)[0] == 256 * 272 // 2
 
 
 FAKE = 0x10000  # a 16-byte aligned non-null address; never dereferenced

@@ -65,18 +65,25 @@ def check_layer(w4, cfg, li):
         assert int(layer.status[0].item()) == 0
         perm = oracle.act_order_perm(L.g_idx)
         assert np.array_equal(layer.perm.cpu().numpy(), perm)
-    # repack: sampled atoms, bit-exact
+    # repack: sampled atoms, bit-exact (atom index: column group, k-atom, tile in group)
     A, NT = K // 64, N // 16
-    n_pick = min(NT * A, 254)
-    atoms = np.unique(np.concatenate([[0, NT * A - 1], rng.choice(NT * A, n_pick, replace=False)]))
+    n_atoms = oracle.tile_words(K, N) // 128
+    n_pick = min(n_atoms, 254)
+    atoms = np.unique(np.concatenate([[0, n_atoms - 1], rng.choice(n_atoms, n_pick, replace=False)]))
     words = layer.qw.view(-1)
     idx = torch.from_numpy((atoms[:, None] * 128 + np.arange(128)[None, :]).reshape(-1)).to(words.device)
     got = words[idx].cpu().numpy().reshape(len(atoms), 128)
     rows = perm if perm is not None else np.arange(K)
     for i, a in enumerate(atoms):
-        nt, kb = divmod(int(a), A)
+        cg, rem = divmod(int(a), 8 * A)
+        kb, wt = divmod(rem, 8)
+        nt = 8 * cg + wt
+        if nt >= NT:  # zero padding of the last column group
+            assert not got[i].any(), (name, int(a))
+            continue
+        assert oracle.tile_atom(kb, nt, K) == int(a)
         block = q[rows[64 * kb:64 * kb + 64], 16 * nt:16 * nt + 16]
-        assert np.array_equal(got[i], oracle.tile_pack(block)), (name, int(a))
+        assert np.array_equal(got[i], oracle.tile_pack(block)[:128]), (name, int(a))
     zstd = oracle.pack_cols_std(z)
     assert np.array_equal(layer.zeros.cpu().numpy().reshape(zstd.shape), zstd)
     assert np.array_equal(half_from_dev(layer.scales).reshape(L.scales.shape), L.scales)

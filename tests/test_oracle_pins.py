@@ -144,14 +144,41 @@ def test_repack_tiny_brute_force():
 # Tile layout (own format: bijection, round trip, scalar vs vectorised)         #
 # --------------------------------------------------------------------------- #
 def test_tile_pos_is_bijection():
-    K, N = 128, 48
+    # 128 x 256: two whole column groups, so every word holds codes
+    K, N = 128, 256
     seen = set()
     for k in range(K):
         for n in range(N):
             seen.add(oracle.tile_pos(k, n, K, N))
     assert len(seen) == K * N
-    words = {w for w, _ in seen}
-    assert words == set(range(K * N // 8))
+    assert {w for w, _ in seen} == set(range(oracle.tile_words(K, N)))
+
+
+def test_tile_padding_is_zero_and_injective():
+    # 128 x 48: three of a group's eight tiles carry codes, the rest is zero padding
+    K, N = 128, 48
+    assert oracle.tile_words(K, N) == K * 128 // 8
+    seen = {oracle.tile_pos(k, n, K, N) for k in range(K) for n in range(N)}
+    assert len(seen) == K * N
+    codes = np.full((K, N), 15, dtype=np.uint8)
+    words = oracle.tile_pack(codes).view(np.uint32)
+    used = {w for w, _ in seen}
+    for w in range(len(words)):
+        assert (words[w] != 0) == (w in used)
+
+
+def test_tile_group_order():
+    # atom (kb, nt) = ((nt // 8) * (K / 64) + kb) * 8 + nt % 8: the eight tiles of
+    # a column group at one k-atom are adjacent, then the next k-atom follows
+    K, N = 192, 272
+    A = K // 64
+    for kb in range(A):
+        for nt in range(N // 16):
+            w, _ = oracle.tile_pos(64 * kb, 16 * nt, K, N)
+            assert w == (((nt // 8) * A + kb) * 8 + nt % 8) * 128
+    assert oracle.tile_pos(64, 0, K, N)[0] == 8 * 128
+    assert oracle.tile_pos(0, 16, K, N)[0] == 128
+    assert oracle.tile_pos(0, 128, K, N)[0] == A * 8 * 128
 
 
 def test_tile_pack_matches_tile_pos():
