@@ -109,7 +109,9 @@ struct SmemLayout {
 // lanes whose token row is beyond M). bars: ring mbarriers, then one per x
 // buffer. cnt: per slot the count of warps done with it (monotonic), per slot
 // the last stage copied into it, per x buffer the last chunk copied into it,
-// and the abort flag. meta: per warp and group slot, one float4 per lane group.
+// and the abort flag. meta: per warp and group slot,
+// the scales of the tile's 16 columns (one float2 per lane group) and the
+// tile's two zero words.
 // xsum: per group slot, the sum of x over the group's rows for each token.
 __host__ __device__ inline SmemLayout smem_layout(int MT, int m_rows, int x_stride, int nbuf,
                                                   int ring, int maxg, int S, int slice) {
@@ -119,7 +121,7 @@ __host__ __device__ inline SmemLayout smem_layout(int MT, int m_rows, int x_stri
   L.bars = L.ring + ring * STAGE_BYTES;
   L.cnt = L.bars + (ring + 2) * 8;
   L.meta = (L.cnt + (2 * ring + 2 + 1) * 4 + 15) & ~15;
-  L.xsum = L.meta + DEC_WARPS * maxg * 8 * 16;
+  L.xsum = L.meta + DEC_WARPS * maxg * (8 * 8 + 8);
   L.recv = L.xsum + maxg * 8 * MT * 4;
   L.total = L.recv + S * slice * 8 * MT * 4;
   return L;
@@ -213,12 +215,17 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 #endif
 constexpr int decode_min_ctas(int MT) { return MT == 1 ? W4_DECODE_MIN_CTAS : 2; }
 
+// With bf16 activations the MMA consumes the codes as 128 + q (exact in bf16)
+// and each group's sum is corrected by (128 + z) s sum(x); those corrections
+// are summed over the chunk's groups before the weight loop (from per-group
+// sums of x taken with all-ones MMAs), so the loop only adds s * acc per group.
+// With fp16 one packed subtraction per register forms q - z exactly (the zero
+// pairs are built per group from the staged zero words).
 template <int MT, bool BF16, bool G64>
 __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
     w4a16_decode_kernel(const DecodeParams p) {
-  constexpr uint32_t MAGIC = Magic<BF16>::pair;
-  constexpr bool BIAS = BF16 && MT <= 2;             // 128 + q operand, group-sum correction
-  constexpr uint32_t ONES = BF16 ? 0x3F803F80u : 0x3C003C00u;  // 1.0 in both halves
+  constexpr uint32_t MAGIC = Magic<BF16>::pair;  // 128 (bf16) / 1024 (fp16) in both halves
+  constexpr uint32_t ONES = 0x3F803F80u;         // bf16 1.0 in both halves
   extern __shared__ __align__(1024) uint8_t smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -239,11 +246,11 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
   int* last_stage = cnt + D;                              // [D] last stage copied into each slot
   int* last_chunk = last_stage + D;                       // [2] last x chunk copied into each buffer
   volatile int* abort_flag = last_chunk + 2;
-  // per (group slot, lane group gg): {s, c, s', c'} for columns gg and gg + 8 of
-  // the warp's tile; c = (128 + z) * s with the bias operand, else the packed
-  // MAGIC + z halves (as bits)
-  float4* meta = reinterpret_cast<float4*>(smem + L.meta) + warp * p.maxg * 8;
-  float* xsum = reinterpret_cast<float*>(smem + L.xsum);  // [maxg][MR]
+  // per (group slot, lane group gg): the scales of columns gg and gg + 8 of the
+  // warp's tile; then per group slot the tile's two zero words
+  float2* meta = reinterpret_cast<float2*>(smem + L.meta) + warp * p.maxg * 8;
+  uint2* zraw = reinterpret_cast<uint2*>(smem + L.meta + DEC_WARPS * p.maxg * 64) + warp * p.maxg;
+  float* xsum = reinterpret_cast<float*>(smem + L.xsum);  // [maxg][MR] (bf16 only)
   float* recv = reinterpret_cast<float*>(smem + L.recv);
   constexpr int NCOL = 16 * DEC_WARPS;
 
@@ -290,27 +297,16 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
     if (p.pf > 0 && pa < ka1 && j >= D)
       prefetch_l2(gsrc + (size_t)pa * KROW_BYTES, (uint32_t)min(SA, ka1 - pa) * KROW_BYTES);
   };
-  // one group's 16 scales and 16 zeros (of this warp's tile) into its 8 meta entries
+  // one group's 16 scales (of this warp's tile) into its 8 meta entries, and its
+  // zero words
   auto stage_meta = [&](int gl, const uint4 a, const uint4 b, const uint2 z) {
     const uint32_t sv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const float s_lo = half_bits_to_float<BF16>((uint16_t)(sv[c >> 1] >> (16 * (c & 1))));
-      const float s_hi = half_bits_to_float<BF16>((uint16_t)(sv[4 + (c >> 1)] >> (16 * (c & 1))));
-      const uint32_t z_lo = (z.x >> (4 * c)) & 0xF;
-      const uint32_t z_hi = (z.y >> (4 * c)) & 0xF;
-      float4 e;
-      e.x = s_lo;
-      e.z = s_hi;
-      if constexpr (BIAS) {
-        e.y = (float)(128 + z_lo) * s_lo;
-        e.w = (float)(128 + z_hi) * s_hi;
-      } else {
-        e.y = __uint_as_float(MAGIC | z_lo | (z_lo << 16));
-        e.w = __uint_as_float(MAGIC | z_hi | (z_hi << 16));
-      }
-      meta[gl * 8 + c] = e;
-    }
+    for (int c = 0; c < 8; ++c)
+      meta[gl * 8 + c] =
+          make_float2(half_bits_to_float<BF16>((uint16_t)(sv[c >> 1] >> (16 * (c & 1)))),
+                      half_bits_to_float<BF16>((uint16_t)(sv[4 + (c >> 1)] >> (16 * (c & 1)))));
+    zraw[gl] = z;
   };
   // scales / zeros of the groups of chunk ci for this warp's tile; in the first
   // chunk the ring fill waits until every warp has issued these loads, so they
@@ -378,32 +374,25 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
     if (NB == 2 && nchunks > 1) issue_x(1);
   }
 
-  float acc[MT][4], tot[MT][4];
+  // acc: the open group's MMA sums; tc: the CTA's total
+  float acc[MT][4], tc[MT][4];
 #pragma unroll
   for (int i = 0; i < MT; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = tot[i][j] = 0.f;
-  float4 gf = make_float4(0.f, 0.f, 0.f, 0.f);  // factors of the open group
-  int gslot = -1;                               // its slot in meta / xsum (-1: none open)
-  uint32_t rslot = 0, rphase = 0;               // ring slot of the next stage, its parity
+    for (int j = 0; j < 4; ++j) acc[i][j] = tc[i][j] = 0.f;
+  float2 gf = make_float2(0.f, 0.f);  // scales of the open group (columns gg, gg + 8)
+  uint32_t zl = 0, zh = 0;            // fp16: MAGIC + z pairs of the open group
+  int gslot = -1;                     // its slot in meta (-1: none open)
+  uint32_t rslot = 0, rphase = 0;     // ring slot of the next stage, its parity
 
-  // tot += s * acc - (128 + z) * s * sum(x) with the bias operand, else s * acc; acc = 0
-  // ((128 + z) * s is exact in fp32: two 8-bit significands)
+  // tc += s * acc; acc = 0
   auto flush = [&]() {
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
-      if constexpr (BIAS) {
-        const float2 xg = *reinterpret_cast<const float2*>(xsum + gslot * MR + 8 * mt + 2 * t);
-        tot[mt][0] = fmaf(gf.x, acc[mt][0], fmaf(-gf.y, xg.x, tot[mt][0]));
-        tot[mt][1] = fmaf(gf.x, acc[mt][1], fmaf(-gf.y, xg.y, tot[mt][1]));
-        tot[mt][2] = fmaf(gf.z, acc[mt][2], fmaf(-gf.w, xg.x, tot[mt][2]));
-        tot[mt][3] = fmaf(gf.z, acc[mt][3], fmaf(-gf.w, xg.y, tot[mt][3]));
-      } else {
-        tot[mt][0] = fmaf(gf.x, acc[mt][0], tot[mt][0]);
-        tot[mt][1] = fmaf(gf.x, acc[mt][1], tot[mt][1]);
-        tot[mt][2] = fmaf(gf.z, acc[mt][2], tot[mt][2]);
-        tot[mt][3] = fmaf(gf.z, acc[mt][3], tot[mt][3]);
-      }
+      tc[mt][0] = fmaf(gf.x, acc[mt][0], tc[mt][0]);
+      tc[mt][1] = fmaf(gf.x, acc[mt][1], tc[mt][1]);
+      tc[mt][2] = fmaf(gf.y, acc[mt][2], tc[mt][2]);
+      tc[mt][3] = fmaf(gf.y, acc[mt][3], tc[mt][3]);
       acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
     }
   };
@@ -412,6 +401,11 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
     if (gslot >= 0) flush();
     ++gslot;
     gf = meta[gslot * 8 + gg];
+    if constexpr (!BF16) {
+      const uint2 zw = zraw[gslot];
+      zl = MAGIC + ((zw.x >> (4 * gg)) & 0xFu) * 0x00010001u;
+      zh = MAGIC + ((zw.y >> (4 * gg)) & 0xFu) * 0x00010001u;
+    }
   };
 
   for (int ci = 0; ci < nchunks; ++ci) {
@@ -444,50 +438,57 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
         v.w = h[6] | ((uint32_t)h[7] << 16);
         *reinterpret_cast<uint4*>(xb + (size_t)m * p.x_stride + 8 * c) = v;
       }
-      if constexpr (BIAS) __syncthreads();  // the sums below read every warp's rows
+      if constexpr (BF16) __syncthreads();  // the sums below read every warp's rows
     } else if (live) {
       bounded_wait(xbar0 + 8 * b, (uint32_t)((NB == 2 ? ci >> 1 : ci) & 1), abort_flag);
     }
-    // 3) per-group sums of x (bias operand): warp w takes group slots w, w + 8, ...
-    //    and runs the 32-row halves of the group's part of this chunk through MMAs
-    //    whose A operand is all ones (four independent accumulator chains)
-    if constexpr (BIAS) {
+    // 3) per-group sums of x (bf16): warp w takes group slots w, w + 8, ... and runs
+    //    the group's 32-row halves in this chunk through all-ones MMAs (two chains)
+    if constexpr (BF16) {
       for (int gl = warp; gl < ng; gl += DEC_WARPS) {
         const int gi = g_first + gl;
         const int r0 = max(c0 * ATOM_K, p.gshift >= 31 ? 0 : gi << p.gshift);
         const int r1 = min(c1 * ATOM_K, p.gshift >= 31 ? p.K : (gi + 1) << p.gshift);
-        float sacc[4][MT][4];
+        for (int mt = 0; mt < MT; ++mt) {
+          const int row = 8 * mt + gg;
+          const uint16_t* xr = (row < p.M ? xb + (size_t)row * p.x_stride : xzero) + 8 * t;
+          float sa[2][4] = {};
+          for (int r = r0; r < r1; r += 64) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt)
-            sacc[c][mt][0] = sacc[c][mt][1] = sacc[c][mt][2] = sacc[c][mt][3] = 0.f;
-        for (int r = r0; r < r1; r += 128) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            if (r + 32 * c < r1) {
-#pragma unroll
-              for (int mt = 0; mt < MT; ++mt) {
-                const int row = 8 * mt + gg;
-                const uint16_t* xr = row < p.M ? xb + (size_t)row * p.x_stride : xzero;
+            for (int c = 0; c < 2; ++c) {
+              if (r + 32 * c < r1) {
                 const uint4 xf =
-                    *reinterpret_cast<const uint4*>(xr + (r + 32 * c - c0 * ATOM_K) + 8 * t);
-                mma16816<BF16>(sacc[c][mt], ONES, ONES, ONES, ONES, xf.x, xf.y);
-                mma16816<BF16>(sacc[c][mt], ONES, ONES, ONES, ONES, xf.z, xf.w);
+                    *reinterpret_cast<const uint4*>(xr + (r + 32 * c - c0 * ATOM_K));
+                mma16816<true>(sa[c], ONES, ONES, ONES, ONES, xf.x, xf.y);
+                mma16816<true>(sa[c], ONES, ONES, ONES, ONES, xf.z, xf.w);
               }
             }
           }
-        }
-        if (gg == 0) {
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt)
+          if (gg == 0)
             *reinterpret_cast<float2*>(xsum + gl * MR + 8 * mt + 2 * t) =
-                make_float2((sacc[0][mt][0] + sacc[1][mt][0]) + (sacc[2][mt][0] + sacc[3][mt][0]),
-                            (sacc[0][mt][1] + sacc[1][mt][1]) + (sacc[2][mt][1] + sacc[3][mt][1]));
+                make_float2(sa[0][0] + sa[1][0], sa[0][1] + sa[1][1]);
         }
       }
     }
     __syncthreads();  // x, the group sums and every warp's scale / zero stage are ready
+    // 4) bf16: remove every group's (128 + z) s sum(x) from the total up front
+    //    ((128 + z) s is exact in fp32: two 8-bit significands)
+    if (BF16 && has_cols) {
+      for (int gl = 0; gl < ng; ++gl) {
+        const float2 sc = meta[gl * 8 + gg];
+        const uint2 zw = zraw[gl];
+        const float cl = sc.x * (float)(128 + ((zw.x >> (4 * gg)) & 0xF));
+        const float ch = sc.y * (float)(128 + ((zw.y >> (4 * gg)) & 0xF));
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const float2 xg = *reinterpret_cast<const float2*>(xsum + gl * MR + 8 * mt + 2 * t);
+          tc[mt][0] = fmaf(-cl, xg.x, tc[mt][0]);
+          tc[mt][1] = fmaf(-cl, xg.y, tc[mt][1]);
+          tc[mt][2] = fmaf(-ch, xg.x, tc[mt][2]);
+          tc[mt][3] = fmaf(-ch, xg.y, tc[mt][3]);
+        }
+      }
+    }
 
     // 4) consume this chunk's stages. Shared-memory operands are addressed with
     //    32-bit shared-window addresses with constant offsets inside a stage.
@@ -514,12 +515,11 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
         af[step][2] = lop3_and_or(wlo >> (sh + 4), 0x000F000Fu, MAGIC);
         af[step][1] = lop3_and_or(whi >> sh, 0x000F000Fu, MAGIC);
         af[step][3] = lop3_and_or(whi >> (sh + 4), 0x000F000Fu, MAGIC);
-        if constexpr (!BIAS) {
-          const uint32_t zl = __float_as_uint(gf.y), zh = __float_as_uint(gf.w);
-          af[step][0] = sub_x2<BF16>(af[step][0], zl);
-          af[step][2] = sub_x2<BF16>(af[step][2], zl);
-          af[step][1] = sub_x2<BF16>(af[step][1], zh);
-          af[step][3] = sub_x2<BF16>(af[step][3], zh);
+        if constexpr (!BF16) {
+          af[step][0] = sub_x2<false>(af[step][0], zl);
+          af[step][2] = sub_x2<false>(af[step][2], zl);
+          af[step][1] = sub_x2<false>(af[step][1], zh);
+          af[step][3] = sub_x2<false>(af[step][3], zh);
         }
       }
 #pragma unroll
@@ -577,6 +577,10 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
             atom(lds128(st + u * KROW_BYTES), xo + u * (ATOM_K * 2),
                  ((a_base + u) & (apg - 1)) == 0);
         }
+        // groups longer than a stage are flushed at every stage as well (the
+        // flush is linear and the zero-point part was removed up front), which
+        // bounds the length of an fp32 MMA accumulation to one stage
+        if (G64 && apg > SA && gslot >= 0) flush();
       }
       __syncwarp();
       // release the slot; the last of the eight warps refills it with stage j + D
@@ -632,12 +636,12 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
       const int m0 = 8 * mt + 2 * t;
       const int ca = warp * 16 + gg, cb = ca + 8;
       if (m0 < p.M) {
-        push(ca, m0, tot[mt][0]);
-        push(cb, m0, tot[mt][2]);
+        push(ca, m0, tc[mt][0]);
+        push(cb, m0, tc[mt][2]);
       }
       if (m0 + 1 < p.M) {
-        push(ca, m0 + 1, tot[mt][1]);
-        push(cb, m0 + 1, tot[mt][3]);
+        push(ca, m0 + 1, tc[mt][1]);
+        push(cb, m0 + 1, tc[mt][3]);
       }
     }
   }
@@ -740,54 +744,40 @@ DecodePlan fit_ring(int S, int A, int Mc, int MT, int gshift, int per_sm, int sm
   return d;
 }
 
-// Choose the split-K factor (and with it the ring) with a small time model.
-// CTAs run in waves; each wave pays a fixed start-up / drain cost plus the
-// longer of its weight stream and its instruction stream. A CTA streams at
-// most the bytes it keeps in flight (its ring) per memory latency, and the
-// CTAs of an SM share that SM's part of the HBM bandwidth. Chunked x staging
-// adds a barrier per extra chunk.
+// Choose the split-K factor, then the ring. The rule is calibrated on GB300
+// sweeps over S for the Llama-2 7B / 70B decode shapes:
+//  * x of the CTA's K range is staged in one piece when it fits (chunked x costs
+//    a barrier per chunk), so S is at least the smallest split that makes it fit;
+//  * a CTA's K range stays between 16 and 64 k-atoms (shorter runs are
+//    dominated by the fixed prologue / reduction cost, longer ones by the wait
+//    for the slowest CTA);
+//  * with one token tile the launch aims at about 2.6 CTAs per SM (enough warps
+//    to hide the loop's latencies, few enough to stay near one wave).
+// The ring is then as deep as fits with 3 resident CTAs per SM (2 when the
+// register budget allows only 2), at least 2 stages.
 DecodePlan plan_decode(int N, int K, int Mc, int MT, int gshift, const DeviceInfo& info) {
   const int NG = (N / 16 + DEC_WARPS - 1) / DEC_WARPS, A = K / ATOM_K;
-  const int reg_ctas = decode_min_ctas(MT);
-  const double overhead = 2.0e-6, bw = 6.6e12, lat = 1.5e-6, chunk_cost = 0.5e-6;
-  const double issue_rate = 4.0 * 1.9e9 * 0.6;         // warp instructions per second per SM
-  const double inst_per_atom = 40.0 + 10.0 * MT;
-  const double sm_bw = bw / info.sm_count;
-  DecodePlan best = shape_plan(1, A, Mc, MT, gshift, 2);
-  double best_t = 1e30;
   const int nst_all = (A + SA - 1) / SA;
-  for (int S = 1; S <= MAX_SPLIT && S <= nst_all; ++S) {
-    DecodePlan d = fit_ring(S, A, Mc, MT, gshift, 2, info.smem_per_sm);
-    if (reg_ctas >= 3) {
-      const DecodePlan d3 = fit_ring(S, A, Mc, MT, gshift, 3, info.smem_per_sm);
-      if (d3.ring >= 3 && (d3.L.total + 1024) * 3 <= info.smem_per_sm) d = d3;
-    }
-    const int smem_ctas = info.smem_per_sm / (d.L.total + 1024);
-    const int per_sm = std::max(1, std::min(reg_ctas, smem_ctas));
-    const long long slots = (long long)per_sm * info.sm_count;
-    long long left = (long long)NG * S;
-    const double cta_atoms = (double)A / S;
-    const double cta_bytes = cta_atoms * KROW_BYTES;
-    const double cta_inflight = (double)d.ring * STAGE_BYTES;
-    const int nchunks = (int)((cta_atoms + d.chunk_atoms - 1) / d.chunk_atoms);
-    const double cta_inst = (double)DEC_WARPS * cta_atoms * inst_per_atom;
-    double t = 0.0;
-    while (left > 0) {
-      const long long now = std::min(left, slots);
-      const double c = std::max(1.0, (double)now / info.sm_count);  // CTAs sharing an SM
-      const double rate = std::min(sm_bw / c, cta_inflight / lat);
-      const double t_mem = cta_bytes / rate;
-      const double t_issue = cta_inst * c / issue_rate;
-      t += overhead + std::max(t_mem, t_issue) + (nchunks - 1) * chunk_cost;
-      left -= now;
-    }
-    t += 0.05e-6 * S;
-    if (t < best_t) {
-      best_t = t;
-      best = d;
-    }
+  auto cta_atoms = [&](int S) { return (nst_all + S - 1) / S * SA; };
+  const int s_cap = std::min(MAX_SPLIT, nst_all);
+  int s_x = 1;  // x in one piece
+  while (s_x < s_cap && (long long)cta_atoms(s_x) * ATOM_K * Mc * 2 > X_BUDGET) ++s_x;
+  int s_lo = 1;  // at most 64 k-atoms per CTA
+  while (s_lo < s_cap && cta_atoms(s_lo) > 64) ++s_lo;
+  s_lo = std::max(s_lo, s_x);
+  int s_hi = s_cap;  // at least 16 k-atoms per CTA
+  while (s_hi > 1 && cta_atoms(s_hi) < 16) --s_hi;
+  s_hi = std::max(s_hi, s_lo);
+  int S = s_lo;
+  if (MT == 1) {
+    const int target = (int)(2.6 * info.sm_count / NG + 0.5);
+    S = std::min(std::max(target, s_lo), s_hi);
   }
-  return best;
+  const int reg_ctas = decode_min_ctas(MT);
+  DecodePlan d = fit_ring(S, A, Mc, MT, gshift, std::min(3, reg_ctas), info.smem_per_sm);
+  if ((d.L.total + 1024) * std::min(3, reg_ctas) > info.smem_per_sm)
+    d = fit_ring(S, A, Mc, MT, gshift, 2, info.smem_per_sm);
+  return d;
 }
 
 // Plans are cached per (device, shape): planning costs tens of microseconds of
