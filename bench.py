@@ -21,6 +21,11 @@ roofline    = the decode kernel's per-launch durations (CUDA events on the
               copy bandwidth.
 cpu_baseline = the CPU oracle (numpy: unpack, dequantise, fp64 matmul) on the
               o_proj layer at M = 1, 4 and 16.
+dequant_cublas = the same step as w4_dequant to dense bf16 + cuBLAS (torch.matmul),
+              graph-timed like `value`; fused_speedup = its time / ours.
+prefill     = the Llama-2-7B prefill layers (M in {512, 2048, 4096}) on the
+              tcgen05 kernel: TFLOP/s per call and, for M >= 2048, against the
+              measured dense bf16 tensor-core peak.
 --impl reference times that oracle as the reference arm.
 """
 from __future__ import annotations
@@ -46,12 +51,13 @@ import synth  # noqa: E402
 METRIC = ("W4A16 GEMM TFLOP/s and weight GB/s vs M (1–4096), % of HBM / bf16 TC roofline")
 WORKLOAD = synth.WORKLOADS[1]          # Llama-2-7B decode layers
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_TC_TFLOPS = 1900.0
 
 # DRAM bytes per launch of the decode kernel from ncu (dram__bytes_read.sum +
 # dram__bytes_write.sum), keyed by the sha1 of the kernel source they were
 # taken on; see profiles/. A changed kernel source reports null.
 TRAFFIC_RECORDS: dict = {
-    "54c0d3eb0b98": 26502293,   # mean of the 12 launches of one step
+    "83a653689101": 26433600,   # mean of the 12 launches of one step
 }
 
 
@@ -74,6 +80,17 @@ def measured_peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_tc_peak():
+    """Dense bf16 tensor-core peak (burst: the prefill calls are timed alone)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_TC_TFLOPS, "fallback"
 
 
 # --------------------------------------------------------------------------- #
@@ -222,6 +239,82 @@ def per_launch_times(w4, torch, calls, reps: int, device):
     return [t / reps for t in totals]
 
 
+def graph_time(torch, fn, reps: int) -> float:
+    """Seconds per call of `fn` (a sequence of launches), from a CUDA graph of it
+    replayed `reps` times, CUDA events on the launch stream."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    g.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    del g
+    return e0.elapsed_time(e1) * 1e-3 / reps
+
+
+def dequant_cublas_measure(w4, torch, calls, reps: int, device):
+    """The same step as dequantise-then-GEMM: w4_dequant of each call's layer to a
+    dense bf16 [K, N] (one scratch per layer shape), then torch.matmul (cuBLAS)."""
+    scratch = {}
+    for c in calls:
+        key = (c["K"], c["N"])
+        if key not in scratch:
+            scratch[key] = torch.empty((c["K"], c["N"]), dtype=torch.bfloat16, device=device)
+
+    def step():
+        for c in calls:
+            L, W = c["layer"], scratch[(c["K"], c["N"])]
+            w4.w4_dequant(L.qw, L.scales, L.zeros, c["K"], c["N"], L.group, L.dtype, L.layout,
+                          False, W)
+            torch.matmul(c["x"], W, out=c["y2"])
+
+    for c in calls:
+        c["y2"] = torch.empty_like(c["y"])
+    t = graph_time(torch, step, reps)
+    for c in calls:
+        del c["y2"]
+    del scratch
+    return t
+
+
+def prefill_measure(w4, torch, device, reps: int = 10):
+    """The Llama-2-7B prefill layers (same shapes, M in {512, 2048, 4096}) on the
+    tcgen05 kernel: TFLOP/s per (layer, M), two weight copies per layer."""
+    wl = synth.WORKLOADS[2]
+    rows = []
+    for li, (K, N, name) in enumerate(wl.shapes):
+        L = synth.make_workload_layer(wl.index, li)
+        qweight = torch.from_numpy(L.qweight).to(device)
+        qzeros = torch.from_numpy(L.qzeros).to(device)
+        scales = torch.from_numpy(L.scales.view(np.int16)).to(device).view(torch.bfloat16)
+        layers = [w4.repack_awq(qweight, qzeros, scales, K, N, wl.group, torch.bfloat16)
+                  for _ in range(2)]
+        del qweight, qzeros, scales
+        for M in wl.ms:
+            x = torch.randn(M, K, device=device).to(torch.bfloat16)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+
+            def fn():
+                for l in layers:
+                    w4.linear(x, l, y=y)
+
+            t = graph_time(torch, fn, reps) / len(layers)
+            rows.append({"layer": name, "M": M, "us": round(t * 1e6, 2),
+                         "tflops": round(2.0 * M * N * K / t / 1e12, 1)})
+            del x, y
+        del layers
+        torch.cuda.empty_cache()
+    return rows
+
+
 def cpu_baseline_measure(min_seconds: float = 10.0):
     """The oracle as it stands on this host: o_proj (4096 x 4096) at M = 1, 4, 16."""
     import oracle
@@ -336,6 +429,27 @@ def ours(args):
     torch.cuda.synchronize()
     e2e_el = max_over_ranks(time.perf_counter() - t0, world, device)
 
+    # ---- comparison: dequantise then cuBLAS, same step, same timing ------------
+    t_deq = dequant_cublas_measure(w4, torch, calls, reps=min(args.steps, 200), device=device)
+
+    # ---- large-M (prefill) layers on the tensor cores -------------------------
+    prefill = None
+    if not args.no_prefill:
+        rows = prefill_measure(w4, torch, device)
+        big = [r for r in rows if r["M"] >= 2048]
+        kn = {sh[2]: (sh[0], sh[1]) for sh in synth.WORKLOADS[2].shapes}
+        flops = sum(2.0 * r["M"] * kn[r["layer"]][0] * kn[r["layer"]][1] for r in big)
+        tsum = sum(r["us"] for r in big) * 1e-6
+        tc_peak, tc_src = measured_tc_peak()
+        prefill = {"workload": "llama2_7b_prefill: the four layers at M in {512, 2048, 4096}, "
+                               "bf16, two weight copies per layer, CUDA graph of the calls",
+                   "tflops_m_ge_2048": round(flops / tsum / 1e12, 1),
+                   "roofline": {"bound": "tensor", "achieved": round(flops / tsum / 1e12, 1),
+                                "peak": tc_peak, "unit": "TFLOP/s",
+                                "frac": round(flops / tsum / 1e12 / tc_peak, 4),
+                                "peak_source": tc_src, "kernel": "w4a16_prefill_kernel"},
+                   "per_call": rows}
+
     cpu_base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu_base = cpu_baseline_measure(args.cpu_seconds)
@@ -377,6 +491,12 @@ def ours(args):
                          "kernel": "w4a16_decode_kernel",
                          "per_launch": per_call},
             "cpu_baseline": cpu_base,
+            "dequant_cublas": {"value": round(step_bytes / t_deq / 1e9, 2), "unit": "GB/s",
+                               "ms_per_step": round(t_deq * 1e3, 5),
+                               "fused_speedup": round(t_deq / (elapsed / args.steps), 2),
+                               "how": "w4_dequant to dense bf16 [K,N] + torch.matmul (cuBLAS) "
+                                      "per call, CUDA graph of the step"},
+            "prefill": prefill,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -472,6 +592,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip the large-M (prefill) layers")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--single", default=None,
                     help="K,N,M[,dtype]: time one layer shape only (profiling aid)")

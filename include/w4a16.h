@@ -176,9 +176,18 @@ W4_API size_t w4a16_gemm_workspace_size(int M, int N, int K, int group, int dtyp
  *          w4a16_gemm_workspace_size(...) bytes (may be NULL when that is 0).
  * Accumulation is fp32; the result is rounded once to dtype. Deterministic:
  * the same inputs give the same bits. M <= 64 (or N % 32 != 0) runs the
- * small-M kernel (CUDA-core dequantisation into exact (q - z) operands,
- * mma.sync, per-group fp32 scaling); larger M runs the tcgen05 kernel, whose
+ * small-M kernel (CUDA-core dequantisation into exact operands: q - z for
+ * fp16, 128 + q for bf16 with the (128 + z) * s * sum(x) part removed in fp32;
+ * mma.sync; per-group fp32 scaling); larger M runs the tcgen05 kernel, whose
  * B operand is the dequantised weight rounded once to dtype.
+ * Ordering: the kernels are launched with programmatic dependent launch and
+ * the small-M kernel reads qw, scales and zeros before it waits for the kernel
+ * launched just before it on `stream` (x is read and y written only after
+ * that wait). So qw, scales and zeros must not be written by the kernel
+ * launched immediately before this call on the same stream; separate such a
+ * writer by any other stream operation (a copy, an event wait, another
+ * kernel). w4_repack_awq / w4_repack_gptq already end with an empty kernel for
+ * this reason.
  */
 W4_API w4_status w4a16_gemm(const void* x, const int32_t* qw, const void* scales, const int32_t* zeros,
                      const int32_t* perm, void* y, int M, int N, int K, int group, int dtype,
