@@ -585,6 +585,49 @@ def single(args):
                       "device_status": w4.w4_device_status()}), flush=True)
 
 
+def sweep(args):
+    """The Llama-2-70B sweep (three layers, M from 1 to 4096): one JSON line per
+    (layer, M) with time, weight GB/s, TFLOP/s and the fraction of the matching
+    roofline (HBM for M <= 16, dense bf16 tensor peak above)."""
+    import torch
+
+    import int4_weight_only_repack_gb300 as w4
+
+    dev = torch.device("cuda")
+    wl = synth.WORKLOADS[4]
+    hbm, _ = measured_peaks()
+    tc, _ = measured_tc_peak()
+    for li, (K, N, name) in enumerate(wl.shapes):
+        L = synth.make_workload_layer(wl.index, li)
+        qweight = torch.from_numpy(L.qweight).to(dev)
+        qzeros = torch.from_numpy(L.qzeros).to(dev)
+        scales = torch.from_numpy(L.scales.view(np.int16)).to(dev).view(torch.bfloat16)
+        ncopy = max(2, int(400e6 // alg_bytes(K, N)) + 1)
+        layers = [w4.repack_awq(qweight, qzeros, scales, K, N, wl.group, torch.bfloat16)
+                  for _ in range(ncopy)]
+        del qweight, qzeros, scales
+        for M in wl.ms:
+            x = torch.randn(M, K, device=dev).to(torch.bfloat16)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            use = layers if M <= 256 else layers[:2]
+
+            def fn():
+                for l in use:
+                    w4.linear(x, l, y=y)
+
+            t = graph_time(torch, fn, 10) / len(use)
+            gbs = alg_bytes(K, N) / t / 1e9
+            tfl = 2.0 * M * N * K / t / 1e12
+            print(json.dumps({"sweep": wl.name, "layer": name, "K": K, "N": N, "M": M,
+                              "us": round(t * 1e6, 2), "weight_gbs": round(gbs, 1),
+                              "tflops": round(tfl, 1),
+                              "frac": round(gbs / hbm if M <= 16 else tfl / tc, 3),
+                              "bound": "hbm" if M <= 16 else "tensor"}), flush=True)
+            del x, y
+        del layers
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -595,11 +638,15 @@ def main():
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the large-M (prefill) layers")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--sweep", action="store_true",
+                    help="the Llama-2-70B layers at every M of that workload (one line each)")
     ap.add_argument("--single", default=None,
                     help="K,N,M[,dtype]: time one layer shape only (profiling aid)")
     args = ap.parse_args()
     if args.single:
         single(args)
+    elif args.sweep:
+        sweep(args)
     elif args.impl == "reference":
         reference(args)
     else:

@@ -158,7 +158,8 @@ W4_API w4_status w4_repack_gptq(const int32_t* qweight, const int32_t* qzeros, c
 
 /*
  * Workspace bytes w4a16_gemm needs for this call shape (0 = none). Act-order
- * calls with M > 64 stage the gathered activations x[:, perm] there
+ * calls with M > 16 that run the large-M kernel stage the gathered activations
+ * x[:, perm] there
  * (M*K*2 bytes, rounded up to 256). The contents need no initialisation.
  */
 W4_API size_t w4a16_gemm_workspace_size(int M, int N, int K, int group, int dtype, int has_perm);
@@ -175,8 +176,9 @@ W4_API size_t w4a16_gemm_workspace_size(int M, int N, int K, int group, int dtyp
  *   workspace / workspace_bytes: device scratch of at least
  *          w4a16_gemm_workspace_size(...) bytes (may be NULL when that is 0).
  * Accumulation is fp32; the result is rounded once to dtype. Deterministic:
- * the same inputs give the same bits. M <= 64 (or N % 32 != 0) runs the
- * small-M kernel (CUDA-core dequantisation into exact operands: q - z for
+ * the same inputs give the same bits. M <= 16 (M <= 32 unless the large-M
+ * kernel's 128 x 256 output tiles alone fill the GPU; any M when N % 32 != 0)
+ * runs the small-M kernel (CUDA-core dequantisation into exact operands: q - z for
  * fp16, 128 + q for bf16 with the (128 + z) * s * sum(x) part removed in fp32;
  * mma.sync; per-group fp32 scaling); larger M runs the tcgen05 kernel, whose
  * B operand is the dequantised weight rounded once to dtype.

@@ -440,6 +440,13 @@ bool prefill_supported(int M, int N, int K) {
   return M > 0 && N % 32 == 0 && K % BK == 0;
 }
 
+bool use_prefill(int M, int N, int K, int sm_count) {
+  if (M <= 16 || !prefill_supported(M, N, K)) return false;
+  if (M > 32) return true;
+  const long long tiles = (long long)((M + 127) / 128) * ((N + BN - 1) / BN);
+  return tiles >= sm_count;
+}
+
 cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
   DeviceInfo info;
   cudaError_t err = device_info(&info);

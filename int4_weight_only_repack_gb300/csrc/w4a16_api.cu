@@ -217,7 +217,8 @@ w4_status w4_repack_gptq(const int32_t* qweight, const int32_t* qzeros, const vo
 size_t w4a16_gemm_workspace_size(int M, int N, int K, int group, int dtype, int has_perm) {
   (void)group;
   (void)dtype;
-  if (M <= DECODE_MAX_M || !prefill_supported(M, N, K)) return 0;
+  // enough for either kernel: the tcgen05 kernel may serve any M > 16
+  if (M <= 16 || !prefill_supported(M, N, K)) return 0;
   return prefill_workspace_bytes(M, K, has_perm != 0);
 }
 
@@ -267,7 +268,9 @@ w4_status w4a16_gemm(const void* x, const int32_t* qw, const void* scales, const
   a.bf16 = dtype == W4_BF16;
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
-  if (M > DECODE_MAX_M && prefill_supported(M, N, K))
+  DeviceInfo info;
+  if (device_info(&info) != cudaSuccess) return W4_ERR_CUDA;
+  if (use_prefill(M, N, K, info.sm_count))
     return from_cuda(launch_prefill(a, static_cast<cudaStream_t>(stream)));
   return from_cuda(launch_decode(a, static_cast<cudaStream_t>(stream)));
 }

@@ -46,6 +46,13 @@ struct GemmArgs {
 constexpr int DECODE_MAX_M = 64;
 cudaError_t launch_decode(const GemmArgs& a, cudaStream_t s);
 
+// Which kernel a call runs: the small-M kernel for M <= 16, and for M <= 32
+// unless the tcgen05 kernel's 128 x 256 output tiles alone fill the SMs; the
+// tcgen05 kernel above that (when it supports the shape). Measured on GB300
+// over the Llama-2-70B layers: at M = 32 the small-M kernel is 1.8 x faster on
+// qkv / down (40 / 32 output tiles) and 1.4 x slower on gate_up (224 tiles).
+bool use_prefill(int M, int N, int K, int sm_count);
+
 // Large-M tcgen05 kernel (M > DECODE_MAX_M, N % 32 == 0). Act-order calls
 // gather x[:, perm] into the workspace first.
 bool prefill_supported(int M, int N, int K);
