@@ -157,9 +157,12 @@ W4_API w4_status w4_repack_gptq(const int32_t* qweight, const int32_t* qzeros, c
                          int32_t* perm_out, int32_t* status_out, void* stream);
 
 /*
- * Workspace bytes w4a16_gemm needs for this call shape (0 = none). Act-order
+ * Workspace bytes w4a16_gemm wants for this call shape (0 = none). Act-order
  * calls with M > 16 that run the large-M kernel stage the gathered activations
- * x[:, perm] there
+ * x[:, perm] there (required). After that, calls whose 128 x 256 output tiles
+ * cannot fill the GPU keep fp32 partial tiles of a split-K run there (optional:
+ * with a smaller workspace the kernel splits K less, or not at all; the sum
+ * order, and so the result bits, follow the split chosen)
  * (M*K*2 bytes, rounded up to 256). The contents need no initialisation.
  */
 W4_API size_t w4a16_gemm_workspace_size(int M, int N, int K, int group, int dtype, int has_perm);
@@ -173,12 +176,12 @@ W4_API size_t w4a16_gemm_workspace_size(int M, int N, int K, int group, int dtyp
  *   qw     TILE layout words from w4_repack_*; zeros [G][N/8]; scales [G][N].
  *   perm   [K] from w4_repack_gptq for act-order layers, else NULL.
  *   y      [M][N] dtype, row-major; must not overlap any input.
- *   workspace / workspace_bytes: device scratch of at least
- *          w4a16_gemm_workspace_size(...) bytes (may be NULL when that is 0).
+ *   workspace / workspace_bytes: device scratch, ideally
+ *          w4a16_gemm_workspace_size(...) bytes (may be NULL when that is 0);
+ *          W4_ERR_WORKSPACE when it lacks the required act-order staging.
  * Accumulation is fp32; the result is rounded once to dtype. Deterministic:
- * the same inputs give the same bits. M <= 16 (M <= 32 unless the large-M
- * kernel's 128 x 256 output tiles alone fill the GPU; any M when N % 32 != 0)
- * runs the small-M kernel (CUDA-core dequantisation into exact operands: q - z for
+ * the same inputs give the same bits. M <= 16 (any M when N % 32 != 0) runs
+ * the small-M kernel (CUDA-core dequantisation into exact operands: q - z for
  * fp16, 128 + q for bf16 with the (128 + z) * s * sum(x) part removed in fp32;
  * mma.sync; per-group fp32 scaling); larger M runs the tcgen05 kernel, whose
  * B operand is the dequantised weight rounded once to dtype.
@@ -208,11 +211,14 @@ W4_API w4_status w4a16_gemm(const void* x, const int32_t* qw, const void* scales
  * the library behind an interface with no allocator.)
  *
  * Same arguments, layouts, results and error statuses as w4a16_gemm, minus
- * workspace / workspace_bytes. Where w4a16_gemm would need a workspace
- * (act-order calls with M > 64), this call stages x[:, perm] in one static
- * device array of W4_NOALLOC_SCRATCH_BYTES that the library holds on every
- * GPU that loads it, until the process exits; calls whose staging would
- * exceed it (M * K * 2 bytes) return W4_ERR_WORKSPACE and launch nothing.
+ * workspace / workspace_bytes. Where w4a16_gemm would use a workspace (calls
+ * of the large-M kernel: act-order staging of x[:, perm], split-K partials),
+ * this call uses one static device array of W4_NOALLOC_SCRATCH_BYTES that the
+ * library holds on every GPU that loads it, until the process exits; calls
+ * whose act-order staging would exceed it (M * K * 2 bytes) return
+ * W4_ERR_WORKSPACE and launch nothing, and split-K partials that do not fit
+ * after the staging make the kernel split K less (then the result bits can
+ * differ from a w4a16_gemm call given the full workspace).
  * It never allocates or frees device memory.
  *   - Set-up: the first call on each device looks up the array's device
  *     address (cudaGetSymbolAddress) with that device current. Make that first

@@ -81,9 +81,26 @@ struct PrefillParams {
   CUtensorMap tm_s;  // scales [G][N], box 256 x 2
   CUtensorMap tm_z;  // zeros [G][N/8], box 32 x 2
   uint16_t* y;
+  float* part;  // split-K partial tiles [ksplit][M][N] fp32 (ksplit > 1)
   int M, N, K, group;
-  int m_blocks, num_tiles, k_blocks;
+  int m_blocks, n_blocks, num_tiles, k_blocks, ksplit;
 };
+
+// Work unit `tile` -> (M block, N block, K slice [kb0, kb1) of k-blocks).
+// Units run M fastest, then N, then the K slice.
+struct Unit {
+  int m_blk, n_blk, ks, kb0, kb1;
+};
+__device__ __forceinline__ Unit unit_of(const PrefillParams& p, int tile) {
+  Unit u;
+  u.m_blk = tile % p.m_blocks;
+  const int rest = tile / p.m_blocks;
+  u.n_blk = rest % p.n_blocks;
+  u.ks = rest / p.n_blocks;
+  u.kb0 = (int)((long long)u.ks * p.k_blocks / p.ksplit);
+  u.kb1 = (int)((long long)(u.ks + 1) * p.k_blocks / p.ksplit);
+  return u;
+}
 
 template <int NBUF>
 struct Bars {
@@ -180,7 +197,6 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const int KB = p.k_blocks;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -190,8 +206,9 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
       for (int s = 0; s < STAGES; ++s) last_armed[s] = -1;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-        const int m_blk = tile % p.m_blocks, n_blk = tile / p.m_blocks;
-        for (int kb = 0; kb < KB; ++kb, ++it) {
+        const Unit u = unit_of(p, tile);
+        const int m_blk = u.m_blk, n_blk = u.n_blk;
+        for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           if (!wait_phase(bars.empty(s), ph ^ 1, abort_flag)) {
@@ -230,7 +247,8 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem + buf * (BN * NACC);
-        for (int kb = 0; kb < KB; ++kb, ++it) {
+        const Unit u = unit_of(p, tile);
+        for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           if (!wait_phase(bars.full(s), ph, abort_flag) || !wait_phase(bars.bfull(s), ph, abort_flag)) {
@@ -246,7 +264,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
               // accumulator i: rows 128 i .. 128 i + 127 of the A tile; advance
               // 16 elements (32 bytes) along K inside the swizzled rows
               const uint64_t adesc = smem_desc_k128(sbase + OFF_A + s * A_BYTES + i * (128 * BK * 2));
-              umma_f16(d_tmem + i * BN, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb | k) != 0);
+              umma_f16(d_tmem + i * BN, adesc + 2 * k, bdesc + 2 * k, IDESC, kb != u.kb0 || k != 0);
             }
           }
           issued = true;
@@ -264,7 +282,8 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     int lt = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++lt) {
-      const int m_blk = tile % p.m_blocks, n_blk = tile / p.m_blocks;
+      const Unit u = unit_of(p, tile);
+      const int m_blk = u.m_blk, n_blk = u.n_blk;
       const int buf = lt % NBUF;
       const uint32_t aph = (lt / NBUF) & 1;
       if (!wait_phase(bars.accfull(buf), aph, abort_flag)) break;
@@ -279,7 +298,16 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
           tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + buf * (BN * NACC) + i * BN + c0, r);
           tmem_ld_wait();
           const int n = n_blk * BN + c0;
-          if (m < p.M) {
+          if (p.ksplit > 1) {
+            // split K: this slice's fp32 partial tile (N % 32 == 0: whole 32-column chunks)
+            if (m < p.M && n < p.N) {
+              float4* dst = reinterpret_cast<float4*>(p.part + ((size_t)u.ks * p.M + m) * p.N + n);
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                     __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+            }
+          } else if (m < p.M) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               if (n + 8 * q < p.N) {
@@ -306,7 +334,8 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
     int it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-      for (int kb = 0; kb < KB; ++kb, ++it) {
+      const Unit u = unit_of(p, tile);
+      for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
         if (!wait_phase(bars.full(s), ph, abort_flag)) {
@@ -371,6 +400,24 @@ __global__ void __launch_bounds__(256) gather_columns_kernel(const uint16_t* __r
   }
 }
 
+// ---- split K: y = RN(sum over the K slices of the fp32 partials), in slice order --
+template <bool BF16>
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4* __restrict__ part,
+                                                            uint2* __restrict__ y, size_t n4,
+                                                            int ksplit) {
+  for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < n4; i += (size_t)gridDim.x * 256) {
+    float4 a = part[i];
+    for (int s = 1; s < ksplit; ++s) {
+      const float4 b = part[(size_t)s * n4 + i];
+      a.x += b.x;
+      a.y += b.y;
+      a.z += b.z;
+      a.w += b.w;
+    }
+    y[i] = make_uint2(pack_half2(a.x, a.y, BF16), pack_half2(a.z, a.w, BF16));
+  }
+}
+
 // ---- host side ------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static std::mutex mu;
@@ -429,6 +476,33 @@ cudaError_t ensure_prefill_smem(void* fn, int which, int bytes) {
   return e;
 }
 
+// Tiling and K split of a call. Two accumulators per CTA (256-row tiles) when
+// that takes fewer estimated wave-times: a 256-row tile does the MMA work of
+// two 128-row tiles in ~1.25x the time (it dequantises each B tile once for
+// both). When the output tiles cannot fill the SMs, K is split into slices of
+// at least 8 k-blocks so that tiles x slices still fit in one wave.
+struct PrefillPlan {
+  int nacc, m_blocks, n_blocks, ksplit;
+};
+PrefillPlan prefill_plan(int M, int N, int K, int sm_count) {
+  PrefillPlan pl;
+  pl.n_blocks = (N + BN - 1) / BN;
+  const long long t128 = (long long)((M + 127) / 128) * pl.n_blocks;
+  const long long t256 = (long long)((M + 255) / 256) * pl.n_blocks;
+  const double w128 = (double)((t128 + sm_count - 1) / sm_count);
+  const double w256 = 1.25 * (double)((t256 + sm_count - 1) / sm_count);
+  pl.nacc = w256 < w128 ? 2 : 1;
+  pl.m_blocks = (M + 128 * pl.nacc - 1) / (128 * pl.nacc);
+  const long long tiles = (long long)pl.m_blocks * pl.n_blocks;
+  pl.ksplit = 1;
+  if (tiles < sm_count) pl.ksplit = (int)std::max(1LL, std::min<long long>(K / BK / 8, sm_count / tiles));
+  return pl;
+}
+
+size_t split_bytes(int M, int N, int ksplit) {
+  return ksplit > 1 ? (size_t)ksplit * M * N * 4 : 0;
+}
+
 }  // namespace
 
 size_t prefill_workspace_bytes(int M, int K, bool has_perm) {
@@ -436,15 +510,19 @@ size_t prefill_workspace_bytes(int M, int K, bool has_perm) {
   return ((size_t)M * K * 2 + 255) & ~(size_t)255;
 }
 
+size_t prefill_split_workspace_bytes(int M, int N, int K) {
+  DeviceInfo info;
+  if (device_info(&info) != cudaSuccess) return 0;
+  return split_bytes(M, N, prefill_plan(M, N, K, info.sm_count).ksplit);
+}
+
 bool prefill_supported(int M, int N, int K) {
   return M > 0 && N % 32 == 0 && K % BK == 0;
 }
 
 bool use_prefill(int M, int N, int K, int sm_count) {
-  if (M <= 16 || !prefill_supported(M, N, K)) return false;
-  if (M > 32) return true;
-  const long long tiles = (long long)((M + 127) / 128) * ((N + BN - 1) / BN);
-  return tiles >= sm_count;
+  (void)sm_count;
+  return M > 16 && prefill_supported(M, N, K);
 }
 
 cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
@@ -461,17 +539,16 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     x = xg;
   }
-  // Two accumulators per CTA (256-row tiles) once they still give every SM a tile.
-  const int n_blocks = (a.N + BN - 1) / BN;
-  // A 256-row tile does the MMA work of two 128-row tiles in ~1.25x the time
-  // (it dequantises each B tile once for both). Pick the tiling with fewer
-  // estimated wave-times.
-  const long long t128 = (long long)((a.M + 127) / 128) * n_blocks;
-  const long long t256 = (long long)((a.M + 255) / 256) * n_blocks;
-  const double w128 = (double)((t128 + info.sm_count - 1) / info.sm_count);
-  const double w256 = 1.25 * (double)((t256 + info.sm_count - 1) / info.sm_count);
-  const int nacc = w256 < w128 ? 2 : 1;
+  PrefillPlan pl = prefill_plan(a.M, a.N, a.K, info.sm_count);
+  // the split-K partials go after the act-order staging, when the workspace
+  // has room for them; with less room the split shrinks (down to none)
+  const size_t staged = prefill_workspace_bytes(a.M, a.K, a.perm != nullptr);
+  const size_t room = a.workspace_bytes > staged ? a.workspace_bytes - staged : 0;
+  while (pl.ksplit > 1 && (a.workspace == nullptr || split_bytes(a.M, a.N, pl.ksplit) > room))
+    --pl.ksplit;
+  const int nacc = pl.nacc;
   const int BM = 128 * nacc;
+  const int n_blocks = pl.n_blocks;
   PrefillParams p;
   const int G = a.K / a.group;
   const CUtensorMapDataType act = a.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -483,12 +560,16 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
                        (uint64_t)a.N / 2, BN / 8, 2, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (!ok) return cudaErrorInvalidValue;
   p.y = static_cast<uint16_t*>(a.y);
+  p.part = pl.ksplit > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + staged)
+                         : nullptr;
   p.M = a.M;
   p.N = a.N;
   p.K = a.K;
   p.group = a.group;
   p.m_blocks = (a.M + BM - 1) / BM;
-  p.num_tiles = p.m_blocks * n_blocks;
+  p.n_blocks = n_blocks;
+  p.ksplit = pl.ksplit;
+  p.num_tiles = p.m_blocks * n_blocks * pl.ksplit;
   p.k_blocks = a.K / BK;
 
   void* fn;
@@ -515,7 +596,19 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   void* args[] = {&p};
-  return cudaLaunchKernelExC(&cfg, fn, args);
+  if ((err = cudaLaunchKernelExC(&cfg, fn, args)) != cudaSuccess) return err;
+  if (pl.ksplit > 1) {
+    const size_t n4 = (size_t)a.M * a.N / 4;
+    const unsigned g = (unsigned)std::min<size_t>((n4 + 255) / 256, (size_t)info.sm_count * 8);
+    if (a.bf16)
+      splitk_reduce_kernel<true><<<g, 256, 0, stream>>>(reinterpret_cast<const float4*>(p.part),
+                                                         static_cast<uint2*>(a.y), n4, pl.ksplit);
+    else
+      splitk_reduce_kernel<false><<<g, 256, 0, stream>>>(reinterpret_cast<const float4*>(p.part),
+                                                          static_cast<uint2*>(a.y), n4, pl.ksplit);
+    err = cudaGetLastError();
+  }
+  return err;
 }
 
 // ---- static scratch for w4a16_gemm_noalloc ------------------------------------

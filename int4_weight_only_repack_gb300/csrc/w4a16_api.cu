@@ -217,9 +217,12 @@ w4_status w4_repack_gptq(const int32_t* qweight, const int32_t* qzeros, const vo
 size_t w4a16_gemm_workspace_size(int M, int N, int K, int group, int dtype, int has_perm) {
   (void)group;
   (void)dtype;
-  // enough for either kernel: the tcgen05 kernel may serve any M > 16
+  // enough for either kernel: the tcgen05 kernel may serve any M > 16; the
+  // act-order staging is required, the split-K partials after it are used when
+  // present
   if (M <= 16 || !prefill_supported(M, N, K)) return 0;
-  return prefill_workspace_bytes(M, K, has_perm != 0);
+  const size_t staged = prefill_workspace_bytes(M, K, has_perm != 0);
+  return staged + prefill_split_workspace_bytes(M, N, K);
 }
 
 w4_status w4_device_status(int32_t* status_out, int clear) {
@@ -242,7 +245,11 @@ w4_status w4a16_gemm(const void* x, const int32_t* qw, const void* scales, const
   if (!aligned16(x) || !aligned16(qw) || !aligned16(scales) || !aligned16(zeros) ||
       !aligned16(perm) || !aligned16(y) || !aligned16(workspace))
     return W4_ERR_ALIGN;
-  const size_t need = w4a16_gemm_workspace_size(M, N, K, group, dtype, perm != nullptr);
+  // required: the act-order staging of the tcgen05 kernel (split-K partials are
+  // optional and sized by the kernel from what the workspace holds)
+  const size_t need = (M > 16 && prefill_supported(M, N, K))
+                          ? prefill_workspace_bytes(M, K, perm != nullptr)
+                          : 0;
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return W4_ERR_WORKSPACE;
   if (M == 0) return W4_OK;
   const int g = resolve_group(group, K);
@@ -282,10 +289,12 @@ w4_status w4a16_gemm_noalloc(const void* x, const int32_t* qw, const void* scale
   if (st) return st;
   if (M < 0 || M > MAX_DIM) return W4_ERR_SHAPE;
   if ((st = check_layout_dims(K, N, W4_LAYOUT_TILE))) return st;
-  const size_t need = w4a16_gemm_workspace_size(M, N, K, group, dtype, perm != nullptr);
+  const size_t need = (M > 16 && prefill_supported(M, N, K))
+                          ? prefill_workspace_bytes(M, K, perm != nullptr)
+                          : 0;
   if (need > W4_NOALLOC_SCRATCH_BYTES) return W4_ERR_WORKSPACE;
-  if (need == 0 || M == 0) {
-    // nothing to stage: the call is w4a16_gemm without a workspace
+  if (M == 0 || M <= 16 || !prefill_supported(M, N, K)) {
+    // the small-M kernel uses no workspace: the call is w4a16_gemm without one
     return w4a16_gemm(x, qw, scales, zeros, perm, y, M, N, K, group, dtype, nullptr, 0, stream);
   }
   // validate everything the scratch does not decide before touching the device

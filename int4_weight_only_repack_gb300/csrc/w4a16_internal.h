@@ -46,17 +46,22 @@ struct GemmArgs {
 constexpr int DECODE_MAX_M = 64;
 cudaError_t launch_decode(const GemmArgs& a, cudaStream_t s);
 
-// Which kernel a call runs: the small-M kernel for M <= 16, and for M <= 32
-// unless the tcgen05 kernel's 128 x 256 output tiles alone fill the SMs; the
-// tcgen05 kernel above that (when it supports the shape). Measured on GB300
-// over the Llama-2-70B layers: at M = 32 the small-M kernel is 1.8 x faster on
-// qkv / down (40 / 32 output tiles) and 1.4 x slower on gate_up (224 tiles).
+// Which kernel a call runs: the small-M kernel for M <= 16, the tcgen05 kernel
+// above that when it supports the shape (N % 32 == 0). Measured on GB300 over
+// the Llama-2-70B layers: at M = 32 the small-M kernel (4 token tiles) takes
+// 57 / 191 / 178 us (qkv / gate_up / down) against 41 / 193 / 91 us for the
+// tcgen05 kernel at M = 64 with K split across otherwise idle SMs; at M = 16
+// the small-M kernel is still ahead on qkv and gate_up.
 bool use_prefill(int M, int N, int K, int sm_count);
 
 // Large-M tcgen05 kernel (M > DECODE_MAX_M, N % 32 == 0). Act-order calls
 // gather x[:, perm] into the workspace first.
 bool prefill_supported(int M, int N, int K);
 size_t prefill_workspace_bytes(int M, int K, bool has_perm);
+// Further workspace bytes the tcgen05 kernel uses, when given, for a split-K
+// run of a call whose output tiles cannot fill the GPU (0 when it would not
+// split, or when no device is current).
+size_t prefill_split_workspace_bytes(int M, int N, int K);
 cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t s);
 
 // Device address and size of the static scratch array of w4a16_gemm_noalloc

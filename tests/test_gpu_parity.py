@@ -216,15 +216,8 @@ def ulp_error(y_bits, y_ref, dtype):
 
 
 def small_m_kernel(M, N):
-    """Whether a call runs the small-M kernel: M <= 16, or N % 32 != 0, or M <= 32
-    with fewer 128 x 256 output tiles than the GPU has SMs."""
-    import torch
-    if M <= 16 or N % 32:
-        return True
-    if M > 32:
-        return False
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    return ((M + 127) // 128) * ((N + 255) // 256) < sms
+    """Whether a call runs the small-M kernel: M <= 16, or N % 32 != 0."""
+    return M <= 16 or N % 32 != 0
 
 
 GEMM_CASES = [
@@ -329,6 +322,8 @@ PREFILL_CASES = [
     (256, 4096, 128, "bf16", (2048,)),           # 256 tiles: several per CTA
     (128, 4128, 128, "bf16", (2600,)),           # 256-row tiles, ragged in M and N
     (256, 4096, 32, "fp16", (2560,)),            # 256-row tiles, group 32
+    (4096, 256, 128, "bf16", (128, 100)),        # one output tile: K split 8 ways
+    (2048, 512, 64, "fp16", (65,)),              # two output tiles: K split 4 ways
 ]
 
 
@@ -380,6 +375,28 @@ def test_gemm_large_m_workspace_checked(w4):
     small = torch.empty(M * K * 2 - 256, dtype=torch.uint8, device="cuda")
     with pytest.raises(w4.W4Error):
         w4.w4a16_gemm(x, qw, scales, zeros, perm, y, M, N, K, 128, "fp16", small)
+
+
+def test_gemm_split_k_follows_the_workspace(w4):
+    """With less workspace than w4a16_gemm_workspace_size the tcgen05 kernel splits
+    K less (down to no split): every size gives a correct result."""
+    import torch
+    K, N, M = 4096, 256, 128
+    L = synth.make_custom_layer([121], K, N, group=128, dtype="bf16")
+    qw, zeros, scales, perm, _ = repack(w4, L, w4.W4_LAYOUT_TILE)
+    xb = synth.make_custom_x([122], M, K, "bf16")
+    x = half_to_dev(xb, "bf16")
+    y_rw = rounded_w_reference(xb, L, 128)
+    full = w4.w4a16_gemm_workspace_size(M, N, K, 128, "bf16", False)
+    assert full >= 2 * M * N * 4  # this shape wants a split
+    for size in (full, M * N * 4 * 3, M * N * 4 * 2, 16, 0):
+        ws = torch.zeros(max(size, 16), dtype=torch.uint8, device="cuda") if size else None
+        y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        w4.w4a16_gemm(x, qw, scales, zeros, perm, y, M, N, K, 128, "bf16", ws)
+        torch.cuda.synchronize()
+        yb = half_from_dev(y)
+        assert ulp_error(yb, y_rw, "bf16") <= 1.0, (size, ulp_error(yb, y_rw, "bf16"))
+    assert w4.w4_device_status() == 0
 
 
 def test_gemm_large_m_non_multiple_of_32_columns(w4):
