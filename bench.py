@@ -199,6 +199,13 @@ def build_calls(w4, torch, device):
             y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
             calls.append(dict(name=name, K=K, N=N, M=M, layer=layer, x=x, y=y, x_bits=x_bits))
         del qweight, qzeros, scales
+    # one workspace for the stream, as big as the largest call asks for (the
+    # calls run in stream order, so they can share it)
+    need = max(w4.w4a16_gemm_workspace_size(c["M"], c["N"], c["K"], WORKLOAD.group,
+                                            torch.bfloat16, False) for c in calls)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+    for c in calls:
+        c["ws"] = ws
     torch.cuda.synchronize()
     return calls
 
@@ -207,7 +214,7 @@ def run_step(w4, calls):
     for c in calls:
         L = c["layer"]
         w4.w4a16_gemm(c["x"], L.qw, L.scales, L.zeros, None, c["y"], c["M"], c["N"], c["K"],
-                      L.group, L.dtype)
+                      L.group, L.dtype, c["ws"])
 
 
 def per_launch_times(w4, torch, calls, reps: int, device):
@@ -230,7 +237,7 @@ def per_launch_times(w4, torch, calls, reps: int, device):
             L = c["layer"]
             e0.record(stream)
             w4.w4a16_gemm(c["x"], L.qw, L.scales, L.zeros, None, c["y"], c["M"], c["N"], c["K"],
-                          L.group, L.dtype)
+                          L.group, L.dtype, c["ws"])
             e1.record(stream)
         torch.cuda.synchronize()
         for i, (e0, e1) in enumerate(evs):

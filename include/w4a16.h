@@ -108,6 +108,14 @@ enum { W4_LAYOUT_STD = 0, W4_LAYOUT_TILE = 1 };
 /* Human-readable name of a status code (static string, never NULL). */
 W4_API const char* w4_status_string(w4_status status);
 
+/*
+ * After an entry point returned W4_ERR_CUDA on this host thread: the CUDA
+ * runtime's name and description of the error it got ("cudaErrorInvalidValue:
+ * invalid argument"), in a buffer of the calling thread that the next call
+ * overwrites. "no CUDA error" before any such return.
+ */
+W4_API const char* w4_last_cuda_error(void);
+
 /* ABI version of this library (increments on incompatible changes). */
 W4_API int w4_abi_version(void);
 

@@ -16,8 +16,9 @@ import torch
 
 __all__ = [
     "W4_F16", "W4_BF16", "W4_LAYOUT_STD", "W4_LAYOUT_TILE", "W4Error", "lib", "library_path",
-    "dtype_code", "w4_status_string", "w4_abi_version", "w4_repack_sizes", "w4_repack_awq",
-    "w4_repack_gptq", "w4a16_gemm_workspace_size", "w4a16_gemm", "w4a16_gemm_noalloc", "w4_dequant",
+    "dtype_code", "w4_status_string", "w4_last_cuda_error", "w4_abi_version", "w4_repack_sizes", "w4_repack_awq",
+    "w4_repack_gptq", "w4a16_gemm_workspace_size", "w4a16_gemm", "w4a16_gemm_noalloc",
+    "w4_dequant", "gemm_workspace",
     "w4_device_status",
     "RepackedLayer", "repack_awq", "repack_gptq", "linear",
 ]
@@ -25,6 +26,7 @@ __all__ = [
 W4_F16, W4_BF16 = 0, 1
 W4_LAYOUT_STD, W4_LAYOUT_TILE = 0, 1
 W4_OK = 0
+W4_ERR_CUDA = 9
 W4_ERR_GIDX = 11
 
 _PKG_DIR = os.path.dirname(os.path.abspath(__file__))
@@ -34,6 +36,7 @@ _LIB: Optional[ctypes.CDLL] = None
 _c_int, _c_size, _c_void_p = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
 _SIGNATURES = {
     "w4_status_string": (ctypes.c_char_p, [_c_int]),
+    "w4_last_cuda_error": (ctypes.c_char_p, []),
     "w4_abi_version": (_c_int, []),
     "w4_repack_sizes": (_c_int, [_c_int, _c_int, _c_int, _c_int, ctypes.POINTER(_c_size),
                                  ctypes.POINTER(_c_size), ctypes.POINTER(_c_size)]),
@@ -81,13 +84,20 @@ def w4_status_string(status: int) -> str:
     return lib().w4_status_string(status).decode()
 
 
+def w4_last_cuda_error() -> str:
+    return lib().w4_last_cuda_error().decode()
+
+
 def w4_abi_version() -> int:
     return lib().w4_abi_version()
 
 
 def _check(status: int):
     if status != W4_OK:
-        raise W4Error(status, w4_status_string(status))
+        msg = w4_status_string(status)
+        if status == W4_ERR_CUDA:
+            msg += f" ({w4_last_cuda_error()})"
+        raise W4Error(status, msg)
 
 
 def _ptr(t) -> Optional[int]:
@@ -213,15 +223,33 @@ def repack_gptq(qweight, qzeros, scales, g_idx, K, N, group, dtype, layout=W4_LA
     return RepackedLayer(K, N, group, dtype, layout, qw, zeros, sc, perm, status)
 
 
+_WORKSPACES: dict = {}
+
+
+def gemm_workspace(nbytes: int, device, stream=None):
+    """A workspace of at least nbytes on `device` for calls on `stream`, kept
+    and reused across calls (calls on one stream run in order, so they can
+    share it, and no call allocates device memory once it is big enough)."""
+    dev = torch.device(device)
+    key = (dev.index if dev.index is not None else torch.cuda.current_device(), _stream(stream))
+    ws = _WORKSPACES.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        _WORKSPACES[key] = ws
+    return ws
+
+
 def linear(x, layer: RepackedLayer, y=None, workspace=None, stream=None):
-    """y = x · W for a TILE-layout layer; x is [M, K] fp16/bf16 on the device."""
+    """y = x · W for a TILE-layout layer; x is [M, K] fp16/bf16 on the device.
+    Without `workspace`, the one kept for (device, stream) is used (grown as
+    needed); a caller's own workspace must follow w4a16_gemm_workspace_size."""
     M = x.shape[0]
     if y is None:
         y = torch.empty((M, layer.N), dtype=x.dtype, device=x.device)
     need = w4a16_gemm_workspace_size(M, layer.N, layer.K, layer.group, layer.dtype,
                                      layer.perm is not None)
     if need and workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+        workspace = gemm_workspace(need, x.device, stream)
     w4a16_gemm(x, layer.qw, layer.scales, layer.zeros, layer.perm, y, M, layer.N, layer.K,
                layer.group, layer.dtype, workspace, None, stream)
     return y

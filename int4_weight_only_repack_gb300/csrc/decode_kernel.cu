@@ -37,8 +37,10 @@
 //    fixed order (deterministic, no global workspace, no atomics:
 //    "vLLM AWQ 4-bit 量化实践" §5.3 names split-K for the fused kernel).
 //  * Launches use programmatic stream serialization: a CTA may become resident
-//    while the previous kernel drains; it waits for it (griddepcontrol.wait)
-//    before reading x or staging anything from global memory.
+//    while the previous kernel drains. It requests its weights, scales and
+//    zeros at once, waits for that kernel (griddepcontrol.wait) before reading
+//    x or writing anything, and then lets the next kernel on the stream launch
+//    so that its prologue overlaps this kernel's tail.
 //  * Every wait is bounded (one second). A timed-out wait records
 //    W4_ERR_TIMEOUT in the device status word and raises a CTA abort flag that
 //    ends every other wait at once; the CTA lets its copies in flight land
@@ -50,6 +52,7 @@
 #include <type_traits>
 #include <unordered_map>
 
+#include "decode_common.cuh"
 #include "sm100_ptx.cuh"
 #include "w4a16_device.cuh"
 #include "w4a16_internal.h"
@@ -58,11 +61,10 @@ namespace cg = cooperative_groups;
 
 namespace w4 {
 
-extern __device__ int g_device_status;
-
 namespace {
 
 using namespace sm100;
+using namespace dec;
 
 constexpr int DEC_WARPS = 8;                  // one warp per tile of a 128-column group
 constexpr int DEC_THREADS = DEC_WARPS * 32;
@@ -80,7 +82,6 @@ constexpr int X_BUDGET = 48 * 1024;           // bytes of staged x per CTA
 #ifndef W4_DECODE_PF
 #define W4_DECODE_PF 2  // stages prefetched into L2 beyond the ring
 #endif
-constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
 
 struct DecodeParams {
   const uint16_t* x;       // [M][K]
@@ -99,6 +100,7 @@ struct DecodeParams {
   int x_stride;            // shared x row stride in halves
   int maxg;                // group slots per chunk
   int slice;               // output columns owned by each CTA of a cluster
+  int* status;             // the library's device status word
 };
 
 struct SmemLayout {
@@ -125,88 +127,6 @@ __host__ __device__ inline SmemLayout smem_layout(int MT, int m_rows, int x_stri
   L.recv = L.xsum + maxg * 8 * MT * 4;
   L.total = L.recv + S * slice * 8 * MT * 4;
   return L;
-}
-
-__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-// Weight-stream copy: the weights are read once per call, so they are marked
-// evict-first in L2, which keeps x, scales and zeros resident.
-__device__ __forceinline__ void bulk_copy_stream(uint32_t dst, const void* src, uint32_t bytes,
-                                                 uint32_t bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
-      "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
-      : "memory");
-}
-
-// Bring [src, src + bytes) into L2 (16-byte aligned, a multiple of 16 bytes).
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ uint64_t evict_first_policy() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-
-// 16-byte shared-memory load from a 32-bit shared-window address.
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
-  return v;
-}
-
-// Bounded wait that also gives up at once when the CTA's abort flag is up;
-// false when it gave up (a timeout raises the flag and records the status).
-__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity,
-                                             volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
-      *abort_flag = 1;
-      atomicExch(&g_device_status, W4_ERR_TIMEOUT);
-      return false;
-    }
-  }
-  return true;
-}
-
-// Bounded wait used only while draining after an abort.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) return;
-}
-
-// D += A * B for one m16n8k16 tile, fp32 accumulate (non-volatile: the
-// compiler may schedule it freely; its outputs keep it alive).
-template <bool BF16>
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-  if constexpr (BF16) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-  } else {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-  }
 }
 
 // MT: token tiles of 8 (M <= 8 * MT). G64: every 64-row atom lies in one group.
@@ -369,6 +289,9 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
   if (nchunks > 0) stage_chunk_meta(0);
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // every CTA of this grid is resident: the next kernel may start its own
+  // prologue as resources free up
+  asm volatile("griddepcontrol.launch_dependents;");
   if (tid == 0 && x_async && nchunks > 0) {
     issue_x(0);
     if (NB == 2 && nchunks > 1) issue_x(1);
@@ -440,7 +363,7 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
       }
       if constexpr (BF16) __syncthreads();  // the sums below read every warp's rows
     } else if (live) {
-      bounded_wait(xbar0 + 8 * b, (uint32_t)((NB == 2 ? ci >> 1 : ci) & 1), abort_flag);
+      bounded_wait(xbar0 + 8 * b, (uint32_t)((NB == 2 ? ci >> 1 : ci) & 1), abort_flag, p.status);
     }
     // 3) per-group sums of x (bf16): warp w takes group slots w, w + 8, ... and runs
     //    the group's 32-row halves in this chunk through all-ones MMAs (two chains)
@@ -558,7 +481,7 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
     const int j1 = min(NS, (c1 - ka0 + SA - 1) / SA);
     const uint32_t wbase = ring_s + (uint32_t)warp * ATOM_BYTES + (uint32_t)lane * 16u;
     for (int j = j0; j < j1; ++j) {
-      const bool ready = live && bounded_wait(full0 + 8 * rslot, rphase, abort_flag);
+      const bool ready = live && bounded_wait(full0 + 8 * rslot, rphase, abort_flag, p.status);
       if (ready && has_cols) {
         const int a_base = ka0 + j * SA;
         const uint32_t st = wbase + rslot * STAGE_BYTES;
@@ -606,8 +529,6 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
       issue_x(ci + 2);
     }
   }
-  // the weight stream is done: the next kernel on the stream may start launching
-  asm volatile("griddepcontrol.launch_dependents;");
 
   // ---- after an abort: let every copy in flight land before the CTA exits ------
   if (*abort_flag) {
@@ -830,6 +751,8 @@ cudaError_t launch_decode(const GemmArgs& a, cudaStream_t stream) {
   if (a.group == a.K || gshift < 0) gshift = 31;  // one group over all of K
   const int A = a.K / ATOM_K;
   const bool g64 = gshift >= 6;  // groups of 64 or more: one group per atom
+  int* status = nullptr;
+  if ((err = device_status_ptr(&status)) != cudaSuccess) return err;
   for (int r0 = 0; r0 < a.M; r0 += DECODE_MAX_M) {
     const int Mc = std::min(DECODE_MAX_M, a.M - r0);
     const int MT = Mc <= 8 ? 1 : Mc <= 16 ? 2 : Mc <= 32 ? 4 : 8;
@@ -857,6 +780,7 @@ cudaError_t launch_decode(const GemmArgs& a, cudaStream_t stream) {
     p.x_stride = plan.x_stride;
     p.maxg = plan.maxg;
     p.slice = plan.slice;
+    p.status = status;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((a.N / 16 + DEC_WARPS - 1) / DEC_WARPS, plan.S, 1);

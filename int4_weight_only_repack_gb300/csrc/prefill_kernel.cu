@@ -635,6 +635,25 @@ cudaError_t noalloc_scratch(void** out, size_t* bytes) {
   return cudaSuccess;
 }
 
+// Device address of the status word, for the kernels of the other translation
+// units (each .cu compiles on its own, so they cannot name the symbol).
+cudaError_t device_status_ptr(int** out) {
+  static std::mutex mu;
+  static int* addr[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_device_status)) != cudaSuccess) return e;
+    addr[dev] = static_cast<int*>(p);
+  }
+  *out = addr[dev];
+  return cudaSuccess;
+}
+
 cudaError_t read_device_status(int* out, int clear) {
   int v = 0;
   cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int));

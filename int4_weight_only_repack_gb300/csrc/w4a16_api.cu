@@ -4,6 +4,7 @@
 // reported even on a machine without a GPU, and nothing is launched on error.
 #include <cuda_runtime.h>
 
+#include <cstdio>
 #include <mutex>
 
 #include "w4a16_internal.h"
@@ -61,7 +62,14 @@ w4_status check_arch() {
   return W4_OK;
 }
 
-w4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? W4_OK : W4_ERR_CUDA; }
+// The last CUDA error an entry point reported on this thread (w4_last_cuda_error).
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+w4_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return W4_OK;
+  g_last_cuda_error = e;
+  return W4_ERR_CUDA;
+}
 
 }  // namespace
 
@@ -115,6 +123,14 @@ const char* w4_status_string(w4_status s) {
     case W4_ERR_TIMEOUT: return "W4_ERR_TIMEOUT: a kernel gave up on a pipeline wait";
     default: return "unknown w4_status";
   }
+}
+
+const char* w4_last_cuda_error(void) {
+  static thread_local char buf[256];
+  if (g_last_cuda_error == cudaSuccess) return "no CUDA error";
+  snprintf(buf, sizeof(buf), "%s: %s", cudaGetErrorName(g_last_cuda_error),
+           cudaGetErrorString(g_last_cuda_error));
+  return buf;
 }
 
 int w4_abi_version(void) { return 2; }

@@ -68,8 +68,11 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t s);
 // (looked up once per device, with that device current).
 cudaError_t noalloc_scratch(void** out, size_t* bytes);
 
-// The device status word the kernels raise on a timed-out wait.
+// The device status word the kernels raise on a timed-out wait, and its device
+// address (looked up once per device) for the kernels of other translation
+// units, which take it as a parameter.
 cudaError_t read_device_status(int* out, int clear);
+cudaError_t device_status_ptr(int** out);
 
 // Device properties cached per device.
 struct DeviceInfo {

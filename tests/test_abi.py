@@ -38,6 +38,7 @@ def test_status_strings_and_version():
     assert w4.w4_abi_version() == 2
     for st in range(12):
         assert w4.w4_status_string(st)
+    assert w4.w4_last_cuda_error() == "no CUDA error"
     assert "unknown" in w4.w4_status_string(99)
 
 

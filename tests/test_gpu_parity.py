@@ -254,6 +254,52 @@ def test_gemm_vs_oracle(w4, K, N, group, dtype, Ms):
             assert ulp_error(y, y_rw, dtype) <= 1.0, (M, ulp_error(y, y_rw, dtype))
 
 
+# Small-M shapes with several column groups, K split across a cluster, a
+# partial last column group (N = 1184 / 2080 / 1056 / 32), groups of 64, 128
+# and all of K, both activation types and token counts on both sides of 8.
+SMALL_M_CASES = [
+    # K, N, group, dtype, Ms
+    (4096, 1184, 128, "bf16", (1, 4, 9, 16)),
+    (4096, 4096, 128, "fp16", (1, 16)),
+    (1536, 2080, -1, "bf16", (2, 16)),
+    (1536, 1056, 64, "fp16", (3, 8)),
+    (64, 32, 64, "bf16", (1, 16)),
+]
+
+
+def gemm_with(w4, L, x_bits, parts, M, group, ws):
+    import torch
+    qw, zeros, scales, perm, _ = parts
+    raw, y = guarded(M * L.N, hdt(L.dtype))
+    w4.w4a16_gemm(half_to_dev(x_bits, L.dtype), qw, scales, zeros, perm, y, M, L.N, L.K, group,
+                  L.dtype, ws)
+    torch.cuda.synchronize()
+    check_guards(raw, M * L.N, 2)
+    return half_from_dev(y).reshape(M, L.N)
+
+
+@pytest.mark.parametrize("K,N,group,dtype,Ms", SMALL_M_CASES)
+def test_gemm_small_m_vs_oracle(w4, K, N, group, dtype, Ms):
+    """The small-M kernel against the oracle, exact up to the final rounding,
+    with the same bits on a repeated call and whatever workspace is passed (it
+    uses none)."""
+    import torch
+    g = K if group == -1 else group
+    L = synth.make_custom_layer([121, K, N], K, N, group=g, dtype=dtype)
+    parts = repack_layer_group(w4, L, w4.W4_LAYOUT_TILE, group)
+    for M in Ms:
+        x = synth.make_custom_x([123, K, M], M, K, dtype)
+        y_ref = oracle.reference_y(x, L.qweight, L.qzeros, L.scales, g, dtype, "awq")
+        assert w4.w4a16_gemm_workspace_size(M, N, K, group, dtype, False) == 0
+        junk = torch.full((4096,), 0xA5, dtype=torch.uint8, device="cuda")
+        outs = [gemm_with(w4, L, x, parts, M, group, ws) for ws in (None, junk, None)]
+        for y in outs:
+            assert oracle.rel_err(oracle.half_bits_to_f64(y, dtype), y_ref) <= TOL, M
+            assert ulp_error(y, y_ref, dtype) <= 1.0, (M, ulp_error(y, y_ref, dtype))
+        assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2]), M
+    assert w4.w4_device_status() == 0
+
+
 @pytest.mark.parametrize("K,N,group,Ms", [(512, 272, 128, (1, 4, 16, 40)),
                                           (1536, 64, 64, (1, 9)), (1024, 96, 32, (2, 17))])
 def test_gemm_act_order_vs_oracle(w4, K, N, group, Ms):
