@@ -57,7 +57,7 @@ FALLBACK_TC_TFLOPS = 1900.0
 # dram__bytes_write.sum), keyed by the sha1 of the kernel source they were
 # taken on; see profiles/. A changed kernel source reports null.
 TRAFFIC_RECORDS: dict = {
-    "83a653689101": 26433600,   # mean of the 12 launches of one step
+    "7cef53ccda72": 26435392,   # mean of the 12 launches of one step
 }
 
 
@@ -593,29 +593,37 @@ def single(args):
 
 
 def sweep(args):
-    """The Llama-2-70B sweep (three layers, M from 1 to 4096): one JSON line per
-    (layer, M) with time, weight GB/s, TFLOP/s and the fraction of the matching
-    roofline (HBM for M <= 16, dense bf16 tensor peak above)."""
+    """A layer sweep over M: one JSON line per (layer, M) with time, weight
+    GB/s, TFLOP/s and the fraction of the matching roofline (HBM for M <= 16,
+    dense bf16 tensor peak above). Default: the Llama-2-70B layers, M from 1 to
+    4096 (--sweep-config 4); --sweep-config 3: the Llama-2-13B GPTQ act-order
+    layers (fp16, M in {1, 16, 1024})."""
     import torch
 
     import int4_weight_only_repack_gb300 as w4
 
     dev = torch.device("cuda")
-    wl = synth.WORKLOADS[4]
+    wl = synth.WORKLOADS[args.sweep_config]
     hbm, _ = measured_peaks()
     tc, _ = measured_tc_peak()
+    hdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float16
     for li, (K, N, name) in enumerate(wl.shapes):
         L = synth.make_workload_layer(wl.index, li)
         qweight = torch.from_numpy(L.qweight).to(dev)
         qzeros = torch.from_numpy(L.qzeros).to(dev)
-        scales = torch.from_numpy(L.scales.view(np.int16)).to(dev).view(torch.bfloat16)
+        scales = torch.from_numpy(L.scales.view(np.int16)).to(dev).view(hdt)
+        g_idx = torch.from_numpy(L.g_idx).to(dev) if L.g_idx is not None else None
         ncopy = max(2, int(400e6 // alg_bytes(K, N)) + 1)
-        layers = [w4.repack_awq(qweight, qzeros, scales, K, N, wl.group, torch.bfloat16)
-                  for _ in range(ncopy)]
+        if wl.fmt == "gptq":
+            layers = [w4.repack_gptq(qweight, qzeros, scales, g_idx, K, N, wl.group, hdt)
+                      for _ in range(ncopy)]
+        else:
+            layers = [w4.repack_awq(qweight, qzeros, scales, K, N, wl.group, hdt)
+                      for _ in range(ncopy)]
         del qweight, qzeros, scales
         for M in wl.ms:
-            x = torch.randn(M, K, device=dev).to(torch.bfloat16)
-            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            x = torch.randn(M, K, device=dev).to(hdt)
+            y = torch.empty((M, N), dtype=hdt, device=dev)
             use = layers if M <= 256 else layers[:2]
 
             def fn():
@@ -626,6 +634,7 @@ def sweep(args):
             gbs = alg_bytes(K, N) / t / 1e9
             tfl = 2.0 * M * N * K / t / 1e12
             print(json.dumps({"sweep": wl.name, "layer": name, "K": K, "N": N, "M": M,
+                              "dtype": wl.dtype, "act_order": g_idx is not None,
                               "us": round(t * 1e6, 2), "weight_gbs": round(gbs, 1),
                               "tflops": round(tfl, 1),
                               "frac": round(gbs / hbm if M <= 16 else tfl / tc, 3),
@@ -633,6 +642,7 @@ def sweep(args):
             del x, y
         del layers
         torch.cuda.empty_cache()
+    print(json.dumps({"sweep_done": wl.name, "device_status": w4.w4_device_status()}), flush=True)
 
 
 def main():
@@ -645,8 +655,10 @@ def main():
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the large-M (prefill) layers")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--sweep-config", type=int, default=4, choices=(3, 4),
+                    help="workload of --sweep: 4 = Llama-2-70B, 3 = Llama-2-13B GPTQ act-order")
     ap.add_argument("--sweep", action="store_true",
-                    help="the Llama-2-70B layers at every M of that workload (one line each)")
+                    help="every layer of --sweep-config at every M of that workload (one line each)")
     ap.add_argument("--single", default=None,
                     help="K,N,M[,dtype]: time one layer shape only (profiling aid)")
     args = ap.parse_args()

@@ -165,13 +165,17 @@ W4_API w4_status w4_repack_gptq(const int32_t* qweight, const int32_t* qzeros, c
                          int32_t* perm_out, int32_t* status_out, void* stream);
 
 /*
- * Workspace bytes w4a16_gemm wants for this call shape (0 = none). Act-order
- * calls with M > 16 that run the large-M kernel stage the gathered activations
- * x[:, perm] there (required). After that, calls whose 128 x 256 output tiles
- * cannot fill the GPU keep fp32 partial tiles of a split-K run there (optional:
- * with a smaller workspace the kernel splits K less, or not at all; the sum
- * order, and so the result bits, follow the split chosen)
- * (M*K*2 bytes, rounded up to 256). The contents need no initialisation.
+ * Workspace bytes w4a16_gemm wants for this call shape (0 = none). The
+ * contents need no initialisation.
+ *   - Act-order calls stage the gathered activations x[:, perm] there first
+ *     (M*K*2 bytes, rounded up to 256): required for calls that run the
+ *     large-M kernel; optional for the small-M kernel, whose CTAs otherwise
+ *     each gather the columns they need (slower at larger M: every column
+ *     group's CTAs read the same columns).
+ *   - After that, large-M calls whose 128 x 256 output tiles cannot fill the
+ *     GPU keep fp32 partial tiles of a split-K run there (optional: with a
+ *     smaller workspace the kernel splits K less, or not at all; the sum
+ *     order, and so the result bits, follow the split chosen).
  */
 W4_API size_t w4a16_gemm_workspace_size(int M, int N, int K, int group, int dtype, int has_perm);
 
@@ -219,14 +223,15 @@ W4_API w4_status w4a16_gemm(const void* x, const int32_t* qw, const void* scales
  * the library behind an interface with no allocator.)
  *
  * Same arguments, layouts, results and error statuses as w4a16_gemm, minus
- * workspace / workspace_bytes. Where w4a16_gemm would use a workspace (calls
- * of the large-M kernel: act-order staging of x[:, perm], split-K partials),
+ * workspace / workspace_bytes. Where w4a16_gemm would use a workspace
+ * (act-order staging of x[:, perm]; split-K partials of the large-M kernel),
  * this call uses one static device array of W4_NOALLOC_SCRATCH_BYTES that the
- * library holds on every GPU that loads it, until the process exits; calls
- * whose act-order staging would exceed it (M * K * 2 bytes) return
- * W4_ERR_WORKSPACE and launch nothing, and split-K partials that do not fit
- * after the staging make the kernel split K less (then the result bits can
- * differ from a w4a16_gemm call given the full workspace).
+ * library holds on every GPU that loads it, until the process exits. Large-M
+ * calls whose act-order staging would exceed it (M * K * 2 bytes) return
+ * W4_ERR_WORKSPACE and launch nothing (small-M ones gather in the kernel
+ * instead), and split-K partials that do not fit after the staging make the
+ * kernel split K less (then the result bits can differ from a w4a16_gemm call
+ * given the full workspace).
  * It never allocates or frees device memory.
  *   - Set-up: the first call on each device looks up the array's device
  *     address (cudaGetSymbolAddress) with that device current. Make that first

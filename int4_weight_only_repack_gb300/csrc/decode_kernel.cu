@@ -673,7 +673,9 @@ DecodePlan fit_ring(int S, int A, int Mc, int MT, int gshift, int per_sm, int sm
 //    dominated by the fixed prologue / reduction cost, longer ones by the wait
 //    for the slowest CTA);
 //  * with one token tile the launch aims at about 2.6 CTAs per SM (enough warps
-//    to hide the loop's latencies, few enough to stay near one wave).
+//    to hide the loop's latencies, few enough to stay near one wave);
+//  * with more token tiles, a split that would take more than three waves is
+//    replaced by the longest CTA ranges (x in chunks) at about one wave.
 // The ring is then as deep as fits with 3 resident CTAs per SM (2 when the
 // register budget allows only 2), at least 2 stages.
 DecodePlan plan_decode(int N, int K, int Mc, int MT, int gshift, const DeviceInfo& info) {
@@ -685,6 +687,7 @@ DecodePlan plan_decode(int N, int K, int Mc, int MT, int gshift, const DeviceInf
   while (s_x < s_cap && (long long)cta_atoms(s_x) * ATOM_K * Mc * 2 > X_BUDGET) ++s_x;
   int s_lo = 1;  // at most 64 k-atoms per CTA
   while (s_lo < s_cap && cta_atoms(s_lo) > 64) ++s_lo;
+  const int s64 = s_lo;
   s_lo = std::max(s_lo, s_x);
   int s_hi = s_cap;  // at least 16 k-atoms per CTA
   while (s_hi > 1 && cta_atoms(s_hi) < 16) --s_hi;
@@ -693,6 +696,12 @@ DecodePlan plan_decode(int N, int K, int Mc, int MT, int gshift, const DeviceInf
   if (MT == 1) {
     const int target = (int)(2.6 * info.sm_count / NG + 0.5);
     S = std::min(std::max(target, s_lo), s_hi);
+  } else if ((long long)NG * S > 3LL * info.sm_count * decode_min_ctas(MT)) {
+    // more than three waves of short CTAs, each paying the prologue and the
+    // cluster reduction again: one wave's worth of the longest CTAs instead,
+    // x staged in chunks (measured on GB300, M = 16: Llama-2-70B gate_up
+    // 135 -> 108 us, down 88 -> 71 us; shapes of up to three waves lose)
+    S = std::max(s64, (int)(2.0 * info.sm_count / NG + 0.5));
   }
   const int reg_ctas = decode_min_ctas(MT);
   DecodePlan d = fit_ring(S, A, Mc, MT, gshift, std::min(3, reg_ctas), info.smem_per_sm);
@@ -743,6 +752,10 @@ int log2_exact(int v) {
 
 }  // namespace
 
+size_t decode_workspace_bytes(int M, int K, bool has_perm) {
+  return has_perm && M > 0 ? ((size_t)M * K * 2 + 255) & ~(size_t)255 : 0;
+}
+
 cudaError_t launch_decode(const GemmArgs& a, cudaStream_t stream) {
   DeviceInfo info;
   cudaError_t err = device_info(&info);
@@ -753,6 +766,16 @@ cudaError_t launch_decode(const GemmArgs& a, cudaStream_t stream) {
   const bool g64 = gshift >= 6;  // groups of 64 or more: one group per atom
   int* status = nullptr;
   if ((err = device_status_ptr(&status)) != cudaSuccess) return err;
+  // act-order with room in the workspace: gather x[:, perm] once for all CTAs
+  // instead of once per CTA (every column group's CTAs read the same columns)
+  const void* xsrc = a.x;
+  const int32_t* perm = a.perm;
+  if (perm && a.workspace && a.workspace_bytes >= decode_workspace_bytes(a.M, a.K, true)) {
+    if ((err = launch_gather_columns(a.x, perm, a.workspace, a.M, a.K, stream)) != cudaSuccess)
+      return err;
+    xsrc = a.workspace;
+    perm = nullptr;
+  }
   for (int r0 = 0; r0 < a.M; r0 += DECODE_MAX_M) {
     const int Mc = std::min(DECODE_MAX_M, a.M - r0);
     const int MT = Mc <= 8 ? 1 : Mc <= 16 ? 2 : Mc <= 32 ? 4 : 8;
@@ -762,11 +785,11 @@ cudaError_t launch_decode(const GemmArgs& a, cudaStream_t stream) {
     if ((err = ensure_smem(fn, plan.L.total)) != cudaSuccess) return err;
 
     DecodeParams p;
-    p.x = static_cast<const uint16_t*>(a.x) + (size_t)r0 * a.K;
+    p.x = static_cast<const uint16_t*>(xsrc) + (size_t)r0 * a.K;
     p.qw = a.qw;
     p.scales = static_cast<const uint16_t*>(a.scales);
     p.zeros = a.zeros;
-    p.perm = a.perm;
+    p.perm = perm;
     p.y = static_cast<uint16_t*>(a.y) + (size_t)r0 * a.N;
     p.M = Mc;
     p.N = a.N;

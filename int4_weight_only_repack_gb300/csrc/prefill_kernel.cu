@@ -389,14 +389,30 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
 }
 
 // ---- act-order: x'[m][j] = x[m][perm[j]] --------------------------------------
+// One thread: eight consecutive columns, for the rows blockIdx.y, blockIdx.y +
+// gridDim.y, ... (grid: column blocks x up to 65535 rows). perm comes in as two
+// 16-byte loads, the eight x values of a row as independent 2-byte loads, and
+// they leave as one 16-byte store (K % 64 == 0, 16-byte aligned buffers).
 __global__ void __launch_bounds__(256) gather_columns_kernel(const uint16_t* __restrict__ x,
                                                              const int32_t* __restrict__ perm,
-                                                             uint16_t* __restrict__ xg, int M, int K) {
-  const size_t total = (size_t)M * K;
-  for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < total; i += (size_t)gridDim.x * 256) {
-    const size_t m = i / K;
-    const int j = (int)(i - m * K);
-    xg[i] = x[m * K + perm[j]];
+                                                             uint16_t* __restrict__ xg, int M,
+                                                             int K) {
+  // launched with programmatic stream serialization: x may come from the kernel
+  // before this one; the GEMM after it may start its weight prologue at once
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int c = blockIdx.x * 256 + threadIdx.x;  // eight-column chunk
+  if (c >= K / 8) return;
+  const int4* pp = reinterpret_cast<const int4*>(perm) + 2 * c;
+  const int4 pa = __ldg(pp), pb = __ldg(pp + 1);
+  for (size_t m = blockIdx.y; m < (size_t)M; m += gridDim.y) {
+    const uint16_t* xr = x + m * K;
+    uint4 v;
+    v.x = __ldg(xr + pa.x) | ((uint32_t)__ldg(xr + pa.y) << 16);
+    v.y = __ldg(xr + pa.z) | ((uint32_t)__ldg(xr + pa.w) << 16);
+    v.z = __ldg(xr + pb.x) | ((uint32_t)__ldg(xr + pb.y) << 16);
+    v.w = __ldg(xr + pb.z) | ((uint32_t)__ldg(xr + pb.w) << 16);
+    reinterpret_cast<uint4*>(xg + m * K)[c] = v;
   }
 }
 
@@ -505,6 +521,23 @@ size_t split_bytes(int M, int N, int ksplit) {
 
 }  // namespace
 
+cudaError_t launch_gather_columns(const void* x, const int32_t* perm, void* xg, int M, int K,
+                                  cudaStream_t stream) {
+  if (M <= 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((K / 8 + 255) / 256), (unsigned)std::min(M, 65535), 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const uint16_t* xs = static_cast<const uint16_t*>(x);
+  uint16_t* xd = static_cast<uint16_t*>(xg);
+  return cudaLaunchKernelEx(&cfg, gather_columns_kernel, xs, perm, xd, M, K);
+}
+
 size_t prefill_workspace_bytes(int M, int K, bool has_perm) {
   if (!has_perm) return 0;
   return ((size_t)M * K * 2 + 255) & ~(size_t)255;
@@ -531,13 +564,9 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
   if (err != cudaSuccess) return err;
   const void* x = a.x;
   if (a.perm) {
-    uint16_t* xg = static_cast<uint16_t*>(a.workspace);
-    const size_t total = (size_t)a.M * a.K;
-    const unsigned g = (unsigned)std::min<size_t>((total + 255) / 256, (size_t)info.sm_count * 16);
-    gather_columns_kernel<<<g, 256, 0, stream>>>(static_cast<const uint16_t*>(a.x), a.perm, xg,
-                                                  a.M, a.K);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    x = xg;
+    if ((err = launch_gather_columns(a.x, a.perm, a.workspace, a.M, a.K, stream)) != cudaSuccess)
+      return err;
+    x = a.workspace;
   }
   PrefillPlan pl = prefill_plan(a.M, a.N, a.K, info.sm_count);
   // the split-K partials go after the act-order staging, when the workspace

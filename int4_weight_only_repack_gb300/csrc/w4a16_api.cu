@@ -233,10 +233,11 @@ w4_status w4_repack_gptq(const int32_t* qweight, const int32_t* qzeros, const vo
 size_t w4a16_gemm_workspace_size(int M, int N, int K, int group, int dtype, int has_perm) {
   (void)group;
   (void)dtype;
-  // enough for either kernel: the tcgen05 kernel may serve any M > 16; the
-  // act-order staging is required, the split-K partials after it are used when
-  // present
-  if (M <= 16 || !prefill_supported(M, N, K)) return 0;
+  // the small-M kernel: act-order calls stage x[:, perm] there once per call
+  // (optional: without it every CTA gathers its own slice)
+  if (M <= 16 || !prefill_supported(M, N, K)) return decode_workspace_bytes(M, K, has_perm != 0);
+  // the tcgen05 kernel: the act-order staging is required, the split-K partials
+  // after it are used when present
   const size_t staged = prefill_workspace_bytes(M, K, has_perm != 0);
   return staged + prefill_split_workspace_bytes(M, N, K);
 }
@@ -309,8 +310,8 @@ w4_status w4a16_gemm_noalloc(const void* x, const int32_t* qw, const void* scale
                           ? prefill_workspace_bytes(M, K, perm != nullptr)
                           : 0;
   if (need > W4_NOALLOC_SCRATCH_BYTES) return W4_ERR_WORKSPACE;
-  if (M == 0 || M <= 16 || !prefill_supported(M, N, K)) {
-    // the small-M kernel uses no workspace: the call is w4a16_gemm without one
+  if (M == 0 || ((M <= 16 || !prefill_supported(M, N, K)) && perm == nullptr)) {
+    // the small-M kernel without act-order uses no workspace
     return w4a16_gemm(x, qw, scales, zeros, perm, y, M, N, K, group, dtype, nullptr, 0, stream);
   }
   // validate everything the scratch does not decide before touching the device

@@ -42,9 +42,18 @@ struct GemmArgs {
   size_t workspace_bytes;
 };
 
-// Small-M kernel: M rows processed in chunks of up to 64.
+// Small-M kernel: M rows processed in chunks of up to 64. An act-order call
+// given a workspace of decode_workspace_bytes stages x[:, perm] there once
+// (launch_gather_columns) and runs the kernel on the staged rows; without it
+// every CTA gathers its own slice of x.
 constexpr int DECODE_MAX_M = 64;
 cudaError_t launch_decode(const GemmArgs& a, cudaStream_t s);
+size_t decode_workspace_bytes(int M, int K, bool has_perm);
+
+// xg[m][j] = x[m][perm[j]] for M rows of K (16-byte aligned, K % 64 == 0),
+// launched with programmatic stream serialization.
+cudaError_t launch_gather_columns(const void* x, const int32_t* perm, void* xg, int M, int K,
+                                  cudaStream_t s);
 
 // Which kernel a call runs: the small-M kernel for M <= 16, the tcgen05 kernel
 // above that when it supports the shape (N % 32 == 0). Measured on GB300 over

@@ -315,6 +315,10 @@ def test_gemm_act_order_vs_oracle(w4, K, N, group, Ms):
         assert err <= TOL, (M, err)
         if small_m_kernel(M, N):
             assert ulp_error(y, y_ref, "fp16") <= 1.0
+            # with the workspace x[:, perm] is staged once per call; without it
+            # every CTA gathers its columns: the same operands, the same bits
+            assert w4.w4a16_gemm_workspace_size(M, N, K, group, "fp16", True) >= M * K * 2
+            assert np.array_equal(gemm_with(w4, L, x, parts, M, group, None), y), M
         else:
             assert ulp_error(y, rounded_w_reference(x, L, group, fmt="gptq"), "fp16") <= 1.0
 
