@@ -136,8 +136,14 @@ W4_API w4_status w4_repack_sizes(int K, int N, int group, int layout,
  * kernel's own repack; "vLLM AWQ 4-bit 量化实践" §5.1).
  *   qweight  [K][N/8] int32 (AWQ order), qzeros [G][N/8] int32 (AWQ order),
  *   scales   [G][N] (dtype).
+ *   qzeros NULL: symmetric weights (the zero_point=False setting of the AWQ
+ *            quant_config, "vLLM AWQ 4-bit 量化实践" §二): no zero points are
+ *            stored and every code has the fixed zero point 8,
+ *            W = (q - 8) * s (the middle of the 4-bit range: the codes are
+ *            signed values stored with an offset of 8).
  *   qw_out   layout STD: [K/8][N]; layout TILE: K*N/8 words as described above.
- *   zeros_out [G][N/8] standard order; scales_out [G][N] (a copy).
+ *   zeros_out [G][N/8] standard order (all 8 for symmetric weights);
+ *   scales_out [G][N] (a copy).
  * Inputs are never modified; outputs must not overlap inputs (W4_ERR_ALIAS).
  * Deterministic and re-runnable on new weights.
  */
@@ -149,7 +155,8 @@ W4_API w4_status w4_repack_awq(const int32_t* qweight, const int32_t* qzeros, co
 /*
  * One-time repack of a GPTQ checkpoint (standard packing), with optional
  * act-order ("量化层加载" 设计动机: desc_act / g_idx).
- *   qweight [K/8][N] int32, qzeros [G][N/8] int32 (standard order), scales [G][N].
+ *   qweight [K/8][N] int32, qzeros [G][N/8] int32 (standard order) or NULL
+ *   (symmetric: zero point 8, as for w4_repack_awq), scales [G][N].
  *   g_idx   [K] int32 or NULL. When given, rows are stored sorted by group and
  *           perm_out [K] (required) receives the row order: stored row j is
  *           input row perm_out[j]. *status_out (required, one int32) receives
@@ -209,6 +216,19 @@ W4_API size_t w4a16_gemm_workspace_size(int M, int N, int K, int group, int dtyp
 W4_API w4_status w4a16_gemm(const void* x, const int32_t* qw, const void* scales, const int32_t* zeros,
                      const int32_t* perm, void* y, int M, int N, int K, int group, int dtype,
                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * w4a16_gemm with a bias epilogue: y[m][n] = x[m][:] · W[:, n] + bias[n], the
+ * bias added to the fp32 sum before the one rounding to dtype (the bias of
+ * "apply_weights(layer, x, bias)": "量化层加载" 关键文件, AutoGPTQLinearMethod and
+ * AutoAWQMarlinLinearMethod apply). bias [N] in dtype, 16-byte aligned, or
+ * NULL (then this is w4a16_gemm); y must not overlap it (W4_ERR_ALIAS). All
+ * other arguments, the workspace and the ordering rules are w4a16_gemm's.
+ */
+W4_API w4_status w4a16_gemm_bias(const void* x, const int32_t* qw, const void* scales,
+                                 const int32_t* zeros, const int32_t* perm, const void* bias,
+                                 void* y, int M, int N, int K, int group, int dtype,
+                                 void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Size of the static device scratch array that w4a16_gemm_noalloc uses (32 MiB).

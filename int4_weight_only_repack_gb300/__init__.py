@@ -17,7 +17,8 @@ import torch
 __all__ = [
     "W4_F16", "W4_BF16", "W4_LAYOUT_STD", "W4_LAYOUT_TILE", "W4Error", "lib", "library_path",
     "dtype_code", "w4_status_string", "w4_last_cuda_error", "w4_abi_version", "w4_repack_sizes", "w4_repack_awq",
-    "w4_repack_gptq", "w4a16_gemm_workspace_size", "w4a16_gemm", "w4a16_gemm_noalloc",
+    "w4_repack_gptq", "w4a16_gemm_workspace_size", "w4a16_gemm", "w4a16_gemm_bias",
+    "w4a16_gemm_noalloc",
     "w4_dequant", "gemm_workspace",
     "w4_device_status",
     "RepackedLayer", "repack_awq", "repack_gptq", "linear",
@@ -49,6 +50,9 @@ _SIGNATURES = {
     "w4a16_gemm": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                             _c_int, _c_int, _c_int, _c_int, _c_int, _c_void_p, _c_size,
                             _c_void_p]),
+    "w4a16_gemm_bias": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                 _c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                 _c_void_p, _c_size, _c_void_p]),
     "w4_dequant": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int,
                             _c_int, _c_int, _c_void_p, _c_void_p]),
     "w4_device_status": (_c_int, [ctypes.POINTER(ctypes.c_int32), _c_int]),
@@ -164,6 +168,15 @@ def w4a16_gemm(x, qw, scales, zeros, perm, y, M, N, K, group, dtype, workspace=N
                             _stream(stream)))
 
 
+def w4a16_gemm_bias(x, qw, scales, zeros, perm, bias, y, M, N, K, group, dtype, workspace=None,
+                    workspace_bytes=None, stream=None):
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().w4a16_gemm_bias(_ptr(x), _ptr(qw), _ptr(scales), _ptr(zeros), _ptr(perm),
+                                 _ptr(bias), _ptr(y), M, N, K, group, dtype_code(dtype),
+                                 _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
 def w4a16_gemm_noalloc(x, qw, scales, zeros, perm, y, M, N, K, group, dtype, stream=None):
     """w4a16_gemm for callers that cannot allocate device memory: act-order
     staging goes to the library's static device array instead of a workspace."""
@@ -239,10 +252,10 @@ def gemm_workspace(nbytes: int, device, stream=None):
     return ws
 
 
-def linear(x, layer: RepackedLayer, y=None, workspace=None, stream=None):
-    """y = x · W for a TILE-layout layer; x is [M, K] fp16/bf16 on the device.
-    Without `workspace`, the one kept for (device, stream) is used (grown as
-    needed); a caller's own workspace must follow w4a16_gemm_workspace_size."""
+def linear(x, layer: RepackedLayer, y=None, workspace=None, stream=None, bias=None):
+    """y = x · W (+ bias) for a TILE-layout layer; x is [M, K] fp16/bf16 on the
+    device, bias [N] in the same dtype or None. Without `workspace`, the one kept
+    for (device, stream) is used (grown as needed)."""
     M = x.shape[0]
     if y is None:
         y = torch.empty((M, layer.N), dtype=x.dtype, device=x.device)
@@ -250,6 +263,6 @@ def linear(x, layer: RepackedLayer, y=None, workspace=None, stream=None):
                                      layer.perm is not None)
     if need and workspace is None:
         workspace = gemm_workspace(need, x.device, stream)
-    w4a16_gemm(x, layer.qw, layer.scales, layer.zeros, layer.perm, y, M, layer.N, layer.K,
-               layer.group, layer.dtype, workspace, None, stream)
+    w4a16_gemm_bias(x, layer.qw, layer.scales, layer.zeros, layer.perm, bias, y, M, layer.N,
+                    layer.K, layer.group, layer.dtype, workspace, None, stream)
     return y

@@ -90,6 +90,7 @@ struct DecodeParams {
   const uint32_t* zeros;   // [G][N/8] standard order
   const int32_t* perm;     // [K] or nullptr
   uint16_t* y;             // [M][N]
+  const uint16_t* bias;    // [N] or nullptr
   int M, N, K;
   int gshift;              // group = 1 << gshift; 31 = one group over all of K
   int A;                   // K / 64
@@ -577,6 +578,7 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
       if (n >= p.N) continue;
       float sum = 0.f;
       for (int r = 0; r < S; ++r) sum += recv[((size_t)r * SL + cl) * MR + m];
+      if (p.bias != nullptr) sum += half_bits_to_float<BF16>(p.bias[n]);  // one rounding below
       p.y[(size_t)m * p.N + n] = float_to_half_bits<BF16>(sum);
     }
   }
@@ -791,6 +793,7 @@ cudaError_t launch_decode(const GemmArgs& a, cudaStream_t stream) {
     p.zeros = a.zeros;
     p.perm = perm;
     p.y = static_cast<uint16_t*>(a.y) + (size_t)r0 * a.N;
+    p.bias = static_cast<const uint16_t*>(a.bias);
     p.M = Mc;
     p.N = a.N;
     p.K = a.K;

@@ -81,6 +81,7 @@ struct PrefillParams {
   CUtensorMap tm_s;  // scales [G][N], box 256 x 2
   CUtensorMap tm_z;  // zeros [G][N/8], box 32 x 2
   uint16_t* y;
+  const uint16_t* bias;  // [N] in the activation dtype, or nullptr
   float* part;  // split-K partial tiles [ksplit][M][N] fp32 (ksplit > 1)
   int M, N, K, group;
   int m_blocks, n_blocks, num_tiles, k_blocks, ksplit;
@@ -308,6 +309,21 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
                                      __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
             }
           } else if (m < p.M) {
+            if (p.bias != nullptr) {
+              // y = RN(acc + bias): the bias joins the fp32 sum before the one rounding
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                if (n + 8 * q < p.N) {
+                  const uint4 b = __ldg(reinterpret_cast<const uint4*>(p.bias + n + 8 * q));
+                  const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                  for (int e = 0; e < 8; ++e)
+                    r[8 * q + e] = __float_as_uint(
+                        __uint_as_float(r[8 * q + e]) +
+                        half_bits_to_float<BF16>((uint16_t)(bw[e >> 1] >> (16 * (e & 1)))));
+                }
+              }
+            }
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               if (n + 8 * q < p.N) {
@@ -417,10 +433,13 @@ __global__ void __launch_bounds__(256) gather_columns_kernel(const uint16_t* __r
 }
 
 // ---- split K: y = RN(sum over the K slices of the fp32 partials), in slice order --
+// With a bias, y = RN(sum + bias[n]) (n4_row: float4 groups per row, N / 4).
 template <bool BF16>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4* __restrict__ part,
                                                             uint2* __restrict__ y, size_t n4,
-                                                            int ksplit) {
+                                                            int ksplit,
+                                                            const uint2* __restrict__ bias,
+                                                            size_t n4_row) {
   for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < n4; i += (size_t)gridDim.x * 256) {
     float4 a = part[i];
     for (int s = 1; s < ksplit; ++s) {
@@ -429,6 +448,13 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4* __rest
       a.y += b.y;
       a.z += b.z;
       a.w += b.w;
+    }
+    if (bias != nullptr) {
+      const uint2 b = __ldg(bias + i % n4_row);
+      a.x += half_bits_to_float<BF16>((uint16_t)b.x);
+      a.y += half_bits_to_float<BF16>((uint16_t)(b.x >> 16));
+      a.z += half_bits_to_float<BF16>((uint16_t)b.y);
+      a.w += half_bits_to_float<BF16>((uint16_t)(b.y >> 16));
     }
     y[i] = make_uint2(pack_half2(a.x, a.y, BF16), pack_half2(a.z, a.w, BF16));
   }
@@ -589,6 +615,7 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
                        (uint64_t)a.N / 2, BN / 8, 2, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (!ok) return cudaErrorInvalidValue;
   p.y = static_cast<uint16_t*>(a.y);
+  p.bias = static_cast<const uint16_t*>(a.bias);
   p.part = pl.ksplit > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + staged)
                          : nullptr;
   p.M = a.M;
@@ -629,12 +656,15 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
   if (pl.ksplit > 1) {
     const size_t n4 = (size_t)a.M * a.N / 4;
     const unsigned g = (unsigned)std::min<size_t>((n4 + 255) / 256, (size_t)info.sm_count * 8);
+    const uint2* bias = static_cast<const uint2*>(a.bias);
     if (a.bf16)
       splitk_reduce_kernel<true><<<g, 256, 0, stream>>>(reinterpret_cast<const float4*>(p.part),
-                                                         static_cast<uint2*>(a.y), n4, pl.ksplit);
+                                                         static_cast<uint2*>(a.y), n4, pl.ksplit,
+                                                         bias, (size_t)a.N / 4);
     else
       splitk_reduce_kernel<false><<<g, 256, 0, stream>>>(reinterpret_cast<const float4*>(p.part),
-                                                          static_cast<uint2*>(a.y), n4, pl.ksplit);
+                                                          static_cast<uint2*>(a.y), n4, pl.ksplit,
+                                                          bias, (size_t)a.N / 4);
     err = cudaGetLastError();
   }
   return err;

@@ -148,9 +148,10 @@ __global__ void __launch_bounds__(BLOCK_THREADS) meta_kernel(
     uint32_t* __restrict__ zeros_out, uint4* __restrict__ scales_out, size_t units) {
   for (size_t i = (size_t)blockIdx.x * BLOCK_THREADS + threadIdx.x; i < units;
        i += (size_t)gridDim.x * BLOCK_THREADS) {
-    const uint32_t w = qzeros[i];
+    // symmetric weights (no zeros stored): the zero point is 8 everywhere
+    const uint32_t w = qzeros != nullptr ? qzeros[i] : 0x88888888u;
     uint32_t v = w;
-    if (zeros_are_awq) {
+    if (zeros_are_awq && qzeros != nullptr) {
       v = 0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) v |= ((w >> (4 * awq_nibble_pos(j))) & 0xFu) << (4 * j);

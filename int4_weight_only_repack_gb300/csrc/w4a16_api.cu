@@ -155,7 +155,7 @@ w4_status w4_repack_awq(const int32_t* qweight, const int32_t* qzeros, const voi
   w4_status st = check_dims(K, N, group, dtype);
   if (st) return st;
   if ((st = check_layout_dims(K, N, layout))) return st;
-  if (!qweight || !qzeros || !scales || !qw_out || !zeros_out || !scales_out) return W4_ERR_NULL;
+  if (!qweight || !scales || !qw_out || !zeros_out || !scales_out) return W4_ERR_NULL;
   if (!aligned16(qweight) || !aligned16(qzeros) || !aligned16(scales) || !aligned16(qw_out) ||
       !aligned16(zeros_out) || !aligned16(scales_out))
     return W4_ERR_ALIGN;
@@ -165,7 +165,7 @@ w4_status w4_repack_awq(const int32_t* qweight, const int32_t* qzeros, const voi
   size_t qw_out_b = 0;
   w4_repack_sizes(K, N, group, layout, &qw_out_b, nullptr, nullptr);
   const void* ins[3] = {qweight, qzeros, scales};
-  const size_t in_b[3] = {qw_b, z_b, s_b};
+  const size_t in_b[3] = {qw_b, qzeros ? z_b : 0, s_b};
   const void* outs[3] = {qw_out, zeros_out, scales_out};
   const size_t out_b[3] = {qw_out_b, z_b, s_b};
   for (int i = 0; i < 3; ++i)
@@ -189,7 +189,7 @@ w4_status w4_repack_gptq(const int32_t* qweight, const int32_t* qzeros, const vo
   w4_status st = check_dims(K, N, group, dtype);
   if (st) return st;
   if ((st = check_layout_dims(K, N, layout))) return st;
-  if (!qweight || !qzeros || !scales || !qw_out || !zeros_out || !scales_out) return W4_ERR_NULL;
+  if (!qweight || !scales || !qw_out || !zeros_out || !scales_out) return W4_ERR_NULL;
   if (g_idx && (!perm_out || !status_out)) return W4_ERR_NULL;
   if (!aligned16(qweight) || !aligned16(qzeros) || !aligned16(scales) || !aligned16(qw_out) ||
       !aligned16(zeros_out) || !aligned16(scales_out) || !aligned16(g_idx) ||
@@ -203,7 +203,7 @@ w4_status w4_repack_gptq(const int32_t* qweight, const int32_t* qzeros, const vo
   w4_repack_sizes(K, N, group, layout, &qw_out_b, nullptr, nullptr);
   const size_t gi_b = g_idx ? (size_t)K * 4 : 0;
   const void* ins[4] = {qweight, qzeros, scales, g_idx};
-  const size_t in_b[4] = {qw_b, z_b, s_b, gi_b};
+  const size_t in_b[4] = {qw_b, qzeros ? z_b : 0, s_b, gi_b};
   const void* outs[5] = {qw_out, zeros_out, scales_out, g_idx ? perm_out : nullptr,
                          g_idx ? status_out : nullptr};
   const size_t out_b[5] = {qw_out_b, z_b, s_b, gi_b, g_idx ? (size_t)4 : 0};
@@ -253,6 +253,14 @@ w4_status w4_device_status(int32_t* status_out, int clear) {
 w4_status w4a16_gemm(const void* x, const int32_t* qw, const void* scales, const int32_t* zeros,
                      const int32_t* perm, void* y, int M, int N, int K, int group, int dtype,
                      void* workspace, size_t workspace_bytes, void* stream) {
+  return w4a16_gemm_bias(x, qw, scales, zeros, perm, nullptr, y, M, N, K, group, dtype, workspace,
+                         workspace_bytes, stream);
+}
+
+w4_status w4a16_gemm_bias(const void* x, const int32_t* qw, const void* scales,
+                          const int32_t* zeros, const int32_t* perm, const void* bias, void* y,
+                          int M, int N, int K, int group, int dtype, void* workspace,
+                          size_t workspace_bytes, void* stream) {
   w4_status st = check_dims(K, N, group, dtype);
   if (st) return st;
   if (M < 0 || M > MAX_DIM) return W4_ERR_SHAPE;
@@ -260,7 +268,7 @@ w4_status w4a16_gemm(const void* x, const int32_t* qw, const void* scales, const
   if (!qw || !scales || !zeros) return W4_ERR_NULL;
   if (M > 0 && (!x || !y)) return W4_ERR_NULL;
   if (!aligned16(x) || !aligned16(qw) || !aligned16(scales) || !aligned16(zeros) ||
-      !aligned16(perm) || !aligned16(y) || !aligned16(workspace))
+      !aligned16(perm) || !aligned16(bias) || !aligned16(y) || !aligned16(workspace))
     return W4_ERR_ALIGN;
   // required: the act-order staging of the tcgen05 kernel (split-K partials are
   // optional and sized by the kernel from what the workspace holds)
@@ -272,10 +280,11 @@ w4_status w4a16_gemm(const void* x, const int32_t* qw, const void* scales, const
   const int g = resolve_group(group, K);
   const size_t G = (size_t)K / g;
   const size_t y_b = (size_t)M * N * 2;
-  const void* ins[6] = {x, qw, scales, zeros, perm, workspace};
-  const size_t in_b[6] = {(size_t)M * K * 2, (size_t)K * N / 2, G * N * 2, G * N / 2,
-                          perm ? (size_t)K * 4 : 0, workspace ? workspace_bytes : 0};
-  for (int j = 0; j < 6; ++j)
+  const void* ins[7] = {x, qw, scales, zeros, perm, workspace, bias};
+  const size_t in_b[7] = {(size_t)M * K * 2, (size_t)K * N / 2, G * N * 2, G * N / 2,
+                          perm ? (size_t)K * 4 : 0, workspace ? workspace_bytes : 0,
+                          bias ? (size_t)N * 2 : 0};
+  for (int j = 0; j < 7; ++j)
     if (overlaps(y, y_b, ins[j], in_b[j])) return W4_ERR_ALIAS;
   if ((st = check_arch())) return st;
   GemmArgs a;
@@ -285,6 +294,7 @@ w4_status w4a16_gemm(const void* x, const int32_t* qw, const void* scales, const
   a.zeros = reinterpret_cast<const uint32_t*>(zeros);
   a.perm = perm;
   a.y = y;
+  a.bias = bias;
   a.M = M;
   a.N = N;
   a.K = K;

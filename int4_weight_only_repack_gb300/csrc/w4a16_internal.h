@@ -36,6 +36,7 @@ struct GemmArgs {
   const uint32_t* zeros;
   const int32_t* perm;
   void* y;
+  const void* bias;  // [N] in the activation dtype, or nullptr
   int M, N, K, group;
   int bf16;
   void* workspace;

@@ -320,25 +320,37 @@ def gemm(x: np.ndarray, W: np.ndarray) -> np.ndarray:
 # --------------------------------------------------------------------------- #
 # Whole-layer references                                                        #
 # --------------------------------------------------------------------------- #
+# Zero point of every code of a symmetric checkpoint (AWQ zero_point=False, [AWQ]
+# §二 quant_config: no qzeros are stored). Reading: the 4-bit codes are signed
+# values stored with an offset of 8, the middle of the range, so W = (q - 8) * s.
+SYMMETRIC_ZERO = 8
+
+
 def layer_codes(qweight, qzeros, scales_bits, dtype: str, fmt: str):
-    """Checkpoint words -> (q [K, N], z [G, N], s [G, N] float64)."""
+    """Checkpoint words -> (q [K, N], z [G, N], s [G, N] float64). qzeros None:
+    a symmetric checkpoint, z = SYMMETRIC_ZERO everywhere."""
     if fmt == "awq":
         q = unpack_awq(qweight)
-        z = unpack_awq(qzeros)
+        z = unpack_awq(qzeros) if qzeros is not None else None
     elif fmt == "gptq":
         q = unpack_rows_std(qweight)
-        z = unpack_cols_std(qzeros)
+        z = unpack_cols_std(qzeros) if qzeros is not None else None
     else:
         raise ValueError(fmt)
     s = half_bits_to_f64(scales_bits, dtype)
+    if z is None:
+        z = np.full(s.shape, SYMMETRIC_ZERO, dtype=np.uint8)
     return q, z, s
 
 
 def reference_y(x_bits, qweight, qzeros, scales_bits, group: int, dtype: str, fmt: str,
-                g_idx=None, rows=None, cols=None, col_chunk: int = 4096) -> np.ndarray:
+                g_idx=None, rows=None, cols=None, col_chunk: int = 4096,
+                bias_bits=None) -> np.ndarray:
     """fp64 y for the layer, optionally on a subset of rows and/or columns.
 
     Dequantises column chunks so memory stays bounded on the largest layers.
+    bias_bits ([N] half bits): y[m, n] += bias[n], the bias of the layer's
+    apply ([QL] 关键文件: apply_weights(layer, x, bias)).
     """
     q, z, s = layer_codes(qweight, qzeros, scales_bits, dtype, fmt)
     K, N = q.shape
@@ -351,6 +363,8 @@ def reference_y(x_bits, qweight, qzeros, scales_bits, group: int, dtype: str, fm
     for c0 in range(0, col_list.shape[0], col_chunk):
         cc = col_list[c0:c0 + col_chunk]
         y[:, c0:c0 + len(cc)] = gemm(x, dequant(q, z, s, gk, cols=cc))
+    if bias_bits is not None:
+        y += half_bits_to_f64(np.asarray(bias_bits), dtype)[col_list][None, :]
     return y
 
 

@@ -3,8 +3,9 @@
 This module plays the part of the checkpoint writer (the AWQ / GPTQ quantiser and
 packer), which sits outside the repack + GEMM path. It draws float weights and
 activations from seeded generators, quantises the weights with a per-(group,
-column) asymmetric min/max rule and stores the codes in the two checkpoint
-formats the path reads. It holds none of the path's own arithmetic: no unpack,
+column) asymmetric min/max rule (or, for symmetric layers, a max-abs rule with
+the zero point fixed at 8 and no zeros stored) and stores the codes in the two
+checkpoint formats the path reads. It holds none of the path's own arithmetic: no unpack,
 no repack, no dequantisation and no matrix product. Both the CPU oracle (which
 derives every code it uses by unpacking these words itself) and the CUDA path
 consume exactly the arrays produced here.
@@ -115,7 +116,7 @@ class Layer:
     dtype: str
     fmt: str                          # "awq" or "gptq"
     qweight: np.ndarray               # int32, AWQ [K, N/8] or GPTQ [K/8, N]
-    qzeros: np.ndarray                # int32 [G, N/8] (AWQ order or standard order)
+    qzeros: Optional[np.ndarray]      # int32 [G, N/8] (AWQ or standard order); None: symmetric
     scales: np.ndarray                # uint16 bits [G, N]
     g_idx: Optional[np.ndarray] = None  # int32 [K] (GPTQ act-order only)
     # Writer-side codes, kept for generator self-checks only.
@@ -156,6 +157,34 @@ def _quantise_minmax(w: np.ndarray, group: int, g_idx: Optional[np.ndarray], dty
         v = np.rint(w[k0:k1] / s_eff[gg]) + z[gg].astype(np.float32)
         q[k0:k1] = np.clip(v, 0, 15).astype(np.uint8)
     return q, z, s_bits
+
+
+def _quantise_symmetric(w: np.ndarray, group: int, g_idx: Optional[np.ndarray], dtype: str):
+    """Symmetric 4-bit quantiser per (group, column), zero point fixed at 8.
+
+    scale = max|w| / 7 in fp32, stored in the activation dtype (1 when the
+    group is all zeros); code = clamp(rint(w / scale) + 8, 0, 15).
+    """
+    K, N = w.shape
+    G = K // group
+    if g_idx is None:
+        order = np.arange(K)
+        gk = order // group
+    else:
+        order = np.argsort(g_idx, kind="stable")
+        gk = g_idx
+    amax = np.abs(w[order].reshape(G, group, N)).max(axis=1)
+    s32 = (amax / np.float32(7.0)).astype(np.float32)
+    s32[amax == 0] = 1.0
+    s_bits = f32_to_bits(s32, dtype)
+    s_eff = bits_to_f32(s_bits, dtype)
+    q = np.empty((K, N), dtype=np.uint8)
+    step = max(1, (1 << 24) // max(N, 1))
+    for k0 in range(0, K, step):
+        k1 = min(K, k0 + step)
+        v = np.rint(w[k0:k1] / s_eff[gk[k0:k1]]) + np.float32(8.0)
+        q[k0:k1] = np.clip(v, 0, 15).astype(np.uint8)
+    return q, np.full((G, N), 8, dtype=np.uint8), s_bits
 
 
 def _pack_awq(codes: np.ndarray) -> np.ndarray:
@@ -201,19 +230,21 @@ def act_order_gidx(rng: np.random.Generator, K: int, group: int) -> np.ndarray:
 def make_layer_from_rng(rng: np.random.Generator, K: int, N: int, group: int, dtype: str,
                         fmt: str = "awq", act_order: bool = False,
                         keep_codes: bool = False, keep_float: bool = False,
-                        sigma: float = 0.02) -> Layer:
+                        sigma: float = 0.02, symmetric: bool = False) -> Layer:
+    """symmetric: no zero points (qzeros None), every code's zero point is 8."""
     w = rng.standard_normal((K, N), dtype=np.float32)
     w *= np.float32(sigma)
     g_idx = act_order_gidx(rng, K, group) if act_order else None
-    q, z, s_bits = _quantise_minmax(w, group, g_idx, dtype)
+    quantise = _quantise_symmetric if symmetric else _quantise_minmax
+    q, z, s_bits = quantise(w, group, g_idx, dtype)
     if fmt == "awq":
         if act_order:
             raise ValueError("AWQ checkpoints carry no g_idx")
         qweight = _pack_awq(q)
-        qzeros = _pack_awq(z)
+        qzeros = None if symmetric else _pack_awq(z)
     elif fmt == "gptq":
         qweight = _pack_rows_std(q)
-        qzeros = _pack_cols_std(z)
+        qzeros = None if symmetric else _pack_cols_std(z)
     else:
         raise ValueError(fmt)
     return Layer(K, N, group, dtype, fmt, qweight, qzeros, s_bits, g_idx,

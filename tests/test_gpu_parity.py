@@ -61,7 +61,8 @@ def repack(w4, L, layout, device="cuda"):
     qw_raw, qw = guarded(qw_b // 4, torch.int32)
     z_raw, zeros = guarded(z_b // 4, torch.int32)
     s_raw, scales = guarded(s_b // 2, hdt(L.dtype))
-    qweight, qzeros = to_dev(L.qweight), to_dev(L.qzeros)
+    qweight = to_dev(L.qweight)
+    qzeros = to_dev(L.qzeros) if L.qzeros is not None else None  # None: symmetric
     sc_in = half_to_dev(L.scales, L.dtype)
     perm = status = None
     if L.fmt == "awq":
@@ -321,6 +322,80 @@ def test_gemm_act_order_vs_oracle(w4, K, N, group, Ms):
             assert np.array_equal(gemm_with(w4, L, x, parts, M, group, None), y), M
         else:
             assert ulp_error(y, rounded_w_reference(x, L, group, fmt="gptq"), "fp16") <= 1.0
+
+
+@pytest.mark.parametrize("fmt,dtype,K,N,act_order,Ms", [
+    ("awq", "bf16", 1024, 512, False, (1, 16, 300)),
+    ("gptq", "fp16", 512, 256, True, (4, 64)),
+])
+def test_symmetric_repack_dequant_gemm(w4, fmt, dtype, K, N, act_order, Ms):
+    """Symmetric checkpoints (no qzeros): the repack stores zero point 8 for
+    every group and column, the dequantised weights are bit-exact and both
+    GEMM kernels match the oracle."""
+    import torch
+    L = synth.make_custom_layer([124, K, N], K, N, group=128, dtype=dtype, fmt=fmt,
+                                act_order=act_order, symmetric=True)
+    assert L.qzeros is None
+    q, z, s = oracle_codes(L)
+    eights = oracle.pack_cols_std(np.full((K // 128, N), 8, np.uint8))
+    for layout in (w4.W4_LAYOUT_STD, w4.W4_LAYOUT_TILE):
+        qw, zeros, scales, perm, _ = repack(w4, L, layout)
+        assert np.array_equal(zeros.cpu().numpy().reshape(eights.shape), eights)
+        if act_order:
+            continue  # the dequant entry point reads rows in stored (sorted) order
+        raw, w32 = guarded(K * N, torch.float32)
+        w4.w4_dequant(qw, scales, zeros, K, N, 128, dtype, layout, 1, w32)
+        torch.cuda.synchronize()
+        check_guards(raw, K * N, 4)
+        W_ref = oracle.dequant(q, z, s, oracle.group_of_rows(K, 128))
+        assert np.array_equal(w32.cpu().numpy().reshape(K, N), W_ref)
+    parts = repack(w4, L, w4.W4_LAYOUT_TILE)
+    for M in Ms:
+        x = synth.make_custom_x([125, K, M], M, K, dtype)
+        y = run_gemm(w4, L, x, parts, M)
+        y_ref = oracle.reference_y(x, L.qweight, None, L.scales, 128, dtype, fmt, g_idx=L.g_idx)
+        assert oracle.rel_err(oracle.half_bits_to_f64(y, dtype), y_ref) <= TOL, M
+        if small_m_kernel(M, N):
+            assert ulp_error(y, y_ref, dtype) <= 1.0, M
+        else:
+            assert ulp_error(y, rounded_w_reference(x, L, 128, fmt=fmt), dtype) <= 1.0, M
+
+
+@pytest.mark.parametrize("K,N,dtype,fmt,act_order,Ms", [
+    (1024, 512, "bf16", "awq", False, (1, 9, 16, 40, 128, 300)),   # both kernels; M=128 splits K
+    (512, 272, "fp16", "gptq", True, (3, 16, 100)),               # act-order, N % 32 != 0
+    (256, 2048, "bf16", "awq", False, (4096,)),                    # tcgen05, no split
+])
+def test_gemm_bias(w4, K, N, dtype, fmt, act_order, Ms):
+    """y = x W + bias with the bias added before the one rounding: the small-M
+    kernel (exact operands) within one ulp of the exact result, the tcgen05
+    kernel (with and without split K) within one ulp of the rounded-W result."""
+    import torch
+    L = synth.make_custom_layer([126, K, N], K, N, group=128, dtype=dtype, fmt=fmt,
+                                act_order=act_order)
+    parts = repack(w4, L, w4.W4_LAYOUT_TILE)
+    qw, zeros, scales, perm, _ = parts
+    b = synth.f32_to_bits(np.random.default_rng(127).standard_normal(N).astype(np.float32), dtype)
+    bias = half_to_dev(b, dtype)
+    for M in Ms:
+        xb = synth.make_custom_x([128, K, M], M, K, dtype)
+        need = w4.w4a16_gemm_workspace_size(M, N, K, 128, dtype, perm is not None)
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda") if need else None
+        raw, y = guarded(M * N, hdt(dtype))
+        w4.w4a16_gemm_bias(half_to_dev(xb, dtype), qw, scales, zeros, perm, bias, y, M, N, K, 128,
+                           dtype, ws)
+        torch.cuda.synchronize()
+        check_guards(raw, M * N, 2)
+        yb = half_from_dev(y).reshape(M, N)
+        y_ref = oracle.reference_y(xb, L.qweight, L.qzeros, L.scales, 128, dtype, fmt,
+                                   g_idx=L.g_idx, bias_bits=b)
+        assert oracle.rel_err(oracle.half_bits_to_f64(yb, dtype), y_ref) <= TOL, M
+        if small_m_kernel(M, N):
+            assert ulp_error(yb, y_ref, dtype) <= 1.0, (M, ulp_error(yb, y_ref, dtype))
+        else:
+            y_rw = rounded_w_reference(xb, L, 128, fmt=fmt) + oracle.half_bits_to_f64(b, dtype)
+            assert ulp_error(yb, y_rw, dtype) <= 1.0, (M, ulp_error(yb, y_rw, dtype))
+    assert w4.w4_device_status() == 0
 
 
 def test_gemm_is_deterministic(w4):

@@ -282,6 +282,55 @@ def test_dequant_vs_writer():
     check_dequant_vs_writer()
 
 
+def test_symmetric_checkpoint():
+    """A symmetric checkpoint (no qzeros) reads as zero point 8 everywhere:
+    code 8 dequantises to 0, codes 0 / 15 to -8 s / +7 s, and the whole-layer
+    reference equals that of the same checkpoint with an explicit all-8 qzeros
+    (packed by the writer) for both formats; the writer's symmetric codes stay
+    within s/2 of the float weights wherever they are not clamped."""
+    K, N, g = 256, 64, 128
+    for fmt in ("awq", "gptq"):
+        L = synth.make_custom_layer([22, fmt == "awq"], K, N, group=g, dtype="bf16", fmt=fmt,
+                                    symmetric=True, keep_codes=True, keep_float=True)
+        assert L.qzeros is None
+        q, z, s = oracle.layer_codes(L.qweight, None, L.scales, "bf16", fmt)
+        assert z.shape == (K // g, N) and np.all(z == 8)
+        gk = oracle.group_of_rows(K, g)
+        W = oracle.dequant(q, z, s, gk).astype(np.float64)
+        assert np.array_equal(W[q == 8], np.zeros(int((q == 8).sum())))
+        assert np.array_equal(W[q == 0], -8 * s[gk][q == 0])
+        assert np.array_equal(W[q == 15], 7 * s[gk][q == 15])
+        unclamped = (L.q > 0) & (L.q < 15)
+        assert unclamped.mean() > 0.95
+        assert np.all(np.abs(W - L.w)[unclamped] <= (s[gk] * 0.5 * (1 + 1e-6))[unclamped])
+        eights = np.full((K // g, N), 8, np.uint8)
+        qz = synth._pack_awq(eights) if fmt == "awq" else synth._pack_cols_std(eights)
+        x = synth.make_custom_x([23], 3, K, "bf16")
+        assert np.array_equal(oracle.reference_y(x, L.qweight, None, L.scales, g, "bf16", fmt),
+                              oracle.reference_y(x, L.qweight, qz, L.scales, g, "bf16", fmt))
+
+
+def test_reference_bias_closed_forms():
+    """With x = 0 the reference is the bias itself; a zero bias changes nothing;
+    the bias shifts every row by the same vector (on a column subset too)."""
+    K, N = 256, 48
+    L = synth.make_custom_layer([26], K, N, group=128, dtype="fp16")
+    b = synth.f32_to_bits(np.random.default_rng(27).standard_normal(N).astype(np.float32), "fp16")
+    bf = oracle.half_bits_to_f64(b, "fp16")
+    zero_x = synth.f32_to_bits(np.zeros((2, K), np.float32), "fp16")
+    assert np.array_equal(oracle.reference_y(zero_x, L.qweight, L.qzeros, L.scales, 128, "fp16",
+                                             "awq", bias_bits=b), np.tile(bf, (2, 1)))
+    x = synth.make_custom_x([28], 3, K, "fp16")
+    plain = oracle.reference_y(x, L.qweight, L.qzeros, L.scales, 128, "fp16", "awq")
+    zb = synth.f32_to_bits(np.zeros(N, np.float32), "fp16")
+    assert np.array_equal(oracle.reference_y(x, L.qweight, L.qzeros, L.scales, 128, "fp16", "awq",
+                                             bias_bits=zb), plain)
+    cols = np.array([3, 17, 40])
+    with_b = oracle.reference_y(x, L.qweight, L.qzeros, L.scales, 128, "fp16", "awq",
+                                cols=cols, bias_bits=b)
+    assert np.allclose(with_b - plain[:, cols], bf[cols][None, :], rtol=0, atol=1e-12)
+
+
 def test_dequant_is_exact_in_fp32():
     # (q - z) * s for every q, z and many scales: fp32 result equals the exact rational.
     rng = np.random.default_rng(4)
