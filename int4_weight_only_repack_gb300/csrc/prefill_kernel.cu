@@ -537,7 +537,34 @@ PrefillPlan prefill_plan(int M, int N, int K, int sm_count) {
   pl.m_blocks = (M + 128 * pl.nacc - 1) / (128 * pl.nacc);
   const long long tiles = (long long)pl.m_blocks * pl.n_blocks;
   pl.ksplit = 1;
-  if (tiles < sm_count) pl.ksplit = (int)std::max(1LL, std::min<long long>(K / BK / 8, sm_count / tiles));
+  if (tiles < sm_count) {
+    // Split K over otherwise idle SMs, in slices of at least 8 k-blocks. First
+    // choice: as many slices as one wave holds. Another split replaces it when
+    // a cost model, in units of one unsplit tile's time T1, predicts it at least
+    // 10 % faster: ceil(tiles*ks / SMs) waves of units that take 1/ks of T1 plus
+    // about 4 k-blocks of pipeline fill and drain, plus writing and reading ks
+    // fp32 partial tiles (8*M*N*ks bytes at about 6.6 TB/s) and the reduce
+    // launch (about 3 us). T1 = 2 * rows * 256 * K / 8 TFLOP/s (one SM's
+    // measured tcgen05 rate). It moves the shapes whose tiles fill more than
+    // half the SMs but not all of them (one wave with no split leaves the rest
+    // idle): measured on GB300, Llama-2-70B qkv at M = 256 98.7 -> 86.3 us and
+    // Llama-2-13B down at M = 1024 232 -> 199 us; the other sweep shapes keep
+    // their split.
+    const int kmax = std::max(1, K / BK / 8);
+    const int kb_total = K / BK;
+    const double t1 = 2.0 * 128 * pl.nacc * BN * (double)K / 8e12;
+    const double part = 8.0 * M * (double)N / 6.6e12 / t1;
+    const double launch = 3e-6 / t1;
+    auto cost = [&](int ks) {
+      const double waves = (double)((tiles * ks + sm_count - 1) / sm_count);
+      return waves * (1.0 / ks + 4.0 / kb_total) + (ks > 1 ? part * ks + launch : 0.0);
+    };
+    const int one_wave = (int)std::max(1LL, std::min<long long>(kmax, sm_count / tiles));
+    int best = one_wave;
+    for (int ks = 1; ks <= kmax; ++ks)
+      if (cost(ks) < cost(best)) best = ks;
+    pl.ksplit = cost(best) < 0.9 * cost(one_wave) ? best : one_wave;
+  }
   return pl;
 }
 
