@@ -231,6 +231,20 @@ W4_API w4_status w4a16_gemm_bias(const void* x, const int32_t* qw, const void* s
                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Test hook for the timeout path (no counterpart in the pages). Runs the
+ * small-M kernel (1 <= M <= 16, no act-order, no workspace) exactly as
+ * w4a16_gemm would, except that it withholds the copies of the weights into
+ * its shared-memory ring: every ring wait then runs out after its one-second
+ * limit, the kernel records W4_ERR_TIMEOUT in the device status word, lets its
+ * other copies land and exits normally. The GPU context stays usable; y is
+ * left unspecified. A caller checks the result with w4_device_status (and
+ * clears it). For tests only; takes about one second.
+ */
+W4_API w4_status w4_test_stalled_gemm(const void* x, const int32_t* qw, const void* scales,
+                                      const int32_t* zeros, void* y, int M, int N, int K,
+                                      int group, int dtype, void* stream);
+
+/*
  * Size of the static device scratch array that w4a16_gemm_noalloc uses (32 MiB).
  */
 #define W4_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)

@@ -20,7 +20,7 @@ __all__ = [
     "w4_repack_gptq", "w4a16_gemm_workspace_size", "w4a16_gemm", "w4a16_gemm_bias",
     "w4a16_gemm_noalloc",
     "w4_dequant", "gemm_workspace",
-    "w4_device_status",
+    "w4_device_status", "w4_test_stalled_gemm",
     "RepackedLayer", "repack_awq", "repack_gptq", "linear",
 ]
 
@@ -50,6 +50,8 @@ _SIGNATURES = {
     "w4a16_gemm": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                             _c_int, _c_int, _c_int, _c_int, _c_int, _c_void_p, _c_size,
                             _c_void_p]),
+    "w4_test_stalled_gemm": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                      _c_int, _c_int, _c_int, _c_int, _c_int, _c_void_p]),
     "w4a16_gemm_bias": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                                  _c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int,
                                  _c_void_p, _c_size, _c_void_p]),
@@ -175,6 +177,12 @@ def w4a16_gemm_bias(x, qw, scales, zeros, perm, bias, y, M, N, K, group, dtype, 
     _check(lib().w4a16_gemm_bias(_ptr(x), _ptr(qw), _ptr(scales), _ptr(zeros), _ptr(perm),
                                  _ptr(bias), _ptr(y), M, N, K, group, dtype_code(dtype),
                                  _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def w4_test_stalled_gemm(x, qw, scales, zeros, y, M, N, K, group, dtype, stream=None):
+    """The small-M GEMM with its weight copies withheld (the timeout test hook)."""
+    _check(lib().w4_test_stalled_gemm(_ptr(x), _ptr(qw), _ptr(scales), _ptr(zeros), _ptr(y), M, N,
+                                      K, group, dtype_code(dtype), _stream(stream)))
 
 
 def w4a16_gemm_noalloc(x, qw, scales, zeros, perm, y, M, N, K, group, dtype, stream=None):

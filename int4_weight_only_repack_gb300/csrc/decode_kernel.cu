@@ -102,6 +102,7 @@ struct DecodeParams {
   int maxg;                // group slots per chunk
   int slice;               // output columns owned by each CTA of a cluster
   int* status;             // the library's device status word
+  int stall;               // test hook: withhold the weight copies (every ring wait runs out)
 };
 
 struct SmemLayout {
@@ -249,7 +250,7 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
     }
     if (ci == 0) {
       __syncthreads();  // every warp has issued its gating loads
-      if (tid == 0) {
+      if (tid == 0 && !p.stall) {
         for (int j = 0; j < min(D, NS); ++j) issue_stage(j);
         // and the pf stages beyond the ring into L2
         const int a0 = ka0 + min(D, NS) * SA, a1 = min(ka1, ka0 + (D + p.pf) * SA);
@@ -807,6 +808,7 @@ cudaError_t launch_decode(const GemmArgs& a, cudaStream_t stream) {
     p.maxg = plan.maxg;
     p.slice = plan.slice;
     p.status = status;
+    p.stall = a.test_stall;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((a.N / 16 + DEC_WARPS - 1) / DEC_WARPS, plan.S, 1);

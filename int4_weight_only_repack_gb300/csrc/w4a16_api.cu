@@ -65,6 +65,12 @@ w4_status check_arch() {
 // The last CUDA error an entry point reported on this thread (w4_last_cuda_error).
 thread_local cudaError_t g_last_cuda_error = cudaSuccess;
 
+// The GEMM entry points' implementation (defined below the C ABI).
+w4_status gemm_impl(const void* x, const int32_t* qw, const void* scales, const int32_t* zeros,
+                    const int32_t* perm, const void* bias, void* y, int M, int N, int K,
+                    int group, int dtype, void* workspace, size_t workspace_bytes, void* stream,
+                    int test_stall);
+
 w4_status from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return W4_OK;
   g_last_cuda_error = e;
@@ -261,6 +267,27 @@ w4_status w4a16_gemm_bias(const void* x, const int32_t* qw, const void* scales,
                           const int32_t* zeros, const int32_t* perm, const void* bias, void* y,
                           int M, int N, int K, int group, int dtype, void* workspace,
                           size_t workspace_bytes, void* stream) {
+  return gemm_impl(x, qw, scales, zeros, perm, bias, y, M, N, K, group, dtype, workspace,
+                   workspace_bytes, stream, 0);
+}
+
+w4_status w4_test_stalled_gemm(const void* x, const int32_t* qw, const void* scales,
+                               const int32_t* zeros, void* y, int M, int N, int K, int group,
+                               int dtype, void* stream) {
+  if (M < 1 || M > 16) return W4_ERR_SHAPE;  // the small-M kernel only
+  return gemm_impl(x, qw, scales, zeros, nullptr, nullptr, y, M, N, K, group, dtype, nullptr, 0,
+                   stream, 1);
+}
+
+}  // extern "C"
+
+namespace w4 {
+namespace {
+
+w4_status gemm_impl(const void* x, const int32_t* qw, const void* scales, const int32_t* zeros,
+                    const int32_t* perm, const void* bias, void* y, int M, int N, int K,
+                    int group, int dtype, void* workspace, size_t workspace_bytes, void* stream,
+                    int test_stall) {
   w4_status st = check_dims(K, N, group, dtype);
   if (st) return st;
   if (M < 0 || M > MAX_DIM) return W4_ERR_SHAPE;
@@ -302,12 +329,18 @@ w4_status w4a16_gemm_bias(const void* x, const int32_t* qw, const void* scales,
   a.bf16 = dtype == W4_BF16;
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
+  a.test_stall = test_stall;
   DeviceInfo info;
   if (device_info(&info) != cudaSuccess) return W4_ERR_CUDA;
-  if (use_prefill(M, N, K, info.sm_count))
+  if (!test_stall && use_prefill(M, N, K, info.sm_count))
     return from_cuda(launch_prefill(a, static_cast<cudaStream_t>(stream)));
   return from_cuda(launch_decode(a, static_cast<cudaStream_t>(stream)));
 }
+
+}  // namespace
+}  // namespace w4
+
+extern "C" {
 
 w4_status w4a16_gemm_noalloc(const void* x, const int32_t* qw, const void* scales,
                              const int32_t* zeros, const int32_t* perm, void* y, int M, int N,

@@ -41,6 +41,7 @@ struct GemmArgs {
   int bf16;
   void* workspace;
   size_t workspace_bytes;
+  int test_stall = 0;  // w4_test_stalled_gemm: the small-M kernel withholds its weight copies
 };
 
 // Small-M kernel: M rows processed in chunks of up to 64. An act-order call
