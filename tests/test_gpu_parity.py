@@ -398,6 +398,38 @@ def test_gemm_bias(w4, K, N, dtype, fmt, act_order, Ms):
     assert w4.w4_device_status() == 0
 
 
+@pytest.mark.parametrize("K,N,group,dtype,Ms", [
+    (64, 1 << 20, 64, "bf16", (1, 3, 33)),      # N at the API limit: 8192 column groups
+    (1 << 20, 32, 128, "fp16", (1, 17)),        # K at the API limit: 8192 groups, x in chunks
+    (64, 16, 64, "bf16", (1, 2, 100)),          # one atom; N % 32 != 0 stays on the small-M kernel
+])
+def test_gemm_extreme_shapes(w4, K, N, group, dtype, Ms):
+    """The largest K and N the ABI accepts, and the smallest layer, through the
+    repack and both kernels: sampled columns against the oracle."""
+    import torch
+    L = synth.make_custom_layer([132, K, N], K, N, group=group, dtype=dtype)
+    parts = repack(w4, L, w4.W4_LAYOUT_TILE)
+    rng = np.random.default_rng([133, K, N])
+    cols = np.unique(np.concatenate([[0, N - 1], rng.choice(N, min(N, 96), replace=False)]))
+    for M in Ms:
+        x = synth.make_custom_x([134, K, M], M, K, dtype)
+        need = w4.w4a16_gemm_workspace_size(M, N, K, group, dtype, False)
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda") if need else None
+        y = torch.empty((M, N), dtype=hdt(dtype), device="cuda")
+        qw, zeros, scales, _, _ = parts
+        w4.w4a16_gemm(half_to_dev(x, dtype), qw, scales, zeros, None, y, M, N, K, group, dtype,
+                      ws)
+        torch.cuda.synchronize()
+        got = half_from_dev(y[:, torch.from_numpy(cols).cuda()]).reshape(M, len(cols))
+        y_ref = oracle.reference_y(x, L.qweight, L.qzeros, L.scales, group, dtype, "awq",
+                                   cols=cols)
+        err = oracle.rel_err(oracle.half_bits_to_f64(got, dtype), y_ref)
+        assert err <= TOL, (M, err)
+        if small_m_kernel(M, N):
+            assert ulp_error(got, y_ref, dtype) <= 1.0, (M, ulp_error(got, y_ref, dtype))
+    assert w4.w4_device_status() == 0
+
+
 def test_gemm_is_deterministic(w4):
     K, N, M = 2048, 1024, 16
     L = synth.make_custom_layer([108], K, N, group=128, dtype="bf16")
