@@ -645,6 +645,66 @@ def sweep(args):
     print(json.dumps({"sweep_done": wl.name, "device_status": w4.w4_device_status()}), flush=True)
 
 
+def moe(args):
+    """Grouped W4A16 GEMM over an MoE layer's experts (w4a16_moe_gemm): the two
+    expert projections of a Mixtral-8x7B-shaped layer (8 experts; w13: K 4096 ->
+    N 28672, w2: K 14336 -> N 4096), a decode batch of 16 tokens routed top-2 by
+    a seeded draw (32 rows sorted by expert). One JSON line per projection:
+    time of the grouped call (CUDA graph), weight GB/s over the routed experts'
+    bytes (experts without rows are skipped by the kernel), and the same rows as
+    one w4a16_gemm call per routed expert for comparison."""
+    import torch
+
+    import int4_weight_only_repack_gb300 as w4
+
+    dev = torch.device("cuda")
+    E, T, topk = 8, 16, 2
+    rng = np.random.default_rng([0, 17])
+    choice = np.stack([rng.choice(E, topk, replace=False) for _ in range(T)])
+    counts = np.bincount(choice.reshape(-1), minlength=E)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    rows = int(off[-1])
+    hbm, _ = measured_peaks()
+    for name, K, N in (("w13", 4096, 28672), ("w2", 14336, 4096)):
+        qws, qzs, scs = [], [], []
+        for e in range(E):
+            L = synth.make_custom_layer([0, 17, e, K, N], K, N, group=128, dtype="bf16")
+            qws.append(torch.from_numpy(L.qweight).to(dev))
+            qzs.append(torch.from_numpy(L.qzeros).to(dev))
+            scs.append(torch.from_numpy(L.scales.view(np.int16)).to(dev).view(torch.bfloat16))
+        experts = w4.repack_awq_experts(qws, qzs, scs, K, N, 128, torch.bfloat16)
+        del qws, qzs, scs
+        x = torch.randn(rows, K, device=dev).to(torch.bfloat16)
+        y = torch.empty((rows, N), dtype=torch.bfloat16, device=dev)
+        offd = torch.from_numpy(off).to(dev)
+        mx = int(counts.max())
+        t_grouped = graph_time(torch, lambda: w4.moe_linear(x, experts, offd, mx, y=y), 50)
+        qw_b, z_b, s_b = w4.w4_repack_sizes(K, N, 128, w4.W4_LAYOUT_TILE)
+
+        def per_expert():
+            for e in range(E):
+                r0, r1 = int(off[e]), int(off[e + 1])
+                if r1 > r0:
+                    w4.w4a16_gemm(x[r0:r1], experts.qw[e * qw_b // 4:(e + 1) * qw_b // 4],
+                                  experts.scales[e * s_b // 2:(e + 1) * s_b // 2],
+                                  experts.zeros[e * z_b // 4:(e + 1) * z_b // 4], None, y[r0:r1],
+                                  r1 - r0, N, K, 128, torch.bfloat16)
+
+        t_loop = graph_time(torch, per_expert, 50)
+        active = int((counts > 0).sum())
+        wb = active * alg_bytes(K, N)
+        print(json.dumps({"moe": "mixtral_8x7b_shaped", "proj": name, "K": K, "N": N,
+                          "experts": E, "tokens": T, "topk": topk, "rows": rows,
+                          "rows_per_expert": counts.tolist(), "routed_experts": active,
+                          "us": round(t_grouped * 1e6, 2),
+                          "weight_gbs": round(wb / t_grouped / 1e9, 1),
+                          "frac_hbm": round(wb / t_grouped / 1e9 / hbm, 3),
+                          "per_expert_calls_us": round(t_loop * 1e6, 2),
+                          "device_status": w4.w4_device_status()}), flush=True)
+        del experts, x, y
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -659,6 +719,8 @@ def main():
                     help="workload of --sweep: 4 = Llama-2-70B, 3 = Llama-2-13B GPTQ act-order")
     ap.add_argument("--sweep", action="store_true",
                     help="every layer of --sweep-config at every M of that workload (one line each)")
+    ap.add_argument("--moe", action="store_true",
+                    help="the grouped MoE GEMM on a Mixtral-8x7B-shaped layer (one line per projection)")
     ap.add_argument("--single", default=None,
                     help="K,N,M[,dtype]: time one layer shape only (profiling aid)")
     args = ap.parse_args()
@@ -666,6 +728,8 @@ def main():
         single(args)
     elif args.sweep:
         sweep(args)
+    elif args.moe:
+        moe(args)
     elif args.impl == "reference":
         reference(args)
     else:

@@ -99,7 +99,9 @@ enum {
     W4_ERR_CUDA = 9,       /* a CUDA runtime call or kernel launch failed               */
     W4_ERR_WORKSPACE = 10, /* workspace NULL or smaller than w4a16_gemm_workspace_size  */
     W4_ERR_GIDX = 11,      /* (written to *status_out by the device) g_idx irregular    */
-    W4_ERR_TIMEOUT = 12    /* (device status word) a kernel gave up on a pipeline wait  */
+    W4_ERR_TIMEOUT = 12,   /* (device status word) a kernel gave up on a pipeline wait  */
+    W4_ERR_EXPERT_ROWS = 13 /* (device status word) w4a16_moe_gemm: an expert's row range
+                              was invalid or longer than max_rows_per_expert          */
 };
 
 enum { W4_F16 = 0, W4_BF16 = 1 };
@@ -229,6 +231,34 @@ W4_API w4_status w4a16_gemm_bias(const void* x, const int32_t* qw, const void* s
                                  const int32_t* zeros, const int32_t* perm, const void* bias,
                                  void* y, int M, int N, int K, int group, int dtype,
                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Grouped W4A16 GEMM over the experts of an MoE layer (the AWQ MoE support of
+ * "vLLM AWQ 4-bit 量化实践" §5.4: 4-bit expert weights in the kernel's layout).
+ * For every expert e, the rows [off[e], off[e+1]) of x, sorted by expert, are
+ * multiplied by expert e's weights into the same rows of y:
+ *   y[m][:] = x[m][:] · W_e  for off[e] <= m < off[e+1].
+ *   x [total_rows][K], y [total_rows][N] in dtype, row-major.
+ *   qw / scales / zeros: the experts' TILE-layout weights, zeros and scales from
+ *          w4_repack_awq / w4_repack_gptq (no act-order), stored one expert
+ *          after another: expert e's qw at byte e * qw_bytes, scales at element
+ *          e * G * N, zeros at word e * G * N / 8 (sizes from w4_repack_sizes).
+ *   expert_offsets: device int32 [num_experts + 1], non-decreasing, 0 <= off[e]
+ *          <= total_rows; read on the device after the wait for the kernel
+ *          before this call (a routing kernel may write them).
+ *   max_rows_per_expert: 1..64, the most rows any expert has; it sizes the
+ *          launch. An expert whose range is invalid or longer records
+ *          W4_ERR_EXPERT_ROWS in the device status word and leaves its rows of y
+ *          unwritten. Experts with no rows skip their weights altogether.
+ * It runs the small-M kernel (one launch for all experts, the expert in the
+ * grid's z dimension), with its results, determinism and ordering rules.
+ * Errors (host side): those of w4a16_gemm, plus W4_ERR_SHAPE for num_experts < 1,
+ * max_rows_per_expert outside 1..64 or total_rows < 0.
+ */
+W4_API w4_status w4a16_moe_gemm(const void* x, const int32_t* qw, const void* scales,
+                                const int32_t* zeros, const int32_t* expert_offsets, void* y,
+                                int num_experts, int max_rows_per_expert, int total_rows, int N,
+                                int K, int group, int dtype, void* stream);
 
 /*
  * Test hook for the timeout path (no counterpart in the pages). Runs the

@@ -21,7 +21,8 @@ __all__ = [
     "w4a16_gemm_noalloc",
     "w4_dequant", "gemm_workspace",
     "w4_device_status", "w4_test_stalled_gemm",
-    "RepackedLayer", "repack_awq", "repack_gptq", "linear",
+    "RepackedLayer", "repack_awq", "repack_gptq", "linear", "w4a16_moe_gemm", "RepackedExperts",
+    "repack_awq_experts", "moe_linear",
 ]
 
 W4_F16, W4_BF16 = 0, 1
@@ -50,6 +51,9 @@ _SIGNATURES = {
     "w4a16_gemm": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                             _c_int, _c_int, _c_int, _c_int, _c_int, _c_void_p, _c_size,
                             _c_void_p]),
+    "w4a16_moe_gemm": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                _c_void_p]),
     "w4_test_stalled_gemm": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                                       _c_int, _c_int, _c_int, _c_int, _c_int, _c_void_p]),
     "w4a16_gemm_bias": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
@@ -177,6 +181,52 @@ def w4a16_gemm_bias(x, qw, scales, zeros, perm, bias, y, M, N, K, group, dtype, 
     _check(lib().w4a16_gemm_bias(_ptr(x), _ptr(qw), _ptr(scales), _ptr(zeros), _ptr(perm),
                                  _ptr(bias), _ptr(y), M, N, K, group, dtype_code(dtype),
                                  _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def w4a16_moe_gemm(x, qw, scales, zeros, expert_offsets, y, num_experts, max_rows_per_expert,
+                   total_rows, N, K, group, dtype, stream=None):
+    _check(lib().w4a16_moe_gemm(_ptr(x), _ptr(qw), _ptr(scales), _ptr(zeros), _ptr(expert_offsets),
+                                _ptr(y), num_experts, max_rows_per_expert, total_rows, N, K, group,
+                                dtype_code(dtype), _stream(stream)))
+
+
+class RepackedExperts:
+    """Device buffers of an MoE layer's experts, one expert after another."""
+
+    def __init__(self, E, K, N, group, dtype, qw, zeros, scales):
+        self.E, self.K, self.N, self.group, self.dtype = E, K, N, group, dtype
+        self.qw, self.zeros, self.scales = qw, zeros, scales
+
+
+def repack_awq_experts(qweights, qzeros, scales, K, N, group, dtype, stream=None):
+    """Per-expert w4_repack_awq (TILE layout) into stacked buffers: qweights /
+    qzeros / scales are sequences of the experts' checkpoint tensors (qzeros
+    entries may be None for symmetric experts)."""
+    E = len(qweights)
+    qw_b, z_b, s_b = w4_repack_sizes(K, N, group, W4_LAYOUT_TILE)
+    dev = qweights[0].device
+    qw = torch.empty(E * qw_b // 4, dtype=torch.int32, device=dev)
+    zeros = torch.empty(E * z_b // 4, dtype=torch.int32, device=dev)
+    sc = torch.empty(E * s_b // 2, dtype=_half_dtype(dtype), device=dev)
+    nq, nz, ns = qw_b // 4, z_b // 4, s_b // 2
+    for e in range(E):
+        w4_repack_awq(qweights[e], qzeros[e], scales[e], K, N, group, dtype, W4_LAYOUT_TILE,
+                      qw[e * nq:(e + 1) * nq], zeros[e * nz:(e + 1) * nz],
+                      sc[e * ns:(e + 1) * ns], stream)
+    return RepackedExperts(E, K, N, group, dtype, qw, zeros, sc)
+
+
+def moe_linear(x, experts: RepackedExperts, expert_offsets, max_rows_per_expert, y=None,
+               stream=None):
+    """y[m] = x[m] · W_e for the rows m of expert e ([off[e], off[e+1]), x sorted
+    by expert); expert_offsets: int32 [E + 1] on the device."""
+    T = x.shape[0]
+    if y is None:
+        y = torch.empty((T, experts.N), dtype=x.dtype, device=x.device)
+    w4a16_moe_gemm(x, experts.qw, experts.scales, experts.zeros, expert_offsets, y, experts.E,
+                   max_rows_per_expert, T, experts.N, experts.K, experts.group, experts.dtype,
+                   stream)
+    return y
 
 
 def w4_test_stalled_gemm(x, qw, scales, zeros, y, M, N, K, group, dtype, stream=None):

@@ -103,6 +103,12 @@ struct DecodeParams {
   int slice;               // output columns owned by each CTA of a cluster
   int* status;             // the library's device status word
   int stall;               // test hook: withhold the weight copies (every ring wait runs out)
+  // grouped (expert) calls: blockIdx.z is the expert, whose weights sit qw_estride
+  // words / s_estride scales / z_estride zero words after the previous expert's
+  // and whose rows of x and y are [eoff[e], eoff[e+1]) (at most M of them)
+  const int32_t* eoff;
+  size_t qw_estride, s_estride, z_estride;
+  int total_rows;
 };
 
 struct SmemLayout {
@@ -158,6 +164,16 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
   const int D = p.ring;
   const int NB = p.nbuf;
   const SmemLayout L = smem_layout(MT, p.M, p.x_stride, NB, D, p.maxg, S, p.slice);
+  // grouped calls: this CTA's expert and its weights; its rows come after the wait
+  const bool grouped = p.eoff != nullptr;
+  const int ex = blockIdx.z;
+  const uint32_t* qwp = p.qw + (size_t)ex * p.qw_estride;
+  const uint16_t* scp = p.scales + (size_t)ex * p.s_estride;
+  const uint32_t* zp = p.zeros + (size_t)ex * p.z_estride;
+  int M = p.M;  // rows of this call (the shared-memory layout is sized for p.M)
+  const uint16_t* xg = p.x;
+  uint16_t* yg = p.y;
+  __shared__ int grp_rows[2];
 
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem + L.xs);
   uint16_t* xzero = xs + (size_t)NB * p.M * p.x_stride;  // the zero row
@@ -189,7 +205,7 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
   const int nt = cgi * DEC_WARPS + warp;
   const bool has_cols = nt < p.N / 16;
   // the column group's run: k-atom a at byte offset a * KROW_BYTES
-  const uint8_t* gsrc = reinterpret_cast<const uint8_t*>(p.qw) + (size_t)cgi * p.A * KROW_BYTES;
+  const uint8_t* gsrc = reinterpret_cast<const uint8_t*>(qwp) + (size_t)cgi * p.A * KROW_BYTES;
   const uint64_t stream_policy = evict_first_policy();
   const bool x_async = p.perm == nullptr;
 
@@ -200,9 +216,9 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
     const int b = NB == 2 ? (ci & 1) : 0;
     uint16_t* dst = xs + (size_t)b * p.M * p.x_stride;
     last_chunk[b] = ci;
-    mbar_arrive_expect_tx(xbar0 + 8 * b, (uint32_t)(p.M * KC * 2));
-    for (int m = 0; m < p.M; ++m)
-      bulk_copy(smem_addr(dst + (size_t)m * p.x_stride), p.x + (size_t)m * p.K + c0 * ATOM_K,
+    mbar_arrive_expect_tx(xbar0 + 8 * b, (uint32_t)(M * KC * 2));
+    for (int m = 0; m < M; ++m)
+      bulk_copy(smem_addr(dst + (size_t)m * p.x_stride), xg + (size_t)m * p.K + c0 * ATOM_K,
                 (uint32_t)(KC * 2), xbar0 + 8 * b);
   };
   // stage j (k-atoms [ka0 + j*SA, ...)) into ring slot j % D (one thread)
@@ -230,6 +246,12 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
                       half_bits_to_float<BF16>((uint16_t)(sv[4 + (c >> 1)] >> (16 * (c & 1)))));
     zraw[gl] = z;
   };
+  // the first ring stages, and the pf stages beyond the ring into L2 (one thread)
+  auto fill_ring = [&]() {
+    for (int j = 0; j < min(D, NS); ++j) issue_stage(j);
+    const int a0 = ka0 + min(D, NS) * SA, a1 = min(ka1, ka0 + (D + p.pf) * SA);
+    if (a1 > a0) prefetch_l2(gsrc + (size_t)a0 * KROW_BYTES, (uint32_t)(a1 - a0) * KROW_BYTES);
+  };
   // scales / zeros of the groups of chunk ci for this warp's tile; in the first
   // chunk the ring fill waits until every warp has issued these loads, so they
   // are not queued behind the weight stream
@@ -243,28 +265,22 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
     const bool mine = has_cols && lane < ng;
     if (mine) {
       const int gi = g_first + lane;
-      const uint4* sp = reinterpret_cast<const uint4*>(p.scales + (size_t)gi * p.N + nt * 16);
+      const uint4* sp = reinterpret_cast<const uint4*>(scp + (size_t)gi * p.N + nt * 16);
       ms0 = __ldg(sp);
       ms1 = __ldg(sp + 1);
-      mz = __ldg(reinterpret_cast<const uint2*>(p.zeros + (size_t)gi * (p.N / 8) + nt * 2));
+      mz = __ldg(reinterpret_cast<const uint2*>(zp + (size_t)gi * (p.N / 8) + nt * 2));
     }
     if (ci == 0) {
       __syncthreads();  // every warp has issued its gating loads
-      if (tid == 0 && !p.stall) {
-        for (int j = 0; j < min(D, NS); ++j) issue_stage(j);
-        // and the pf stages beyond the ring into L2
-        const int a0 = ka0 + min(D, NS) * SA, a1 = min(ka1, ka0 + (D + p.pf) * SA);
-        if (a1 > a0)
-          prefetch_l2(gsrc + (size_t)a0 * KROW_BYTES, (uint32_t)(a1 - a0) * KROW_BYTES);
-      }
+      if (tid == 0 && !p.stall && !grouped) fill_ring();
     }
     if (mine) stage_meta(lane, ms0, ms1, mz);
     for (int gl = lane + 32; has_cols && gl < ng; gl += 32) {
       const int gi = g_first + gl;
-      const uint4* sp = reinterpret_cast<const uint4*>(p.scales + (size_t)gi * p.N + nt * 16);
+      const uint4* sp = reinterpret_cast<const uint4*>(scp + (size_t)gi * p.N + nt * 16);
       const uint4 a = __ldg(sp), bb = __ldg(sp + 1);
       const uint2 z =
-          __ldg(reinterpret_cast<const uint2*>(p.zeros + (size_t)gi * (p.N / 8) + nt * 2));
+          __ldg(reinterpret_cast<const uint2*>(zp + (size_t)gi * (p.N / 8) + nt * 2));
       stage_meta(gl, a, bb, z);
     }
   };
@@ -294,7 +310,27 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
   // every CTA of this grid is resident: the next kernel may start its own
   // prologue as resources free up
   asm volatile("griddepcontrol.launch_dependents;");
-  if (tid == 0 && x_async && nchunks > 0) {
+  if (grouped) {
+    // the expert's rows (the offsets may come from the kernel before this one);
+    // an expert with no rows skips its weight stream altogether
+    if (tid == 0) {
+      const int r0 = *reinterpret_cast<const volatile int32_t*>(p.eoff + ex);
+      const int r1 = *reinterpret_cast<const volatile int32_t*>(p.eoff + ex + 1);
+      int m = r1 - r0;
+      if (r0 < 0 || m < 0 || r1 > p.total_rows || m > p.M) {
+        atomicExch(p.status, W4_ERR_EXPERT_ROWS);
+        m = 0;
+      }
+      grp_rows[0] = r0;
+      grp_rows[1] = m;
+    }
+    __syncthreads();
+    M = grp_rows[1];
+    xg = p.x + (size_t)grp_rows[0] * p.K;
+    yg = p.y + (size_t)grp_rows[0] * p.N;
+    if (tid == 0 && M > 0 && !p.stall) fill_ring();
+  }
+  if (tid == 0 && x_async && nchunks > 0 && M > 0) {
     issue_x(0);
     if (NB == 2 && nchunks > 1) issue_x(1);
   }
@@ -333,7 +369,7 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
     }
   };
 
-  for (int ci = 0; ci < nchunks; ++ci) {
+  for (int ci = 0; M > 0 && ci < nchunks; ++ci) {
     const int c0 = ka0 + ci * p.chunk_atoms;
     const int c1 = min(ka1, c0 + p.chunk_atoms);
     const int KC = (c1 - c0) * ATOM_K;
@@ -350,9 +386,9 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
       // act-order: gather x[:, perm] with plain loads
       const int chunks = KC / 8;
       const int kx0 = c0 * ATOM_K;
-      for (int i = tid; live && i < p.M * chunks; i += DEC_THREADS) {
+      for (int i = tid; live && i < M * chunks; i += DEC_THREADS) {
         const int m = i / chunks, c = i - m * chunks;
-        const uint16_t* xr = p.x + (size_t)m * p.K;
+        const uint16_t* xr = xg + (size_t)m * p.K;
         uint16_t h[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) h[e] = __ldg(xr + __ldg(p.perm + kx0 + 8 * c + e));
@@ -376,7 +412,7 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
         const int r1 = min(c1 * ATOM_K, p.gshift >= 31 ? p.K : (gi + 1) << p.gshift);
         for (int mt = 0; mt < MT; ++mt) {
           const int row = 8 * mt + gg;
-          const uint16_t* xr = (row < p.M ? xb + (size_t)row * p.x_stride : xzero) + 8 * t;
+          const uint16_t* xr = (row < M ? xb + (size_t)row * p.x_stride : xzero) + 8 * t;
           float sa[2][4] = {};
           for (int r = r0; r < r1; r += 64) {
 #pragma unroll
@@ -421,7 +457,7 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
       const int row = 8 * mt + gg;
-      xa[mt] = smem_addr(row < p.M ? xb + (size_t)row * p.x_stride : xzero) + 16u * (uint32_t)t;
+      xa[mt] = smem_addr(row < M ? xb + (size_t)row * p.x_stride : xzero) + 16u * (uint32_t)t;
     }
     // k-atoms per group (groups of 64 rows or more); a chunk that starts inside
     // a group (only possible for groups longer than a stage) opens it at once
@@ -558,11 +594,11 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
     for (int mt = 0; mt < MT; ++mt) {
       const int m0 = 8 * mt + 2 * t;
       const int ca = warp * 16 + gg, cb = ca + 8;
-      if (m0 < p.M) {
+      if (m0 < M) {
         push(ca, m0, tc[mt][0]);
         push(cb, m0, tc[mt][2]);
       }
-      if (m0 + 1 < p.M) {
+      if (m0 + 1 < M) {
         push(ca, m0 + 1, tc[mt][1]);
         push(cb, m0 + 1, tc[mt][3]);
       }
@@ -573,14 +609,14 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
     const int c_lo = srank * SL;
     const int c_hi = min(NCOL, c_lo + SL);
     const int width = c_hi - c_lo;
-    for (int o = tid; o < width * p.M; o += DEC_THREADS) {
+    for (int o = tid; o < width * M; o += DEC_THREADS) {
       const int m = o / width, cl = o - m * width;
       const int n = cgi * NCOL + c_lo + cl;
       if (n >= p.N) continue;
       float sum = 0.f;
       for (int r = 0; r < S; ++r) sum += recv[((size_t)r * SL + cl) * MR + m];
       if (p.bias != nullptr) sum += half_bits_to_float<BF16>(p.bias[n]);  // one rounding below
-      p.y[(size_t)m * p.N + n] = float_to_half_bits<BF16>(sum);
+      yg[(size_t)m * p.N + n] = float_to_half_bits<BF16>(sum);
     }
   }
 }
@@ -675,14 +711,17 @@ DecodePlan fit_ring(int S, int A, int Mc, int MT, int gshift, int per_sm, int sm
 //  * a CTA's K range stays between 16 and 64 k-atoms (shorter runs are
 //    dominated by the fixed prologue / reduction cost, longer ones by the wait
 //    for the slowest CTA);
+//  * CTA counts below count every (column group, expert) pair of a grouped call;
 //  * with one token tile the launch aims at about 2.6 CTAs per SM (enough warps
 //    to hide the loop's latencies, few enough to stay near one wave);
-//  * with more token tiles, a split that would take more than three waves is
-//    replaced by the longest CTA ranges (x in chunks) at about one wave.
+//  * a split that would take more than three waves is replaced by the longest
+//    CTA ranges (x in chunks) at about one wave.
 // The ring is then as deep as fits with 3 resident CTAs per SM (2 when the
 // register budget allows only 2), at least 2 stages.
-DecodePlan plan_decode(int N, int K, int Mc, int MT, int gshift, const DeviceInfo& info) {
+DecodePlan plan_decode(int N, int K, int Mc, int MT, int gshift, int experts,
+                       const DeviceInfo& info) {
   const int NG = (N / 16 + DEC_WARPS - 1) / DEC_WARPS, A = K / ATOM_K;
+  const long long units = (long long)NG * experts;  // (column group, expert) pairs of the grid
   const int nst_all = (A + SA - 1) / SA;
   auto cta_atoms = [&](int S) { return (nst_all + S - 1) / S * SA; };
   const int s_cap = std::min(MAX_SPLIT, nst_all);
@@ -697,14 +736,16 @@ DecodePlan plan_decode(int N, int K, int Mc, int MT, int gshift, const DeviceInf
   s_hi = std::max(s_hi, s_lo);
   int S = s_lo;
   if (MT == 1) {
-    const int target = (int)(2.6 * info.sm_count / NG + 0.5);
+    const int target = (int)(2.6 * info.sm_count / units + 0.5);
     S = std::min(std::max(target, s_lo), s_hi);
-  } else if ((long long)NG * S > 3LL * info.sm_count * decode_min_ctas(MT)) {
+  }
+  if (units * S > 3LL * info.sm_count * decode_min_ctas(MT)) {
     // more than three waves of short CTAs, each paying the prologue and the
     // cluster reduction again: one wave's worth of the longest CTAs instead,
     // x staged in chunks (measured on GB300, M = 16: Llama-2-70B gate_up
-    // 135 -> 108 us, down 88 -> 71 us; shapes of up to three waves lose)
-    S = std::max(s64, (int)(2.0 * info.sm_count / NG + 0.5));
+    // 135 -> 108 us, down 88 -> 71 us; a grouped Mixtral-shaped w13 at up to
+    // 8 rows per expert 164 -> 160 us; shapes of up to three waves lose)
+    S = std::max(s64, (int)(2.0 * info.sm_count / units + 0.5));
   }
   const int reg_ctas = decode_min_ctas(MT);
   DecodePlan d = fit_ring(S, A, Mc, MT, gshift, std::min(3, reg_ctas), info.smem_per_sm);
@@ -716,9 +757,10 @@ DecodePlan plan_decode(int N, int K, int Mc, int MT, int gshift, const DeviceInf
 // Plans are cached per (device, shape): planning costs tens of microseconds of
 // host time, more than a decode launch.
 struct PlanKey {
-  int dev, N, K, Mc, gshift;
+  int dev, N, K, Mc, gshift, experts;
   bool operator==(const PlanKey& o) const {
-    return dev == o.dev && N == o.N && K == o.K && Mc == o.Mc && gshift == o.gshift;
+    return dev == o.dev && N == o.N && K == o.K && Mc == o.Mc && gshift == o.gshift &&
+           experts == o.experts;
   }
 };
 struct PlanKeyHash {
@@ -728,21 +770,23 @@ struct PlanKeyHash {
     h ^= (uint64_t)k.K + 0x7F4A7C15ull + (h << 6) + (h >> 2);
     h ^= (uint64_t)k.Mc + 0x7F4A7C15ull + (h << 6) + (h >> 2);
     h ^= (uint64_t)k.gshift + 0x7F4A7C15ull + (h << 6) + (h >> 2);
+    h ^= (uint64_t)k.experts + 0x7F4A7C15ull + (h << 6) + (h >> 2);
     return (size_t)h;
   }
 };
 
-cudaError_t cached_plan(int N, int K, int Mc, int MT, int gshift, const DeviceInfo& info,
-                        DecodePlan* out) {
+cudaError_t cached_plan(int N, int K, int Mc, int MT, int gshift, int experts,
+                        const DeviceInfo& info, DecodePlan* out) {
   static std::mutex mu;
   static std::unordered_map<PlanKey, DecodePlan, PlanKeyHash> plans;
   int dev = 0;
   const cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const PlanKey key{dev, N, K, Mc, gshift};
+  const PlanKey key{dev, N, K, Mc, gshift, experts};
   std::lock_guard<std::mutex> lock(mu);
   auto it = plans.find(key);
-  if (it == plans.end()) it = plans.emplace(key, plan_decode(N, K, Mc, MT, gshift, info)).first;
+  if (it == plans.end())
+    it = plans.emplace(key, plan_decode(N, K, Mc, MT, gshift, experts, info)).first;
   *out = it->second;
   return cudaSuccess;
 }
@@ -783,7 +827,9 @@ cudaError_t launch_decode(const GemmArgs& a, cudaStream_t stream) {
     const int Mc = std::min(DECODE_MAX_M, a.M - r0);
     const int MT = Mc <= 8 ? 1 : Mc <= 16 ? 2 : Mc <= 32 ? 4 : 8;
     DecodePlan plan;
-    if ((err = cached_plan(a.N, a.K, Mc, MT, gshift, info, &plan)) != cudaSuccess) return err;
+    const int experts = a.eoff != nullptr ? a.num_experts : 1;
+    if ((err = cached_plan(a.N, a.K, Mc, MT, gshift, experts, info, &plan)) != cudaSuccess)
+      return err;
     void* fn = pick_kernel(MT, a.bf16 != 0, g64);
     if ((err = ensure_smem(fn, plan.L.total)) != cudaSuccess) return err;
 
@@ -809,9 +855,15 @@ cudaError_t launch_decode(const GemmArgs& a, cudaStream_t stream) {
     p.slice = plan.slice;
     p.status = status;
     p.stall = a.test_stall;
+    p.eoff = a.eoff;
+    p.qw_estride = a.qw_estride;
+    p.s_estride = a.s_estride;
+    p.z_estride = a.z_estride;
+    p.total_rows = a.total_rows;
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((a.N / 16 + DEC_WARPS - 1) / DEC_WARPS, plan.S, 1);
+    cfg.gridDim = dim3((a.N / 16 + DEC_WARPS - 1) / DEC_WARPS, plan.S,
+                       a.eoff != nullptr ? (unsigned)a.num_experts : 1u);
     cfg.blockDim = dim3(DEC_THREADS, 1, 1);
     cfg.dynamicSmemBytes = plan.L.total;
     cfg.stream = stream;

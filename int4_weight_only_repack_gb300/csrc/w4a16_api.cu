@@ -127,6 +127,8 @@ const char* w4_status_string(w4_status s) {
     case W4_ERR_WORKSPACE: return "W4_ERR_WORKSPACE: workspace missing or too small";
     case W4_ERR_GIDX: return "W4_ERR_GIDX: g_idx out of range or groups not of equal size";
     case W4_ERR_TIMEOUT: return "W4_ERR_TIMEOUT: a kernel gave up on a pipeline wait";
+    case W4_ERR_EXPERT_ROWS:
+      return "W4_ERR_EXPERT_ROWS: an expert's rows were invalid or more than max_rows_per_expert";
     default: return "unknown w4_status";
   }
 }
@@ -269,6 +271,58 @@ w4_status w4a16_gemm_bias(const void* x, const int32_t* qw, const void* scales,
                           size_t workspace_bytes, void* stream) {
   return gemm_impl(x, qw, scales, zeros, perm, bias, y, M, N, K, group, dtype, workspace,
                    workspace_bytes, stream, 0);
+}
+
+w4_status w4a16_moe_gemm(const void* x, const int32_t* qw, const void* scales,
+                         const int32_t* zeros, const int32_t* expert_offsets, void* y,
+                         int num_experts, int max_rows_per_expert, int total_rows, int N, int K,
+                         int group, int dtype, void* stream) {
+  w4_status st = check_dims(K, N, group, dtype);
+  if (st) return st;
+  if ((st = check_layout_dims(K, N, W4_LAYOUT_TILE))) return st;
+  if (num_experts < 1 || num_experts > 65535 || max_rows_per_expert < 1 ||
+      max_rows_per_expert > DECODE_MAX_M || total_rows < 0 || total_rows > MAX_DIM)
+    return W4_ERR_SHAPE;
+  if (!qw || !scales || !zeros || !expert_offsets) return W4_ERR_NULL;
+  if (total_rows > 0 && (!x || !y)) return W4_ERR_NULL;
+  if (!aligned16(x) || !aligned16(qw) || !aligned16(scales) || !aligned16(zeros) ||
+      !aligned16(expert_offsets) || !aligned16(y))
+    return W4_ERR_ALIGN;
+  const int g = resolve_group(group, K);
+  const size_t G = (size_t)K / g;
+  size_t qw_b = 0;
+  w4_repack_sizes(K, N, group, W4_LAYOUT_TILE, &qw_b, nullptr, nullptr);
+  const size_t E = (size_t)num_experts;
+  const size_t y_b = (size_t)total_rows * N * 2;
+  const void* ins[5] = {x, qw, scales, zeros, expert_offsets};
+  const size_t in_b[5] = {(size_t)total_rows * K * 2, E * qw_b, E * G * N * 2, E * G * N / 2,
+                          (E + 1) * 4};
+  for (int j = 0; j < 5; ++j)
+    if (overlaps(y, y_b, ins[j], in_b[j])) return W4_ERR_ALIAS;
+  if ((st = check_arch())) return st;
+  if (total_rows == 0) return W4_OK;
+  GemmArgs a;
+  a.x = x;
+  a.qw = reinterpret_cast<const uint32_t*>(qw);
+  a.scales = scales;
+  a.zeros = reinterpret_cast<const uint32_t*>(zeros);
+  a.perm = nullptr;
+  a.y = y;
+  a.bias = nullptr;
+  a.M = max_rows_per_expert;
+  a.N = N;
+  a.K = K;
+  a.group = g;
+  a.bf16 = dtype == W4_BF16;
+  a.workspace = nullptr;
+  a.workspace_bytes = 0;
+  a.eoff = expert_offsets;
+  a.num_experts = num_experts;
+  a.total_rows = total_rows;
+  a.qw_estride = qw_b / 4;
+  a.s_estride = G * N;
+  a.z_estride = G * N / 8;
+  return from_cuda(launch_decode(a, static_cast<cudaStream_t>(stream)));
 }
 
 w4_status w4_test_stalled_gemm(const void* x, const int32_t* qw, const void* scales,

@@ -42,6 +42,12 @@ struct GemmArgs {
   void* workspace;
   size_t workspace_bytes;
   int test_stall = 0;  // w4_test_stalled_gemm: the small-M kernel withholds its weight copies
+  // grouped (expert) calls of the small-M kernel (w4a16_moe_gemm): M is the most
+  // rows any expert has; expert e's rows are [eoff[e], eoff[e + 1]) of x / y
+  const int32_t* eoff = nullptr;
+  int num_experts = 1;
+  int total_rows = 0;
+  size_t qw_estride = 0, s_estride = 0, z_estride = 0;  // words / elements / words per expert
 };
 
 // Small-M kernel: M rows processed in chunks of up to 64. An act-order call
