@@ -648,23 +648,27 @@ def sweep(args):
 def moe(args):
     """Grouped W4A16 GEMM over an MoE layer's experts (w4a16_moe_gemm): the two
     expert projections of a Mixtral-8x7B-shaped layer (8 experts; w13: K 4096 ->
-    N 28672, w2: K 14336 -> N 4096), a decode batch of 16 tokens routed top-2 by
-    a seeded draw (32 rows sorted by expert). One JSON line per projection:
-    time of the grouped call (CUDA graph), weight GB/s over the routed experts'
-    bytes (experts without rows are skipped by the kernel), and the same rows as
-    one w4a16_gemm call per routed expert for comparison."""
+    N 28672, w2: K 14336 -> N 4096), for a decode batch of 16 tokens and a
+    prefill batch of 4096 tokens, each routed top-2 by a seeded draw (rows sorted
+    by expert). One JSON line per projection and batch: time of the grouped call
+    (CUDA graph); for the decode batch weight GB/s over the routed experts' bytes
+    (experts without rows are skipped by the kernel), for the prefill batch
+    TFLOP/s (2 * rows * K * N); and the same rows as one w4a16_gemm call per
+    routed expert for comparison."""
     import torch
 
     import int4_weight_only_repack_gb300 as w4
 
     dev = torch.device("cuda")
-    E, T, topk = 8, 16, 2
-    rng = np.random.default_rng([0, 17])
-    choice = np.stack([rng.choice(E, topk, replace=False) for _ in range(T)])
-    counts = np.bincount(choice.reshape(-1), minlength=E)
-    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
-    rows = int(off[-1])
+    E, topk = 8, 2
     hbm, _ = measured_peaks()
+    tc, _ = measured_tc_peak()
+    routes = []
+    for T in (16, 4096):
+        rng = np.random.default_rng([0, 17] if T == 16 else [0, 17, T])
+        choice = np.stack([rng.choice(E, topk, replace=False) for _ in range(T)])
+        counts = np.bincount(choice.reshape(-1), minlength=E)
+        routes.append((T, counts, np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)))
     for name, K, N in (("w13", 4096, 28672), ("w2", 14336, 4096)):
         qws, qzs, scs = [], [], []
         for e in range(E):
@@ -674,34 +678,50 @@ def moe(args):
             scs.append(torch.from_numpy(L.scales.view(np.int16)).to(dev).view(torch.bfloat16))
         experts = w4.repack_awq_experts(qws, qzs, scs, K, N, 128, torch.bfloat16)
         del qws, qzs, scs
-        x = torch.randn(rows, K, device=dev).to(torch.bfloat16)
-        y = torch.empty((rows, N), dtype=torch.bfloat16, device=dev)
-        offd = torch.from_numpy(off).to(dev)
-        mx = int(counts.max())
-        t_grouped = graph_time(torch, lambda: w4.moe_linear(x, experts, offd, mx, y=y), 50)
         qw_b, z_b, s_b = w4.w4_repack_sizes(K, N, 128, w4.W4_LAYOUT_TILE)
+        for T, counts, off in routes:
+            rows = int(off[-1])
+            x = torch.randn(rows, K, device=dev).to(torch.bfloat16)
+            y = torch.empty((rows, N), dtype=torch.bfloat16, device=dev)
+            ws = torch.empty(max(1, max(w4.w4a16_gemm_workspace_size(int(c), N, K, 128,
+                                                                    torch.bfloat16, False)
+                                        for c in counts if c > 0)),
+                             dtype=torch.uint8, device=dev)
+            offd = torch.from_numpy(off).to(dev)
+            mx = int(counts.max())
+            reps = 50 if T == 16 else 10
+            t_grouped = graph_time(torch, lambda: w4.moe_linear(x, experts, offd, mx, y=y), reps)
 
-        def per_expert():
-            for e in range(E):
-                r0, r1 = int(off[e]), int(off[e + 1])
-                if r1 > r0:
-                    w4.w4a16_gemm(x[r0:r1], experts.qw[e * qw_b // 4:(e + 1) * qw_b // 4],
-                                  experts.scales[e * s_b // 2:(e + 1) * s_b // 2],
-                                  experts.zeros[e * z_b // 4:(e + 1) * z_b // 4], None, y[r0:r1],
-                                  r1 - r0, N, K, 128, torch.bfloat16)
+            def per_expert():
+                for e in range(E):
+                    r0, r1 = int(off[e]), int(off[e + 1])
+                    if r1 > r0:
+                        w4.w4a16_gemm(x[r0:r1], experts.qw[e * qw_b // 4:(e + 1) * qw_b // 4],
+                                      experts.scales[e * s_b // 2:(e + 1) * s_b // 2],
+                                      experts.zeros[e * z_b // 4:(e + 1) * z_b // 4], None,
+                                      y[r0:r1], r1 - r0, N, K, 128, torch.bfloat16,
+                                      workspace=ws)
 
-        t_loop = graph_time(torch, per_expert, 50)
-        active = int((counts > 0).sum())
-        wb = active * alg_bytes(K, N)
-        print(json.dumps({"moe": "mixtral_8x7b_shaped", "proj": name, "K": K, "N": N,
-                          "experts": E, "tokens": T, "topk": topk, "rows": rows,
-                          "rows_per_expert": counts.tolist(), "routed_experts": active,
-                          "us": round(t_grouped * 1e6, 2),
-                          "weight_gbs": round(wb / t_grouped / 1e9, 1),
-                          "frac_hbm": round(wb / t_grouped / 1e9 / hbm, 3),
-                          "per_expert_calls_us": round(t_loop * 1e6, 2),
-                          "device_status": w4.w4_device_status()}), flush=True)
-        del experts, x, y
+            t_loop = graph_time(torch, per_expert, reps)
+            active = int((counts > 0).sum())
+            line = {"moe": "mixtral_8x7b_shaped", "proj": name, "K": K, "N": N,
+                    "experts": E, "tokens": T, "topk": topk, "rows": rows,
+                    "rows_per_expert": counts.tolist(), "routed_experts": active,
+                    "kernel": "w4a16_decode_kernel" if mx <= 16 else "w4a16_prefill_kernel",
+                    "us": round(t_grouped * 1e6, 2),
+                    "per_expert_calls_us": round(t_loop * 1e6, 2)}
+            if mx <= 16:
+                wb = active * alg_bytes(K, N)
+                line["weight_gbs"] = round(wb / t_grouped / 1e9, 1)
+                line["frac_hbm"] = round(wb / t_grouped / 1e9 / hbm, 3)
+            else:
+                tfl = 2.0 * rows * K * N / t_grouped / 1e12
+                line["tflops"] = round(tfl, 1)
+                line["frac_tc"] = round(tfl / tc, 3)
+            line["device_status"] = w4.w4_device_status()
+            print(json.dumps(line), flush=True)
+            del x, y, ws
+        del experts
         torch.cuda.empty_cache()
 
 

@@ -246,14 +246,20 @@ W4_API w4_status w4a16_gemm_bias(const void* x, const int32_t* qw, const void* s
  *   expert_offsets: device int32 [num_experts + 1], non-decreasing, 0 <= off[e]
  *          <= total_rows; read on the device after the wait for the kernel
  *          before this call (a routing kernel may write them).
- *   max_rows_per_expert: 1..64, the most rows any expert has; it sizes the
- *          launch. An expert whose range is invalid or longer records
- *          W4_ERR_EXPERT_ROWS in the device status word and leaves its rows of y
- *          unwritten. Experts with no rows skip their weights altogether.
- * It runs the small-M kernel (one launch for all experts, the expert in the
- * grid's z dimension), with its results, determinism and ordering rules.
- * Errors (host side): those of w4a16_gemm, plus W4_ERR_SHAPE for num_experts < 1,
- * max_rows_per_expert outside 1..64 or total_rows < 0.
+ *   max_rows_per_expert: the most rows any expert has (at least 1); it picks
+ *          the kernel and sizes the launch. An expert whose range is invalid or
+ *          longer records W4_ERR_EXPERT_ROWS in the device status word and
+ *          leaves its rows of y unwritten. Experts with no rows skip their
+ *          weights altogether.
+ * Up to 16 rows an expert (or any N % 32 != 0, then up to 64 rows) it runs the
+ * small-M kernel, one launch for all experts with the expert in the grid's z
+ * dimension. Above that (N % 32 == 0, num_experts <= 4096) it runs the tcgen05
+ * kernel: one persistent launch whose CTAs walk the experts' 128 x 256 output
+ * tiles (counted on the device from the offsets) expert by expert. Either way
+ * the results, determinism and ordering rules are w4a16_gemm's.
+ * Errors (host side): those of w4a16_gemm, plus W4_ERR_SHAPE for num_experts
+ * outside 1..65535, max_rows_per_expert < 1 or above the kernel's limit (64
+ * for the small-M kernel, 2^20 otherwise), or total_rows outside 0..2^20.
  */
 W4_API w4_status w4a16_moe_gemm(const void* x, const int32_t* qw, const void* scales,
                                 const int32_t* zeros, const int32_t* expert_offsets, void* y,

@@ -85,21 +85,70 @@ struct PrefillParams {
   float* part;  // split-K partial tiles [ksplit][M][N] fp32 (ksplit > 1)
   int M, N, K, group;
   int m_blocks, n_blocks, num_tiles, k_blocks, ksplit;
+  // Grouped (MoE) calls: eoff != nullptr. x and y hold the rows of all experts,
+  // sorted by expert ([eoff[e], eoff[e+1]) for expert e); tm_p spans the
+  // experts' TILE buffers one after another (ng128 column groups each), tm_s
+  // and tm_z their [E * groups] group rows. M is then the most rows an expert
+  // may have, and the tile count comes from the offsets on the device.
+  const int32_t* eoff;
+  int num_experts, groups, ng128, total_rows;
 };
 
-// Work unit `tile` -> (M block, N block, K slice [kb0, kb1) of k-blocks).
-// Units run M fastest, then N, then the K slice.
+// Per-CTA table of a grouped call, after the pipeline's shared memory:
+// tile0[E + 1] (first work unit of each expert; tile0[E] = all units), then
+// the first row r0[E] and the end row r1[E] of each expert.
+__host__ __device__ constexpr int grouped_table_bytes(int E) { return (12 * (E + 1) + 15) & ~15; }
+// Experts one launch takes: with 128-row tiles, and with 256-row tiles (less
+// shared memory left beside that pipeline).
+constexpr int GROUPED_MAX_EXPERTS = 4096;
+constexpr int GROUPED_MAX_EXPERTS_256 = 256;
+static_assert(Cfg<1>::SMEM_BYTES + grouped_table_bytes(GROUPED_MAX_EXPERTS) <= 227 * 1024,
+              "the grouped tile table must fit beside the 128-row pipeline");
+static_assert(Cfg<2>::SMEM_BYTES + grouped_table_bytes(GROUPED_MAX_EXPERTS_256) <= 227 * 1024,
+              "the grouped tile table must fit beside the 256-row pipeline");
+
+// Work unit `tile` -> (expert, M block, N block, K slice [kb0, kb1) of
+// k-blocks, first row and end row of the unit's rows). Ungrouped units run M
+// fastest, then N, then the K slice; grouped ones expert by expert, M fastest
+// within the expert, then N (no K split).
 struct Unit {
-  int m_blk, n_blk, ks, kb0, kb1;
+  int e, m_blk, n_blk, ks, kb0, kb1, row0, row_end;
 };
-__device__ __forceinline__ Unit unit_of(const PrefillParams& p, int tile) {
+__device__ __forceinline__ Unit unit_of(const PrefillParams& p, const int* tab, int BM, int tile) {
   Unit u;
-  u.m_blk = tile % p.m_blocks;
-  const int rest = tile / p.m_blocks;
-  u.n_blk = rest % p.n_blocks;
-  u.ks = rest / p.n_blocks;
-  u.kb0 = (int)((long long)u.ks * p.k_blocks / p.ksplit);
-  u.kb1 = (int)((long long)(u.ks + 1) * p.k_blocks / p.ksplit);
+  if (p.eoff == nullptr) {
+    u.e = 0;
+    u.m_blk = tile % p.m_blocks;
+    const int rest = tile / p.m_blocks;
+    u.n_blk = rest % p.n_blocks;
+    u.ks = rest / p.n_blocks;
+    u.kb0 = (int)((long long)u.ks * p.k_blocks / p.ksplit);
+    u.kb1 = (int)((long long)(u.ks + 1) * p.k_blocks / p.ksplit);
+    u.row0 = u.m_blk * BM;
+    u.row_end = p.M;
+    return u;
+  }
+  // the last expert whose first unit is at or before `tile` (experts with no
+  // units share their tile0 with the next one and are passed over)
+  const int E = p.num_experts;
+  int lo = 0, hi = E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tab[mid] <= tile) lo = mid;
+    else hi = mid;
+  }
+  const int* r0 = tab + (E + 1);
+  const int* r1 = r0 + E;
+  const int local = tile - tab[lo];
+  const int mb = (r1[lo] - r0[lo] + BM - 1) / BM;
+  u.e = lo;
+  u.m_blk = local % mb;
+  u.n_blk = local / mb;
+  u.ks = 0;
+  u.kb0 = 0;
+  u.kb1 = p.k_blocks;
+  u.row0 = r0[lo] + u.m_blk * BM;
+  u.row_end = r1[lo];
   return u;
 }
 
@@ -188,6 +237,44 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
     tmem_alloc(smem_addr(tmem_holder), TMEM_COLS);
     tmem_relinquish();
   }
+  int* tab = reinterpret_cast<int*>(smem + C::SMEM_USED);
+  if (p.eoff != nullptr && warp == 3) {
+    // grouped call: each expert's rows (the offsets may come from the kernel
+    // before this one) and its first work unit, by a prefix sum over the
+    // experts 32 at a time. An invalid range or one longer than M records
+    // W4_ERR_EXPERT_ROWS and gets no units (its rows of y stay unwritten).
+    const int E = p.num_experts;
+    int* r0 = tab + (E + 1);
+    int* r1 = r0 + E;
+    int carry = 0;
+    bool bad = false;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      int units = 0;
+      if (e < E) {
+        const int a = *reinterpret_cast<const volatile int32_t*>(p.eoff + e);
+        const int b = *reinterpret_cast<const volatile int32_t*>(p.eoff + e + 1);
+        int rows = b - a;
+        if (a < 0 || rows < 0 || b > p.total_rows || rows > p.M) {
+          bad = true;
+          rows = 0;
+        }
+        r0[e] = a;
+        r1[e] = a + rows;
+        units = (rows + C::BM - 1) / C::BM * p.n_blocks;
+      }
+      int incl = units;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+      }
+      if (e < E) tab[e + 1] = carry + incl;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) tab[0] = 0;
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicExch(&g_device_status, W4_ERR_EXPERT_ROWS);
+  }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&p.tm_a);
     prefetch_tmap(&p.tm_p);
@@ -198,6 +285,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  const int num_tiles = p.eoff != nullptr ? tab[p.num_experts] : p.num_tiles;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -206,9 +294,9 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
       int last_armed[STAGES];
       for (int s = 0; s < STAGES; ++s) last_armed[s] = -1;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-        const Unit u = unit_of(p, tile);
-        const int m_blk = u.m_blk, n_blk = u.n_blk;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        const Unit u = unit_of(p, tab, BM, tile);
+        const int n_blk = u.n_blk;
         for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
@@ -219,11 +307,15 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
           mbar_arrive_expect_tx(bars.full(s), STAGE_TX);
           last_armed[s] = it;
           const int gi = (kb * BK) / p.group;
-          tma_load_2d(sbase + OFF_A + s * A_BYTES, &p.tm_a, bars.full(s), kb * BK, m_blk * BM);
+          // (a grouped call's unit reads its expert's rows of x, column groups
+          // and group rows; rows past the expert's end are computed but not stored)
+          const int grow = u.e * p.groups + gi;
+          tma_load_2d(sbase + OFF_A + s * A_BYTES, &p.tm_a, bars.full(s), kb * BK, u.row0);
           // the 16 atoms (two column groups) of this N block at k-atom kb
-          tma_load_4d(sbase + OFF_P + s * P_BYTES, &p.tm_p, bars.full(s), 0, 0, kb, n_blk * (BN / 128));
-          tma_load_2d(sbase + OFF_S + s * S_BYTES, &p.tm_s, bars.full(s), n_blk * BN, gi);
-          tma_load_2d(sbase + OFF_Z + s * Z_SLOT, &p.tm_z, bars.full(s), n_blk * (BN / 8), gi);
+          tma_load_4d(sbase + OFF_P + s * P_BYTES, &p.tm_p, bars.full(s), 0, 0, kb,
+                      u.e * p.ng128 + n_blk * (BN / 128));
+          tma_load_2d(sbase + OFF_S + s * S_BYTES, &p.tm_s, bars.full(s), n_blk * BN, grow);
+          tma_load_2d(sbase + OFF_Z + s * Z_SLOT, &p.tm_z, bars.full(s), n_blk * (BN / 8), grow);
         }
       }
       if (!ok) {
@@ -239,7 +331,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
       int it = 0, lt = 0;
       bool ok = true;
       bool issued = false;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++lt) {
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++lt) {
         const int buf = lt % NBUF;
         const uint32_t aph = (lt / NBUF) & 1;
         if (!wait_phase(bars.accempty(buf), aph ^ 1, abort_flag)) {
@@ -248,7 +340,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem + buf * (BN * NACC);
-        const Unit u = unit_of(p, tile);
+        const Unit u = unit_of(p, tab, BM, tile);
         for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
@@ -282,16 +374,16 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
     // ---------------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     int lt = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++lt) {
-      const Unit u = unit_of(p, tile);
-      const int m_blk = u.m_blk, n_blk = u.n_blk;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++lt) {
+      const Unit u = unit_of(p, tab, BM, tile);
+      const int n_blk = u.n_blk;
       const int buf = lt % NBUF;
       const uint32_t aph = (lt / NBUF) & 1;
       if (!wait_phase(bars.accfull(buf), aph, abort_flag)) break;
       tc_fence_after();
 #pragma unroll 1
       for (int i = 0; i < NACC; ++i) {
-        const int m = m_blk * BM + i * 128 + quarter * 32 + lane;
+        const int m = u.row0 + i * 128 + quarter * 32 + lane;
         uint16_t* yrow = p.y + (size_t)m * p.N;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -301,14 +393,14 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
           const int n = n_blk * BN + c0;
           if (p.ksplit > 1) {
             // split K: this slice's fp32 partial tile (N % 32 == 0: whole 32-column chunks)
-            if (m < p.M && n < p.N) {
+            if (m < u.row_end && n < p.N) {
               float4* dst = reinterpret_cast<float4*>(p.part + ((size_t)u.ks * p.M + m) * p.N + n);
 #pragma unroll
               for (int q = 0; q < 8; ++q)
                 dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
                                      __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
             }
-          } else if (m < p.M) {
+          } else if (m < u.row_end) {
             if (p.bias != nullptr) {
               // y = RN(acc + bias): the bias joins the fp32 sum before the one rounding
 #pragma unroll
@@ -349,8 +441,8 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
     const bool two_groups = p.group < BK;  // group 32: each K half has its own group row
     int it = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-      const Unit u = unit_of(p, tile);
+    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      const Unit u = unit_of(p, tab, BM, tile);
       for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
@@ -490,12 +582,13 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint6
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// TILE words viewed as [column group][k-atom][tile in group][word]: one box is
-// the 8 atoms of `box_groups` consecutive column groups at one k-atom.
-bool encode_tile_4d(CUtensorMap* map, const void* qw, int K, int N, uint32_t box_groups) {
+// TILE words viewed as [column group][k-atom][tile in group][word] (NG column
+// groups): one box is the 8 atoms of `box_groups` consecutive column groups at
+// one k-atom.
+bool encode_tile_4d(CUtensorMap* map, const void* qw, int K, uint64_t NG, uint32_t box_groups) {
   auto fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t A = (cuuint64_t)K / 64, NG = ((cuuint64_t)N + 127) / 128;
+  const cuuint64_t A = (cuuint64_t)K / 64;
   const cuuint64_t dims[4] = {128, 8, A, NG};
   const cuuint64_t strides[3] = {512, 8 * 512, A * 8 * 512};
   const cuuint32_t box[4] = {128, 8, 1, box_groups};
@@ -606,6 +699,10 @@ bool prefill_supported(int M, int N, int K) {
   return M > 0 && N % 32 == 0 && K % BK == 0;
 }
 
+bool grouped_prefill_supported(int N, int K, int num_experts) {
+  return N % 32 == 0 && K % BK == 0 && num_experts >= 1 && num_experts <= GROUPED_MAX_EXPERTS;
+}
+
 bool use_prefill(int M, int N, int K, int sm_count) {
   (void)sm_count;
   return M > 16 && prefill_supported(M, N, K);
@@ -621,7 +718,24 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
       return err;
     x = a.workspace;
   }
-  PrefillPlan pl = prefill_plan(a.M, a.N, a.K, info.sm_count);
+  const bool grouped = a.eoff != nullptr;
+  PrefillPlan pl;
+  if (grouped) {
+    // experts: no K split (the units come from the offsets, which only the
+    // device reads). 256-row tiles when, at the mean rows per expert, they
+    // take fewer estimated tile-times than 128-row ones (a 256-row tile costs
+    // ~1.25x a 128-row tile: the same rule as ungrouped calls), and the
+    // experts' table fits beside that pipeline.
+    const int mean = (a.total_rows + a.num_experts - 1) / a.num_experts;
+    const double t128 = (double)((mean + 127) / 128);
+    const double t256 = 1.25 * (double)((mean + 255) / 256);
+    pl.nacc = (t256 < t128 && a.num_experts <= GROUPED_MAX_EXPERTS_256) ? 2 : 1;
+    pl.n_blocks = (a.N + BN - 1) / BN;
+    pl.m_blocks = 0;
+    pl.ksplit = 1;
+  } else {
+    pl = prefill_plan(a.M, a.N, a.K, info.sm_count);
+  }
   // the split-K partials go after the act-order staging, when the workspace
   // has room for them; with less room the split shrinks (down to none)
   const size_t staged = prefill_workspace_bytes(a.M, a.K, a.perm != nullptr);
@@ -633,12 +747,17 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
   const int n_blocks = pl.n_blocks;
   PrefillParams p;
   const int G = a.K / a.group;
+  const int E = grouped ? a.num_experts : 1;
+  const int x_rows = grouped ? a.total_rows : a.M;
+  const int ng128 = (a.N + 127) / 128;
   const CUtensorMapDataType act = a.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  bool ok = encode_2d(&p.tm_a, act, x, a.K, a.M, (uint64_t)a.K * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && encode_tile_4d(&p.tm_p, a.qw, a.K, a.N, BN / 128);
-  ok = ok && encode_2d(&p.tm_s, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.scales, a.N, G, (uint64_t)a.N * 2,
-                       BN, 2, CU_TENSOR_MAP_SWIZZLE_NONE);
-  ok = ok && encode_2d(&p.tm_z, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.zeros, a.N / 8, G,
+  bool ok = encode_2d(&p.tm_a, act, x, a.K, x_rows, (uint64_t)a.K * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
+  // stacked experts are further column groups of one TILE tensor, and further
+  // group rows of the scales and zeros
+  ok = ok && encode_tile_4d(&p.tm_p, a.qw, a.K, (uint64_t)E * ng128, BN / 128);
+  ok = ok && encode_2d(&p.tm_s, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.scales, a.N, (uint64_t)E * G,
+                       (uint64_t)a.N * 2, BN, 2, CU_TENSOR_MAP_SWIZZLE_NONE);
+  ok = ok && encode_2d(&p.tm_z, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.zeros, a.N / 8, (uint64_t)E * G,
                        (uint64_t)a.N / 2, BN / 8, 2, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (!ok) return cudaErrorInvalidValue;
   p.y = static_cast<uint16_t*>(a.y);
@@ -654,22 +773,33 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
   p.ksplit = pl.ksplit;
   p.num_tiles = p.m_blocks * n_blocks * pl.ksplit;
   p.k_blocks = a.K / BK;
+  p.eoff = a.eoff;
+  p.num_experts = E;
+  p.groups = G;
+  p.ng128 = ng128;
+  p.total_rows = x_rows;
+  // CTAs: one per SM at most; a grouped call has at most
+  // (total_rows / 128 + E) row tiles over the N blocks
+  const long long max_units =
+      grouped ? (long long)n_blocks * ((x_rows + BM - 1) / BM + E) : (long long)p.num_tiles;
 
   void* fn;
-  int smem_bytes;
+  int smem_bytes, smem_max;
   if (nacc == 2) {
     fn = a.bf16 ? reinterpret_cast<void*>(&w4a16_prefill_kernel<true, 2>)
                 : reinterpret_cast<void*>(&w4a16_prefill_kernel<false, 2>);
-    smem_bytes = Cfg<2>::SMEM_BYTES;
+    smem_bytes = Cfg<2>::SMEM_BYTES + (grouped ? grouped_table_bytes(E) : 0);
+    smem_max = Cfg<2>::SMEM_BYTES + grouped_table_bytes(GROUPED_MAX_EXPERTS_256);
   } else {
     fn = a.bf16 ? reinterpret_cast<void*>(&w4a16_prefill_kernel<true, 1>)
                 : reinterpret_cast<void*>(&w4a16_prefill_kernel<false, 1>);
-    smem_bytes = Cfg<1>::SMEM_BYTES;
+    smem_bytes = Cfg<1>::SMEM_BYTES + (grouped ? grouped_table_bytes(E) : 0);
+    smem_max = Cfg<1>::SMEM_BYTES + grouped_table_bytes(GROUPED_MAX_EXPERTS);
   }
-  if ((err = ensure_prefill_smem(fn, (a.bf16 ? 1 : 0) + 2 * (nacc - 1), smem_bytes)) != cudaSuccess)
+  if ((err = ensure_prefill_smem(fn, (a.bf16 ? 1 : 0) + 2 * (nacc - 1), smem_max)) != cudaSuccess)
     return err;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(std::min(p.num_tiles, info.sm_count), 1, 1);
+  cfg.gridDim = dim3((unsigned)std::min<long long>(max_units, info.sm_count), 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
   cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = stream;

@@ -280,8 +280,12 @@ w4_status w4a16_moe_gemm(const void* x, const int32_t* qw, const void* scales,
   w4_status st = check_dims(K, N, group, dtype);
   if (st) return st;
   if ((st = check_layout_dims(K, N, W4_LAYOUT_TILE))) return st;
+  // more than 16 rows an expert: the tcgen05 kernel, when N is a multiple of
+  // 32 (as w4a16_gemm routes M); otherwise the small-M kernel, up to 64 rows
+  const bool large = max_rows_per_expert > 16 && grouped_prefill_supported(N, K, num_experts);
   if (num_experts < 1 || num_experts > 65535 || max_rows_per_expert < 1 ||
-      max_rows_per_expert > DECODE_MAX_M || total_rows < 0 || total_rows > MAX_DIM)
+      max_rows_per_expert > (large ? MAX_DIM : DECODE_MAX_M) || total_rows < 0 ||
+      total_rows > MAX_DIM)
     return W4_ERR_SHAPE;
   if (!qw || !scales || !zeros || !expert_offsets) return W4_ERR_NULL;
   if (total_rows > 0 && (!x || !y)) return W4_ERR_NULL;
@@ -322,6 +326,7 @@ w4_status w4a16_moe_gemm(const void* x, const int32_t* qw, const void* scales,
   a.qw_estride = qw_b / 4;
   a.s_estride = G * N;
   a.z_estride = G * N / 8;
+  if (large) return from_cuda(launch_prefill(a, static_cast<cudaStream_t>(stream)));
   return from_cuda(launch_decode(a, static_cast<cudaStream_t>(stream)));
 }
 

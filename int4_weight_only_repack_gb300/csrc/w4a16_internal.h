@@ -42,7 +42,7 @@ struct GemmArgs {
   void* workspace;
   size_t workspace_bytes;
   int test_stall = 0;  // w4_test_stalled_gemm: the small-M kernel withholds its weight copies
-  // grouped (expert) calls of the small-M kernel (w4a16_moe_gemm): M is the most
+  // grouped (expert) calls of either kernel (w4a16_moe_gemm): M is the most
   // rows any expert has; expert e's rows are [eoff[e], eoff[e + 1]) of x / y
   const int32_t* eoff = nullptr;
   int num_experts = 1;
@@ -74,6 +74,8 @@ bool use_prefill(int M, int N, int K, int sm_count);
 // Large-M tcgen05 kernel (M > DECODE_MAX_M, N % 32 == 0). Act-order calls
 // gather x[:, perm] into the workspace first.
 bool prefill_supported(int M, int N, int K);
+// Whether the large-M kernel takes a grouped (MoE) call of this shape.
+bool grouped_prefill_supported(int N, int K, int num_experts);
 size_t prefill_workspace_bytes(int M, int K, bool has_perm);
 // Further workspace bytes the tcgen05 kernel uses, when given, for a split-K
 // run of a call whose output tiles cannot fill the GPU (0 when it would not

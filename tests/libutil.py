@@ -44,3 +44,14 @@ def half_from_dev(t):
     """torch fp16 / bf16 tensor -> numpy uint16 bit patterns."""
     import torch
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def rounded_w_reference(x_bits, L, group, fmt="awq"):
+    """fp64 y with the weight rounded once to the activation dtype (the large-M
+    kernel's B operand): a composition of oracle steps, used for a tight check."""
+    from oracle import w4a16_oracle as oracle
+    q, z, s = oracle.layer_codes(L.qweight, L.qzeros, L.scales, L.dtype, fmt)
+    K = q.shape[0]
+    W = oracle.dequant(q, z, s, oracle.group_of_rows(K, group, L.g_idx))
+    Wr = oracle.half_bits_to_f64(oracle.round_f64_to_half_bits(W, L.dtype), L.dtype)
+    return oracle.gemm(oracle.half_bits_to_f64(x_bits, L.dtype), Wr)

@@ -10,7 +10,7 @@ import pytest
 
 import oracle
 import synth
-from libutil import ensure_built, half_from_dev, half_to_dev, to_dev
+from libutil import ensure_built, half_from_dev, half_to_dev, rounded_w_reference, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -459,16 +459,6 @@ def test_gemm_one_hot_rows_exact(w4):
 # --------------------------------------------------------------------------- #
 # Large-M (tcgen05) path                                                        #
 # --------------------------------------------------------------------------- #
-def rounded_w_reference(x_bits, L, group, fmt="awq"):
-    """fp64 y with the weight rounded once to the activation dtype (the large-M
-    kernel's B operand): a composition of oracle steps, used for a tight check."""
-    q, z, s = oracle.layer_codes(L.qweight, L.qzeros, L.scales, L.dtype, fmt)
-    K = q.shape[0]
-    W = oracle.dequant(q, z, s, oracle.group_of_rows(K, group, L.g_idx))
-    Wr = oracle.half_bits_to_f64(oracle.round_f64_to_half_bits(W, L.dtype), L.dtype)
-    return oracle.gemm(oracle.half_bits_to_f64(x_bits, L.dtype), Wr)
-
-
 PREFILL_CASES = [
     # K, N, group, dtype, Ms
     (256, 256, 128, "bf16", (65, 128, 130)),
