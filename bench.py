@@ -648,9 +648,9 @@ def sweep(args):
 def moe(args):
     """Grouped W4A16 GEMM over an MoE layer's experts (w4a16_moe_gemm): the two
     expert projections of a Mixtral-8x7B-shaped layer (8 experts; w13: K 4096 ->
-    N 28672, w2: K 14336 -> N 4096), for a decode batch of 16 tokens and a
-    prefill batch of 4096 tokens, each routed top-2 by a seeded draw (rows sorted
-    by expert). One JSON line per projection and batch: time of the grouped call
+    N 28672, w2: K 14336 -> N 4096), by default for a decode batch of 16 tokens
+    and a prefill batch of 4096 tokens (--moe-tokens), each routed top-2 by a
+    seeded draw (rows sorted by expert). One JSON line per projection and batch: time of the grouped call
     (CUDA graph); for the decode batch weight GB/s over the routed experts' bytes
     (experts without rows are skipped by the kernel), for the prefill batch
     TFLOP/s (2 * rows * K * N); and the same rows as one w4a16_gemm call per
@@ -664,12 +664,14 @@ def moe(args):
     hbm, _ = measured_peaks()
     tc, _ = measured_tc_peak()
     routes = []
-    for T in (16, 4096):
+    for T in [int(t) for t in args.moe_tokens.split(",")]:
         rng = np.random.default_rng([0, 17] if T == 16 else [0, 17, T])
         choice = np.stack([rng.choice(E, topk, replace=False) for _ in range(T)])
         counts = np.bincount(choice.reshape(-1), minlength=E)
         routes.append((T, counts, np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)))
     for name, K, N in (("w13", 4096, 28672), ("w2", 14336, 4096)):
+        if args.moe_proj not in ("all", name):
+            continue
         qws, qzs, scs = [], [], []
         for e in range(E):
             L = synth.make_custom_layer([0, 17, e, K, N], K, N, group=128, dtype="bf16")
@@ -741,6 +743,10 @@ def main():
                     help="every layer of --sweep-config at every M of that workload (one line each)")
     ap.add_argument("--moe", action="store_true",
                     help="the grouped MoE GEMM on a Mixtral-8x7B-shaped layer (one line per projection)")
+    ap.add_argument("--moe-tokens", default="16,4096",
+                    help="comma-separated token counts of --moe (routed top-2 over 8 experts)")
+    ap.add_argument("--moe-proj", default="all", choices=("all", "w13", "w2"),
+                    help="the projection(s) --moe runs")
     ap.add_argument("--single", default=None,
                     help="K,N,M[,dtype]: time one layer shape only (profiling aid)")
     args = ap.parse_args()
