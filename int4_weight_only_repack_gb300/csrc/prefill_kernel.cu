@@ -114,9 +114,10 @@ static_assert(Cfg<2>::SMEM_BYTES + grouped_table_bytes(GROUPED_MAX_EXPERTS_256) 
 struct Unit {
   int e, m_blk, n_blk, ks, kb0, kb1, row0, row_end;
 };
+template <bool GROUPED>
 __device__ __forceinline__ Unit unit_of(const PrefillParams& p, const int* tab, int BM, int tile) {
   Unit u;
-  if (p.eoff == nullptr) {
+  if (!GROUPED) {
     u.e = 0;
     u.m_blk = tile % p.m_blocks;
     const int rest = tile / p.m_blocks;
@@ -198,7 +199,9 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi, bool bf16) {
   return d;
 }
 
-template <bool BF16, int NACC>
+// GROUPED: a grouped (MoE) call, p.eoff != nullptr (its own instantiation, so
+// that ungrouped calls carry none of its per-tile work).
+template <bool BF16, int NACC, bool GROUPED>
 __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_constant__ PrefillParams p) {
   using C = Cfg<NACC>;
   constexpr int BM = C::BM, NBUF = C::NBUF, A_BYTES = C::A_BYTES;
@@ -238,7 +241,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
     tmem_relinquish();
   }
   int* tab = reinterpret_cast<int*>(smem + C::SMEM_USED);
-  if (p.eoff != nullptr && warp == 3) {
+  if (GROUPED && warp == 3) {
     // grouped call: each expert's rows (the offsets may come from the kernel
     // before this one) and its first work unit, by a prefix sum over the
     // experts 32 at a time. An invalid range or one longer than M records
@@ -285,7 +288,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const int num_tiles = p.eoff != nullptr ? tab[p.num_experts] : p.num_tiles;
+  const int num_tiles = GROUPED ? tab[p.num_experts] : p.num_tiles;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -295,7 +298,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
       for (int s = 0; s < STAGES; ++s) last_armed[s] = -1;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        const Unit u = unit_of(p, tab, BM, tile);
+        const Unit u = unit_of<GROUPED>(p, tab, BM, tile);
         const int n_blk = u.n_blk;
         for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
           const int s = it % STAGES;
@@ -340,7 +343,11 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem + buf * (BN * NACC);
-        const Unit u = unit_of(p, tab, BM, tile);
+        const Unit u = unit_of<GROUPED>(p, tab, BM, tile);
+        // a grouped call's 256-row tile whose second half holds no rows (the
+        // last rows of an expert) skips that accumulator's MMAs (the epilogue
+        // still drains it, but every row it would store is masked)
+        const bool second = NACC == 2 && (!GROUPED || u.row0 + 128 < u.row_end);
         for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
@@ -350,15 +357,22 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
           }
           tc_fence_after();
           const uint64_t bdesc = smem_desc_k128(sbase + OFF_B + s * B_BYTES);
+          // accumulator i: rows 128 i .. 128 i + 127 of the A tile; each MMA
+          // advances 16 elements (32 bytes) along K inside the swizzled rows
+          if (NACC == 1 || second) {
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
+            for (int k = 0; k < BK / 16; ++k) {
 #pragma unroll
-            for (int i = 0; i < NACC; ++i) {
-              // accumulator i: rows 128 i .. 128 i + 127 of the A tile; advance
-              // 16 elements (32 bytes) along K inside the swizzled rows
-              const uint64_t adesc = smem_desc_k128(sbase + OFF_A + s * A_BYTES + i * (128 * BK * 2));
-              umma_f16(d_tmem + i * BN, adesc + 2 * k, bdesc + 2 * k, IDESC, kb != u.kb0 || k != 0);
+              for (int i = 0; i < NACC; ++i) {
+                const uint64_t adesc = smem_desc_k128(sbase + OFF_A + s * A_BYTES + i * (128 * BK * 2));
+                umma_f16(d_tmem + i * BN, adesc + 2 * k, bdesc + 2 * k, IDESC, kb != u.kb0 || k != 0);
+              }
             }
+          } else {
+            const uint64_t adesc = smem_desc_k128(sbase + OFF_A + s * A_BYTES);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)
+              umma_f16(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, kb != u.kb0 || k != 0);
           }
           issued = true;
           umma_commit(bars.empty(s));
@@ -375,7 +389,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     int lt = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++lt) {
-      const Unit u = unit_of(p, tab, BM, tile);
+      const Unit u = unit_of<GROUPED>(p, tab, BM, tile);
       const int n_blk = u.n_blk;
       const int buf = lt % NBUF;
       const uint32_t aph = (lt / NBUF) & 1;
@@ -442,7 +456,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
     int it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-      const Unit u = unit_of(p, tab, BM, tile);
+      const Unit u = unit_of<GROUPED>(p, tab, BM, tile);
       for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
@@ -600,7 +614,7 @@ bool encode_tile_4d(CUtensorMap* map, const void* qw, int K, uint64_t NG, uint32
 
 cudaError_t ensure_prefill_smem(void* fn, int which, int bytes) {
   static std::mutex mu;
-  static bool done[64][4] = {};
+  static bool done[64][8] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -722,14 +736,16 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
   PrefillPlan pl;
   if (grouped) {
     // experts: no K split (the units come from the offsets, which only the
-    // device reads). 256-row tiles when, at the mean rows per expert, they
-    // take fewer estimated tile-times than 128-row ones (a 256-row tile costs
-    // ~1.25x a 128-row tile: the same rule as ungrouped calls), and the
-    // experts' table fits beside that pipeline.
-    const int mean = (a.total_rows + a.num_experts - 1) / a.num_experts;
-    const double t128 = (double)((mean + 127) / 128);
-    const double t256 = 1.25 * (double)((mean + 255) / 256);
-    pl.nacc = (t256 < t128 && a.num_experts <= GROUPED_MAX_EXPERTS_256) ? 2 : 1;
+    // device reads). 256-row tiles when an expert may have more than 128 rows
+    // and the experts' table fits beside that pipeline: an expert's last tile
+    // skips its second accumulator when it holds no more than 128 rows, so
+    // they never do more MMA work than 128-row tiles, and they dequantise each
+    // B tile once for 256 rows. When every expert fits one 128-row tile, the
+    // 128-row pipeline is faster: it double-buffers the accumulator and loads
+    // half the x tile (measured on GB300 over a Mixtral-8x7B-shaped layer,
+    // 23-75 rows per expert: 10-12 % faster; 115-143 rows: the 256-row tiles
+    // 18-38 % faster).
+    pl.nacc = (a.M > 128 && a.num_experts <= GROUPED_MAX_EXPERTS_256) ? 2 : 1;
     pl.n_blocks = (a.N + BN - 1) / BN;
     pl.m_blocks = 0;
     pl.ksplit = 1;
@@ -783,21 +799,26 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
   const long long max_units =
       grouped ? (long long)n_blocks * ((x_rows + BM - 1) / BM + E) : (long long)p.num_tiles;
 
-  void* fn;
+  static void* const kernels[2][2][2] = {  // [grouped][nacc - 1][bf16]
+      {{reinterpret_cast<void*>(&w4a16_prefill_kernel<false, 1, false>),
+        reinterpret_cast<void*>(&w4a16_prefill_kernel<true, 1, false>)},
+       {reinterpret_cast<void*>(&w4a16_prefill_kernel<false, 2, false>),
+        reinterpret_cast<void*>(&w4a16_prefill_kernel<true, 2, false>)}},
+      {{reinterpret_cast<void*>(&w4a16_prefill_kernel<false, 1, true>),
+        reinterpret_cast<void*>(&w4a16_prefill_kernel<true, 1, true>)},
+       {reinterpret_cast<void*>(&w4a16_prefill_kernel<false, 2, true>),
+        reinterpret_cast<void*>(&w4a16_prefill_kernel<true, 2, true>)}}};
+  void* fn = kernels[grouped ? 1 : 0][nacc - 1][a.bf16 ? 1 : 0];
   int smem_bytes, smem_max;
   if (nacc == 2) {
-    fn = a.bf16 ? reinterpret_cast<void*>(&w4a16_prefill_kernel<true, 2>)
-                : reinterpret_cast<void*>(&w4a16_prefill_kernel<false, 2>);
     smem_bytes = Cfg<2>::SMEM_BYTES + (grouped ? grouped_table_bytes(E) : 0);
-    smem_max = Cfg<2>::SMEM_BYTES + grouped_table_bytes(GROUPED_MAX_EXPERTS_256);
+    smem_max = Cfg<2>::SMEM_BYTES + (grouped ? grouped_table_bytes(GROUPED_MAX_EXPERTS_256) : 0);
   } else {
-    fn = a.bf16 ? reinterpret_cast<void*>(&w4a16_prefill_kernel<true, 1>)
-                : reinterpret_cast<void*>(&w4a16_prefill_kernel<false, 1>);
     smem_bytes = Cfg<1>::SMEM_BYTES + (grouped ? grouped_table_bytes(E) : 0);
-    smem_max = Cfg<1>::SMEM_BYTES + grouped_table_bytes(GROUPED_MAX_EXPERTS);
+    smem_max = Cfg<1>::SMEM_BYTES + (grouped ? grouped_table_bytes(GROUPED_MAX_EXPERTS) : 0);
   }
-  if ((err = ensure_prefill_smem(fn, (a.bf16 ? 1 : 0) + 2 * (nacc - 1), smem_max)) != cudaSuccess)
-    return err;
+  const int which = (a.bf16 ? 1 : 0) + 2 * (nacc - 1) + 4 * (grouped ? 1 : 0);
+  if ((err = ensure_prefill_smem(fn, which, smem_max)) != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)std::min<long long>(max_units, info.sm_count), 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);

@@ -85,6 +85,31 @@ def test_moe_gemm_vs_oracle(w4, E, K, N, dtype, rows, group):
     assert w4.w4_device_status() == 0
 
 
+def test_moe_gemm_many_experts(w4):
+    """More experts than fit the 256-row pipeline's table (128-row tiles): 300
+    small experts, most of them without rows."""
+    import torch
+    E, K, N, dtype = 300, 128, 64, "bf16"
+    layers, experts = make_experts(w4, E, K, N, dtype, 143)
+    rng = np.random.default_rng(144)
+    rows = np.zeros(E, dtype=np.int64)
+    busy = rng.choice(E, 24, replace=False)
+    rows[busy] = rng.integers(1, 140, size=24)
+    rows[busy[0]] = 139
+    off = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+    T = int(off[-1])
+    x = synth.make_custom_x([145], T, K, dtype)
+    y = torch.full((T, N), float("nan"), dtype=hdt(dtype), device="cuda")
+    w4.moe_linear(half_to_dev(x, dtype), experts, to_dev(off), int(rows.max()), y=y)
+    torch.cuda.synchronize()
+    yb = half_from_dev(y).reshape(T, N)
+    for e in busy:
+        r0, r1 = int(off[e]), int(off[e + 1])
+        y_ref = rounded_w_reference(x[r0:r1], layers[e], 128)
+        assert ulp_error(yb[r0:r1], y_ref, dtype) <= 1.0, e
+    assert w4.w4_device_status() == 0
+
+
 def test_moe_gemm_rejects_oversized_expert(w4):
     """An expert with more rows than max_rows_per_expert records
     W4_ERR_EXPERT_ROWS and leaves its rows of y unwritten; the others are exact."""

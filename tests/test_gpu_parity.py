@@ -469,6 +469,7 @@ PREFILL_CASES = [
     (256, 4096, 128, "bf16", (2048,)),           # 256 tiles: several per CTA
     (128, 4128, 128, "bf16", (2600,)),           # 256-row tiles, ragged in M and N
     (256, 4096, 32, "fp16", (2560,)),            # 256-row tiles, group 32
+    (256, 4096, 128, "fp16", (1900, 2200)),      # 256-row tiles: last one 108 / 152 rows
     (4096, 256, 128, "bf16", (128, 100)),        # one output tile: K split 8 ways
     (2048, 512, 64, "fp16", (65,)),              # two output tiles: K split 4 ways
 ]
