@@ -139,3 +139,37 @@ def test_binding_raises_on_error():
         w4.w4a16_gemm(FAKE, FAKE * 2, FAKE * 3, FAKE * 4, None, FAKE * 5, 4, 264, 256, 128,
                       "bf16", stream=0)
     assert e.value.status == W4_ERR_SHAPE
+
+
+def _moe(lib, x=FAKE, qw=FAKE * 2, sc=FAKE * 3, z=FAKE * 4, off=FAKE * 6, y=FAKE * 5, E=4,
+         max_rows=16, total_rows=64, N=256, K=256, group=128, dtype=1):
+    return lib.w4a16_moe_gemm(x, qw, sc, z, off, y, E, max_rows, total_rows, N, K, group, dtype,
+                              None)
+
+
+def test_moe_gemm_rejects_bad_arguments(lib):
+    """Host-side checks of w4a16_moe_gemm, and which kernel's row limit applies:
+    a call that passes the shape checks is stopped by an aliased y (x == y), so
+    no case reaches a launch."""
+    assert _moe(lib, E=0) == W4_ERR_SHAPE
+    assert _moe(lib, E=65536) == W4_ERR_SHAPE
+    assert _moe(lib, max_rows=0) == W4_ERR_SHAPE
+    assert _moe(lib, total_rows=-1) == W4_ERR_SHAPE
+    assert _moe(lib, total_rows=(1 << 20) + 1) == W4_ERR_SHAPE
+    assert _moe(lib, off=None) == W4_ERR_NULL
+    assert _moe(lib, x=None) == W4_ERR_NULL
+    assert _moe(lib, y=FAKE * 5 + 8) == W4_ERR_ALIGN
+    assert _moe(lib, off=FAKE * 6 + 4) == W4_ERR_ALIGN
+    assert _moe(lib, N=264) == W4_ERR_SHAPE                      # TILE needs N % 16
+    assert _moe(lib, group=16) == W4_ERR_GROUP
+    assert _moe(lib, y=FAKE) == W4_ERR_ALIAS
+    # N % 32 == 0, more than 16 rows an expert: the tcgen05 kernel (no 64-row limit)
+    assert _moe(lib, max_rows=65, y=FAKE) == W4_ERR_ALIAS
+    assert _moe(lib, max_rows=1 << 20, total_rows=1 << 20, y=FAKE) == W4_ERR_ALIAS
+    assert _moe(lib, max_rows=(1 << 20) + 1, y=FAKE) == W4_ERR_SHAPE
+    # N % 32 != 0: the small-M kernel only, up to 64 rows an expert
+    assert _moe(lib, N=272, max_rows=64, y=FAKE) == W4_ERR_ALIAS
+    assert _moe(lib, N=272, max_rows=65, y=FAKE) == W4_ERR_SHAPE
+    # more than 4096 experts: beyond the tcgen05 kernel's table, so 64 rows at most
+    assert _moe(lib, E=4097, max_rows=64, y=FAKE) == W4_ERR_ALIAS
+    assert _moe(lib, E=4097, max_rows=65, y=FAKE) == W4_ERR_SHAPE
