@@ -28,6 +28,9 @@ What the path computes and where the pages say so:
      with g(k) = k // group, or g_idx[k]. Exact in fp32: |q - z| <= 15 needs 4
      bits and the scale has at most 11 significant bits.
   6. GEMM: y[m, n] = sum_k x[m, k] * W[k, n], accumulated in fp64.
+  7. Grouped GEMM over MoE experts ([AWQ] §5.4, 4-bit expert weights): rows of x
+     sorted by expert, expert e owning rows [off[e], off[e+1]); each row is
+     multiplied by its own expert's W_e, i.e. item 6 per expert.
 
 Parity pins for every function live in tests/test_oracle_pins.py. The TILE
 layout is this library's own format: its pins are bijectivity, round trip and
@@ -365,6 +368,26 @@ def reference_y(x_bits, qweight, qzeros, scales_bits, group: int, dtype: str, fm
         y[:, c0:c0 + len(cc)] = gemm(x, dequant(q, z, s, gk, cols=cc))
     if bias_bits is not None:
         y += half_bits_to_f64(np.asarray(bias_bits), dtype)[col_list][None, :]
+    return y
+
+
+def moe_reference_y(x_bits, experts, offsets, group: int, dtype: str, fmt: str) -> np.ndarray:
+    """fp64 y of the grouped GEMM over an MoE layer's experts ([AWQ] §5.4): for
+    every expert e, y[m] = x[m] . W_e for off[e] <= m < off[e+1]. experts: one
+    (qweight, qzeros, scales_bits) checkpoint triple per expert; offsets: E + 1
+    non-decreasing row offsets from 0 to the row count of x. Rows outside every
+    range do not exist (off[E] = rows of x)."""
+    off = [int(v) for v in offsets]
+    if off[0] != 0 or off[-1] != len(x_bits) or any(b < a for a, b in zip(off, off[1:])):
+        raise ValueError("offsets must run from 0 to the row count, non-decreasing")
+    if len(off) != len(experts) + 1:
+        raise ValueError("one offset more than experts")
+    N = half_bits_to_f64(experts[0][2], dtype).shape[1]
+    y = np.zeros((len(x_bits), N), dtype=np.float64)
+    for e, (qweight, qzeros, scales_bits) in enumerate(experts):
+        r0, r1 = off[e], off[e + 1]
+        if r1 > r0:
+            y[r0:r1] = reference_y(x_bits[r0:r1], qweight, qzeros, scales_bits, group, dtype, fmt)
     return y
 
 

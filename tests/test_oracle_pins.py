@@ -384,6 +384,65 @@ def test_gemm_exact_rational():
     check_gemm_exact_rational()
 
 
+MOE_CASES = (
+    # dtype, K, N, group, row offsets (E + 1)
+    ("fp16", 128, 8, 64, [0, 2, 2, 5]),   # an expert without rows between two with rows
+    ("bf16", 128, 16, 32, [0, 0, 3]),     # the first expert without rows
+)
+
+
+def _moe_case(dtype, K, N, group, off):
+    E = len(off) - 1
+    layers = [synth.make_custom_layer([51, e, K, N], K, N, group=group, dtype=dtype,
+                                      keep_codes=True) for e in range(E)]
+    x = synth.make_custom_x([52, K], off[-1], K, dtype)
+    return layers, x
+
+
+def check_moe_exact_rational(moe_fn):
+    """The grouped reference vs exact rational sums from the writer's codes, each
+    row's expert found by scanning the offsets."""
+    for dtype, K, N, group, off in MOE_CASES:
+        layers, x = _moe_case(dtype, K, N, group, off)
+        y = moe_fn(x, [(L.qweight, L.qzeros, L.scales) for L in layers], off, group, dtype, "awq")
+        assert y.shape == (off[-1], N)
+        xv = synth.bits_to_f32(x, dtype)
+        for m in range(off[-1]):
+            e = next(i for i in range(len(layers)) if off[i] <= m < off[i + 1])
+            L = layers[e]
+            sv = synth.bits_to_f32(L.scales, dtype)
+            for n in range(N):
+                acc = Fraction(0)
+                for k in range(K):
+                    g = k // group
+                    acc += Fraction(float(xv[m, k])) * (int(L.q[k, n]) - int(L.z[g, n])) * \
+                        Fraction(float(sv[g, n]))
+                assert abs(Fraction(float(y[m, n])) - acc) <= abs(acc) * Fraction(1, 2**50) + \
+                    Fraction(1, 2**80), (m, n, e)
+
+
+def test_moe_reference_exact_rational():
+    check_moe_exact_rational(oracle.moe_reference_y)
+
+
+def test_moe_reference_single_expert_is_plain_gemm():
+    """One expert owning every row: the grouped GEMM is the plain one."""
+    L = synth.make_custom_layer(53, 256, 48, group=128, dtype="bf16")
+    x = synth.make_custom_x(54, 7, 256, "bf16")
+    assert np.array_equal(
+        oracle.moe_reference_y(x, [(L.qweight, L.qzeros, L.scales)], [0, 7], 128, "bf16", "awq"),
+        oracle.reference_y(x, L.qweight, L.qzeros, L.scales, 128, "bf16", "awq"))
+
+
+def test_moe_reference_rejects_bad_offsets():
+    L = synth.make_custom_layer(55, 128, 8, group=64, dtype="fp16")
+    x = synth.make_custom_x(56, 4, 128, "fp16")
+    ex = [(L.qweight, L.qzeros, L.scales)] * 2
+    for off in ([1, 2, 4], [0, 3, 2], [0, 2, 3], [0, 4]):
+        with pytest.raises(ValueError):
+            oracle.moe_reference_y(x, ex, off, 64, "fp16", "awq")
+
+
 def test_gemm_one_hot_rows():
     L = synth.make_custom_layer(31, 256, 64, group=128, dtype="bf16")
     q, z, s = oracle.layer_codes(L.qweight, L.qzeros, L.scales, "bf16", "awq")
@@ -536,3 +595,31 @@ def _rebind_reference(gemm_fn):
         gk = oracle.group_of_rows(K, group, g_idx)
         return gemm_fn(x, oracle.dequant(q, z, s, gk))
     return reference_y
+
+
+def _mutant_moe_next_expert(x_bits, experts, offsets, group, dtype, fmt):
+    """Planted: each range multiplied by the following expert's weights."""
+    y = np.zeros((len(x_bits), oracle.half_bits_to_f64(experts[0][2], dtype).shape[1]))
+    for e in range(len(experts)):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 > r0:
+            qw, qz, sc = experts[min(e + 1, len(experts) - 1)]
+            y[r0:r1] = oracle.reference_y(x_bits[r0:r1], qw, qz, sc, group, dtype, fmt)
+    return y
+
+
+def _mutant_moe_shifted_ranges(x_bits, experts, offsets, group, dtype, fmt):
+    """Planted: expert e takes rows [off[e] + 1, off[e+1] + 1) (an off-by-one)."""
+    T = len(x_bits)
+    y = np.zeros((T, oracle.half_bits_to_f64(experts[0][2], dtype).shape[1]))
+    for e, (qw, qz, sc) in enumerate(experts):
+        r0, r1 = min(int(offsets[e]) + 1, T), min(int(offsets[e + 1]) + 1, T)
+        if r1 > r0:
+            y[r0:r1] = oracle.reference_y(x_bits[r0:r1], qw, qz, sc, group, dtype, fmt)
+    return y
+
+
+@pytest.mark.parametrize("bad", [_mutant_moe_next_expert, _mutant_moe_shifted_ranges])
+def test_mutant_moe_is_caught(bad):
+    with pytest.raises(AssertionError):
+        check_moe_exact_rational(bad)
