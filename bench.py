@@ -294,7 +294,9 @@ def dequant_cublas_measure(w4, torch, calls, reps: int, device):
 
 def prefill_measure(w4, torch, device, reps: int = 10):
     """The Llama-2-7B prefill layers (same shapes, M in {512, 2048, 4096}) on the
-    tcgen05 kernel: TFLOP/s per (layer, M), two weight copies per layer."""
+    tcgen05 kernel: TFLOP/s per (layer, M), two weight copies per layer; beside
+    each, a dense bf16 GEMM of the same shape through torch.matmul (cuBLAS), the
+    ceiling a weight-only kernel approaches at compute-bound sizes."""
     wl = synth.WORKLOADS[2]
     rows = []
     for li, (K, N, name) in enumerate(wl.shapes):
@@ -314,9 +316,19 @@ def prefill_measure(w4, torch, device, reps: int = 10):
                     w4.linear(x, l, y=y)
 
             t = graph_time(torch, fn, reps) / len(layers)
+            wd = [torch.randn(K, N, device=device).to(torch.bfloat16) for _ in range(2)]
+            yd = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+
+            def dense():
+                for w in wd:
+                    torch.matmul(x, w, out=yd)
+
+            td = graph_time(torch, dense, reps) / len(wd)
             rows.append({"layer": name, "M": M, "us": round(t * 1e6, 2),
-                         "tflops": round(2.0 * M * N * K / t / 1e12, 1)})
-            del x, y
+                         "tflops": round(2.0 * M * N * K / t / 1e12, 1),
+                         "dense_bf16_cublas_us": round(td * 1e6, 2),
+                         "dense_bf16_cublas_tflops": round(2.0 * M * N * K / td / 1e12, 1)})
+            del x, y, wd, yd
         del layers
         torch.cuda.empty_cache()
     return rows
