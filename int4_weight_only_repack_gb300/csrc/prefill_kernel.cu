@@ -6,9 +6,14 @@
 // 量化" §5.3: dequantisation fused with the multiply; "vLLM AWQ 4-bit 量化实践"
 // §5.3: W = (b - zeros) * scales):
 //
-//  * Persistent kernel, one CTA per SM, CTA tile 128 (M) x 256 (N), K blocks of
-//    64. Tiles are walked with M fastest so neighbouring CTAs share a weight
-//    column block in L2.
+//  * Persistent kernel, one CTA per SM, CTA tile 128 or 256 (M) x 256 (N), K
+//    blocks of 64. Tiles are walked with M fastest so neighbouring CTAs share a
+//    weight column block in L2. When the output tiles cannot fill the SMs, K is
+//    split into slices whose fp32 partials a second kernel sums.
+//  * Grouped (MoE) calls: one launch over all experts. Each CTA builds a table
+//    of the experts' tiles from the row offsets on the device; a tile maps to
+//    (expert, row block, column block), reads that expert's weights and masks
+//    rows at the expert's end.
 //  * Warp roles (16 warps): warp 0 issues TMA copies (x tile with the 128-byte
 //    swizzle, the packed weight atoms, scales and zeros) into a 3-stage ring;
 //    warps 8-15 dequantise the packed atoms into the bf16/fp16 B operand,

@@ -71,8 +71,9 @@ cudaError_t launch_gather_columns(const void* x, const int32_t* perm, void* xg, 
 // the small-M kernel is still ahead on qkv and gate_up.
 bool use_prefill(int M, int N, int K, int sm_count);
 
-// Large-M tcgen05 kernel (M > DECODE_MAX_M, N % 32 == 0). Act-order calls
-// gather x[:, perm] into the workspace first.
+// Large-M tcgen05 kernel (N % 32 == 0; w4a16_gemm routes M > 16 here).
+// Act-order calls gather x[:, perm] into the workspace first. Grouped calls
+// (GemmArgs::eoff set) walk every expert's output tiles in one launch.
 bool prefill_supported(int M, int N, int K);
 // Whether the large-M kernel takes a grouped (MoE) call of this shape.
 bool grouped_prefill_supported(int N, int K, int num_experts);
