@@ -27,11 +27,12 @@ def hdt(dtype):
     return torch.bfloat16 if dtype == "bf16" else torch.float16
 
 
-def make_experts(w4, E, K, N, dtype, seed, group=128):
-    layers = [synth.make_custom_layer([seed, e, K, N], K, N, group=group, dtype=dtype)
-              for e in range(E)]
+def make_experts(w4, E, K, N, dtype, seed, group=128, symmetric=False):
+    layers = [synth.make_custom_layer([seed, e, K, N], K, N, group=group, dtype=dtype,
+                                      symmetric=symmetric) for e in range(E)]
     experts = w4.repack_awq_experts([to_dev(L.qweight) for L in layers],
-                                    [to_dev(L.qzeros) for L in layers],
+                                    [None if L.qzeros is None else to_dev(L.qzeros)
+                                     for L in layers],
                                     [half_to_dev(L.scales, dtype) for L in layers],
                                     K, N, group, dtype)
     return layers, experts
@@ -84,6 +85,32 @@ def test_moe_gemm_vs_oracle(w4, E, K, N, dtype, rows, group):
             # dtype: within one output ulp of that product
             y_ref = rounded_w_reference(x[r0:r1], L, group)
         assert ulp_error(yb[r0:r1], y_ref, dtype) <= 1.0, (e, ulp_error(yb[r0:r1], y_ref, dtype))
+    assert w4.w4_device_status() == 0
+
+
+@pytest.mark.parametrize("rows", [[5, 0, 12], [40, 0, 150]])
+def test_moe_gemm_symmetric_experts(w4, rows):
+    """Symmetric experts (no qzeros: zero point 8) on both kernels."""
+    import torch
+    E, K, N, dtype = 3, 512, 256, "fp16"
+    layers, experts = make_experts(w4, E, K, N, dtype, 146, symmetric=True)
+    off = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+    T = int(off[-1])
+    x = synth.make_custom_x([147, T], T, K, dtype)
+    y = torch.full((T, N), float("nan"), dtype=hdt(dtype), device="cuda")
+    w4.moe_linear(half_to_dev(x, dtype), experts, to_dev(off), max(rows), y=y)
+    torch.cuda.synchronize()
+    yb = half_from_dev(y).reshape(T, N)
+    y_all = oracle.moe_reference_y(x, [(L.qweight, None, L.scales) for L in layers], off, 128,
+                                   dtype, "awq")
+    large = max(rows) > 16
+    for e, L in enumerate(layers):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        if r1 == r0:
+            continue
+        assert oracle.rel_err(oracle.half_bits_to_f64(yb[r0:r1], dtype), y_all[r0:r1]) <= 4e-3
+        y_ref = rounded_w_reference(x[r0:r1], L, 128) if large else y_all[r0:r1]
+        assert ulp_error(yb[r0:r1], y_ref, dtype) <= 1.0, e
     assert w4.w4_device_status() == 0
 
 
