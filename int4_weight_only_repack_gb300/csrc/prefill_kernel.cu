@@ -246,42 +246,11 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
     tmem_relinquish();
   }
   int* tab = reinterpret_cast<int*>(smem + C::SMEM_USED);
-  if (GROUPED && warp == 3) {
-    // grouped call: each expert's rows (the offsets may come from the kernel
-    // before this one) and its first work unit, by a prefix sum over the
-    // experts 32 at a time. An invalid range or one longer than M records
-    // W4_ERR_EXPERT_ROWS and gets no units (its rows of y stay unwritten).
-    const int E = p.num_experts;
-    int* r0 = tab + (E + 1);
-    int* r1 = r0 + E;
-    int carry = 0;
-    bool bad = false;
-    for (int base = 0; base < E; base += 32) {
-      const int e = base + lane;
-      int units = 0;
-      if (e < E) {
-        const int a = *reinterpret_cast<const volatile int32_t*>(p.eoff + e);
-        const int b = *reinterpret_cast<const volatile int32_t*>(p.eoff + e + 1);
-        int rows = b - a;
-        if (a < 0 || rows < 0 || b > p.total_rows || rows > p.M) {
-          bad = true;
-          rows = 0;
-        }
-        r0[e] = a;
-        r1[e] = a + rows;
-        units = (rows + C::BM - 1) / C::BM * p.n_blocks;
-      }
-      int incl = units;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, d);
-        if (lane >= d) incl += v;
-      }
-      if (e < E) tab[e + 1] = carry + incl;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) tab[0] = 0;
-    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicExch(&g_device_status, W4_ERR_EXPERT_ROWS);
+  if (GROUPED) {
+    // grouped call: the experts' row offsets (they may come from the kernel
+    // before this one), staged in tile0[] by all threads in one pass
+    for (int e = tid; e <= p.num_experts; e += THREADS)
+      tab[e] = *reinterpret_cast<const volatile int32_t*>(p.eoff + e);
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&p.tm_a);
@@ -292,6 +261,45 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (GROUPED) {
+    if (warp == 3) {
+      // Each expert's rows and its first work unit. First every lane checks
+      // its experts' ranges from the staged offsets: an invalid range or one
+      // longer than M records W4_ERR_EXPERT_ROWS and gets no rows (its rows of
+      // y stay unwritten). Then a prefix sum over the experts, 32 at a time,
+      // overwrites the staged offsets with the first unit of each expert.
+      const int E = p.num_experts;
+      int* r0 = tab + (E + 1);
+      int* r1 = r0 + E;
+      bool bad = false;
+      for (int e = lane; e < E; e += 32) {
+        const int a = tab[e], b = tab[e + 1];
+        int rows = b - a;
+        if (a < 0 || rows < 0 || b > p.total_rows || rows > p.M) {
+          bad = true;
+          rows = 0;
+        }
+        r0[e] = a;
+        r1[e] = a + rows;
+      }
+      if (__any_sync(0xffffffffu, bad) && lane == 0) atomicExch(&g_device_status, W4_ERR_EXPERT_ROWS);
+      __syncwarp();
+      int carry = 0;
+      for (int base = 0; base < E; base += 32) {
+        const int e = base + lane;
+        int incl = e < E ? (r1[e] - r0[e] + C::BM - 1) / C::BM * p.n_blocks : 0;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, d);
+          if (lane >= d) incl += v;
+        }
+        if (e < E) tab[e + 1] = carry + incl;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) tab[0] = 0;
+    }
+    __syncthreads();
+  }
   const uint32_t tmem = *tmem_holder;
   const int num_tiles = GROUPED ? tab[p.num_experts] : p.num_tiles;
 
