@@ -469,6 +469,14 @@ def ours(args):
                                 "peak_source": tc_src, "kernel": "w4a16_prefill_kernel"},
                    "per_call": rows}
 
+    # ---- grouped MoE GEMM (one GPU only: a side figure like the CPU baseline) --
+    moe_part = None
+    if world == 1 and not args.no_moe:
+        moe_part = {"workload": "mixtral_8x7b_shaped experts (8; w13 4096->28672, w2 "
+                                "14336->4096), 16 and 4096 tokens routed top-2, bf16, "
+                                "one w4a16_moe_gemm call against one w4a16_gemm per expert",
+                    "per_call": moe_measure((16, 4096))}
+
     cpu_base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu_base = cpu_baseline_measure(args.cpu_seconds)
@@ -516,6 +524,7 @@ def ours(args):
                                "how": "w4_dequant to dense bf16 [K,N] + torch.matmul (cuBLAS) "
                                       "per call, CUDA graph of the step"},
             "prefill": prefill,
+            "moe": moe_part,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -657,16 +666,15 @@ def sweep(args):
     print(json.dumps({"sweep_done": wl.name, "device_status": w4.w4_device_status()}), flush=True)
 
 
-def moe(args):
+def moe_measure(token_counts, proj="all"):
     """Grouped W4A16 GEMM over an MoE layer's experts (w4a16_moe_gemm): the two
     expert projections of a Mixtral-8x7B-shaped layer (8 experts; w13: K 4096 ->
-    N 28672, w2: K 14336 -> N 4096), by default for a decode batch of 16 tokens
-    and a prefill batch of 4096 tokens (--moe-tokens), each routed top-2 by a
-    seeded draw (rows sorted by expert). One JSON line per projection and batch: time of the grouped call
-    (CUDA graph); for the decode batch weight GB/s over the routed experts' bytes
-    (experts without rows are skipped by the kernel), for the prefill batch
-    TFLOP/s (2 * rows * K * N); and the same rows as one w4a16_gemm call per
-    routed expert for comparison."""
+    N 28672, w2: K 14336 -> N 4096), for batches of `token_counts` tokens, each
+    routed top-2 by a seeded draw (rows sorted by expert). One record per
+    projection and batch: time of the grouped call (CUDA graph); up to 16 rows
+    an expert, weight GB/s over the routed experts' bytes (experts without rows
+    are skipped by the kernel), above that TFLOP/s (2 * rows * K * N); and the
+    same rows as one w4a16_gemm call per routed expert for comparison."""
     import torch
 
     import int4_weight_only_repack_gb300 as w4
@@ -675,14 +683,15 @@ def moe(args):
     E, topk = 8, 2
     hbm, _ = measured_peaks()
     tc, _ = measured_tc_peak()
+    out = []
     routes = []
-    for T in [int(t) for t in args.moe_tokens.split(",")]:
+    for T in token_counts:
         rng = np.random.default_rng([0, 17] if T == 16 else [0, 17, T])
         choice = np.stack([rng.choice(E, topk, replace=False) for _ in range(T)])
         counts = np.bincount(choice.reshape(-1), minlength=E)
         routes.append((T, counts, np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)))
     for name, K, N in (("w13", 4096, 28672), ("w2", 14336, 4096)):
-        if args.moe_proj not in ("all", name):
+        if proj not in ("all", name):
             continue
         qws, qzs, scs = [], [], []
         for e in range(E):
@@ -733,10 +742,17 @@ def moe(args):
                 line["tflops"] = round(tfl, 1)
                 line["frac_tc"] = round(tfl / tc, 3)
             line["device_status"] = w4.w4_device_status()
-            print(json.dumps(line), flush=True)
+            out.append(line)
             del x, y, ws
         del experts
         torch.cuda.empty_cache()
+    return out
+
+
+def moe(args):
+    """--moe: one JSON line per projection and batch (see moe_measure)."""
+    for line in moe_measure([int(t) for t in args.moe_tokens.split(",")], args.moe_proj):
+        print(json.dumps(line), flush=True)
 
 
 def main():
@@ -748,6 +764,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the large-M (prefill) layers")
+    ap.add_argument("--no-moe", action="store_true",
+                    help="skip the grouped MoE GEMM figures of the default run")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--sweep-config", type=int, default=4, choices=(3, 4),
                     help="workload of --sweep: 4 = Llama-2-70B, 3 = Llama-2-13B GPTQ act-order")
