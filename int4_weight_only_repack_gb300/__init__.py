@@ -310,6 +310,26 @@ def gemm_workspace(nbytes: int, device, stream=None):
     return ws
 
 
+_WS_SIZES: dict = {}
+_WS_SIZES_MAX = 4096
+
+
+def _workspace_size_cached(M, layer: RepackedLayer, device) -> int:
+    """w4a16_gemm_workspace_size for (device, M, layer shape), remembered: the
+    size depends only on those (and on the device's SM count), and linear()
+    would otherwise pay a second library call on every call."""
+    dev = device.index if device.index is not None else -1
+    key = (dev, M, layer.N, layer.K, layer.group, layer.dtype, layer.perm is not None)
+    need = _WS_SIZES.get(key)
+    if need is None:
+        need = w4a16_gemm_workspace_size(M, layer.N, layer.K, layer.group, layer.dtype,
+                                         layer.perm is not None)
+        if len(_WS_SIZES) >= _WS_SIZES_MAX:
+            _WS_SIZES.clear()
+        _WS_SIZES[key] = need
+    return need
+
+
 def linear(x, layer: RepackedLayer, y=None, workspace=None, stream=None, bias=None):
     """y = x · W (+ bias) for a TILE-layout layer; x is [M, K] fp16/bf16 on the
     device, bias [N] in the same dtype or None. Without `workspace`, the one kept
@@ -317,8 +337,7 @@ def linear(x, layer: RepackedLayer, y=None, workspace=None, stream=None, bias=No
     M = x.shape[0]
     if y is None:
         y = torch.empty((M, layer.N), dtype=x.dtype, device=x.device)
-    need = w4a16_gemm_workspace_size(M, layer.N, layer.K, layer.group, layer.dtype,
-                                     layer.perm is not None)
+    need = _workspace_size_cached(M, layer, x.device)
     if need and workspace is None:
         workspace = gemm_workspace(need, x.device, stream)
     w4a16_gemm_bias(x, layer.qw, layer.scales, layer.zeros, layer.perm, bias, y, M, layer.N,

@@ -173,3 +173,42 @@ def test_moe_gemm_rejects_bad_arguments(lib):
     # more than 4096 experts: beyond the tcgen05 kernel's table, so 64 rows at most
     assert _moe(lib, E=4097, max_rows=64, y=FAKE) == W4_ERR_ALIAS
     assert _moe(lib, E=4097, max_rows=65, y=FAKE) == W4_ERR_SHAPE
+
+
+def test_linear_caches_workspace_size(monkeypatch):
+    """linear() asks the library for a call's workspace size once per (device,
+    M, layer shape): a fake library counts the calls (no GPU needed)."""
+    import torch
+    import int4_weight_only_repack_gb300 as w4
+
+    class FakeLib:
+        def __init__(self):
+            self.size_calls = []
+            self.gemm_calls = 0
+
+        def w4a16_gemm_workspace_size(self, M, N, K, group, dtype, has_perm):
+            self.size_calls.append((M, N, K, group, dtype, has_perm))
+            return 0 if M <= 16 else 4096
+
+        def w4a16_gemm_bias(self, *args):
+            self.gemm_calls += 1
+            return W4_OK
+
+    fake = FakeLib()
+    monkeypatch.setattr(w4, "_LIB", fake)
+    monkeypatch.setattr(w4, "_WS_SIZES", {})
+    monkeypatch.setattr(w4, "gemm_workspace", lambda nbytes, device, stream=None:
+                        torch.empty(nbytes, dtype=torch.uint8))
+    K, N = 256, 128
+    layer = w4.RepackedLayer(K, N, 128, torch.bfloat16, w4.W4_LAYOUT_TILE,
+                             torch.zeros(8), torch.zeros(8), torch.zeros(8))
+    act = w4.RepackedLayer(K, N, 128, torch.bfloat16, w4.W4_LAYOUT_TILE,
+                           torch.zeros(8), torch.zeros(8), torch.zeros(8),
+                           perm=torch.zeros(K, dtype=torch.int32))
+    for M in (1, 1, 4, 1, 64, 64):
+        w4.linear(torch.zeros(M, K, dtype=torch.bfloat16), layer)
+    w4.linear(torch.zeros(4, K, dtype=torch.bfloat16), act)
+    w4.linear(torch.zeros(4, K, dtype=torch.bfloat16), act)
+    assert fake.gemm_calls == 8
+    assert [c[0] for c in fake.size_calls] == [1, 4, 64, 4]
+    assert [c[5] for c in fake.size_calls] == [0, 0, 0, 1]
