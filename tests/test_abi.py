@@ -212,3 +212,45 @@ def test_linear_caches_workspace_size(monkeypatch):
     assert fake.gemm_calls == 8
     assert [c[0] for c in fake.size_calls] == [1, 4, 64, 4]
     assert [c[5] for c in fake.size_calls] == [0, 0, 0, 1]
+
+
+def _declared_signatures():
+    """{name: [parameter type strings]} for every W4_API function of the header."""
+    import re
+    from libutil import HEADER
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    out = {}
+    for m in re.finditer(r"W4_API\s+([\w\s\*]+?)\b(\w+)\s*\(([^)]*)\)\s*;", text):
+        params = [p.strip() for p in m.group(3).split(",")]
+        if params == ["void"] or params == [""]:
+            params = []
+        out[m.group(2)] = (m.group(1).strip(), params)
+    return out
+
+
+def test_binding_matches_header():
+    """The ctypes binding declares every header function with the same number
+    of parameters, pointers where the header has pointers, and integers of the
+    header's widths elsewhere."""
+    import ctypes
+    import int4_weight_only_repack_gb300 as w4
+    decl = _declared_signatures()
+    assert set(decl) == set(w4._SIGNATURES), set(decl) ^ set(w4._SIGNATURES)
+    for name, (ret, params) in decl.items():
+        res, args = w4._SIGNATURES[name]
+        assert len(args) == len(params), name
+        for p, a in zip(params, args):
+            if "*" in p:
+                assert a is ctypes.c_void_p or a is ctypes.c_char_p or \
+                    issubclass(a, ctypes._Pointer), (name, p, a)
+            elif p.split()[0] == "size_t":
+                assert a is ctypes.c_size_t, (name, p)
+            else:
+                assert a in (ctypes.c_int, ctypes.c_int32), (name, p, a)
+        if "char" in ret:
+            assert res is ctypes.c_char_p, name
+        elif ret.split()[-1] in ("w4_status", "int"):
+            assert res in (ctypes.c_int, ctypes.c_int32), name
+        else:
+            assert ret == "size_t" and res is ctypes.c_size_t, (name, ret)
