@@ -1,31 +1,38 @@
 """Benchmark of the W4A16 linear layer on GB300 (one JSON line on stdout).
 
-Workload (default, one GPU): the Llama-2-7B decode layers (K, N) = (4096,
+Headline workload (one GPU): the Llama-2-7B decode layers (K, N) = (4096,
 12288) qkv, (4096, 4096) o_proj, (4096, 22016) gate_up, (11008, 4096) down,
 AWQ group-128 4-bit asymmetric weights, bf16 activations, M in {1, 4, 16}.
-One step runs the fused GEMM for every (layer, M) pair: 12 calls. Every call
-reads its own copy of the repacked weights (12 copies, about 315 MB, well
-above the 129 MB L2), so no call finds its weights in L2.
+One step runs the fused GEMM for every (layer, M) pair: 12 calls. Consecutive
+steps alternate between two sets of weight copies (24 copies, about 630 MB,
+4.9x the 129 MB L2), so no call finds its weights in L2.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-value       = weight GB/s over the timed steps (algorithmic bytes: packed codes
-              K*N/2 + scales G*N*2 + zeros G*N/2 per call), all ranks together.
-tflops      = 2*M*N*K summed over the calls / time.
-e2e         = the same metric through the public Python/C-ABI path with x
-              copied from pinned host memory and y copied back inside the
-              timed region, eager launches.
-roofline    = the decode kernel's per-launch durations (CUDA events on the
-              launch stream, launches front-loaded behind a long device copy
-              so the host never starves the GPU), against the measured HBM
-              copy bandwidth.
+value        = weight GB/s of the timed steps (algorithmic bytes per call:
+               packed codes K*N/2 + scales G*N*2 + zeros G*N/2), all ranks.
+roofline     = the decode kernel in the regime `value` times: each of the 12
+               (layer, M) calls timed as a CUDA graph of back-to-back calls over
+               rotating weight copies totalling at least 3x L2; achieved = the
+               12 calls' algorithmic bytes / the sum of their per-call times,
+               against the measured HBM copy bandwidth. `step_frac` is `value`
+               against the same peak.
+configs      = every workload point, one record each: the 7B decode calls, the
+               7B prefill layers (M 512..4096), the Llama-2-13B GPTQ act-order
+               layers (fp16, M 1/16/1024) and the Llama-2-70B sweep (M 1..4096).
+               Each record: time per call (CUDA graph over rotating copies),
+               weight GB/s, TFLOP/s, the roofline the ridge picks (HBM when the
+               call's bytes at the measured bandwidth take longer than its
+               FLOPs at the measured bf16 tensor peak, else tensor) and the
+               fraction of it; beside it the same call as dequantise-then-
+               cuBLAS (w4_dequant to a dense [K, N] + torch.matmul) and the CPU
+               oracle on a sample of the call (columns, and at most 64 rows),
+               extrapolated to the whole call.
+e2e          = the headline metric through the public Python API (linear())
+               with each step's x copied from pinned host memory and its y
+               copied back inside the timed region, eager launches.
 cpu_baseline = the CPU oracle (numpy: unpack, dequantise, fp64 matmul) on the
-              o_proj layer at M = 1, 4 and 16.
-dequant_cublas = the same step as w4_dequant to dense bf16 + cuBLAS (torch.matmul),
-              graph-timed like `value`; fused_speedup = its time / ours.
-prefill     = the Llama-2-7B prefill layers (M in {512, 2048, 4096}) on the
-              tcgen05 kernel: TFLOP/s per call and, for M >= 2048, against the
-              measured dense bf16 tensor-core peak.
+               o_proj layer at M = 1, 4 and 16.
 --impl reference times that oracle as the reference arm.
 """
 from __future__ import annotations
@@ -33,6 +40,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -52,6 +60,7 @@ METRIC = ("W4A16 GEMM TFLOP/s and weight GB/s vs M (1–4096), % of HBM / bf16 T
 WORKLOAD = synth.WORKLOADS[1]          # Llama-2-7B decode layers
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_TC_TFLOPS = 1900.0
+L2_ROTATION = 3.0                      # weight copies per timing loop: at least 3x L2
 
 # DRAM bytes per launch of the decode kernel from ncu (dram__bytes_read.sum +
 # dram__bytes_write.sum), keyed by the sha1 of the kernel source they were
@@ -66,31 +75,45 @@ def alg_bytes(K: int, N: int, group: int = 128) -> int:
     return K * N // 2 + G * N * 2 + G * N // 2
 
 
-def kernel_source_hash() -> str:
-    p = os.path.join(ROOT, "int4_weight_only_repack_gb300", "csrc", "decode_kernel.cu")
+def kernel_source_hash(name: str = "decode_kernel.cu") -> str:
+    p = os.path.join(ROOT, "int4_weight_only_repack_gb300", "csrc", name)
     with open(p, "rb") as f:
         return hashlib.sha1(f.read()).hexdigest()[:12]
 
 
-def measured_peaks():
+def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(p) as f:
-            d = json.load(f)
+            return json.load(f)
+    except Exception:
+        return None
+
+
+def measured_peaks():
+    d = _peaks()
+    try:
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
 
 
 def measured_tc_peak():
-    """Dense bf16 tensor-core peak (burst: the prefill calls are timed alone)."""
-    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    """Dense bf16 tensor-core peak (burst: every call is timed on its own)."""
+    d = _peaks()
     try:
-        with open(p) as f:
-            d = json.load(f)
         return float(d["bf16_tflops"]), "measured"
     except Exception:
         return FALLBACK_TC_TFLOPS, "fallback"
+
+
+def roofline_point(K, N, M, t, hbm_gbs, tc_tflops):
+    """The roofline of one call: its bytes at the HBM peak against its FLOPs at
+    the tensor peak; the longer of the two is the bound, frac = ideal / t."""
+    tb = alg_bytes(K, N) / (hbm_gbs * 1e9)
+    tf = 2.0 * M * N * K / (tc_tflops * 1e12)
+    bound = "hbm" if tb >= tf else "tensor"
+    return bound, max(tb, tf) / t
 
 
 # --------------------------------------------------------------------------- #
@@ -154,7 +177,7 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- #
-# Our arm                                                                       #
+# Replicas (N > 1)                                                              #
 # --------------------------------------------------------------------------- #
 def setup_dist():
     import torch
@@ -184,68 +207,6 @@ def max_over_ranks(v: float, world: int, device) -> float:
     return float(t.item())
 
 
-def build_calls(w4, torch, device):
-    """Repack one weight copy per (layer, M) and allocate x / y for each call."""
-    calls = []
-    for li, (K, N, name) in enumerate(WORKLOAD.shapes):
-        L = synth.make_workload_layer(WORKLOAD.index, li)
-        qweight = torch.from_numpy(L.qweight).to(device)
-        qzeros = torch.from_numpy(L.qzeros).to(device)
-        scales = torch.from_numpy(L.scales.view(np.int16)).to(device).view(torch.bfloat16)
-        for M in WORKLOAD.ms:
-            layer = w4.repack_awq(qweight, qzeros, scales, K, N, WORKLOAD.group, torch.bfloat16)
-            x_bits = synth.make_workload_x(WORKLOAD.index, li, M)
-            x = torch.from_numpy(x_bits.view(np.int16)).to(device).view(torch.bfloat16)
-            y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
-            calls.append(dict(name=name, K=K, N=N, M=M, layer=layer, x=x, y=y, x_bits=x_bits))
-        del qweight, qzeros, scales
-    # one workspace for the stream, as big as the largest call asks for (the
-    # calls run in stream order, so they can share it)
-    need = max(w4.w4a16_gemm_workspace_size(c["M"], c["N"], c["K"], WORKLOAD.group,
-                                            torch.bfloat16, False) for c in calls)
-    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
-    for c in calls:
-        c["ws"] = ws
-    torch.cuda.synchronize()
-    return calls
-
-
-def run_step(w4, calls):
-    for c in calls:
-        L = c["layer"]
-        w4.w4a16_gemm(c["x"], L.qw, L.scales, L.zeros, None, c["y"], c["M"], c["N"], c["K"],
-                      L.group, L.dtype, c["ws"])
-
-
-def per_launch_times(w4, torch, calls, reps: int, device):
-    """Average duration of each call's kernel, CUDA events on the launch stream.
-
-    A long device-side copy is enqueued first so that every launch and event
-    below is queued before the GPU reaches them: the events then bracket the
-    kernels alone, not host enqueue gaps.
-    """
-    stream = torch.cuda.current_stream()
-    big = torch.empty(1 << 30, dtype=torch.uint8, device=device)
-    big2 = torch.empty_like(big)
-    totals = [0.0] * len(calls)
-    for _ in range(reps):
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in calls]
-        for _ in range(6):
-            big2.copy_(big)
-        for c, (e0, e1) in zip(calls, evs):
-            L = c["layer"]
-            e0.record(stream)
-            w4.w4a16_gemm(c["x"], L.qw, L.scales, L.zeros, None, c["y"], c["M"], c["N"], c["K"],
-                          L.group, L.dtype, c["ws"])
-            e1.record(stream)
-        torch.cuda.synchronize()
-        for i, (e0, e1) in enumerate(evs):
-            totals[i] += e0.elapsed_time(e1) * 1e-3
-    del big, big2
-    return [t / reps for t in totals]
-
-
 def graph_time(torch, fn, reps: int) -> float:
     """Seconds per call of `fn` (a sequence of launches), from a CUDA graph of it
     replayed `reps` times, CUDA events on the launch stream."""
@@ -267,71 +228,230 @@ def graph_time(torch, fn, reps: int) -> float:
     return e0.elapsed_time(e1) * 1e-3 / reps
 
 
-def dequant_cublas_measure(w4, torch, calls, reps: int, device):
-    """The same step as dequantise-then-GEMM: w4_dequant of each call's layer to a
-    dense bf16 [K, N] (one scratch per layer shape), then torch.matmul (cuBLAS)."""
-    scratch = {}
-    for c in calls:
-        key = (c["K"], c["N"])
-        if key not in scratch:
-            scratch[key] = torch.empty((c["K"], c["N"]), dtype=torch.bfloat16, device=device)
-
-    def step():
-        for c in calls:
-            L, W = c["layer"], scratch[(c["K"], c["N"])]
-            w4.w4_dequant(L.qw, L.scales, L.zeros, c["K"], c["N"], L.group, L.dtype, L.layout,
-                          False, W)
-            torch.matmul(c["x"], W, out=c["y2"])
-
-    for c in calls:
-        c["y2"] = torch.empty_like(c["y"])
-    t = graph_time(torch, step, reps)
-    for c in calls:
-        del c["y2"]
-    del scratch
-    return t
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
 
 
-def prefill_measure(w4, torch, device, reps: int = 10):
-    """The Llama-2-7B prefill layers (same shapes, M in {512, 2048, 4096}) on the
-    tcgen05 kernel: TFLOP/s per (layer, M), two weight copies per layer; beside
-    each, a dense bf16 GEMM of the same shape through torch.matmul (cuBLAS), the
-    ceiling a weight-only kernel approaches at compute-bound sizes."""
-    wl = synth.WORKLOADS[2]
-    rows = []
-    for li, (K, N, name) in enumerate(wl.shapes):
-        L = synth.make_workload_layer(wl.index, li)
-        qweight = torch.from_numpy(L.qweight).to(device)
-        qzeros = torch.from_numpy(L.qzeros).to(device)
-        scales = torch.from_numpy(L.scales.view(np.int16)).to(device).view(torch.bfloat16)
-        layers = [w4.repack_awq(qweight, qzeros, scales, K, N, wl.group, torch.bfloat16)
-                  for _ in range(2)]
-        del qweight, qzeros, scales
-        for M in wl.ms:
-            x = torch.randn(M, K, device=device).to(torch.bfloat16)
-            y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+# --------------------------------------------------------------------------- #
+# Layers, weight pools, timing                                                  #
+# --------------------------------------------------------------------------- #
+class LayerPool:
+    """Repacked copies of one synthetic layer (TILE layout) plus a host sample of
+    its checkpoint columns for the oracle."""
 
-            def fn():
-                for l in layers:
-                    w4.linear(x, l, y=y)
+    def __init__(self, w4, torch, device, cfg, li, n_copies, sample_cols=256):
+        wl = synth.WORKLOADS[cfg]
+        K, N, name = wl.shapes[li]
+        self.K, self.N, self.name, self.cfg = K, N, name, cfg
+        self.dtype, self.fmt, self.group = wl.dtype, wl.fmt, wl.group
+        self.tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float16
+        seed = 1000 * cfg + li
+        qweight, qzeros, scales, g_idx = synth.make_layer_torch(
+            seed, K, N, wl.group, wl.dtype, wl.fmt, wl.act_order, device=device)
+        nc = min(N, sample_cols)
+        # host copy of the first nc columns of the checkpoint (a narrower layer)
+        if wl.fmt == "awq":
+            self.h_qweight = qweight[:, :nc // 8].cpu().numpy()
+        else:
+            self.h_qweight = qweight[:, :nc].cpu().numpy()
+        self.h_qzeros = qzeros[:, :nc // 8].cpu().numpy()
+        self.h_scales = scales[:, :nc].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+        self.h_gidx = g_idx.cpu().numpy() if g_idx is not None else None
+        self.sample_cols = nc
+        self.copies = []
+        for _ in range(n_copies):
+            if wl.fmt == "gptq":
+                self.copies.append(w4.repack_gptq(qweight, qzeros, scales, g_idx, K, N, wl.group,
+                                                  self.tdt))
+            else:
+                self.copies.append(w4.repack_awq(qweight, qzeros, scales, K, N, wl.group,
+                                                 self.tdt))
+        torch.cuda.synchronize()
+        for c in self.copies:
+            if c.status is not None and int(c.status[0].item()) != 0:
+                raise RuntimeError(f"{name}: act-order repack reported status {int(c.status[0])}")
+        del qweight, qzeros, scales, g_idx
 
-            t = graph_time(torch, fn, reps) / len(layers)
-            wd = [torch.randn(K, N, device=device).to(torch.bfloat16) for _ in range(2)]
-            yd = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+    @staticmethod
+    def copies_for(K, N, torch, device, minimum=2):
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        return max(minimum, math.ceil(L2_ROTATION * l2 / alg_bytes(K, N)))
 
-            def dense():
-                for w in wd:
-                    torch.matmul(x, w, out=yd)
 
-            td = graph_time(torch, dense, reps) / len(wd)
-            rows.append({"layer": name, "M": M, "us": round(t * 1e6, 2),
-                         "tflops": round(2.0 * M * N * K / t / 1e12, 1),
-                         "dense_bf16_cublas_us": round(td * 1e6, 2),
-                         "dense_bf16_cublas_tflops": round(2.0 * M * N * K / td / 1e12, 1)})
-            del x, y, wd, yd
-        del layers
+def graph_time_reps(torch, fn, reps: int) -> float:
+    """Seconds per replay of a CUDA graph of `fn`, median of `reps` replays timed
+    one by one with CUDA events on the launch stream (after two warm-up replays)."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for e0, e1 in ev:
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    del g
+    return statistics.median(e0.elapsed_time(e1) * 1e-3 for e0, e1 in ev)
+
+
+def call_time(w4, torch, pool, x, y, copies=None, reps=10):
+    """Seconds per w4a16 call: a graph of one call per weight copy (back to back,
+    so every call streams a copy that the others have pushed out of L2)."""
+    use = pool.copies if copies is None else pool.copies[:copies]
+
+    def fn():
+        for l in use:
+            w4.linear(x, l, y=y)
+
+    return graph_time_reps(torch, fn, reps) / len(use)
+
+
+def dequant_cublas_time(w4, torch, pool, x, dense, y2, copies=None, reps=5):
+    """Seconds per call of the dequantise-then-cuBLAS path: w4_dequant of the
+    call's copy to a dense [K, N] in the activation dtype, then torch.matmul (an
+    act-order layer's dense rows come out sorted, so x is gathered by perm first)."""
+    use = pool.copies if copies is None else pool.copies[:copies]
+    perm = use[0].perm.long() if use[0].perm is not None else None
+
+    def fn():
+        for l in use:
+            w4.w4_dequant(l.qw, l.scales, l.zeros, pool.K, pool.N, l.group, l.dtype, l.layout,
+                          False, dense)
+            xs = x if perm is None else torch.index_select(x, 1, perm)
+            torch.matmul(xs, dense, out=y2)
+
+    return graph_time_reps(torch, fn, reps) / len(use)
+
+
+def oracle_sample_time(pool, M, min_seconds=0.05):
+    """The CPU oracle on a sample of one call: the pool's first `sample_cols`
+    output columns and min(M, 64) rows of x, repeated until `min_seconds`; the
+    time is extrapolated to the whole call by N / columns x M / rows."""
+    import oracle
+    rows = min(M, 64)
+    x = synth.make_custom_x([9, pool.cfg, pool.K, rows], rows, pool.K, pool.dtype)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle.reference_y(x, pool.h_qweight, pool.h_qzeros, pool.h_scales, pool.group,
+                           pool.dtype, pool.fmt, g_idx=pool.h_gidx)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds:
+            break
+    t = el / n * (pool.N / pool.sample_cols) * (M / rows)
+    return {"s_per_call": t, "weight_gbs": round(alg_bytes(pool.K, pool.N) / t / 1e9, 5),
+            "sample": f"{pool.sample_cols} of {pool.N} columns x {rows} of {M} rows, "
+                      f"extrapolated", "cores": blas_threads()}
+
+
+def point_record(w4, torch, device, pool, M, hbm, tc, scratch, with_dense=False,
+                 with_oracle=True, reps=10):
+    """One (layer, M) record: our call, dequantise-then-cuBLAS and the oracle."""
+    K, N = pool.K, pool.N
+    x = torch.randn(M, K, device=device).to(pool.tdt)
+    y = torch.empty((M, N), dtype=pool.tdt, device=device)
+    copies = None if M <= 256 else 2
+    t = call_time(w4, torch, pool, x, y, copies, reps)
+    bound, frac = roofline_point(K, N, M, t, hbm, tc)
+    rec = {"layer": pool.name, "K": K, "N": N, "M": M, "us": round(t * 1e6, 2),
+           "weight_gbs": round(alg_bytes(K, N) / t / 1e9, 1),
+           "tflops": round(2.0 * M * N * K / t / 1e12, 2), "bound": bound,
+           "frac": round(frac, 4),
+           "weight_copies": len(pool.copies) if copies is None else copies}
+    key = (K, N, pool.tdt)
+    if key not in scratch:
+        scratch.clear()
         torch.cuda.empty_cache()
-    return rows
+        scratch[key] = torch.empty((K, N), dtype=pool.tdt, device=device)
+    y2 = torch.empty_like(y)
+    td = dequant_cublas_time(w4, torch, pool, x, scratch[key], y2,
+                             copies=min(len(pool.copies), 3 if M <= 256 else 2), reps=5)
+    rec["dequant_cublas_us"] = round(td * 1e6, 2)
+    rec["fused_speedup"] = round(td / t, 2)
+    if with_dense:
+        wd = [torch.randn(K, N, device=device).to(pool.tdt) for _ in range(2)]
+        yd = torch.empty_like(y)
+
+        def dense():
+            for w in wd:
+                torch.matmul(x, w, out=yd)
+
+        tdn = graph_time_reps(torch, dense, 5) / len(wd)
+        rec["dense_cublas_us"] = round(tdn * 1e6, 2)
+        rec["dense_cublas_tflops"] = round(2.0 * M * N * K / tdn / 1e12, 1)
+        del wd, yd
+    if with_oracle:
+        o = oracle_sample_time(pool, M)
+        rec["oracle_weight_gbs"] = o["weight_gbs"]
+        rec["oracle_sample"] = o["sample"]
+    del x, y, y2
+    return rec
+
+
+def config_records(w4, torch, device, cfg, hbm, tc, with_dense_from=None, with_oracle=True):
+    """Records for every (layer, M) of workload `cfg`."""
+    wl = synth.WORKLOADS[cfg]
+    out = []
+    scratch = {}
+    for li, (K, N, name) in enumerate(wl.shapes):
+        n = LayerPool.copies_for(K, N, torch, device)
+        pool = LayerPool(w4, torch, device, cfg, li, n)
+        for M in wl.ms:
+            dense = with_dense_from is not None and M >= with_dense_from
+            out.append(point_record(w4, torch, device, pool, M, hbm, tc, scratch,
+                                    with_dense=dense, with_oracle=with_oracle))
+        del pool
+        torch.cuda.empty_cache()
+    scratch.clear()
+    torch.cuda.empty_cache()
+    return out
+
+
+def repack_measure(w4, torch, device, reps=5):
+    """Throughput of the one-time AWQ -> TILE repack on the Llama-2-70B gate_up
+    layer (K 8192, N 57344): bytes read (qweight, qzeros, scales) + written
+    (TILE words, zeros, scales) per call / time (CUDA events around one call)."""
+    K, N, g = 8192, 57344, 128
+    qweight, qzeros, scales, _ = synth.make_layer_torch(4001, K, N, g, "bf16", device=device)
+    qw_b, z_b, s_b = w4.w4_repack_sizes(K, N, g, w4.W4_LAYOUT_TILE)
+    outs = [(torch.empty(qw_b // 4, dtype=torch.int32, device=device),
+             torch.empty(z_b // 4, dtype=torch.int32, device=device),
+             torch.empty(s_b // 2, dtype=torch.bfloat16, device=device)) for _ in range(2)]
+    times = []
+    for r in range(reps + 1):
+        qw, zz, ss = outs[r % 2]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        w4.w4_repack_awq(qweight, qzeros, scales, K, N, g, torch.bfloat16, w4.W4_LAYOUT_TILE,
+                         qw, zz, ss)
+        e1.record()
+        torch.cuda.synchronize()
+        if r:
+            times.append(e0.elapsed_time(e1) * 1e-3)
+    t = statistics.median(times)
+    moved = (K * N // 2 + z_b + s_b) * 2
+    hbm, _ = measured_peaks()
+    del qweight, qzeros, scales, outs
+    torch.cuda.empty_cache()
+    return {"layer": "llama2_70b gate_up (8192 x 57344), AWQ -> TILE", "us": round(t * 1e6, 1),
+            "gbs": round(moved / t / 1e9, 1), "frac_hbm": round(moved / t / 1e9 / hbm, 4),
+            "bytes": moved, "how": "w4_repack_awq (unpack + TILE words, zeros, scales + the "
+                                   "stream-ordering kernel), CUDA events around one call, median"}
 
 
 def cpu_baseline_measure(min_seconds: float = 10.0):
@@ -358,17 +478,9 @@ def cpu_baseline_measure(min_seconds: float = 10.0):
                       f"fp32 dequantise, fp64 matmul) in {el:.1f} s"}
 
 
-def blas_threads() -> int:
-    try:
-        from threadpoolctl import threadpool_info
-        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
-        if n:
-            return int(max(n))
-    except Exception:
-        pass
-    return os.cpu_count() or 1
-
-
+# --------------------------------------------------------------------------- #
+# Our arm                                                                       #
+# --------------------------------------------------------------------------- #
 def ours(args):
     import torch
 
@@ -380,20 +492,61 @@ def ours(args):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     w4.lib()
+    hbm, hbm_src = measured_peaks()
+    tc, tc_src = measured_tc_peak()
 
-    calls = build_calls(w4, torch, device)
-    step_bytes = sum(alg_bytes(c["K"], c["N"]) for c in calls)
-    step_flops = sum(2 * c["M"] * c["N"] * c["K"] for c in calls)
+    # ---- the headline step: 12 calls, two sets of weight copies -----------------
+    pools = []
+    for li, (K, N, _) in enumerate(WORKLOAD.shapes):
+        n = LayerPool.copies_for(K, N, torch, device, minimum=2 * len(WORKLOAD.ms))
+        pools.append(LayerPool(w4, torch, device, WORKLOAD.index, li, n))
+    calls = []
+    for li, pool in enumerate(pools):
+        for mi, M in enumerate(WORKLOAD.ms):
+            x_bits = synth.make_workload_x(WORKLOAD.index, li, M)
+            calls.append(dict(pool=pool, li=li, M=M, mi=mi, x_bits=x_bits))
+    # every step's inputs live in one buffer (and its outputs in another) so the
+    # end-to-end pass moves them with one copy each way
+    x_elems = sum(c["M"] * c["pool"].K for c in calls)
+    y_elems = sum(c["M"] * c["pool"].N for c in calls)
+    x_all = torch.empty(x_elems, dtype=torch.bfloat16, device=device)
+    y_all = torch.empty(y_elems, dtype=torch.bfloat16, device=device)
+    hx_all = torch.empty(x_elems, dtype=torch.bfloat16).pin_memory()
+    hy_all = torch.empty(y_elems, dtype=torch.bfloat16).pin_memory()
+    xo = yo = 0
+    for c in calls:
+        K, N, M = c["pool"].K, c["pool"].N, c["M"]
+        hx_all[xo:xo + M * K].copy_(torch.from_numpy(c["x_bits"].view(np.int16).reshape(-1))
+                                    .view(torch.bfloat16))
+        c["x"] = x_all[xo:xo + M * K].view(M, K)
+        c["y"] = y_all[yo:yo + M * N].view(M, N)
+        xo += M * K
+        yo += M * N
+    x_all.copy_(hx_all)
+    nsets = 2
 
-    # warm-up (eager), then capture one step as a CUDA graph
+    def step_fn(s):
+        def fn():
+            for c in calls:
+                layer = c["pool"].copies[(c["mi"] + len(WORKLOAD.ms) * s) % len(c["pool"].copies)]
+                w4.linear(c["x"], layer, y=c["y"])
+        return fn
+
+    step_bytes = sum(alg_bytes(c["pool"].K, c["pool"].N) for c in calls)
+    step_flops = sum(2 * c["M"] * c["pool"].N * c["pool"].K for c in calls)
     for _ in range(max(args.warmup, 3)):
-        run_step(w4, calls)
+        for s in range(nsets):
+            step_fn(s)()
     torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        run_step(w4, calls)
-    for _ in range(3):
-        g.replay()
+    graphs = []
+    for s in range(nsets):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step_fn(s)()
+        graphs.append(g)
+    for _ in range(max(args.warmup, 3)):
+        for g in graphs:
+            g.replay()
     torch.cuda.synchronize()
 
     # ---- timed region ----------------------------------------------------------
@@ -405,77 +558,82 @@ def ours(args):
     stream = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        g.replay()
+    for i in range(args.steps):
+        graphs[i % nsets].replay()
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop() if sampler else None
     elapsed = max_over_ranks(e0.elapsed_time(e1) * 1e-3, world, device)
+    del graphs
 
-    # ---- per-launch kernel durations (roofline) ---------------------------------
-    t_launch = per_launch_times(w4, torch, calls, reps=5, device=device)
-    kern_bytes = sum(alg_bytes(c["K"], c["N"]) for c in calls)
-    kern_time = sum(t_launch)
-    peak, peak_src = measured_peaks()
-    achieved = kern_bytes / kern_time / 1e9
-    per_call = [{"layer": c["name"], "M": c["M"], "us": round(t * 1e6, 2),
-                 "gbs": round(alg_bytes(c["K"], c["N"]) / t / 1e9, 1),
-                 "frac": round(alg_bytes(c["K"], c["N"]) / t / 1e9 / peak, 3)}
-                for c, t in zip(calls, t_launch)]
+    # ---- the decode kernel per call, graph-timed over >= 3x L2 of copies --------
+    scratch = {}
+    per_call = []
+    for c in calls:
+        rec = point_record(w4, torch, device, c["pool"], c["M"], hbm, tc, scratch,
+                           with_oracle=rank == 0 and not args.no_cpu_baseline, reps=20)
+        per_call.append(rec)
+    scratch.clear()
+    kern_time = sum(r["us"] for r in per_call) * 1e-6
+    achieved = step_bytes / kern_time / 1e9
     traffic = TRAFFIC_RECORDS.get(kernel_source_hash())
 
     # ---- end to end through the public API, host buffers ------------------------
     e2e_steps = min(args.steps, 200)
-    hx = [torch.from_numpy(c["x_bits"].view(np.int16)).view(torch.bfloat16).pin_memory()
-          for c in calls]
-    hy = [torch.empty((c["M"], c["N"]), dtype=torch.bfloat16).pin_memory() for c in calls]
-    h2d = sum(t.numel() * 2 for t in hx)
-    d2h = sum(t.numel() * 2 for t in hy)
-    for _ in range(2):
-        for c, a, b in zip(calls, hx, hy):
-            c["x"].copy_(a, non_blocking=True)
-            w4.linear(c["x"], c["layer"], y=c["y"])
-            b.copy_(c["y"], non_blocking=True)
+
+    def e2e_step(s):
+        x_all.copy_(hx_all, non_blocking=True)
+        for c in calls:
+            layer = c["pool"].copies[(c["mi"] + len(WORKLOAD.ms) * s) % len(c["pool"].copies)]
+            w4.linear(c["x"], layer, y=c["y"])
+        hy_all.copy_(y_all, non_blocking=True)
+
+    for s in range(2 * nsets):
+        e2e_step(s % nsets)
     torch.cuda.synchronize()
     barrier(world)
     t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        for c, a, b in zip(calls, hx, hy):
-            c["x"].copy_(a, non_blocking=True)
-            w4.linear(c["x"], c["layer"], y=c["y"])
-            b.copy_(c["y"], non_blocking=True)
+    for s in range(e2e_steps):
+        e2e_step(s % nsets)
     torch.cuda.synchronize()
     e2e_el = max_over_ranks(time.perf_counter() - t0, world, device)
 
-    # ---- comparison: dequantise then cuBLAS, same step, same timing ------------
-    t_deq = dequant_cublas_measure(w4, torch, calls, reps=min(args.steps, 200), device=device)
+    # ---- comparison: the same step as dequantise-then-cuBLAS ---------------------
+    t_deq = sum(r["dequant_cublas_us"] for r in per_call) * 1e-6
+    del pools, calls
+    torch.cuda.empty_cache()
 
-    # ---- large-M (prefill) layers on the tensor cores -------------------------
+    # ---- the other workloads, one record per (layer, M) ---------------------------
+    configs = {"llama2_7b_decode": per_call}
     prefill = None
-    if not args.no_prefill:
-        rows = prefill_measure(w4, torch, device)
-        big = [r for r in rows if r["M"] >= 2048]
-        kn = {sh[2]: (sh[0], sh[1]) for sh in synth.WORKLOADS[2].shapes}
-        flops = sum(2.0 * r["M"] * kn[r["layer"]][0] * kn[r["layer"]][1] for r in big)
+    if not args.no_configs and world == 1:
+        oracle_on = rank == 0 and not args.no_cpu_baseline
+        configs["llama2_7b_prefill"] = config_records(w4, torch, device, 2, hbm, tc,
+                                                      with_dense_from=512, with_oracle=oracle_on)
+        configs["llama2_13b_gptq_act_order"] = config_records(w4, torch, device, 3, hbm, tc,
+                                                              with_oracle=oracle_on)
+        configs["llama2_70b_sweep"] = config_records(w4, torch, device, 4, hbm, tc,
+                                                     with_dense_from=1024, with_oracle=oracle_on)
+        big = [r for r in configs["llama2_7b_prefill"] if r["M"] >= 2048]
+        flops = sum(2.0 * r["M"] * r["K"] * r["N"] for r in big)
         tsum = sum(r["us"] for r in big) * 1e-6
-        tc_peak, tc_src = measured_tc_peak()
-        prefill = {"workload": "llama2_7b_prefill: the four layers at M in {512, 2048, 4096}, "
-                               "bf16, two weight copies per layer, CUDA graph of the calls",
+        dense = sum(r["dense_cublas_us"] for r in big) * 1e-6
+        prefill = {"workload": "llama2_7b_prefill at M in {2048, 4096}, bf16",
                    "tflops_m_ge_2048": round(flops / tsum / 1e12, 1),
+                   "vs_dense_bf16_cublas": round(dense / tsum, 3),
                    "roofline": {"bound": "tensor", "achieved": round(flops / tsum / 1e12, 1),
-                                "peak": tc_peak, "unit": "TFLOP/s",
-                                "frac": round(flops / tsum / 1e12 / tc_peak, 4),
-                                "peak_source": tc_src, "kernel": "w4a16_prefill_kernel"},
-                   "per_call": rows}
+                                "peak": tc, "unit": "TFLOP/s",
+                                "frac": round(flops / tsum / 1e12 / tc, 4),
+                                "peak_source": tc_src, "kernel": "w4a16_prefill_kernel"}}
 
-    # ---- grouped MoE GEMM (one GPU only: a side figure like the CPU baseline) --
     moe_part = None
     if world == 1 and not args.no_moe:
         moe_part = {"workload": "mixtral_8x7b_shaped experts (8; w13 4096->28672, w2 "
                                 "14336->4096), 16 and 4096 tokens routed top-2, bf16, "
                                 "one w4a16_moe_gemm call against one w4a16_gemm per expert",
                     "per_call": moe_measure((16, 4096))}
+    repack = repack_measure(w4, torch, device) if world == 1 else None
 
     cpu_base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -499,32 +657,44 @@ def ours(args):
             "config": {
                 "workload": "llama2_7b_decode: (K,N)=(4096,12288),(4096,4096),(4096,22016),"
                             "(11008,4096); M in {1,4,16}; AWQ g128; bf16",
-                "calls_per_step": len(calls),
+                "calls_per_step": len(per_call),
                 "weight_bytes_per_step": step_bytes,
-                "l2": "inputs larger than L2: 12 distinct weight copies (%.0f MB) per step"
-                      % (step_bytes / 1e6),
-                "timing": "CUDA graph of one step replayed; CUDA events on the launch stream",
+                "l2": "inputs larger than L2: consecutive steps alternate between two sets of "
+                      "12 weight copies (%.0f MB per set, %.0f MB in all)"
+                      % (step_bytes / 1e6, nsets * step_bytes / 1e6),
+                "timing": "CUDA graph of one step per set, replayed alternately; CUDA events on "
+                          "the launch stream",
                 "parallelism": "replicas" if world > 1 else "single GPU",
             },
             "tflops": round(step_flops * args.steps * world / elapsed / 1e12, 4),
-            "gpu_launches": len(calls) * args.steps,
+            "gpu_launches": len(per_call) * args.steps,
             "clocks": clocks,
             "e2e": {"value": round(step_bytes * e2e_steps * world / e2e_el / 1e9, 2),
-                    "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "steps": e2e_steps},
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                         "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "traffic": traffic, "peak_source": peak_src,
+                    "unit": "GB/s", "h2d_bytes_per_step": x_elems * 2,
+                    "d2h_bytes_per_step": y_elems * 2, "steps": e2e_steps,
+                    "how": "linear() per call; each step's x in one pinned-host -> device "
+                           "copy and its y in one device -> pinned-host copy, eager"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
+                         "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                         "traffic": traffic, "peak_source": hbm_src,
                          "kernel": "w4a16_decode_kernel",
-                         "per_launch": per_call},
+                         "step_frac": round(value / world / hbm, 4),
+                         "how": "each (layer, M) call as a CUDA graph of back-to-back calls over "
+                                ">= 3x L2 of weight copies; achieved = the step's bytes / the sum "
+                                "of the 12 per-call times (records under configs)"},
             "cpu_baseline": cpu_base,
             "dequant_cublas": {"value": round(step_bytes / t_deq / 1e9, 2), "unit": "GB/s",
                                "ms_per_step": round(t_deq * 1e3, 5),
                                "fused_speedup": round(t_deq / (elapsed / args.steps), 2),
-                               "how": "w4_dequant to dense bf16 [K,N] + torch.matmul (cuBLAS) "
-                                      "per call, CUDA graph of the step"},
+                               "how": "sum over the 12 calls of w4_dequant to dense bf16 [K,N] + "
+                                      "torch.matmul (cuBLAS), each graph-timed over weight copies"},
             "prefill": prefill,
+            "configs": configs,
+            "roofline_peaks": {"hbm_gbs": hbm, "bf16_tflops": tc, "source": hbm_src,
+                               "ridge_M": round(tc * 1e12 / (4 * hbm * 1e9), 1),
+                               "note": "fp16 calls use the bf16 figure (the same dense rate)"},
             "moe": moe_part,
+            "repack": repack,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -614,55 +784,20 @@ def single(args):
 
 
 def sweep(args):
-    """A layer sweep over M: one JSON line per (layer, M) with time, weight
-    GB/s, TFLOP/s and the fraction of the matching roofline (HBM for M <= 16,
-    dense bf16 tensor peak above). Default: the Llama-2-70B layers, M from 1 to
-    4096 (--sweep-config 4); --sweep-config 3: the Llama-2-13B GPTQ act-order
-    layers (fp16, M in {1, 16, 1024})."""
+    """Every (layer, M) record of one workload, one JSON line each (the same
+    records the default line carries under `configs`)."""
     import torch
 
     import int4_weight_only_repack_gb300 as w4
 
     dev = torch.device("cuda")
-    wl = synth.WORKLOADS[args.sweep_config]
+    w4.lib()
     hbm, _ = measured_peaks()
     tc, _ = measured_tc_peak()
-    hdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float16
-    for li, (K, N, name) in enumerate(wl.shapes):
-        L = synth.make_workload_layer(wl.index, li)
-        qweight = torch.from_numpy(L.qweight).to(dev)
-        qzeros = torch.from_numpy(L.qzeros).to(dev)
-        scales = torch.from_numpy(L.scales.view(np.int16)).to(dev).view(hdt)
-        g_idx = torch.from_numpy(L.g_idx).to(dev) if L.g_idx is not None else None
-        ncopy = max(2, int(400e6 // alg_bytes(K, N)) + 1)
-        if wl.fmt == "gptq":
-            layers = [w4.repack_gptq(qweight, qzeros, scales, g_idx, K, N, wl.group, hdt)
-                      for _ in range(ncopy)]
-        else:
-            layers = [w4.repack_awq(qweight, qzeros, scales, K, N, wl.group, hdt)
-                      for _ in range(ncopy)]
-        del qweight, qzeros, scales
-        for M in wl.ms:
-            x = torch.randn(M, K, device=dev).to(hdt)
-            y = torch.empty((M, N), dtype=hdt, device=dev)
-            use = layers if M <= 256 else layers[:2]
-
-            def fn():
-                for l in use:
-                    w4.linear(x, l, y=y)
-
-            t = graph_time(torch, fn, 10) / len(use)
-            gbs = alg_bytes(K, N) / t / 1e9
-            tfl = 2.0 * M * N * K / t / 1e12
-            print(json.dumps({"sweep": wl.name, "layer": name, "K": K, "N": N, "M": M,
-                              "dtype": wl.dtype, "act_order": g_idx is not None,
-                              "us": round(t * 1e6, 2), "weight_gbs": round(gbs, 1),
-                              "tflops": round(tfl, 1),
-                              "frac": round(gbs / hbm if M <= 16 else tfl / tc, 3),
-                              "bound": "hbm" if M <= 16 else "tensor"}), flush=True)
-            del x, y
-        del layers
-        torch.cuda.empty_cache()
+    wl = synth.WORKLOADS[args.sweep_config]
+    for rec in config_records(w4, torch, dev, args.sweep_config, hbm, tc,
+                              with_oracle=not args.no_cpu_baseline):
+        print(json.dumps({"sweep": wl.name, **rec}), flush=True)
     print(json.dumps({"sweep_done": wl.name, "device_status": w4.w4_device_status()}), flush=True)
 
 
@@ -695,10 +830,11 @@ def moe_measure(token_counts, proj="all"):
             continue
         qws, qzs, scs = [], [], []
         for e in range(E):
-            L = synth.make_custom_layer([0, 17, e, K, N], K, N, group=128, dtype="bf16")
-            qws.append(torch.from_numpy(L.qweight).to(dev))
-            qzs.append(torch.from_numpy(L.qzeros).to(dev))
-            scs.append(torch.from_numpy(L.scales.view(np.int16)).to(dev).view(torch.bfloat16))
+            qw_e, qz_e, sc_e, _ = synth.make_layer_torch(17000 + 100 * e + (K // 1024), K, N, 128,
+                                                         "bf16", device=dev)
+            qws.append(qw_e)
+            qzs.append(qz_e)
+            scs.append(sc_e)
         experts = w4.repack_awq_experts(qws, qzs, scs, K, N, 128, torch.bfloat16)
         del qws, qzs, scs
         qw_b, z_b, s_b = w4.w4_repack_sizes(K, N, 128, w4.W4_LAYOUT_TILE)
@@ -761,14 +897,16 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-prefill", action="store_true",
-                    help="skip the large-M (prefill) layers")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip every CPU oracle timing (the headline baseline and the samples)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the prefill, act-order and 70B records of the default run")
     ap.add_argument("--no-moe", action="store_true",
                     help="skip the grouped MoE GEMM figures of the default run")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--sweep-config", type=int, default=4, choices=(3, 4),
-                    help="workload of --sweep: 4 = Llama-2-70B, 3 = Llama-2-13B GPTQ act-order")
+    ap.add_argument("--sweep-config", type=int, default=4, choices=(2, 3, 4),
+                    help="workload of --sweep: 2 = Llama-2-7B prefill, 3 = Llama-2-13B GPTQ "
+                         "act-order, 4 = Llama-2-70B")
     ap.add_argument("--sweep", action="store_true",
                     help="every layer of --sweep-config at every M of that workload (one line each)")
     ap.add_argument("--moe", action="store_true",

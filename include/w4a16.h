@@ -288,9 +288,10 @@ W4_API w4_status w4_test_stalled_gemm(const void* x, const int32_t* qw, const vo
 /*
  * w4a16_gemm without a caller-provided workspace. (This entry point has no
  * counterpart in the pages: it serves callers of this library that cannot
- * allocate device memory at call time, such as code running inside a
- * CUDA-graph capture where cudaMalloc is not allowed, or a host that embeds
- * the library behind an interface with no allocator.)
+ * allocate device memory at call time, such as a host that embeds the library
+ * behind a plain-function interface with no device allocator, or a serving
+ * runtime that reserves all of its device memory up front and hands out none
+ * per call.)
  *
  * Same arguments, layouts, results and error statuses as w4a16_gemm, minus
  * workspace / workspace_bytes. Where w4a16_gemm would use a workspace
@@ -303,9 +304,11 @@ W4_API w4_status w4_test_stalled_gemm(const void* x, const int32_t* qw, const vo
  * kernel split K less (then the result bits can differ from a w4a16_gemm call
  * given the full workspace).
  * It never allocates or frees device memory.
- *   - Set-up: the first call on each device looks up the array's device
- *     address (cudaGetSymbolAddress) with that device current. Make that first
- *     call before any stream capture on the device.
+ *   - Set-up: the first call with M > 0 on each device (whatever its shape,
+ *     once its arguments pass validation) looks up the array's device address
+ *     (cudaGetSymbolAddress, which may also load the library's device code)
+ *     with that device current. Make that first call before any stream capture
+ *     on the device.
  *   - All calls share the one array: calls that may overlap on the GPU (on
  *     different streams, or from different host threads) race on it and must
  *     be ordered by the caller. The array is fully overwritten before it is

@@ -8,6 +8,7 @@ the first call raises, naming the build step.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from typing import Optional
@@ -118,9 +119,21 @@ def _ptr(t) -> Optional[int]:
     return t.data_ptr()
 
 
-def _stream(stream) -> Optional[int]:
+_RAW_STREAM = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream, device_index: Optional[int] = None) -> Optional[int]:
+    """The cudaStream_t handle to pass: `stream` itself (a torch stream or a raw
+    handle), else torch's current stream on `device_index` (the current device
+    when None)."""
     if stream is None:
-        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+        if not torch.cuda.is_available():
+            return None
+        if _RAW_STREAM is not None:
+            if device_index is None:
+                device_index = torch.cuda.current_device()
+            return _RAW_STREAM(device_index)
+        return torch.cuda.current_stream(device_index).cuda_stream
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
@@ -300,12 +313,26 @@ _WORKSPACES: dict = {}
 def gemm_workspace(nbytes: int, device, stream=None):
     """A workspace of at least nbytes on `device` for calls on `stream`, kept
     and reused across calls (calls on one stream run in order, so they can
-    share it, and no call allocates device memory once it is big enough)."""
+    share it, and no call allocates device memory once it is big enough). It is
+    allocated on that stream, so when a larger one replaces it the caching
+    allocator hands the old block out again only in that stream's order (after
+    the calls that may still be reading it)."""
     dev = torch.device(device)
-    key = (dev.index if dev.index is not None else torch.cuda.current_device(), _stream(stream))
+    idx = dev.index if dev.index is not None else torch.cuda.current_device()
+    handle = _stream(stream, idx)
+    key = (idx, handle)
     ws = _WORKSPACES.get(key)
     if ws is None or ws.numel() < nbytes:
-        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        if stream is None:
+            ctx = contextlib.nullcontext()      # the current stream is the one used
+        elif isinstance(stream, int):
+            ext = (torch.cuda.ExternalStream(stream, device=torch.device("cuda", idx)) if stream
+                   else torch.cuda.default_stream(idx))
+            ctx = torch.cuda.stream(ext)
+        else:
+            ctx = torch.cuda.stream(stream)
+        with ctx:
+            ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
         _WORKSPACES[key] = ws
     return ws
 
@@ -340,6 +367,10 @@ def linear(x, layer: RepackedLayer, y=None, workspace=None, stream=None, bias=No
     need = _workspace_size_cached(M, layer, x.device)
     if need and workspace is None:
         workspace = gemm_workspace(need, x.device, stream)
-    w4a16_gemm_bias(x, layer.qw, layer.scales, layer.zeros, layer.perm, bias, y, M, layer.N,
-                    layer.K, layer.group, layer.dtype, workspace, None, stream)
+    handle = _stream(stream, x.device.index)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().w4a16_gemm_bias(x.data_ptr(), layer.qw.data_ptr(), layer.scales.data_ptr(),
+                                 layer.zeros.data_ptr(), _ptr(layer.perm), _ptr(bias),
+                                 y.data_ptr(), M, layer.N, layer.K, layer.group,
+                                 dtype_code(layer.dtype), _ptr(workspace), ws_bytes, handle))
     return y

@@ -412,18 +412,21 @@ w4_status w4a16_gemm_noalloc(const void* x, const int32_t* qw, const void* scale
                           ? prefill_workspace_bytes(M, K, perm != nullptr)
                           : 0;
   if (need > W4_NOALLOC_SCRATCH_BYTES) return W4_ERR_WORKSPACE;
-  if (M == 0 || ((M <= 16 || !prefill_supported(M, N, K)) && perm == nullptr)) {
-    // the small-M kernel without act-order uses no workspace
-    return w4a16_gemm(x, qw, scales, zeros, perm, y, M, N, K, group, dtype, nullptr, 0, stream);
-  }
   // validate everything the scratch does not decide before touching the device
   st = w4a16_gemm(x, qw, scales, zeros, perm, y, 0, N, K, group, dtype, nullptr, 0, stream);
   if (st) return st;
+  if (M == 0) return W4_OK;
   if (!x || !y) return W4_ERR_NULL;
   if ((st = check_arch())) return st;
+  // the array's address is looked up on every path, so that the first call on
+  // a device does the set-up whatever its shape
   void* scratch = nullptr;
   size_t scratch_bytes = 0;
   if (noalloc_scratch(&scratch, &scratch_bytes) != cudaSuccess) return W4_ERR_CUDA;
+  if ((M <= 16 || !prefill_supported(M, N, K)) && perm == nullptr) {
+    // the small-M kernel without act-order uses no workspace
+    return w4a16_gemm(x, qw, scales, zeros, perm, y, M, N, K, group, dtype, nullptr, 0, stream);
+  }
   return w4a16_gemm(x, qw, scales, zeros, perm, y, M, N, K, group, dtype, scratch, scratch_bytes,
                     stream);
 }

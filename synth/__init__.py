@@ -293,3 +293,104 @@ def make_custom_layer(seed, K: int, N: int, group: int = 128, dtype: str = BF16,
 
 def make_custom_x(seed, M: int, K: int, dtype: str = BF16) -> np.ndarray:
     return make_x_from_rng(np.random.default_rng(seed), M, K, dtype)
+
+
+# --------------------------------------------------------------------------- #
+# The same writer on torch tensors (for the benchmark's large layers).
+# --------------------------------------------------------------------------- #
+def quantise_pack_torch(w, group: int, dtype: str, fmt: str = "awq", g_idx=None):
+    """The min/max writer of _quantise_minmax and the packers above, written with
+    torch ops so that it can run on the device: w is a float32 [K, N] tensor (on
+    any device), g_idx an int32 [K] tensor or None. Returns (qweight, qzeros,
+    scales) as torch tensors on w's device: int32 words in the AWQ or GPTQ
+    format and scales as the activation dtype. The rule and the word formats are
+    the numpy writer's; the two agree code for code on the same w."""
+    import torch
+    K, N = w.shape
+    G = K // group
+    if g_idx is None:
+        gk = torch.arange(K, device=w.device) // group
+        wg = w.view(G, group, N)
+    else:
+        gk = g_idx.long()
+        wg = w[torch.argsort(gk, stable=True)].view(G, group, N)
+    mn = wg.amin(dim=1)
+    mx = wg.amax(dim=1)
+    del wg
+    s32 = (mx - mn) / 15.0
+    s32 = torch.where(mx == mn, torch.ones_like(s32), s32)
+    sdt = torch.bfloat16 if dtype == BF16 else torch.float16
+    s_half = s32.to(sdt)                      # round to nearest even
+    s_eff = s_half.float()
+    z = torch.clamp(torch.round(-mn / s_eff), 0, 15)   # round half to even
+    q = torch.empty((K, N), dtype=torch.uint8, device=w.device)
+    step = max(1, (1 << 26) // max(N, 1))
+    for k0 in range(0, K, step):
+        k1 = min(K, k0 + step)
+        gg = gk[k0:k1]
+        v = torch.round(w[k0:k1] / s_eff[gg]) + z[gg]
+        q[k0:k1] = torch.clamp(v, 0, 15).to(torch.uint8)
+    z8 = z.to(torch.uint8)
+
+    def pack_rows(codes):                    # [K, N] -> [K/8, N]; row 8r+i at nibble i
+        R, C = codes.shape
+        blk = codes.view(R // 8, 8, C).to(torch.int64)
+        out = torch.zeros((R // 8, C), dtype=torch.int64, device=codes.device)
+        for i in range(8):
+            out |= blk[:, i, :] << (4 * i)
+        return _i64_to_i32_words(out)
+
+    if fmt == "awq":
+        if g_idx is not None:
+            raise ValueError("AWQ checkpoints carry no g_idx")
+        qweight = _pack_cols_chunked(q, AWQ_PACK_ORDER)
+        qzeros = _pack_cols_chunked(z8, AWQ_PACK_ORDER)
+    elif fmt == "gptq":
+        qweight = torch.cat([pack_rows(q[k0:k0 + 8192]) for k0 in range(0, K, 8192)])
+        qzeros = _pack_cols_chunked(z8, tuple(range(8)))
+    else:
+        raise ValueError(fmt)
+    return qweight, qzeros, s_half
+
+
+def _i64_to_i32_words(v):
+    """int64 tensor of values in [0, 2^32) -> int32 tensor of the same 32 bits."""
+    import torch
+    return torch.where(v >= (1 << 31), v - (1 << 32), v).to(torch.int32)
+
+
+def _pack_cols_chunked(codes, order):
+    """[R, C*8] uint8 codes -> [R, C] int32 words, column 8c+order[p] at nibble p
+    (in row chunks, to bound the int64 temporaries)."""
+    import torch
+    R, C8 = codes.shape
+    outs = []
+    step = max(1, (1 << 26) // max(C8, 1))
+    for r0 in range(0, R, step):
+        blk = codes[r0:r0 + step].reshape(-1, C8 // 8, 8).to(torch.int64)
+        out = torch.zeros(blk.shape[:2], dtype=torch.int64, device=codes.device)
+        for p, col in enumerate(order):
+            out |= blk[:, :, col] << (4 * p)
+        outs.append(_i64_to_i32_words(out))
+    return torch.cat(outs)
+
+
+def make_layer_torch(seed: int, K: int, N: int, group: int, dtype: str, fmt: str = "awq",
+                     act_order: bool = False, device="cuda", sigma: float = 0.02):
+    """A seeded synthetic layer drawn and quantised with torch on `device`:
+    W ~ N(0, sigma) in fp32 from torch.Generator(seed), g_idx (act-order) from a
+    seeded permutation as act_order_gidx does, then quantise_pack_torch. Returns
+    (qweight, qzeros, scales, g_idx or None) on `device`. The benchmark's large
+    layers come from here; the parity tests use the numpy writer."""
+    import torch
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    w = torch.randn((K, N), generator=gen, device=device, dtype=torch.float32)
+    w *= sigma
+    g_idx = None
+    if act_order:
+        P = torch.randperm(K, generator=gen, device=device)
+        g_idx = (P // group).to(torch.int32)
+    out = quantise_pack_torch(w, group, dtype, fmt, g_idx)
+    del w
+    return (*out, g_idx)

@@ -183,6 +183,35 @@ def test_dequant_bitexact(w4, K, N, group, dtype):
                               oracle.round_f64_to_half_bits(W_ref, dtype))
 
 
+@pytest.mark.parametrize("K,N,group,dtype", [(512, 272, 128, "fp16"), (1536, 64, 64, "bf16"),
+                                             (1024, 96, 32, "fp16")])
+def test_dequant_act_order_bitexact(w4, K, N, group, dtype):
+    """w4_dequant of an act-order layer: rows come out in stored (sorted) order,
+    so stored row j is the oracle's row perm[j], dequantised with its own group
+    g_idx[perm[j]] (= j / group); fp32 bit-exact, the activation dtype as one
+    rounding of it, in both layouts."""
+    import torch
+    L = synth.make_custom_layer([128, K, N], K, N, group=group, dtype=dtype, fmt="gptq",
+                                act_order=True)
+    q, z, s = oracle_codes(L)
+    perm_ref = oracle.act_order_perm(L.g_idx)
+    W_ref = oracle.dequant(q, z, s, oracle.group_of_rows(K, group, L.g_idx))[perm_ref]
+    for layout in (w4.W4_LAYOUT_STD, w4.W4_LAYOUT_TILE):
+        qw, zeros, scales, perm, status = repack(w4, L, layout)
+        assert status.cpu().numpy()[0] == 0
+        assert np.array_equal(perm.cpu().numpy(), perm_ref)
+        raw, w32 = guarded(K * N, torch.float32)
+        w4.w4_dequant(qw, scales, zeros, K, N, group, dtype, layout, 1, w32)
+        raw_h, wh = guarded(K * N, hdt(dtype))
+        w4.w4_dequant(qw, scales, zeros, K, N, group, dtype, layout, 0, wh)
+        torch.cuda.synchronize()
+        check_guards(raw, K * N, 4)
+        check_guards(raw_h, K * N, 2)
+        assert np.array_equal(w32.cpu().numpy().reshape(K, N), W_ref)
+        assert np.array_equal(half_from_dev(wh).reshape(K, N),
+                              oracle.round_f64_to_half_bits(W_ref, dtype))
+
+
 def run_gemm(w4, L, x_bits, layout_parts, M, group=None):
     import torch
     qw, zeros, scales, perm, _ = layout_parts
@@ -341,13 +370,14 @@ def test_symmetric_repack_dequant_gemm(w4, fmt, dtype, K, N, act_order, Ms):
     for layout in (w4.W4_LAYOUT_STD, w4.W4_LAYOUT_TILE):
         qw, zeros, scales, perm, _ = repack(w4, L, layout)
         assert np.array_equal(zeros.cpu().numpy().reshape(eights.shape), eights)
-        if act_order:
-            continue  # the dequant entry point reads rows in stored (sorted) order
         raw, w32 = guarded(K * N, torch.float32)
         w4.w4_dequant(qw, scales, zeros, K, N, 128, dtype, layout, 1, w32)
         torch.cuda.synchronize()
         check_guards(raw, K * N, 4)
-        W_ref = oracle.dequant(q, z, s, oracle.group_of_rows(K, 128))
+        W_ref = oracle.dequant(q, z, s, oracle.group_of_rows(K, 128, L.g_idx))
+        if act_order:
+            # w4_dequant returns the rows in stored order: stored row j is input row perm[j]
+            W_ref = W_ref[oracle.act_order_perm(L.g_idx)]
         assert np.array_equal(w32.cpu().numpy().reshape(K, N), W_ref)
     parts = repack(w4, L, w4.W4_LAYOUT_TILE)
     for M in Ms:
