@@ -19,7 +19,8 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_NAME = "libw4a16.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 
-SOURCES = ("w4a16_api.cu", "repack_kernels.cu", "decode_kernel.cu", "prefill_kernel.cu")
+SOURCES = ("w4a16_api.cu", "repack_kernels.cu", "decode_kernel.cu", "decode_stream_kernel.cu",
+           "prefill_kernel.cu")
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CXX_FLAGS = [

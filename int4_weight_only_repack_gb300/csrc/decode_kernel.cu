@@ -804,8 +804,13 @@ size_t decode_workspace_bytes(int M, int K, bool has_perm) {
 }
 
 cudaError_t launch_decode(const GemmArgs& a, cudaStream_t stream) {
+  // M <= 16 on a small layer (at most 96 KB of packed weights per SM), no
+  // experts: the streaming kernel (decode_stream_kernel.cu); otherwise this one
+  bool launched = false;
+  cudaError_t err = launch_decode_stream(a, stream, &launched);
+  if (err != cudaSuccess || launched) return err;
   DeviceInfo info;
-  cudaError_t err = device_info(&info);
+  err = device_info(&info);
   if (err != cudaSuccess) return err;
   int gshift = log2_exact(a.group);
   if (a.group == a.K || gshift < 0) gshift = 31;  // one group over all of K

@@ -41,6 +41,35 @@ namespace w4 {
 // Non-zero once a kernel of this library gave up on a wait (see w4_device_status).
 __device__ int g_device_status = 0;
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::mutex mu;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+bool encode_tile_box(CUtensorMap* map, const void* qw, int K, uint64_t NG, uint32_t box_tiles,
+                     uint32_t box_atoms, uint32_t box_groups) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return false;
+  const cuuint64_t A = (cuuint64_t)K / 64;
+  const cuuint64_t dims[4] = {128, 8, A, NG};
+  const cuuint64_t strides[3] = {512, 8 * 512, A * 8 * 512};
+  const cuuint32_t box[4] = {128, box_tiles, box_atoms, box_groups};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, const_cast<void*>(qw), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 namespace {
 
 using namespace sm100;
@@ -580,25 +609,10 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4* __rest
 }
 
 // ---- host side ------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static std::mutex mu;
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (fn == nullptr) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
 bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
                uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                CUtensorMapSwizzle swz) {
-  auto fn = encode_fn();
+  auto fn = tensor_map_encoder();
   if (!fn) return false;
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {row_bytes};
@@ -613,16 +627,7 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint6
 // groups): one box is the 8 atoms of `box_groups` consecutive column groups at
 // one k-atom.
 bool encode_tile_4d(CUtensorMap* map, const void* qw, int K, uint64_t NG, uint32_t box_groups) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t A = (cuuint64_t)K / 64;
-  const cuuint64_t dims[4] = {128, 8, A, NG};
-  const cuuint64_t strides[3] = {512, 8 * 512, A * 8 * 512};
-  const cuuint32_t box[4] = {128, 8, 1, box_groups};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, const_cast<void*>(qw), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_tile_box(map, qw, K, NG, 8, 1, box_groups);
 }
 
 cudaError_t ensure_prefill_smem(void* fn, int which, int bytes) {

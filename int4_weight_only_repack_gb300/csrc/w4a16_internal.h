@@ -1,6 +1,8 @@
 // Internal declarations shared by the library's translation units (host side).
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -56,6 +58,10 @@ struct GemmArgs {
 // every CTA gathers its own slice of x.
 constexpr int DECODE_MAX_M = 64;
 cudaError_t launch_decode(const GemmArgs& a, cudaStream_t s);
+// The streaming small-M kernel (M <= 16, layers of at most 96 KB of packed
+// weights per SM, no grouped call): *launched says whether it took the call;
+// when it did not, launch_decode runs the clustered kernel instead.
+cudaError_t launch_decode_stream(const GemmArgs& a, cudaStream_t s, bool* launched);
 size_t decode_workspace_bytes(int M, int K, bool has_perm);
 
 // xg[m][j] = x[m][perm[j]] for M rows of K (16-byte aligned, K % 64 == 0),
@@ -93,6 +99,13 @@ cudaError_t noalloc_scratch(void** out, size_t* bytes);
 // units, which take it as a parameter.
 cudaError_t read_device_status(int* out, int clear);
 cudaError_t device_status_ptr(int** out);
+
+// cuTensorMapEncodeTiled from the driver (looked up once), and a map over TILE
+// words viewed as [column group][k-atom][tile in group][word] (NG column
+// groups) whose box is box_tiles tiles x box_atoms k-atoms x box_groups groups.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+bool encode_tile_box(CUtensorMap* map, const void* qw, int K, uint64_t NG, uint32_t box_tiles,
+                     uint32_t box_atoms, uint32_t box_groups);
 
 // Device properties cached per device.
 struct DeviceInfo {
