@@ -1,5 +1,5 @@
-"""CPU oracle for the INT4-weight x FP8-activation form of the layer (not built
-in the kernels yet; this module fixes what such a kernel must compute).
+"""CPU oracle for the INT4-weight x FP8-activation form of the layer: what the
+tcgen05 kind::f8f6f4 kernel (w4a8_gemm) must compute.
 
 TEST INFRASTRUCTURE ONLY, like the rest of `oracle/`: only the test suite, the
 smoke check and the benchmark's CPU arm may import it; it shares no code with
@@ -20,6 +20,10 @@ dynamic). Everything else below is a reading, written out as the definition:
     exactly: the "scales x 512".
   * Activations: dynamic per-tensor scaling, s_x = max|x| / 448 (1 when x is
     all zero), x8 = e4m3(x / s_x) rounded to nearest even and saturated at 448.
+    The pages leave the precision of this step open; since it decides integer
+    codes, it is taken in the kernel's precision: s_x = RN_fp32(max|x| / 448)
+    and x / s_x as one fp32 division rounded to nearest (max|x| is exact in
+    fp32, being an fp16 / bf16 value), then rounded to e4m3.
   * y[m, n] = s_x * sum_k x8[m, k] * W[k, n], in fp64 here.
 """
 from __future__ import annotations
@@ -81,11 +85,14 @@ def int4_diff_to_e4m3(v) -> np.ndarray:
 
 
 def quantize_act_per_tensor(x: np.ndarray):
-    """Dynamic per-tensor fp8 activations: (codes, s_x) with s_x = max|x|/448."""
-    x = np.asarray(x, dtype=np.float64)
-    amax = float(np.max(np.abs(x))) if x.size else 0.0
-    s_x = amax / E4M3_MAX if amax > 0 else 1.0
-    return e4m3_round(x / s_x), s_x
+    """Dynamic per-tensor fp8 activations: (codes, s_x) with s_x = max|x|/448,
+    both divisions in fp32 rounded to nearest (x holds fp16 / bf16 values, exact
+    in fp32); s_x is returned as the fp32 value (in a float64)."""
+    x32 = np.asarray(x, dtype=np.float64).astype(np.float32)
+    amax = np.float32(np.max(np.abs(x32))) if x32.size else np.float32(0.0)
+    s_x = amax / np.float32(E4M3_MAX) if amax > 0 else np.float32(1.0)
+    q = (x32 / s_x).astype(np.float64)
+    return e4m3_round(q), float(s_x)
 
 
 def reference_y_w4a8(x_bits, qweight, qzeros, scales_bits, group: int, dtype: str,

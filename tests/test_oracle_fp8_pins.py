@@ -81,6 +81,28 @@ def test_e4m3_round_matches_torch_in_range():
     assert np.array_equal(f8.e4m3_decode(mine), f8.e4m3_decode(t))
 
 
+def test_activation_quantisation_in_fp32_matches_torch():
+    """The per-tensor quantisation takes its decisions in fp32: s_x is the fp32
+    quotient max|x| / 448 and every code is the e4m3 rounding of the fp32
+    quotient x / s_x, as torch computes them (fp32 tensors, float8_e4m3fn)."""
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("no float8_e4m3fn in this torch")
+    xb = synth.make_custom_x(67, 16, 512, "bf16")
+    codes, s_x = f8.quantize_act_per_tensor(oracle.half_bits_to_f64(xb, "bf16"))
+    xt = torch.from_numpy(synth.bits_to_f32(xb, "bf16"))
+    st = xt.abs().max() / torch.tensor(448.0, dtype=torch.float32)
+    assert np.float32(s_x) == st.item()
+    q = xt / st
+    keep = (q.abs() < 448.0).numpy()  # torch does not saturate; compare inside the range
+    t = q.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(f8.e4m3_decode(codes)[keep], f8.e4m3_decode(t)[keep])
+    # the decision differs from an fp64 one somewhere on a large enough input
+    # only through the quotients' rounding: both lie within one e4m3 step
+    q64 = oracle.half_bits_to_f64(xb, "bf16") / (np.max(np.abs(oracle.half_bits_to_f64(xb, "bf16"))) / 448.0)
+    assert np.max(np.abs(f8.e4m3_decode(codes) - f8.e4m3_decode(f8.e4m3_round(q64)))) <= 32.0
+
+
 def test_int4_weights_in_e4m3_are_exact():
     """(q - z) * 2^-9 is exact in e4m3 for every difference of two 4-bit codes,
     and with the scale times 512 it gives W = (q - z) * s exactly."""
