@@ -319,6 +319,35 @@ W4_API w4_status w4a16_gemm_noalloc(const void* x, const int32_t* qw, const void
                                     int N, int K, int group, int dtype, void* stream);
 
 /*
+ * INT4 weights x FP8 activations ("量化层加载:AWQ / GPTQ / Marlin / fp8",
+ * 边界与失败: with float8_e4m3fn activations the 4-bit weights are
+ * preprocessed and the scales multiplied by 512; 职责: Fp8Config's
+ * per-tensor dynamic activation scheme; the SGLang W4AFp8 article, §五: INT4
+ * weights against FP8 activations in one GEMM).
+ *   y[m][n] = s_x * sum_k x8[m][k] * W[k][n],  W = (q - z) * s,
+ * where the activations are quantised per tensor on the device: s_x =
+ * RN_fp32(max|x| / 448) (1 when x is all zero) and x8 = e4m3(RN_fp32(x / s_x)),
+ * rounded to nearest even and saturated at 448 (float8_e4m3fn). The weights
+ * enter the MMA as the e4m3 numbers q * 2^-9 (exact for every 4-bit code) and
+ * each group's partial sum is taken back to W with 512 s and the zero point:
+ * (512 s) * sum x8 q 2^-9 - (z s) * sum x8. Accumulation is fp32; y is rounded
+ * once to dtype.
+ *   x [M][K] and y [M][N] in dtype; qw / scales / zeros from w4_repack_awq or
+ *   w4_repack_gptq in the TILE layout, without act-order.
+ *   group: 128 or -1 (one group over all of K); other groups -> W4_ERR_GROUP.
+ *   K % 128 == 0 and N % 32 == 0 (else W4_ERR_SHAPE).
+ *   workspace: at least w4a8_gemm_workspace_size(M, K) bytes (the fp8
+ *   activations, their per-group sums and s_x; no initialisation needed),
+ *   else W4_ERR_WORKSPACE; it must not overlap x or y.
+ * Ordering: three kernels in stream order (programmatic dependent launch);
+ * none of them reads the weights before the kernel before it has finished.
+ */
+W4_API size_t w4a8_gemm_workspace_size(int M, int K);
+W4_API w4_status w4a8_gemm(const void* x, const int32_t* qw, const void* scales,
+                           const int32_t* zeros, void* y, int M, int N, int K, int group,
+                           int dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Read the library's device status word: W4_OK, or W4_ERR_TIMEOUT once some
  * kernel of this library gave up on an internal pipeline wait (every such wait
  * is bounded at one second; the kernel then drains its own copies, frees its

@@ -19,7 +19,7 @@ __all__ = [
     "W4_F16", "W4_BF16", "W4_LAYOUT_STD", "W4_LAYOUT_TILE", "W4Error", "lib", "library_path",
     "dtype_code", "w4_status_string", "w4_last_cuda_error", "w4_abi_version", "w4_repack_sizes", "w4_repack_awq",
     "w4_repack_gptq", "w4a16_gemm_workspace_size", "w4a16_gemm", "w4a16_gemm_bias",
-    "w4a16_gemm_noalloc",
+    "w4a16_gemm_noalloc", "w4a8_gemm_workspace_size", "w4a8_gemm", "linear_fp8",
     "w4_dequant", "gemm_workspace",
     "w4_device_status", "w4_test_stalled_gemm",
     "RepackedLayer", "repack_awq", "repack_gptq", "linear", "w4a16_moe_gemm", "RepackedExperts",
@@ -66,6 +66,9 @@ _SIGNATURES = {
     "w4a16_gemm_noalloc": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                                     _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int,
                                     _c_void_p]),
+    "w4a8_gemm_workspace_size": (_c_size, [_c_int, _c_int]),
+    "w4a8_gemm": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_int,
+                           _c_int, _c_int, _c_int, _c_int, _c_void_p, _c_size, _c_void_p]),
 }
 
 
@@ -255,6 +258,19 @@ def w4a16_gemm_noalloc(x, qw, scales, zeros, perm, y, M, N, K, group, dtype, str
                                     _ptr(y), M, N, K, group, dtype_code(dtype), _stream(stream)))
 
 
+def w4a8_gemm_workspace_size(M, K) -> int:
+    return lib().w4a8_gemm_workspace_size(M, K)
+
+
+def w4a8_gemm(x, qw, scales, zeros, y, M, N, K, group, dtype, workspace, workspace_bytes=None,
+              stream=None):
+    """INT4 weights x per-tensor FP8 activations (quantised on the device)."""
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().w4a8_gemm(_ptr(x), _ptr(qw), _ptr(scales), _ptr(zeros), _ptr(y), M, N, K, group,
+                           dtype_code(dtype), _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
 def w4_device_status(clear: bool = False) -> int:
     v = ctypes.c_int32(0)
     _check(lib().w4_device_status(ctypes.byref(v), int(bool(clear))))
@@ -355,6 +371,22 @@ def _workspace_size_cached(M, layer: RepackedLayer, device) -> int:
             _WS_SIZES.clear()
         _WS_SIZES[key] = need
     return need
+
+
+def linear_fp8(x, layer: RepackedLayer, y=None, workspace=None, stream=None):
+    """y = x · W with the activations quantised per tensor to e4m3 on the device
+    and the product on the fp8 tensor cores (w4a8_gemm); layer without act-order,
+    group 128 or -1."""
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, layer.N), dtype=x.dtype, device=x.device)
+    if M == 0:
+        return y
+    if workspace is None:
+        workspace = gemm_workspace(w4a8_gemm_workspace_size(M, layer.K), x.device, stream)
+    w4a8_gemm(x, layer.qw, layer.scales, layer.zeros, y, M, layer.N, layer.K, layer.group,
+              layer.dtype, workspace, None, stream)
+    return y
 
 
 def linear(x, layer: RepackedLayer, y=None, workspace=None, stream=None, bias=None):

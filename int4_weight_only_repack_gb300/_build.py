@@ -20,7 +20,7 @@ LIB_NAME = "libw4a16.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 
 SOURCES = ("w4a16_api.cu", "repack_kernels.cu", "decode_kernel.cu", "decode_stream_kernel.cu",
-           "prefill_kernel.cu")
+           "prefill_kernel.cu", "w4a8_kernel.cu")
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CXX_FLAGS = [

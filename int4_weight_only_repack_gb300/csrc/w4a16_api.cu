@@ -431,6 +431,43 @@ w4_status w4a16_gemm_noalloc(const void* x, const int32_t* qw, const void* scale
                     stream);
 }
 
+size_t w4a8_gemm_workspace_size(int M, int K) {
+  if (M < 1 || K < 1 || K > MAX_DIM || M > MAX_DIM || K % 128) return 0;
+  return w4a8_workspace_bytes(M, K);
+}
+
+w4_status w4a8_gemm(const void* x, const int32_t* qw, const void* scales, const int32_t* zeros,
+                    void* y, int M, int N, int K, int group, int dtype, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  w4_status st = check_dims(K, N, group, dtype);
+  if (st) return st;
+  if (M < 0 || M > MAX_DIM) return W4_ERR_SHAPE;
+  if ((st = check_layout_dims(K, N, W4_LAYOUT_TILE))) return st;
+  if (group != 128 && group != -1) return W4_ERR_GROUP;
+  if (K % 128 || N % 32) return W4_ERR_SHAPE;  // whole K blocks; zero rows of 16-byte multiples
+  if (!qw || !scales || !zeros) return W4_ERR_NULL;
+  if (M > 0 && (!x || !y || !workspace)) return W4_ERR_NULL;
+  if (!aligned16(x) || !aligned16(qw) || !aligned16(scales) || !aligned16(zeros) ||
+      !aligned16(y) || !aligned16(workspace))
+    return W4_ERR_ALIGN;
+  if (M == 0) return W4_OK;
+  if (workspace_bytes < w4a8_workspace_bytes(M, K)) return W4_ERR_WORKSPACE;
+  const int g = resolve_group(group, K);
+  const size_t G = (size_t)K / g;
+  const size_t y_b = (size_t)M * N * 2;
+  size_t qw_b = 0;
+  w4_repack_sizes(K, N, group, W4_LAYOUT_TILE, &qw_b, nullptr, nullptr);
+  const void* ins[5] = {x, qw, scales, zeros, workspace};
+  const size_t in_b[5] = {(size_t)M * K * 2, qw_b, G * N * 2, G * N / 2, workspace_bytes};
+  for (int j = 0; j < 5; ++j)
+    if (overlaps(y, y_b, ins[j], in_b[j])) return W4_ERR_ALIAS;
+  if (overlaps(workspace, workspace_bytes, x, (size_t)M * K * 2)) return W4_ERR_ALIAS;
+  if ((st = check_arch())) return st;
+  return from_cuda(launch_w4a8(x, reinterpret_cast<const uint32_t*>(qw), scales,
+                               reinterpret_cast<const uint32_t*>(zeros), y, M, N, K, g,
+                               dtype == W4_BF16, workspace, static_cast<cudaStream_t>(stream)));
+}
+
 w4_status w4_dequant(const int32_t* qw, const void* scales, const int32_t* zeros, int K, int N,
                      int group, int dtype, int layout, int out_f32, void* w_out, void* stream) {
   w4_status st = check_dims(K, N, group, dtype);

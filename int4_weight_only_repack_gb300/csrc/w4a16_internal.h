@@ -90,6 +90,14 @@ size_t prefill_workspace_bytes(int M, int K, bool has_perm);
 size_t prefill_split_workspace_bytes(int M, int N, int K);
 cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t s);
 
+// INT4 weights x FP8 activations (w4a8_gemm): workspace bytes for M x K
+// activations, and the launch (activation quantisation, then the tcgen05
+// kind::f8f6f4 GEMM; group is 128 or K).
+size_t w4a8_workspace_bytes(int M, int K);
+cudaError_t launch_w4a8(const void* x, const uint32_t* qw, const void* scales,
+                        const uint32_t* zeros, void* y, int M, int N, int K, int group, int bf16,
+                        void* workspace, cudaStream_t stream);
+
 // Device address and size of the static scratch array of w4a16_gemm_noalloc
 // (looked up once per device, with that device current).
 cudaError_t noalloc_scratch(void** out, size_t* bytes);

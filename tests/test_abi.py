@@ -254,3 +254,30 @@ def test_binding_matches_header():
             assert res in (ctypes.c_int, ctypes.c_int32), name
         else:
             assert ret == "size_t" and res is ctypes.c_size_t, (name, ret)
+
+
+def _w4a8(lib, x=FAKE, qw=FAKE * 2, sc=FAKE * 3, z=FAKE * 4, y=FAKE * 5, M=4, N=256, K=256,
+          group=128, dtype=1, ws=FAKE * 6, ws_b=1 << 20):
+    import int4_weight_only_repack_gb300 as w4
+    w4.lib()
+    return lib.w4a8_gemm(x, qw, sc, z, y, M, N, K, group, dtype, ws, ws_b, None)
+
+
+def test_w4a8_gemm_rejects(lib):
+    """w4a8_gemm's host checks: group 128 or -1 only, K % 128, the workspace
+    size and presence, alignment, aliasing; M == 0 is a no-op."""
+    import int4_weight_only_repack_gb300 as w4
+    w4.lib()
+    assert _w4a8(lib, group=64) == W4_ERR_GROUP
+    assert _w4a8(lib, group=32) == W4_ERR_GROUP
+    assert _w4a8(lib, K=320, group=64) == W4_ERR_GROUP
+    assert _w4a8(lib, K=384 + 64, group=-1) == W4_ERR_SHAPE      # K % 128
+    assert _w4a8(lib, N=272) == W4_ERR_SHAPE                      # N % 32
+    assert _w4a8(lib, ws=None) == W4_ERR_NULL
+    assert _w4a8(lib, ws_b=16) == W4_ERR_WORKSPACE
+    assert _w4a8(lib, x=FAKE + 8) == W4_ERR_ALIGN
+    assert _w4a8(lib, y=FAKE * 6) == W4_ERR_ALIAS                 # y on the workspace
+    assert _w4a8(lib, M=0, x=None, y=None, ws=None) == W4_OK
+    assert _w4a8(lib, dtype=3) == W4_ERR_DTYPE
+    assert w4.w4a8_gemm_workspace_size(4, 256) >= 4 * 256
+    assert w4.w4a8_gemm_workspace_size(4, 320) == 0
