@@ -62,11 +62,12 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_TC_TFLOPS = 1900.0
 L2_ROTATION = 3.0                      # weight copies per timing loop: at least 3x L2
 
-# DRAM bytes per launch of the decode kernel from ncu (dram__bytes_read.sum +
-# dram__bytes_write.sum), keyed by the sha1 of the kernel source they were
-# taken on; see profiles/. A changed kernel source reports null.
+# DRAM bytes per launch of the small-M kernels from ncu (dram__bytes_read.sum +
+# dram__bytes_write.sum, the mean over the 12 launches of one step), keyed by
+# the sha1 of the kernels' sources they were taken on (kernel_source_hash);
+# see profiles/. A changed kernel source reports null.
 TRAFFIC_RECORDS: dict = {
-    "c33dd14b5051": 26437227,   # mean of the 12 launches of one step
+    "cea0fb5f0cd8": 26432235,   # mean of the 12 launches of one step (9 clustered, 3 streaming)
 }
 
 
@@ -75,10 +76,13 @@ def alg_bytes(K: int, N: int, group: int = 128) -> int:
     return K * N // 2 + G * N * 2 + G * N // 2
 
 
-def kernel_source_hash(name: str = "decode_kernel.cu") -> str:
-    p = os.path.join(ROOT, "int4_weight_only_repack_gb300", "csrc", name)
-    with open(p, "rb") as f:
-        return hashlib.sha1(f.read()).hexdigest()[:12]
+def kernel_source_hash(names=("decode_kernel.cu", "decode_stream_kernel.cu")) -> str:
+    """sha1 (first 12 hex digits) of the small-M kernels' sources, in order."""
+    h = hashlib.sha1()
+    for name in names:
+        with open(os.path.join(ROOT, "int4_weight_only_repack_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
 
 
 def _peaks():
@@ -422,6 +426,53 @@ def config_records(w4, torch, device, cfg, hbm, tc, with_dense_from=None, with_o
     return out
 
 
+def w4a8_records(w4, torch, device, tc, with_oracle=True, reps=10):
+    """INT4 weights x per-tensor FP8 activations (w4a8_gemm, tcgen05 kind::f8f6f4)
+    on the Llama-2-7B prefill layers at M in {512, 2048, 4096}: TFLOP/s against
+    the dense fp8 peak (the measured bf16 peak x 2, the nominal fp8 / bf16
+    ratio), beside the W4A16 tcgen05 kernel on the same call and the FP8 oracle
+    on a sample of the call."""
+    import oracle
+    from oracle import fp8_oracle as f8
+    fp8_peak = 2.0 * tc
+    out = []
+    wl = synth.WORKLOADS[2]
+    for li, (K, N, name) in enumerate(wl.shapes):
+        pool = LayerPool(w4, torch, device, 2, li, 2)
+        for M in wl.ms:
+            x = torch.randn(M, K, device=device).to(torch.bfloat16)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+            ws = torch.empty(w4.w4a8_gemm_workspace_size(M, K), dtype=torch.uint8, device=device)
+
+            def f8call():
+                for l in pool.copies:
+                    w4.linear_fp8(x, l, y=y, workspace=ws)
+
+            t = graph_time_reps(torch, f8call, reps) / len(pool.copies)
+            t16 = call_time(w4, torch, pool, x, y, None, reps)
+            tfl = 2.0 * M * N * K / t / 1e12
+            rec = {"layer": name, "K": K, "N": N, "M": M, "us": round(t * 1e6, 2),
+                   "tflops": round(tfl, 1), "frac_fp8_peak": round(tfl / fp8_peak, 4),
+                   "w4a16_us": round(t16 * 1e6, 2),
+                   "note": "includes the two activation-quantisation kernels"}
+            if with_oracle:
+                rows = min(M, 64)
+                xb = synth.make_custom_x([9, 2, K, rows], rows, K, "bf16")
+                t0 = time.perf_counter()
+                f8.reference_y_w4a8(xb, pool.h_qweight, pool.h_qzeros, pool.h_scales, 128, "bf16")
+                el = time.perf_counter() - t0
+                tor = el * (N / pool.sample_cols) * (M / rows)
+                rec["oracle_tflops"] = round(2.0 * M * N * K / tor / 1e12, 6)
+                rec["oracle_sample"] = f"{pool.sample_cols} of {N} columns x {rows} of {M} rows, extrapolated"
+            out.append(rec)
+            del x, y, ws
+        del pool
+        torch.cuda.empty_cache()
+    return {"workload": "llama2_7b_prefill layers, bf16 activations quantised per tensor to e4m3",
+            "peak": {"fp8_tflops": fp8_peak, "source": "measured bf16 dense peak x 2 (nominal fp8/bf16)"},
+            "per_call": out}
+
+
 def repack_measure(w4, torch, device, reps=5):
     """Throughput of the one-time AWQ -> TILE repack on the Llama-2-70B gate_up
     layer (K 8192, N 57344): bytes read (qweight, qzeros, scales) + written
@@ -627,6 +678,10 @@ def ours(args):
                                 "frac": round(flops / tsum / 1e12 / tc, 4),
                                 "peak_source": tc_src, "kernel": "w4a16_prefill_kernel"}}
 
+    w4a8 = None
+    if world == 1 and not args.no_configs:
+        w4a8 = w4a8_records(w4, torch, device, tc, with_oracle=rank == 0 and not args.no_cpu_baseline)
+
     moe_part = None
     if world == 1 and not args.no_moe:
         moe_part = {"workload": "mixtral_8x7b_shaped experts (8; w13 4096->28672, w2 "
@@ -693,6 +748,7 @@ def ours(args):
             "roofline_peaks": {"hbm_gbs": hbm, "bf16_tflops": tc, "source": hbm_src,
                                "ridge_M": round(tc * 1e12 / (4 * hbm * 1e9), 1),
                                "note": "fp16 calls use the bf16 figure (the same dense rate)"},
+            "w4a8": w4a8,
             "moe": moe_part,
             "repack": repack,
         }
@@ -754,7 +810,9 @@ def reference(args):
 
 
 def single(args):
-    """One GEMM call shape repeated `--steps` times (for profiler captures)."""
+    """One call shape repeated `--steps` times (for profiler captures):
+    --single K,N,M[,dtype[,fp8]]; fp8 runs w4a8_gemm instead of w4a16_gemm. The
+    layer is repacked once (AWQ -> TILE) before the calls."""
     import torch
 
     import int4_weight_only_repack_gb300 as w4
@@ -762,22 +820,25 @@ def single(args):
     parts = args.single.split(",")
     K, N, M = int(parts[0]), int(parts[1]), int(parts[2])
     dtype = parts[3] if len(parts) > 3 else "bf16"
+    fp8 = len(parts) > 4 and parts[4] == "fp8"
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
     dev = torch.device("cuda")
-    L = synth.make_custom_layer([5, K, N], K, N, group=128, dtype=dtype)
-    layer = w4.repack_awq(torch.from_numpy(L.qweight).to(dev), torch.from_numpy(L.qzeros).to(dev),
-                          torch.from_numpy(L.scales.view(np.int16)).to(dev).view(tdt), K, N, 128, tdt)
-    x = torch.from_numpy(synth.make_custom_x([6, M, K], M, K, dtype).view(np.int16)).to(dev).view(tdt)
+    qweight, qzeros, scales, _ = synth.make_layer_torch(5, K, N, 128, dtype, device=dev)
+    layer = w4.repack_awq(qweight, qzeros, scales, K, N, 128, tdt)
+    x = torch.randn(M, K, device=dev).to(tdt)
     y = torch.empty((M, N), dtype=tdt, device=dev)
+    fn = (lambda: w4.linear_fp8(x, layer, y=y)) if fp8 else (lambda: w4.linear(x, layer, y=y))
+    fn()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(args.steps):
-        w4.linear(x, layer, y=y)
+        fn()
     e1.record()
     torch.cuda.synchronize()
     t = e0.elapsed_time(e1) * 1e-3 / max(1, args.steps)
-    print(json.dumps({"single": [K, N, M, dtype], "us_per_call": round(t * 1e6, 2),
+    print(json.dumps({"single": [K, N, M, dtype, "fp8" if fp8 else "w4a16"],
+                      "us_per_call": round(t * 1e6, 2),
                       "weight_gbs": round(alg_bytes(K, N) / t / 1e9, 1),
                       "tflops": round(2.0 * M * N * K / t / 1e12, 2),
                       "device_status": w4.w4_device_status()}), flush=True)

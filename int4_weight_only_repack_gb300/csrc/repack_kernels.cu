@@ -98,6 +98,124 @@ __global__ void __launch_bounds__(BLOCK_THREADS) to_tile_kernel(
   }
 }
 
+
+// ---- vectorised repacks into the TILE layout (no act-order) ---------------------
+// One block per (128-column group, 64-row k-atom): the source block is read with
+// 16-byte loads into shared memory, turned into the group's 1024 TILE words in
+// registers, and leaves as 4 KB of 16-byte stores. Requires N % 32 == 0 (whole
+// 16-byte source pieces); a partial last group gets zero words.
+// The permutation {0, 2, 4, 6, 1, 3, 5, 7}: nibble p of an AWQ word holds column
+// sigma(p) of its block, and nibble p of a TILE word holds row sigma(p).
+__host__ __device__ constexpr int sigma(int p) { return p < 4 ? 2 * p : 2 * (p - 4) + 1; }
+
+// Word index, inside a column group's eight atoms at one k-atom, of the TILE
+// word holding column cl (0..127 in the group) and rows 8 r .. 8 r + 7 (r 0..7).
+__device__ __forceinline__ int tile_word_index(int cl, int r) {
+  const int tt = cl >> 4, c16 = cl & 15;
+  return tt * 128 + 4 * (4 * (c16 & 7) + (r & 3)) + 2 * (r >> 2) + (c16 >> 3);
+}
+
+// In-register transpose of an 8 x 8 nibble matrix (w[i] nibble p <-> w[p] nibble i).
+__device__ __forceinline__ void transpose8x8_nibbles(uint32_t (&w)[8]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {  // 4 x 4 blocks
+    const uint32_t t = ((w[i] >> 16) ^ w[i + 4]) & 0x0000FFFFu;
+    w[i] ^= t << 16;
+    w[i + 4] ^= t;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; i += (i & 1) ? 3 : 1) {  // 2 x 2 blocks: pairs (0,2) (1,3) (4,6) (5,7)
+    const uint32_t t = ((w[i] >> 8) ^ w[i + 2]) & 0x00FF00FFu;
+    w[i] ^= t << 8;
+    w[i + 2] ^= t;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; i += 2) {  // single nibbles
+    const uint32_t t = ((w[i] >> 4) ^ w[i + 1]) & 0x0F0F0F0Fu;
+    w[i] ^= t << 4;
+    w[i + 1] ^= t;
+  }
+}
+
+// AWQ qweight [K][N/8] -> TILE. Word (k, c) of AWQ holds column 8c + sigma(p) at
+// nibble p (the order {0,4,1,5,2,6,3,7} read backwards), and a TILE word holds
+// row 8r + sigma(p) at nibble p: taking the eight rows in sigma order makes the
+// repack a plain nibble transpose whose word q is column 8c + sigma(q).
+template <int KA>
+__global__ void __launch_bounds__(256) awq_to_tile_vec_kernel(const uint32_t* __restrict__ qweight,
+                                                              uint32_t* __restrict__ out, int K,
+                                                              int N) {
+  // KA k-atoms per CTA: every thread has KA 16-byte loads in flight
+  __shared__ uint32_t in_s[KA * 64][17];
+  __shared__ __align__(16) uint32_t out_s[KA][1024];
+  const int cg = blockIdx.x, a0 = blockIdx.y * KA;
+  const int C = N / 8, A = K / 64;
+  const int ncw = min(16, C - cg * 16);  // column words of this group present (a multiple of 4)
+  {
+    const int row = threadIdx.x >> 2, q4 = threadIdx.x & 3;
+    uint4 v[KA];
+#pragma unroll
+    for (int u = 0; u < KA; ++u) {
+      v[u] = make_uint4(0, 0, 0, 0);
+      if (4 * q4 < ncw)
+        v[u] = *reinterpret_cast<const uint4*>(qweight + (size_t)(64 * (a0 + u) + row) * C +
+                                               16 * cg + 4 * q4);
+    }
+#pragma unroll
+    for (int u = 0; u < KA; ++u) {
+      in_s[64 * u + row][4 * q4] = v[u].x;
+      in_s[64 * u + row][4 * q4 + 1] = v[u].y;
+      in_s[64 * u + row][4 * q4 + 2] = v[u].z;
+      in_s[64 * u + row][4 * q4 + 3] = v[u].w;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < 128 * KA) {
+    const int u = threadIdx.x >> 7, c = threadIdx.x & 15, r = (threadIdx.x >> 4) & 7;
+    uint32_t w[8];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) w[p] = in_s[64 * u + 8 * r + sigma(p)][c];
+    transpose8x8_nibbles(w);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) out_s[u][tile_word_index(8 * c + sigma(q), r)] = w[q];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int u = 0; u < KA; ++u) {
+    uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)cg * A + a0 + u) * 8 * 128);
+    dst[threadIdx.x] = reinterpret_cast<const uint4*>(out_s[u])[threadIdx.x];
+  }
+}
+
+// Standard qweight [K/8][N] (row 8r + e at nibble e) -> TILE (row 8r + e at
+// nibble {0,4,1,5,2,6,3,7}[e]): a nibble shuffle per word, even rows to the low
+// half and odd rows to the high half.
+__global__ void __launch_bounds__(256) std_to_tile_vec_kernel(const uint32_t* __restrict__ src,
+                                                              uint32_t* __restrict__ out, int K,
+                                                              int N) {
+  __shared__ __align__(16) uint32_t out_s[1024];
+  const int cg = blockIdx.x, a = blockIdx.y;
+  const int A = K / 64;
+  const int ncols = min(128, N - cg * 128);
+  // thread: row word r = t / 32 (0..7), columns 4 (t % 32) .. + 3
+  const int r = threadIdx.x >> 5, c4 = (threadIdx.x & 31) * 4;
+  uint4 v = make_uint4(0, 0, 0, 0);
+  if (c4 < ncols)
+    v = *reinterpret_cast<const uint4*>(src + (size_t)(8 * a + r) * N + 128 * cg + c4);
+  const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t ev = in[j] & 0x0F0F0F0Fu, od = (in[j] >> 4) & 0x0F0F0F0Fu;
+    const uint32_t ev2 = ev | (ev >> 4), od2 = od | (od >> 4);
+    uint32_t o;
+    asm("prmt.b32 %0, %1, %2, 0x6420;" : "=r"(o) : "r"(ev2), "r"(od2));
+    out_s[tile_word_index(c4 + j, r)] = o;
+  }
+  __syncthreads();
+  uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)cg * A + a) * 8 * 128);
+  dst[threadIdx.x] = reinterpret_cast<const uint4*>(out_s)[threadIdx.x];
+}
+
 // AWQ qweight [K][N/8] -> standard [K/8][N]: an 8 x 8 nibble transpose per thread.
 __global__ void __launch_bounds__(BLOCK_THREADS) awq_to_std_kernel(
     const uint32_t* __restrict__ qweight, uint32_t* __restrict__ out, int K, int N) {
@@ -273,6 +391,19 @@ cudaError_t launch_awq_to_std(const int32_t* qweight, int32_t* qw_out, int K, in
 cudaError_t launch_to_tile(const int32_t* src, int src_is_awq, const int32_t* perm,
                            int32_t* qw_out, int K, int N, cudaStream_t s) {
   dim3 grid((N + BN - 1) / BN, K / BK);
+  if (perm == nullptr && N % 32 == 0) {
+    // whole 16-byte source pieces: the vectorised repacks
+    if (src_is_awq && (K / BK) % 2 == 0)
+      awq_to_tile_vec_kernel<2><<<dim3(grid.x, grid.y / 2), 256, 0, s>>>(
+          reinterpret_cast<const uint32_t*>(src), reinterpret_cast<uint32_t*>(qw_out), K, N);
+    else if (src_is_awq)
+      awq_to_tile_vec_kernel<1><<<grid, 256, 0, s>>>(reinterpret_cast<const uint32_t*>(src),
+                                                     reinterpret_cast<uint32_t*>(qw_out), K, N);
+    else
+      std_to_tile_vec_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint32_t*>(src),
+                                                  reinterpret_cast<uint32_t*>(qw_out), K, N);
+    return cudaGetLastError();
+  }
   to_tile_kernel<<<grid, BLOCK_THREADS, 0, s>>>(reinterpret_cast<const uint32_t*>(src),
                                                  src_is_awq ? SRC_AWQ : SRC_STD, perm,
                                                  reinterpret_cast<uint32_t*>(qw_out), K, N);

@@ -596,3 +596,15 @@ def test_gemm_large_m_deterministic(w4):
     parts = repack(w4, L, w4.W4_LAYOUT_TILE)
     x = synth.make_custom_x([120], M, K, "bf16")
     assert np.array_equal(run_gemm(w4, L, x, parts, M), run_gemm(w4, L, x, parts, M))
+
+
+@pytest.mark.parametrize("K,N,fmt", [(320, 256, "awq"), (256, 288, "awq"), (1024, 384, "awq"),
+                                     (320, 256, "gptq"), (512, 416, "gptq")])
+def test_vectorised_tile_repack_bitexact(w4, K, N, fmt):
+    """The vectorised TILE repacks (N % 32 == 0, no act-order): one or two
+    k-atoms per CTA (an odd k-atom count takes one), a partial last column
+    group, AWQ and standard sources: bit-exact with the oracle's tile packer."""
+    L = synth.make_custom_layer([129, K, N], K, N, group=64, dtype="bf16", fmt=fmt)
+    qw, zeros, scales, _, _ = repack(w4, L, w4.W4_LAYOUT_TILE)
+    q, _, _ = oracle_codes(L)
+    assert np.array_equal(qw.cpu().numpy(), oracle.tile_pack(q))
