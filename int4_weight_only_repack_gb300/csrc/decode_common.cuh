@@ -47,6 +47,28 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
   return pol;
 }
 
+// 16-byte read-only load of activations (allocated in L1: the CTA's warps read
+// the same rows).
+__device__ __forceinline__ uint4 ldg_x(const uint16_t* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Asynchronous global -> shared copies of 8 / 16 bytes (cp.async), completed
+// per thread by cp_async_wait_all.
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 // 16-byte shared-memory load from a 32-bit shared-window address.
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;

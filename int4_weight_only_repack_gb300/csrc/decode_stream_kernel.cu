@@ -54,7 +54,11 @@ namespace {
 
 using namespace sm100;
 using dec::bounded_wait;
+using dec::cp_async16;
+using dec::cp_async8;
+using dec::cp_async_wait_all;
 using dec::drain_wait;
+using dec::ldg_x;
 using dec::prefetch_l2;
 
 constexpr int SW = 8;                  // warps per CTA
@@ -115,24 +119,6 @@ __host__ __device__ inline StreamLayout stream_layout(int G, int ns, int MR) {
   L.p_off = (L.z_off + G * 4 * ns * 4 + 15) & ~15;
   L.total = L.p_off + SW * 2 * 32 * MR * 4 + 1024;
   return L;
-}
-
-__device__ __forceinline__ uint4 ldg_x(const uint16_t* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
 template <bool BF16>

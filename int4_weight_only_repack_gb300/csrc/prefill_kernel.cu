@@ -78,7 +78,7 @@ using namespace sm100;
 // (128 * NACC) x 256. NACC = 1 double-buffers the accumulator in TMEM (epilogue
 // overlaps the next tile); NACC = 2 fills TMEM with the two accumulators and
 // halves the dequantisation work per MMA.
-constexpr int BN = 256, BK = 64, STAGES = 3;
+constexpr int BN = 256, BK = 64;
 constexpr int THREADS = 512;
 constexpr int DEQ_THREADS = 256;  // warps 8-15
 constexpr int EPI_THREADS = 128;  // warps 4-7
@@ -89,22 +89,44 @@ constexpr int Z_BYTES = 2 * BN / 2;   // two group rows of zeros
 constexpr int Z_SLOT = 1024;
 constexpr int TMEM_COLS = 512;
 
-template <int NACC>
+// Two rings: ST_T stages that TMA fills (the x tile, the packed block, two
+// group rows of scales and of zeros) and ST_B dequantised B tiles. A TMA stage
+// is free again once the MMAs that read its x tile have completed, a B tile
+// once the MMAs that read it have; the dequantising warps need a full TMA stage
+// and a free B tile. Keeping B out of the TMA ring lets that ring run deeper
+// where shared memory allows (a slot's round trip - load, dequantise, MMA - is
+// about 2 us on GB300, so with 3 slots the pipeline, not the MMA, set the pace
+// below M = 128). HALF_A: calls of at most 64 rows load 64 rows of x per stage;
+// the MMA still reads 128 rows, the last 64 from whatever follows in shared
+// memory, and those accumulator rows are never stored.
+template <int NACC, bool GROUPED, bool HALF_A>
 struct Cfg {
   static constexpr int BM = 128 * NACC;
   static constexpr int NBUF = NACC == 1 ? 2 : 1;  // accumulator buffers in TMEM
-  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int A_ROWS = HALF_A ? 64 : BM;  // rows of x the TMA loads per stage
+  static constexpr int A_BYTES = A_ROWS * BK * 2;
+  static constexpr int ST_T = NACC == 2 ? 3 : GROUPED ? 3 : HALF_A ? 6 : 4;
+  static constexpr int ST_B = 3;
+  // Threads that issue the TMA ring's loads. One issuing thread starts the
+  // loads of a 256-row stage (x tile of 256 rows, packed block, scale and zero
+  // rows) more slowly than the MMAs consume them (measured on GB300: 0.9 us a
+  // stage against 0.55 us of MMA; two threads: Llama-2-70B gate_up at
+  // M = 1024 659 -> 625 us; a third, splitting the x tile, gained nothing);
+  // the 128-row pipeline is not bound by it.
+  static constexpr int ISSUERS = NACC == 2 ? 2 : 1;
   static constexpr uint32_t STAGE_TX = A_BYTES + P_BYTES + S_BYTES + Z_BYTES;
   static constexpr int OFF_A = 0;
-  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-  static constexpr int OFF_P = OFF_B + STAGES * B_BYTES;
-  static constexpr int OFF_S = OFF_P + STAGES * P_BYTES;
-  static constexpr int OFF_Z = OFF_S + STAGES * S_BYTES;
-  static constexpr int OFF_BAR = OFF_Z + STAGES * Z_SLOT;
-  static constexpr int NUM_BARS = 3 * STAGES + 2 * NBUF + 1;
+  static constexpr int OFF_P = OFF_A + ST_T * A_BYTES;
+  static constexpr int OFF_S = OFF_P + ST_T * P_BYTES;
+  static constexpr int OFF_Z = OFF_S + ST_T * S_BYTES;
+  static constexpr int OFF_B = OFF_Z + ST_T * Z_SLOT;  // 1024-byte aligned
+  static constexpr int OFF_BAR = OFF_B + ST_B * B_BYTES;
+  static constexpr int NUM_BARS = 2 * ST_T + 2 * ST_B + 2 * NBUF + 1;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
   static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base to 1024
+  static_assert(OFF_B % 1024 == 0, "swizzled B tiles start on 1024 bytes");
+  static_assert(!HALF_A || (NACC == 1 && !GROUPED), "64-row x tiles: ungrouped 128-row tiles only");
 };
 
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;  // 1 s per wait
@@ -136,10 +158,16 @@ __host__ __device__ constexpr int grouped_table_bytes(int E) { return (12 * (E +
 // shared memory left beside that pipeline).
 constexpr int GROUPED_MAX_EXPERTS = 4096;
 constexpr int GROUPED_MAX_EXPERTS_256 = 256;
-static_assert(Cfg<1>::SMEM_BYTES + grouped_table_bytes(GROUPED_MAX_EXPERTS) <= 227 * 1024,
+static_assert(Cfg<1, true, false>::SMEM_BYTES + grouped_table_bytes(GROUPED_MAX_EXPERTS) <=
+                  227 * 1024,
               "the grouped tile table must fit beside the 128-row pipeline");
-static_assert(Cfg<2>::SMEM_BYTES + grouped_table_bytes(GROUPED_MAX_EXPERTS_256) <= 227 * 1024,
+static_assert(Cfg<2, true, false>::SMEM_BYTES + grouped_table_bytes(GROUPED_MAX_EXPERTS_256) <=
+                  227 * 1024,
               "the grouped tile table must fit beside the 256-row pipeline");
+static_assert(Cfg<1, false, false>::SMEM_BYTES <= 227 * 1024 &&
+                  Cfg<1, false, true>::SMEM_BYTES <= 227 * 1024 &&
+                  Cfg<2, false, false>::SMEM_BYTES <= 227 * 1024,
+              "the pipelines fit in shared memory");
 
 // Work unit `tile` -> (expert, M block, N block, K slice [kb0, kb1) of
 // k-blocks, first row and end row of the unit's rows). Ungrouped units run M
@@ -187,15 +215,20 @@ __device__ __forceinline__ Unit unit_of(const PrefillParams& p, const int* tab, 
   return u;
 }
 
-template <int NBUF>
+// full / empty: the TMA ring; bready / bfree: the B ring; accfull / accempty:
+// the TMEM accumulators; mmadone: the abort path's last commit.
+template <int ST_T, int ST_B, int NBUF>
 struct Bars {
   uint32_t base;
   __device__ uint32_t full(int s) const { return base + 8 * s; }
-  __device__ uint32_t bfull(int s) const { return base + 8 * (STAGES + s); }
-  __device__ uint32_t empty(int s) const { return base + 8 * (2 * STAGES + s); }
-  __device__ uint32_t accfull(int b) const { return base + 8 * (3 * STAGES + b); }
-  __device__ uint32_t accempty(int b) const { return base + 8 * (3 * STAGES + NBUF + b); }
-  __device__ uint32_t mmadone() const { return base + 8 * (3 * STAGES + 2 * NBUF); }
+  __device__ uint32_t empty(int s) const { return base + 8 * (ST_T + s); }
+  __device__ uint32_t bready(int b) const { return base + 8 * (2 * ST_T + b); }
+  __device__ uint32_t bfree(int b) const { return base + 8 * (2 * ST_T + ST_B + b); }
+  __device__ uint32_t accfull(int b) const { return base + 8 * (2 * ST_T + 2 * ST_B + b); }
+  __device__ uint32_t accempty(int b) const {
+    return base + 8 * (2 * ST_T + 2 * ST_B + NBUF + b);
+  }
+  __device__ uint32_t mmadone() const { return base + 8 * (2 * ST_T + 2 * ST_B + 2 * NBUF); }
 };
 
 // Wait for an mbarrier phase. Returns false when this CTA is aborting: either
@@ -235,10 +268,11 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi, bool bf16) {
 
 // GROUPED: a grouped (MoE) call, p.eoff != nullptr (its own instantiation, so
 // that ungrouped calls carry none of its per-tile work).
-template <bool BF16, int NACC, bool GROUPED>
+template <bool BF16, int NACC, bool GROUPED, bool HALF_A>
 __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_constant__ PrefillParams p) {
-  using C = Cfg<NACC>;
+  using C = Cfg<NACC, GROUPED, HALF_A>;
   constexpr int BM = C::BM, NBUF = C::NBUF, A_BYTES = C::A_BYTES;
+  constexpr int ST_T = C::ST_T, ST_B = C::ST_B, ISSUERS = C::ISSUERS;
   constexpr int OFF_A = C::OFF_A, OFF_B = C::OFF_B, OFF_P = C::OFF_P, OFF_S = C::OFF_S;
   constexpr int OFF_Z = C::OFF_Z, OFF_BAR = C::OFF_BAR, OFF_MISC = C::OFF_MISC;
   constexpr uint32_t STAGE_TX = C::STAGE_TX;
@@ -246,7 +280,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_addr(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const Bars<NBUF> bars{sbase + OFF_BAR};
+  const Bars<ST_T, ST_B, NBUF> bars{sbase + OFF_BAR};
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
@@ -257,10 +291,13 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
   asm volatile("griddepcontrol.launch_dependents;");
 
   if (tid == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bars.full(s), 1);
-      mbar_init(bars.bfull(s), DEQ_THREADS);
+    for (int s = 0; s < ST_T; ++s) {
+      mbar_init(bars.full(s), ISSUERS);
       mbar_init(bars.empty(s), 1);
+    }
+    for (int b = 0; b < ST_B; ++b) {
+      mbar_init(bars.bready(b), DEQ_THREADS);
+      mbar_init(bars.bfree(b), 1);
     }
     for (int b = 0; b < NBUF; ++b) {
       mbar_init(bars.accfull(b), 1);
@@ -332,43 +369,56 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
   const uint32_t tmem = *tmem_holder;
   const int num_tiles = GROUPED ? tab[p.num_experts] : p.num_tiles;
 
-  if (warp == 0) {
-    // ---------------------------------------------------------------- producer
-    if (lane == 0) {
-      int it = 0;
-      int last_armed[STAGES];
-      for (int s = 0; s < STAGES; ++s) last_armed[s] = -1;
-      bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        const Unit u = unit_of<GROUPED>(p, tab, BM, tile);
-        const int n_blk = u.n_blk;
-        for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
-          if (!wait_phase(bars.empty(s), ph ^ 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(bars.full(s), STAGE_TX);
-          last_armed[s] = it;
-          const int gi = (kb * BK) / p.group;
-          // (a grouped call's unit reads its expert's rows of x, column groups
-          // and group rows; rows past the expert's end are computed but not stored)
-          const int grow = u.e * p.groups + gi;
+  // ------------------------------------------------------------------ producers
+  // ISSUERS threads fill the TMA ring, each arming its own bytes of a stage:
+  // one thread loads everything; with two, warp 0 loads the x tile and the
+  // scale / zero rows and warp 3 the packed block.
+  auto produce = [&](const int role) {
+    const uint32_t tx = ISSUERS == 1 ? STAGE_TX
+                        : role == 0  ? STAGE_TX - P_BYTES
+                                     : (uint32_t)P_BYTES;
+    int it = 0;
+    int last_armed[ST_T];
+    for (int s = 0; s < ST_T; ++s) last_armed[s] = -1;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      const Unit u = unit_of<GROUPED>(p, tab, BM, tile);
+      const int n_blk = u.n_blk;
+      for (int j = 0; j < u.kb1 - u.kb0; ++j, ++it) {
+        const int kb = u.kb0 + j;
+        const int s = it % ST_T;
+        const uint32_t ph = (it / ST_T) & 1;
+        if (!wait_phase(bars.empty(s), ph ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(bars.full(s), tx);
+        last_armed[s] = it;
+        // (a grouped call's unit reads its expert's rows of x, column groups
+        // and group rows; rows past the expert's end are computed but not stored)
+        const int grow = u.e * p.groups + (kb * BK) / p.group;
+        if (role == 0) {
           tma_load_2d(sbase + OFF_A + s * A_BYTES, &p.tm_a, bars.full(s), kb * BK, u.row0);
-          // the 16 atoms (two column groups) of this N block at k-atom kb
-          tma_load_4d(sbase + OFF_P + s * P_BYTES, &p.tm_p, bars.full(s), 0, 0, kb,
-                      u.e * p.ng128 + n_blk * (BN / 128));
           tma_load_2d(sbase + OFF_S + s * S_BYTES, &p.tm_s, bars.full(s), n_blk * BN, grow);
           tma_load_2d(sbase + OFF_Z + s * Z_SLOT, &p.tm_z, bars.full(s), n_blk * (BN / 8), grow);
         }
-      }
-      if (!ok) {
-        // let the copies already issued land before the CTA can exit
-        for (int s = 0; s < STAGES; ++s)
-          if (last_armed[s] >= 0) drain_phase(bars.full(s), (last_armed[s] / STAGES) & 1);
+        if (ISSUERS == 1 || role == 1) {
+          // the 16 atoms (two column groups) of this N block at k-atom kb
+          tma_load_4d(sbase + OFF_P + s * P_BYTES, &p.tm_p, bars.full(s), 0, 0, kb,
+                      u.e * p.ng128 + n_blk * (BN / 128));
+        }
       }
     }
+    if (!ok) {
+      // let the copies already issued land before the CTA can exit
+      for (int s = 0; s < ST_T; ++s)
+        if (last_armed[s] >= 0) drain_phase(bars.full(s), (last_armed[s] / ST_T) & 1);
+    }
+  };
+  if (warp == 0) {
+    if (lane == 0) produce(0);
+  } else if (warp == 3) {
+    if (ISSUERS == 2 && lane == 0) produce(1);
   } else if (warp == 1) {
     // ---------------------------------------------------------------- UMMA issuer
     if (lane == 0) {
@@ -390,15 +440,16 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
         // last rows of an expert) skips that accumulator's MMAs (the epilogue
         // still drains it, but every row it would store is masked)
         const bool second = NACC == 2 && (!GROUPED || u.row0 + 128 < u.row_end);
-        for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
-          if (!wait_phase(bars.full(s), ph, abort_flag) || !wait_phase(bars.bfull(s), ph, abort_flag)) {
+        for (int j = 0; j < u.kb1 - u.kb0; ++j, ++it) {
+          const int s = it % ST_T, b = it % ST_B;
+          const uint32_t ph = (it / ST_T) & 1, phb = (it / ST_B) & 1;
+          if (!wait_phase(bars.full(s), ph, abort_flag) ||
+              !wait_phase(bars.bready(b), phb, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t bdesc = smem_desc_k128(sbase + OFF_B + s * B_BYTES);
+          const uint64_t bdesc = smem_desc_k128(sbase + OFF_B + b * B_BYTES);
           // accumulator i: rows 128 i .. 128 i + 127 of the A tile; each MMA
           // advances 16 elements (32 bytes) along K inside the swizzled rows
           if (NACC == 1 || second) {
@@ -407,17 +458,18 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
 #pragma unroll
               for (int i = 0; i < NACC; ++i) {
                 const uint64_t adesc = smem_desc_k128(sbase + OFF_A + s * A_BYTES + i * (128 * BK * 2));
-                umma_f16(d_tmem + i * BN, adesc + 2 * k, bdesc + 2 * k, IDESC, kb != u.kb0 || k != 0);
+                umma_f16(d_tmem + i * BN, adesc + 2 * k, bdesc + 2 * k, IDESC, j != 0 || k != 0);
               }
             }
           } else {
             const uint64_t adesc = smem_desc_k128(sbase + OFF_A + s * A_BYTES);
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k)
-              umma_f16(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, kb != u.kb0 || k != 0);
+              umma_f16(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, j != 0 || k != 0);
           }
           issued = true;
-          umma_commit(bars.empty(s));
+          umma_commit(bars.empty(s));  // the x tile (and the stage) is free again
+          umma_commit(bars.bfree(b));  // and so is the B tile
         }
         if (ok) umma_commit(bars.accfull(buf));
       }
@@ -494,22 +546,46 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
     constexpr uint32_t MAGIC = Magic<BF16>::pair;
     const int wd = warp - 8;
     const int gg = lane >> 2, t = lane & 3;
+    const bool odd = (gg & 1) != 0;
     const bool two_groups = p.group < BK;  // group 32: each K half has its own group row
     int it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
       const Unit u = unit_of<GROUPED>(p, tab, BM, tile);
-      for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
-        const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
-        if (!wait_phase(bars.full(s), ph, abort_flag)) {
+      for (int j = 0; j < u.kb1 - u.kb0; ++j, ++it) {
+        const int s = it % ST_T, b = it % ST_B;
+        const uint32_t ph = (it / ST_T) & 1, phb = (it / ST_B) & 1;
+        if (!wait_phase(bars.full(s), ph, abort_flag) ||
+            !wait_phase(bars.bfree(b), phb ^ 1, abort_flag)) {
           ok = false;
           break;
         }
         const uint16_t* sS = reinterpret_cast<const uint16_t*>(smem + OFF_S + s * S_BYTES);
         const uint32_t* sZ = reinterpret_cast<const uint32_t*>(smem + OFF_Z + s * Z_SLOT);
         const uint8_t* sP = smem + OFF_P + s * P_BYTES;
-        uint8_t* sB = smem + OFF_B + s * B_BYTES;
+        uint8_t* sB = smem + OFF_B + b * B_BYTES;
+        // the scale pairs (s | s << 16) and MAGIC + z pairs of this lane's four
+        // columns (atoms wd and wd + 8, rows gg and gg + 8), per K half when the
+        // block holds two groups: read once per block, not per word
+        uint32_t ss[2][2][2], zz[2][2][2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int n_loc = (wd + 8 * r) * 16 + gg + 8 * c;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              if (h == 1 && !two_groups) {
+                ss[r][c][1] = ss[r][c][0];
+                zz[r][c][1] = zz[r][c][0];
+                continue;
+              }
+              const uint32_t sb = sS[h * BN + n_loc];
+              const uint32_t z = (sZ[h * (BN / 8) + (n_loc >> 3)] >> (4 * (n_loc & 7))) & 0xF;
+              ss[r][c][h] = sb | (sb << 16);
+              zz[r][c][h] = MAGIC | z | (z << 16);
+            }
+          }
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           const int at = wd + 8 * r;  // atom (16-column tile) inside the block
@@ -518,28 +594,29 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
             // odd gg store the other K half first: the 8 lanes of each store
-            // phase then hit 8 distinct 16-byte bank groups
-            const int j = jj ^ ((gg & 1) << 1);
-            const uint32_t word = wv[j];
-            const int n_loc = at * 16 + gg + 8 * (j & 1);
-            const int h = j >> 1;
-            const int grow = two_groups ? h : 0;
-            const uint32_t sb = sS[grow * BN + n_loc];
-            const uint32_t z = (sZ[grow * (BN / 8) + (n_loc >> 3)] >> (4 * (n_loc & 7))) & 0xF;
-            const uint32_t zz = MAGIC | z | (z << 16);
-            const uint32_t ss = sb | (sb << 16);
+            // phase then hit 8 distinct 16-byte bank groups (word j = jj ^ 2 for
+            // odd gg, picked with selects so every array index stays static)
+            const uint32_t word = odd ? wv[jj ^ 2] : wv[jj];
+            const int n_loc = at * 16 + gg + 8 * (jj & 1);
+            const int h = (jj >> 1) ^ (odd ? 1 : 0);
+            const uint32_t zzw = !two_groups ? zz[r][jj & 1][0]
+                                 : odd       ? zz[r][jj & 1][(jj >> 1) ^ 1]
+                                             : zz[r][jj & 1][jj >> 1];
+            const uint32_t ssw = !two_groups ? ss[r][jj & 1][0]
+                                 : odd       ? ss[r][jj & 1][(jj >> 1) ^ 1]
+                                             : ss[r][jj & 1][jj >> 1];
             uint4 o;
-            o.x = mul_x2<BF16>(sub_x2<BF16>(lop3_and_or(word, 0x000F000Fu, MAGIC), zz), ss);
-            o.y = mul_x2<BF16>(sub_x2<BF16>(lop3_and_or(word >> 4, 0x000F000Fu, MAGIC), zz), ss);
-            o.z = mul_x2<BF16>(sub_x2<BF16>(lop3_and_or(word >> 8, 0x000F000Fu, MAGIC), zz), ss);
-            o.w = mul_x2<BF16>(sub_x2<BF16>(lop3_and_or(word >> 12, 0x000F000Fu, MAGIC), zz), ss);
+            o.x = mul_x2<BF16>(sub_x2<BF16>(lop3_and_or(word, 0x000F000Fu, MAGIC), zzw), ssw);
+            o.y = mul_x2<BF16>(sub_x2<BF16>(lop3_and_or(word >> 4, 0x000F000Fu, MAGIC), zzw), ssw);
+            o.z = mul_x2<BF16>(sub_x2<BF16>(lop3_and_or(word >> 8, 0x000F000Fu, MAGIC), zzw), ssw);
+            o.w = mul_x2<BF16>(sub_x2<BF16>(lop3_and_or(word >> 12, 0x000F000Fu, MAGIC), zzw), ssw);
             const int c = 4 * h + t;  // 16-byte chunk along K inside the 128-byte row
             const int off = (n_loc >> 3) * 1024 + (n_loc & 7) * 128 + ((c ^ (n_loc & 7)) << 4);
             *reinterpret_cast<uint4*>(sB + off) = o;
           }
         }
         fence_proxy_async_smem();
-        mbar_arrive(bars.bfull(s));
+        mbar_arrive(bars.bready(b));
       }
     }
   }
@@ -632,7 +709,7 @@ bool encode_tile_4d(CUtensorMap* map, const void* qw, int K, uint64_t NG, uint32
 
 cudaError_t ensure_prefill_smem(void* fn, int which, int bytes) {
   static std::mutex mu;
-  static bool done[64][8] = {};
+  static bool done[64][10] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -662,19 +739,23 @@ PrefillPlan prefill_plan(int M, int N, int K, int sm_count) {
   pl.m_blocks = (M + 128 * pl.nacc - 1) / (128 * pl.nacc);
   const long long tiles = (long long)pl.m_blocks * pl.n_blocks;
   pl.ksplit = 1;
-  if (tiles < sm_count) {
-    // Split K over otherwise idle SMs, in slices of at least 8 k-blocks. First
-    // choice: as many slices as one wave holds. Another split replaces it when
-    // a cost model, in units of one unsplit tile's time T1, predicts it at least
-    // 10 % faster: ceil(tiles*ks / SMs) waves of units that take 1/ks of T1 plus
-    // about 4 k-blocks of pipeline fill and drain, plus writing and reading ks
-    // fp32 partial tiles (8*M*N*ks bytes at about 6.6 TB/s) and the reduce
-    // launch (about 3 us). T1 = 2 * rows * 256 * K / 8 TFLOP/s (one SM's
-    // measured tcgen05 rate). It moves the shapes whose tiles fill more than
-    // half the SMs but not all of them (one wave with no split leaves the rest
-    // idle): measured on GB300, Llama-2-70B qkv at M = 256 98.7 -> 86.3 us and
-    // Llama-2-13B down at M = 1024 232 -> 199 us; the other sweep shapes keep
-    // their split.
+  if (tiles < sm_count || M <= 128) {
+    // Split K in slices of at least 8 k-blocks. First choice: as many slices as
+    // one wave holds (none when the tiles alone fill the SMs). Another split
+    // replaces it when a cost model, in units of one unsplit tile's time T1,
+    // predicts it at least 10 % faster: ceil(tiles*ks / SMs) waves of units that
+    // take 1/ks of T1 plus about 4 k-blocks of pipeline fill and drain, plus
+    // writing and reading ks fp32 partial tiles (8*M*N*ks bytes at about
+    // 6.6 TB/s) and the reduce launch (about 3 us). T1 = 2 * rows * 256 * K /
+    // 8 TFLOP/s (one SM's measured tcgen05 rate). It moves the shapes whose
+    // tiles fill more than half the SMs but not all of them (one wave with no
+    // split leaves the rest idle): measured on GB300, Llama-2-70B qkv at
+    // M = 256 98.7 -> 86.3 us and Llama-2-13B down at M = 1024 232 -> 199 us;
+    // and, at M <= 128 (small fp32 partials), those whose tiles take one and a
+    // half waves: Llama-2-70B gate_up at M = 32 / 64, 224 tiles, where half the
+    // SMs would run two tiles and the rest one: 192 -> 141 / 194 -> 148 us.
+    // (Above M = 128 the partials cost more than the model charges: 70B qkv at
+    // M = 1024, 160 tiles, measured no faster split three ways.)
     const int kmax = std::max(1, K / BK / 8);
     const int kb_total = K / BK;
     const double t1 = 2.0 * 128 * pl.nacc * BN * (double)K / 8e12;
@@ -778,6 +859,8 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
     --pl.ksplit;
   const int nacc = pl.nacc;
   const int BM = 128 * nacc;
+  // 64-row x tiles (and a deeper TMA ring) for ungrouped calls of at most 64 rows
+  const bool half_a = !grouped && nacc == 1 && a.M <= 64;
   const int n_blocks = pl.n_blocks;
   PrefillParams p;
   const int G = a.K / a.group;
@@ -785,7 +868,8 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
   const int x_rows = grouped ? a.total_rows : a.M;
   const int ng128 = (a.N + 127) / 128;
   const CUtensorMapDataType act = a.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  bool ok = encode_2d(&p.tm_a, act, x, a.K, x_rows, (uint64_t)a.K * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
+  bool ok = encode_2d(&p.tm_a, act, x, a.K, x_rows, (uint64_t)a.K * 2, BK, half_a ? 64 : BM,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
   // stacked experts are further column groups of one TILE tensor, and further
   // group rows of the scales and zeros
   ok = ok && encode_tile_4d(&p.tm_p, a.qw, a.K, (uint64_t)E * ng128, BN / 128);
@@ -817,25 +901,30 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
   const long long max_units =
       grouped ? (long long)n_blocks * ((x_rows + BM - 1) / BM + E) : (long long)p.num_tiles;
 
-  static void* const kernels[2][2][2] = {  // [grouped][nacc - 1][bf16]
-      {{reinterpret_cast<void*>(&w4a16_prefill_kernel<false, 1, false>),
-        reinterpret_cast<void*>(&w4a16_prefill_kernel<true, 1, false>)},
-       {reinterpret_cast<void*>(&w4a16_prefill_kernel<false, 2, false>),
-        reinterpret_cast<void*>(&w4a16_prefill_kernel<true, 2, false>)}},
-      {{reinterpret_cast<void*>(&w4a16_prefill_kernel<false, 1, true>),
-        reinterpret_cast<void*>(&w4a16_prefill_kernel<true, 1, true>)},
-       {reinterpret_cast<void*>(&w4a16_prefill_kernel<false, 2, true>),
-        reinterpret_cast<void*>(&w4a16_prefill_kernel<true, 2, true>)}}};
-  void* fn = kernels[grouped ? 1 : 0][nacc - 1][a.bf16 ? 1 : 0];
-  int smem_bytes, smem_max;
-  if (nacc == 2) {
-    smem_bytes = Cfg<2>::SMEM_BYTES + (grouped ? grouped_table_bytes(E) : 0);
-    smem_max = Cfg<2>::SMEM_BYTES + (grouped ? grouped_table_bytes(GROUPED_MAX_EXPERTS_256) : 0);
-  } else {
-    smem_bytes = Cfg<1>::SMEM_BYTES + (grouped ? grouped_table_bytes(E) : 0);
-    smem_max = Cfg<1>::SMEM_BYTES + (grouped ? grouped_table_bytes(GROUPED_MAX_EXPERTS) : 0);
-  }
-  const int which = (a.bf16 ? 1 : 0) + 2 * (nacc - 1) + 4 * (grouped ? 1 : 0);
+  // [variant][bf16]: 0 ungrouped 128-row, 1 ungrouped 128-row with 64-row x
+  // tiles, 2 ungrouped 256-row, 3 grouped 128-row, 4 grouped 256-row
+  static void* const kernels[5][2] = {
+      {reinterpret_cast<void*>(&w4a16_prefill_kernel<false, 1, false, false>),
+       reinterpret_cast<void*>(&w4a16_prefill_kernel<true, 1, false, false>)},
+      {reinterpret_cast<void*>(&w4a16_prefill_kernel<false, 1, false, true>),
+       reinterpret_cast<void*>(&w4a16_prefill_kernel<true, 1, false, true>)},
+      {reinterpret_cast<void*>(&w4a16_prefill_kernel<false, 2, false, false>),
+       reinterpret_cast<void*>(&w4a16_prefill_kernel<true, 2, false, false>)},
+      {reinterpret_cast<void*>(&w4a16_prefill_kernel<false, 1, true, false>),
+       reinterpret_cast<void*>(&w4a16_prefill_kernel<true, 1, true, false>)},
+      {reinterpret_cast<void*>(&w4a16_prefill_kernel<false, 2, true, false>),
+       reinterpret_cast<void*>(&w4a16_prefill_kernel<true, 2, true, false>)}};
+  const int variant = grouped ? (nacc == 2 ? 4 : 3) : (nacc == 2 ? 2 : half_a ? 1 : 0);
+  void* fn = kernels[variant][a.bf16 ? 1 : 0];
+  static const int cfg_bytes[5] = {Cfg<1, false, false>::SMEM_BYTES, Cfg<1, false, true>::SMEM_BYTES,
+                                   Cfg<2, false, false>::SMEM_BYTES, Cfg<1, true, false>::SMEM_BYTES,
+                                   Cfg<2, true, false>::SMEM_BYTES};
+  const int table_max = variant == 3 ? grouped_table_bytes(GROUPED_MAX_EXPERTS)
+                        : variant == 4 ? grouped_table_bytes(GROUPED_MAX_EXPERTS_256)
+                                       : 0;
+  const int smem_bytes = cfg_bytes[variant] + (grouped ? grouped_table_bytes(E) : 0);
+  const int smem_max = cfg_bytes[variant] + table_max;
+  const int which = (a.bf16 ? 1 : 0) + 2 * variant;
   if ((err = ensure_prefill_smem(fn, which, smem_max)) != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)std::min<long long>(max_units, info.sm_count), 1, 1);
