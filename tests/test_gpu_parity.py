@@ -15,6 +15,12 @@ from libutil import ensure_built, half_from_dev, half_to_dev, rounded_w_referenc
 pytestmark = pytest.mark.gpu
 
 TOL = 4e-3
+# The tcgen05 path (M > 16) multiplies dequantised weights rounded to the
+# activation type, as fused-dequantisation kernels do; against the exact-W
+# oracle its error is the output rounding plus that weight rounding, which on
+# N(0, 1) activations reaches 4.19e-3 (512 x 1024, M = 65, bf16). Its exact
+# property is checked separately: within one output ulp of x . RN(W).
+TOL_ROUNDED_W = 5e-3
 GUARD = 64
 CANARY = 0x5A5A5A5A
 
@@ -505,6 +511,24 @@ PREFILL_CASES = [
 ]
 
 
+# 16 < M <= 128 on the tcgen05 kernel: ragged token counts (64-row x tiles up
+# to 64, 128-row tiles above), several and single column blocks, groups 32 / 64
+# / 128 / one, K split across CTAs on the narrow and long shapes
+MID_M_CASES = [
+    # K, N, group, dtype, Ms
+    (512, 1024, 128, "bf16", (17, 32, 33, 64, 65, 96, 100, 127, 128)),
+    (1024, 384, 64, "fp16", (24, 80)),
+    (2048, 256, 32, "bf16", (40,)),
+    (768, 512, -1, "fp16", (50,)),
+    (8192, 128, 128, "bf16", (128, 20)),
+]
+
+
+@pytest.mark.parametrize("K,N,group,dtype,Ms", MID_M_CASES)
+def test_gemm_mid_m_vs_oracle(w4, K, N, group, dtype, Ms):
+    test_gemm_large_m_vs_oracle(w4, K, N, group, dtype, Ms)
+
+
 @pytest.mark.parametrize("K,N,group,dtype,Ms", PREFILL_CASES)
 def test_gemm_large_m_vs_oracle(w4, K, N, group, dtype, Ms):
     g = K if group == -1 else group
@@ -516,7 +540,7 @@ def test_gemm_large_m_vs_oracle(w4, K, N, group, dtype, Ms):
         yv = oracle.half_bits_to_f64(y, dtype)
         y_ref = oracle.reference_y(x, L.qweight, L.qzeros, L.scales, g, dtype, "awq")
         err = oracle.rel_err(yv, y_ref)
-        assert err <= TOL, (M, err)
+        assert err <= TOL_ROUNDED_W, (M, err)
         # against x . RN(W): only fp32 accumulation and the final rounding remain
         y_rw = rounded_w_reference(x, L, g)
         assert ulp_error(y, y_rw, dtype) <= 1.0, (M, ulp_error(y, y_rw, dtype))
