@@ -343,6 +343,7 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
     for (int j = 0; j < 4; ++j) acc[i][j] = tc[i][j] = 0.f;
   float2 gf = make_float2(0.f, 0.f);  // scales of the open group (columns gg, gg + 8)
   uint32_t zl = 0, zh = 0;            // fp16: MAGIC + z pairs of the open group
+  uint32_t nl = 0, nh = 0;            // fp16: -(64 + z) pairs (the high slot's offset)
   int gslot = -1;                     // its slot in meta (-1: none open)
   uint32_t rslot = 0, rphase = 0;     // ring slot of the next stage, its parity
 
@@ -364,8 +365,12 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
     gf = meta[gslot * 8 + gg];
     if constexpr (!BF16) {
       const uint2 zw = zraw[gslot];
-      zl = MAGIC + ((zw.x >> (4 * gg)) & 0xFu) * 0x00010001u;
-      zh = MAGIC + ((zw.y >> (4 * gg)) & 0xFu) * 0x00010001u;
+      const uint32_t z0 = (zw.x >> (4 * gg)) & 0xFu, z1 = (zw.y >> (4 * gg)) & 0xFu;
+      zl = MAGIC + z0 * 0x00010001u;
+      zh = MAGIC + z1 * 0x00010001u;
+      // -(64 + z) in fp16: 64 is 0x5400, whose last mantissa bit is 1/16
+      nl = (0xD400u + 16u * z0) * 0x00010001u;
+      nh = (0xD400u + 16u * z1) * 0x00010001u;
     }
   };
 
@@ -472,15 +477,21 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
 #pragma unroll
       for (int step = 0; step < 2; ++step) {
         const int sh = 8 * step;
-        af[step][0] = lop3_and_or(wlo >> sh, 0x000F000Fu, MAGIC);
-        af[step][2] = lop3_and_or(wlo >> (sh + 4), 0x000F000Fu, MAGIC);
-        af[step][1] = lop3_and_or(whi >> sh, 0x000F000Fu, MAGIC);
-        af[step][3] = lop3_and_or(whi >> (sh + 4), 0x000F000Fu, MAGIC);
-        if constexpr (!BF16) {
-          af[step][0] = sub_x2<false>(af[step][0], zl);
-          af[step][2] = sub_x2<false>(af[step][2], zl);
-          af[step][1] = sub_x2<false>(af[step][1], zh);
-          af[step][3] = sub_x2<false>(af[step][3], zh);
+        if constexpr (BF16) {
+          af[step][0] = lop3_and_or(wlo >> sh, 0x000F000Fu, MAGIC);
+          af[step][2] = lop3_and_or(wlo >> (sh + 4), 0x000F000Fu, MAGIC);
+          af[step][1] = lop3_and_or(whi >> sh, 0x000F000Fu, MAGIC);
+          af[step][3] = lop3_and_or(whi >> (sh + 4), 0x000F000Fu, MAGIC);
+        } else {
+          // fp16 has two 4-bit slots below its 10 mantissa bits: the nibbles
+          // at bits 4-7 / 20-23 give 1024 + 16q in place, and one fused
+          // multiply-add by 1/16 takes it to q - z exactly (64 + q is exact),
+          // so one shift serves four nibble pairs instead of three shifts
+          const uint32_t lo = wlo >> sh, hi = whi >> sh;
+          af[step][0] = sub_x2<false>(lop3_and_or(lo, 0x000F000Fu, MAGIC), zl);
+          af[step][2] = fma_x2_f16(lop3_and_or(lo, 0x00F000F0u, MAGIC), 0x2C002C00u, nl);
+          af[step][1] = sub_x2<false>(lop3_and_or(hi, 0x000F000Fu, MAGIC), zh);
+          af[step][3] = fma_x2_f16(lop3_and_or(hi, 0x00F000F0u, MAGIC), 0x2C002C00u, nh);
         }
       }
 #pragma unroll

@@ -46,6 +46,13 @@ __device__ __forceinline__ uint32_t sub_x2(uint32_t a, uint32_t b) {
   return d;
 }
 
+// a * b + c on fp16 pairs, one rounding.
+__device__ __forceinline__ uint32_t fma_x2_f16(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
 template <bool BF16>
 __device__ __forceinline__ uint32_t mul_x2(uint32_t a, uint32_t b) {
   uint32_t d;
