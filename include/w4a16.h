@@ -268,13 +268,16 @@ W4_API w4_status w4a16_moe_gemm(const void* x, const int32_t* qw, const void* sc
 
 /*
  * Test hook for the timeout path (no counterpart in the pages). Runs the
- * small-M kernel (1 <= M <= 16, no act-order, no workspace) exactly as
- * w4a16_gemm would, except that it withholds the copies of the weights into
- * its shared-memory ring: every ring wait then runs out after its one-second
- * limit, the kernel records W4_ERR_TIMEOUT in the device status word, lets its
- * other copies land and exits normally. The GPU context stays usable; y is
- * left unspecified. A caller checks the result with w4_device_status (and
- * clears it). For tests only; takes about one second.
+ * kernel w4a16_gemm would run (no act-order, no workspace), except that it
+ * withholds the loads its pipeline waits on: the small-M kernel (M <= 16)
+ * never copies the weights into its shared-memory ring, the large-M tcgen05
+ * kernel (M > 16; N % 32 == 0, else W4_ERR_SHAPE) issues none of its TMA loads.
+ * Every such wait then runs out after its one-second limit, the kernel records
+ * W4_ERR_TIMEOUT in the device status word, winds its other roles down (the
+ * tcgen05 kernel frees its tensor memory), lets the copies already in flight
+ * land and exits normally. The GPU context stays usable; y is left
+ * unspecified. A caller checks the result with w4_device_status (and clears
+ * it). For tests only; takes about one second.
  */
 W4_API w4_status w4_test_stalled_gemm(const void* x, const int32_t* qw, const void* scales,
                                       const int32_t* zeros, void* y, int M, int N, int K,

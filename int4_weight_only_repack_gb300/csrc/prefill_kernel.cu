@@ -148,6 +148,7 @@ struct PrefillParams {
   // may have, and the tile count comes from the offsets on the device.
   const int32_t* eoff;
   int num_experts, groups, ng128, total_rows;
+  int stall;  // test hook: the producers issue nothing (every wait on the ring runs out)
 };
 
 // Per-CTA table of a grouped call, after the pipeline's shared memory:
@@ -374,6 +375,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
   // one thread loads everything; with two, warp 0 loads the x tile and the
   // scale / zero rows and warp 3 the packed block.
   auto produce = [&](const int role) {
+    if (p.stall) return;
     const uint32_t tx = ISSUERS == 1 ? STAGE_TX
                         : role == 0  ? STAGE_TX - P_BYTES
                                      : (uint32_t)P_BYTES;
@@ -896,6 +898,7 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
   p.groups = G;
   p.ng128 = ng128;
   p.total_rows = x_rows;
+  p.stall = a.test_stall;
   // CTAs: one per SM at most; a grouped call has at most
   // (total_rows / 128 + E) row tiles over the N blocks
   const long long max_units =

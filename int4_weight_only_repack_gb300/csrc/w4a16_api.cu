@@ -333,7 +333,7 @@ w4_status w4a16_moe_gemm(const void* x, const int32_t* qw, const void* scales,
 w4_status w4_test_stalled_gemm(const void* x, const int32_t* qw, const void* scales,
                                const int32_t* zeros, void* y, int M, int N, int K, int group,
                                int dtype, void* stream) {
-  if (M < 1 || M > 16) return W4_ERR_SHAPE;  // the small-M kernel only
+  if (M < 1 || (M > 16 && !prefill_supported(M, N, K))) return W4_ERR_SHAPE;
   return gemm_impl(x, qw, scales, zeros, nullptr, nullptr, y, M, N, K, group, dtype, nullptr, 0,
                    stream, 1);
 }
@@ -391,7 +391,7 @@ w4_status gemm_impl(const void* x, const int32_t* qw, const void* scales, const 
   a.test_stall = test_stall;
   DeviceInfo info;
   if (device_info(&info) != cudaSuccess) return W4_ERR_CUDA;
-  if (!test_stall && use_prefill(M, N, K, info.sm_count))
+  if (use_prefill(M, N, K, info.sm_count))
     return from_cuda(launch_prefill(a, static_cast<cudaStream_t>(stream)));
   return from_cuda(launch_decode(a, static_cast<cudaStream_t>(stream)));
 }

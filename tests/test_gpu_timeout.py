@@ -1,10 +1,11 @@
 """Failure detection without a GPU fault: the timeout path of the pipeline waits.
 
 Every wait inside the kernels is bounded (one second). w4_test_stalled_gemm runs
-the small-M kernel with its weight copies withheld, so its ring waits run out:
-the kernel must record W4_ERR_TIMEOUT in the device status word (read through
-w4_device_status), let its other copies land, exit, and leave the context
-usable for the next call.
+the kernel a call would run with the loads its pipeline waits on withheld (the
+small-M kernel's weight copies; all of the tcgen05 kernel's TMA loads), so its
+waits run out: the kernel must record W4_ERR_TIMEOUT in the device status word
+(read through w4_device_status), wind down, exit, and leave the context usable
+for the next call.
 """
 import time
 
@@ -30,9 +31,12 @@ def w4():
     return mod
 
 
-def test_stalled_kernel_reports_timeout_and_recovers(w4):
+# M = 4: the small-M kernel; 64: the tcgen05 kernel with 64-row x tiles; 200:
+# its 128-row tiles over two row blocks
+@pytest.mark.parametrize("M", [4, 64, 200])
+def test_stalled_kernel_reports_timeout_and_recovers(w4, M):
     import torch
-    K, N, M = 512, 256, 4
+    K, N = 512, 256
     L = synth.make_custom_layer([130], K, N, group=128, dtype="bf16")
     qweight = torch.from_numpy(L.qweight).cuda()
     qzeros = torch.from_numpy(L.qzeros).cuda()
@@ -58,14 +62,16 @@ def test_stalled_kernel_reports_timeout_and_recovers(w4):
     torch.cuda.synchronize()
     y_ref = oracle.reference_y(xb, L.qweight, L.qzeros, L.scales, 128, "bf16", "awq")
     got = oracle.half_bits_to_f64(half_from_dev(y2).reshape(M, N), "bf16")
-    assert oracle.rel_err(got, y_ref) <= 4e-3
+    # (the tcgen05 path multiplies weights rounded to bf16: 5e-3, as in its parity tests)
+    assert oracle.rel_err(got, y_ref) <= (4e-3 if M <= 16 else 5e-3)
     assert w4.w4_device_status() == 0
 
 
-def test_stall_hook_rejects_large_m(w4):
+def test_stall_hook_rejects_unsupported_large_m(w4):
+    """Above M = 16 the hook needs the tcgen05 kernel (N % 32 == 0)."""
     import torch
     x = torch.empty((32, 64), dtype=torch.bfloat16, device="cuda")
-    y = torch.empty((32, 32), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((32, 48), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(w4.W4Error) as e:
-        w4.w4_test_stalled_gemm(x, x, x, x, y, 32, 32, 64, 64, "bf16")
+        w4.w4_test_stalled_gemm(x, x, x, x, y, 32, 48, 64, 64, "bf16")
     assert e.value.status == 2  # W4_ERR_SHAPE
