@@ -99,6 +99,21 @@ W4a8Ws w4a8_ws(int M, int K) {
 
 // ---- activations --------------------------------------------------------------
 // Partial max|x| of this CTA's slice (eight values per 16-byte load).
+// Two fp32 lanes in one 64-bit register, and a * b + c on both lanes with one
+// rounding each (fma.rn.f32x2: one instruction for two of the epilogue's FMAs).
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ float f32x2_lo(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float f32x2_hi(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+
 template <bool BF16>
 __global__ void __launch_bounds__(256) w4a8_amax_kernel(const uint4* __restrict__ x, size_t n8,
                                                         float* __restrict__ parts) {
@@ -328,9 +343,9 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_gemm_kernel(const __grid_cons
       const int m_blk = tile % p.m_blocks, n_blk = tile / p.m_blocks;
       const int row = m_blk * BM + quarter * 32 + lane;
       const float* xs_row = p.xs + (size_t)min(row, p.M - 1) * KB;
-      float y[64];
+      uint64_t y2[32];  // the 64 columns' running sums, two per register
 #pragma unroll
-      for (int c = 0; c < 64; ++c) y[c] = 0.f;
+      for (int c = 0; c < 32; ++c) y2[c] = 0;
       float xs_next = __ldg(xs_row);
       for (int kb = 0; kb < KB; ++kb, ++it) {
         const int s = it % STAGES, buf = it & 1;
@@ -343,6 +358,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_gemm_kernel(const __grid_cons
         }
         tc_fence_after();
         const float* ab = reinterpret_cast<const float*>(smem + OFF_AB + s * AB_BYTES);
+        const uint64_t nxs2 = f32x2_pack(-xs, -xs);
 #pragma unroll
         for (int c0 = 0; c0 < 64; c0 += 32) {
           uint32_t r[32];
@@ -352,12 +368,17 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_gemm_kernel(const __grid_cons
           for (int q = 0; q < 8; ++q) {
             const float4 a4 = *reinterpret_cast<const float4*>(ab + 64 * half + c0 + 4 * q);
             const float4 b4 = *reinterpret_cast<const float4*>(ab + BN + 64 * half + c0 + 4 * q);
-            const float av[4] = {a4.x, a4.y, a4.z, a4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c = c0 + 4 * q + e;
-              y[c] = fmaf(av[e], __uint_as_float(r[4 * q + e]), fmaf(-bv[e], xs, y[c]));
-            }
+            // y = fma(512 s, acc, fma(-z s, xs, y)), two columns per instruction
+            // (the same two roundings per column as scalar FMAs)
+            const int c = (c0 + 4 * q) / 2;
+            y2[c] = f32x2_fma(f32x2_pack(b4.x, b4.y), nxs2, y2[c]);
+            y2[c + 1] = f32x2_fma(f32x2_pack(b4.z, b4.w), nxs2, y2[c + 1]);
+            y2[c] = f32x2_fma(f32x2_pack(a4.x, a4.y),
+                              f32x2_pack(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1])),
+                              y2[c]);
+            y2[c + 1] = f32x2_fma(
+                f32x2_pack(a4.z, a4.w),
+                f32x2_pack(__uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3])), y2[c + 1]);
           }
         }
         tc_fence_before();
@@ -380,8 +401,8 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_gemm_kernel(const __grid_cons
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              w[e] = (uint32_t)float_to_half_bits<BF16>(sx * y[8 * q + 2 * e]) |
-                     ((uint32_t)float_to_half_bits<BF16>(sx * y[8 * q + 2 * e + 1]) << 16);
+              w[e] = (uint32_t)float_to_half_bits<BF16>(sx * f32x2_lo(y2[4 * q + e])) |
+                     ((uint32_t)float_to_half_bits<BF16>(sx * f32x2_hi(y2[4 * q + e])) << 16);
             v.x = w[0];
             v.y = w[1];
             v.z = w[2];
