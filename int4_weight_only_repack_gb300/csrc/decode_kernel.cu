@@ -115,8 +115,8 @@ struct SmemLayout {
   int xs, ring, bars, cnt, meta, xsum, recv, total;
 };
 
-// xs: nbuf buffers of M token rows, then one row of zeros (read by the MMA
-// lanes whose token row is beyond M). bars: ring mbarriers, then one per x
+// xs: nbuf buffers of M token rows (the MMA lanes whose token row is beyond M
+// read row 0: their output columns are never stored). bars: ring mbarriers, then one per x
 // buffer. cnt: per slot the count of warps done with it (monotonic), per slot
 // the last stage copied into it, per x buffer the last chunk copied into it,
 // and the abort flag. meta: per warp and group slot,
@@ -127,7 +127,7 @@ __host__ __device__ inline SmemLayout smem_layout(int MT, int m_rows, int x_stri
                                                   int ring, int maxg, int S, int slice) {
   SmemLayout L;
   L.xs = 0;
-  L.ring = (((nbuf * m_rows + 1) * x_stride * 2) + 1023) & ~1023;
+  L.ring = ((nbuf * m_rows * x_stride * 2) + 1023) & ~1023;
   L.bars = L.ring + ring * STAGE_BYTES;
   L.cnt = L.bars + (ring + 2) * 8;
   L.meta = (L.cnt + (2 * ring + 2 + 1) * 4 + 15) & ~15;
@@ -176,7 +176,6 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
   __shared__ int grp_rows[2];
 
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem + L.xs);
-  uint16_t* xzero = xs + (size_t)NB * p.M * p.x_stride;  // the zero row
   const uint32_t ring_s = smem_addr(smem + L.ring);
   const uint32_t full0 = smem_addr(smem + L.bars);       // + 8 * slot
   const uint32_t xbar0 = full0 + 8 * D;                   // + 8 * buffer
@@ -301,9 +300,7 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
     *abort_flag = 0;
     fence_mbar_init();
   }
-  for (int i = tid; i < p.x_stride / 8; i += DEC_THREADS)
-    reinterpret_cast<uint4*>(xzero)[i] = make_uint4(0, 0, 0, 0);
-  __syncthreads();  // barrier initialisation, counters and the zero row
+  __syncthreads();  // barrier initialisation and counters
   if (nchunks > 0) stage_chunk_meta(0);
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -417,7 +414,7 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
         const int r1 = min(c1 * ATOM_K, p.gshift >= 31 ? p.K : (gi + 1) << p.gshift);
         for (int mt = 0; mt < MT; ++mt) {
           const int row = 8 * mt + gg;
-          const uint16_t* xr = (row < M ? xb + (size_t)row * p.x_stride : xzero) + 8 * t;
+          const uint16_t* xr = xb + (size_t)(row < M ? row : 0) * p.x_stride + 8 * t;
           float sa[2][4] = {};
           for (int r = r0; r < r1; r += 64) {
 #pragma unroll
@@ -458,11 +455,13 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
 
     // 4) consume this chunk's stages. Shared-memory operands are addressed with
     //    32-bit shared-window addresses with constant offsets inside a stage.
-    uint32_t xa[MT];  // this lane's x row (or the zero row) at the chunk's first atom, column 8t
+    // this lane's x row at the chunk's first atom, column 8t; lanes whose token
+    // row is beyond M read row 0 (their output columns are discarded)
+    uint32_t xa[MT];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
       const int row = 8 * mt + gg;
-      xa[mt] = smem_addr(row < M ? xb + (size_t)row * p.x_stride : xzero) + 16u * (uint32_t)t;
+      xa[mt] = smem_addr(xb + (size_t)(row < M ? row : 0) * p.x_stride) + 16u * (uint32_t)t;
     }
     // k-atoms per group (groups of 64 rows or more); a chunk that starts inside
     // a group (only possible for groups longer than a stage) opens it at once
