@@ -119,9 +119,9 @@ struct SmemLayout {
 // read row 0: their output columns are never stored). bars: ring mbarriers, then one per x
 // buffer. cnt: per slot the count of warps done with it (monotonic), per slot
 // the last stage copied into it, per x buffer the last chunk copied into it,
-// and the abort flag. meta: per warp and group slot,
-// the scales of the tile's 16 columns (one float2 per lane group) and the
-// tile's two zero words.
+// and the abort flag. meta: per warp and group slot, the scales of the tile's
+// 16 columns as they are stored (one 32-bit word per lane group: columns gg
+// and gg + 8), then per warp and group slot the tile's two zero words.
 // xsum: per group slot, the sum of x over the group's rows for each token.
 __host__ __device__ inline SmemLayout smem_layout(int MT, int m_rows, int x_stride, int nbuf,
                                                   int ring, int maxg, int S, int slice) {
@@ -131,7 +131,7 @@ __host__ __device__ inline SmemLayout smem_layout(int MT, int m_rows, int x_stri
   L.bars = L.ring + ring * STAGE_BYTES;
   L.cnt = L.bars + (ring + 2) * 8;
   L.meta = (L.cnt + (2 * ring + 2 + 1) * 4 + 15) & ~15;
-  L.xsum = L.meta + DEC_WARPS * maxg * (8 * 8 + 8);
+  L.xsum = L.meta + DEC_WARPS * maxg * (8 * 4 + 8);
   L.recv = L.xsum + maxg * 8 * MT * 4;
   L.total = L.recv + S * slice * 8 * MT * 4;
   return L;
@@ -185,8 +185,13 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
   volatile int* abort_flag = last_chunk + 2;
   // per (group slot, lane group gg): the scales of columns gg and gg + 8 of the
   // warp's tile; then per group slot the tile's two zero words
-  float2* meta = reinterpret_cast<float2*>(smem + L.meta) + warp * p.maxg * 8;
-  uint2* zraw = reinterpret_cast<uint2*>(smem + L.meta + DEC_WARPS * p.maxg * 64) + warp * p.maxg;
+  uint32_t* meta = reinterpret_cast<uint32_t*>(smem + L.meta) + warp * p.maxg * 8;
+  uint2* zraw = reinterpret_cast<uint2*>(smem + L.meta + DEC_WARPS * p.maxg * 32) + warp * p.maxg;
+  // a meta word as the fp32 scales of columns gg and gg + 8 (exact)
+  auto scale_pair = [](const uint32_t w) {
+    return make_float2(half_bits_to_float<BF16>((uint16_t)(w & 0xFFFFu)),
+                       half_bits_to_float<BF16>((uint16_t)(w >> 16)));
+  };
   float* xsum = reinterpret_cast<float*>(smem + L.xsum);  // [maxg][MR] (bf16 only)
   float* recv = reinterpret_cast<float*>(smem + L.recv);
   constexpr int NCOL = 16 * DEC_WARPS;
@@ -234,15 +239,14 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
     if (p.pf > 0 && pa < ka1 && j >= D)
       prefetch_l2(gsrc + (size_t)pa * KROW_BYTES, (uint32_t)min(SA, ka1 - pa) * KROW_BYTES);
   };
-  // one group's 16 scales (of this warp's tile) into its 8 meta entries, and its
-  // zero words
+  // one group's 16 scales (of this warp's tile) into its 8 meta entries (entry
+  // c: column c in the low half, column c + 8 in the high half), and its zero
+  // words
   auto stage_meta = [&](int gl, const uint4 a, const uint4 b, const uint2 z) {
     const uint32_t sv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
     for (int c = 0; c < 8; ++c)
-      meta[gl * 8 + c] =
-          make_float2(half_bits_to_float<BF16>((uint16_t)(sv[c >> 1] >> (16 * (c & 1)))),
-                      half_bits_to_float<BF16>((uint16_t)(sv[4 + (c >> 1)] >> (16 * (c & 1)))));
+      meta[gl * 8 + c] = __byte_perm(sv[c >> 1], sv[4 + (c >> 1)], (c & 1) ? 0x7632u : 0x5410u);
     zraw[gl] = z;
   };
   // the first ring stages, and the pf stages beyond the ring into L2 (one thread)
@@ -359,7 +363,7 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
   auto next_group = [&]() {
     if (gslot >= 0) flush();
     ++gslot;
-    gf = meta[gslot * 8 + gg];
+    gf = scale_pair(meta[gslot * 8 + gg]);
     if constexpr (!BF16) {
       const uint2 zw = zraw[gslot];
       const uint32_t z0 = (zw.x >> (4 * gg)) & 0xFu, z1 = (zw.y >> (4 * gg)) & 0xFu;
@@ -438,7 +442,7 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
     //    ((128 + z) s is exact in fp32: two 8-bit significands)
     if (BF16 && has_cols) {
       for (int gl = 0; gl < ng; ++gl) {
-        const float2 sc = meta[gl * 8 + gg];
+        const float2 sc = scale_pair(meta[gl * 8 + gg]);
         const uint2 zw = zraw[gl];
         const float cl = sc.x * (float)(128 + ((zw.x >> (4 * gg)) & 0xF));
         const float ch = sc.y * (float)(128 + ((zw.y >> (4 * gg)) & 0xF));
@@ -701,15 +705,26 @@ DecodePlan shape_plan(int S, int A, int Mc, int MT, int gshift, int ring) {
   return d;
 }
 
+// CTAs of `fn` resident per SM with `smem` bytes of dynamic shared memory, as
+// the runtime's occupancy calculator counts them (registers, shared memory with
+// its allocation granularity and per-CTA reservation); 0 on an error.
+int resident_ctas(void* fn, int smem) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, DEC_THREADS, (size_t)smem) !=
+      cudaSuccess)
+    return 0;
+  return n;
+}
+
 // Deepest ring (2..MAX_RING stages, no deeper than the CTA's stage count) that
 // keeps `per_sm` CTAs resident.
-DecodePlan fit_ring(int S, int A, int Mc, int MT, int gshift, int per_sm, int smem_per_sm) {
+DecodePlan fit_ring(int S, int A, int Mc, int MT, int gshift, int per_sm, void* fn) {
   const int stages = ((A + SA - 1) / SA + S - 1) / S;
   const int need = std::max(2, std::min(MAX_RING, stages));
   DecodePlan d = shape_plan(S, A, Mc, MT, gshift, 2);
   for (int r = need; r >= 2; --r) {
     d = shape_plan(S, A, Mc, MT, gshift, r);
-    if ((d.L.total + 1024) * per_sm <= smem_per_sm) break;
+    if (resident_ctas(fn, d.L.total) >= per_sm) break;
   }
   return d;
 }
@@ -727,9 +742,12 @@ DecodePlan fit_ring(int S, int A, int Mc, int MT, int gshift, int per_sm, int sm
 //  * a split that would take more than three waves is replaced by the longest
 //    CTA ranges (x in chunks) at about one wave.
 // The ring is then as deep as fits with 3 resident CTAs per SM (2 when the
-// register budget allows only 2), at least 2 stages.
+// register budget allows only 2), at least 2 stages; residency is the runtime's
+// occupancy count for the kernel (a plan that looked like three CTAs by plain
+// byte arithmetic but ran two per SM took a second wave: Llama-2-70B qkv at
+// M = 8 22.9 us against 17.0 us with three).
 DecodePlan plan_decode(int N, int K, int Mc, int MT, int gshift, int experts,
-                       const DeviceInfo& info) {
+                       const DeviceInfo& info, void* fn) {
   const int NG = (N / 16 + DEC_WARPS - 1) / DEC_WARPS, A = K / ATOM_K;
   const long long units = (long long)NG * experts;  // (column group, expert) pairs of the grid
   const int nst_all = (A + SA - 1) / SA;
@@ -758,9 +776,8 @@ DecodePlan plan_decode(int N, int K, int Mc, int MT, int gshift, int experts,
     S = std::max(s64, (int)(2.0 * info.sm_count / units + 0.5));
   }
   const int reg_ctas = decode_min_ctas(MT);
-  DecodePlan d = fit_ring(S, A, Mc, MT, gshift, std::min(3, reg_ctas), info.smem_per_sm);
-  if ((d.L.total + 1024) * std::min(3, reg_ctas) > info.smem_per_sm)
-    d = fit_ring(S, A, Mc, MT, gshift, 2, info.smem_per_sm);
+  DecodePlan d = fit_ring(S, A, Mc, MT, gshift, std::min(3, reg_ctas), fn);
+  if (resident_ctas(fn, d.L.total) < std::min(3, reg_ctas)) d = fit_ring(S, A, Mc, MT, gshift, 2, fn);
   return d;
 }
 
@@ -768,9 +785,10 @@ DecodePlan plan_decode(int N, int K, int Mc, int MT, int gshift, int experts,
 // host time, more than a decode launch.
 struct PlanKey {
   int dev, N, K, Mc, gshift, experts;
+  void* fn;  // the kernel (its register budget decides residency)
   bool operator==(const PlanKey& o) const {
     return dev == o.dev && N == o.N && K == o.K && Mc == o.Mc && gshift == o.gshift &&
-           experts == o.experts;
+           experts == o.experts && fn == o.fn;
   }
 };
 struct PlanKeyHash {
@@ -781,22 +799,23 @@ struct PlanKeyHash {
     h ^= (uint64_t)k.Mc + 0x7F4A7C15ull + (h << 6) + (h >> 2);
     h ^= (uint64_t)k.gshift + 0x7F4A7C15ull + (h << 6) + (h >> 2);
     h ^= (uint64_t)k.experts + 0x7F4A7C15ull + (h << 6) + (h >> 2);
+    h ^= reinterpret_cast<uint64_t>(k.fn) + 0x7F4A7C15ull + (h << 6) + (h >> 2);
     return (size_t)h;
   }
 };
 
 cudaError_t cached_plan(int N, int K, int Mc, int MT, int gshift, int experts,
-                        const DeviceInfo& info, DecodePlan* out) {
+                        const DeviceInfo& info, void* fn, DecodePlan* out) {
   static std::mutex mu;
   static std::unordered_map<PlanKey, DecodePlan, PlanKeyHash> plans;
   int dev = 0;
   const cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const PlanKey key{dev, N, K, Mc, gshift, experts};
+  const PlanKey key{dev, N, K, Mc, gshift, experts, fn};
   std::lock_guard<std::mutex> lock(mu);
   auto it = plans.find(key);
   if (it == plans.end())
-    it = plans.emplace(key, plan_decode(N, K, Mc, MT, gshift, experts, info)).first;
+    it = plans.emplace(key, plan_decode(N, K, Mc, MT, gshift, experts, info, fn)).first;
   *out = it->second;
   return cudaSuccess;
 }
@@ -843,10 +862,15 @@ cudaError_t launch_decode(const GemmArgs& a, cudaStream_t stream) {
     const int MT = Mc <= 8 ? 1 : Mc <= 16 ? 2 : Mc <= 32 ? 4 : 8;
     DecodePlan plan;
     const int experts = a.eoff != nullptr ? a.num_experts : 1;
-    if ((err = cached_plan(a.N, a.K, Mc, MT, gshift, experts, info, &plan)) != cudaSuccess)
-      return err;
     void* fn = pick_kernel(MT, a.bf16 != 0, g64);
-    if ((err = ensure_smem(fn, plan.L.total)) != cudaSuccess) return err;
+    // the occupancy queries of the plan need the kernel's dynamic limit at the
+    // device's maximum (the opt-in limit less the kernel's static shared memory)
+    cudaFuncAttributes fa;
+    if ((err = cudaFuncGetAttributes(&fa, fn)) != cudaSuccess) return err;
+    if ((err = ensure_smem(fn, (size_t)info.max_smem_optin - fa.sharedSizeBytes)) != cudaSuccess)
+      return err;
+    if ((err = cached_plan(a.N, a.K, Mc, MT, gshift, experts, info, fn, &plan)) != cudaSuccess)
+      return err;
 
     DecodeParams p;
     p.x = static_cast<const uint16_t*>(xsrc) + (size_t)r0 * a.K;
