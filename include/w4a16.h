@@ -333,14 +333,16 @@ W4_API w4_status w4a16_gemm_noalloc(const void* x, const int32_t* qw, const void
  * rounded to nearest even and saturated at 448 (float8_e4m3fn). The weights
  * enter the MMA as the e4m3 numbers q * 2^-9 (exact for every 4-bit code) and
  * each group's partial sum is taken back to W with 512 s and the zero point:
- * (512 s) * sum x8 q 2^-9 - (z s) * sum x8. Accumulation is fp32; y is rounded
- * once to dtype.
+ * (512 s) * (sum x8 q 2^-9 - z 2^-9 sum x8), the zero-point term added in the
+ * tensor cores exactly (sum x8 as seven e4m3 digits). Accumulation is fp32; y
+ * is rounded once to dtype.
  *   x [M][K] and y [M][N] in dtype; qw / scales / zeros from w4_repack_awq or
  *   w4_repack_gptq in the TILE layout, without act-order.
  *   group: 128 or -1 (one group over all of K); other groups -> W4_ERR_GROUP.
  *   K % 128 == 0 and N % 32 == 0 (else W4_ERR_SHAPE).
  *   workspace: at least w4a8_gemm_workspace_size(M, K) bytes (the fp8
- *   activations, their per-group sums and s_x; no initialisation needed),
+ *   activations, the digits of their per-group sums and s_x; no initialisation
+ *   needed),
  *   else W4_ERR_WORKSPACE; it must not overlap x or y.
  * Ordering: three kernels in stream order (programmatic dependent launch);
  * none of them reads the weights before the kernel before it has finished.

@@ -9,24 +9,34 @@
 //  * Activations, two small kernels: the per-tensor max|x| (one partial per
 //    CTA, no initialised memory needed), then every CTA reduces the partials,
 //    takes s_x = RN(max|x| / 448) and writes x8 = e4m3(RN(x / s_x)) (round to
-//    nearest even, saturating) with, for every row and group of 128 columns,
-//    xs = sum of the e4m3 values (fp32), which the zero points need.
+//    nearest even, saturating) and, for every row and group of 128 columns,
+//    the group's sum of the codes as seven e4m3 digits (below).
 //  * Weights: a 4-bit code q becomes the e4m3 byte q itself, the number
 //    q * 2^-9 (0..7 subnormal, 8..15 the first binade: exact), so the B
 //    operand costs one mask, one shift, one mask and two byte permutes per
 //    eight codes. The "scales x 512" of the page: 512 s restores the factor,
 //    and the zero point is applied to the group's sum:
-//        sum_k x8 (q - z) s = (512 s) * sum_k x8 (q 2^-9) - (z s) * xs.
+//        sum_k x8 (q - z) s = (512 s) * (sum_k x8 (q 2^-9) - z 2^-9 xs),
+//    xs = sum_k x8. The second term is one more K = 32 MMA per group on the
+//    tensor cores, exact: xs is a multiple of 2^-9 below 2^16, so
+//    I = 512 xs is an integer below 2^25 with seven base-16 digits u_j, and
+//    z 2^-9 xs = sum_j (sign(I) u_j 2^a_j) (z 2^b_j) with a_j + b_j = 4j - 18;
+//    both factors are e4m3 numbers for the exponents chosen (F8_DIGIT_A / _B),
+//    and the MMA adds its 32 exact products with one rounding. The digits of
+//    four groups share one 128-byte swizzled row (32 bytes a group), loaded by
+//    TMA once per four K blocks; the weights' side is written per block.
 //  * Persistent kernel, one CTA per SM, 128 x 128 output tiles, K blocks of
 //    128 = one group (group 128; group -1 applies the same per-column scale at
 //    every block). Warp 0 issues TMA copies (x8 rows with the 128-byte
 //    swizzle, the packed TILE atoms, one group row of scales and zeros) into a
-//    STAGES-deep ring; warps 12-15 expand the atoms into the K-major swizzled
-//    e4m3 B tile and stage the block's 512 s and z s per column; warp 1 issues
-//    four UMMAs per block (M 128, N 128, K 32) into one of two TMEM
-//    accumulators; warps 4-11 take each block's accumulator out of TMEM and
-//    fold it into fp32 running sums held in registers (two FFMAs per output
-//    and block), then scale by s_x, round once and store y.
+//    STAGES-deep ring, and every fourth block the digit rows into a ring of
+//    two; warps 12-15 expand the atoms into the K-major swizzled e4m3 B tile,
+//    write the block's -z 2^b_j digits and stage its 512 s per column; warp 1
+//    issues five UMMAs per block (M 128, N 128, K 32: four for the weights,
+//    one for the zero point) into one of two TMEM accumulators; warps 4-11
+//    take each block's accumulator out of TMEM and fold it into fp32 running
+//    sums held in registers (one FFMA per output and block), then scale by
+//    s_x, round once and store y.
 //  * Every mbarrier wait is bounded (one second); a timed-out wait records
 //    W4_ERR_TIMEOUT in the device status word and the CTA drains its copies
 //    and MMAs before it frees its tensor memory and exits.
@@ -48,6 +58,8 @@ using dec::drain_wait;
 
 constexpr int BM = 128, BN = 128, BK = 128;  // BK bytes of e4m3 = one 128-byte swizzle row
 constexpr int STAGES = 4;
+constexpr int DIGITS = 7;       // base-16 digits of 512 * (a group's sum of the codes)
+constexpr int DG = 4;           // groups whose digits share one 128-byte row (32 bytes each)
 constexpr int THREADS = 512;
 constexpr int EPI_WARPS = 8, DEQ_WARPS = 4;
 constexpr int A_BYTES = BM * BK;           // x8 tile
@@ -55,7 +67,14 @@ constexpr int B_BYTES = BN * BK;           // expanded weights
 constexpr int P_BYTES = BN * BK / 2;       // packed atoms: 8 tiles x 2 k-atoms
 constexpr int S_BYTES = BN * 2;            // one group row of scales
 constexpr int Z_BYTES = BN / 2;            // one group row of zeros (16 words)
-constexpr int AB_BYTES = 2 * BN * 4;       // 512 s and z s per column (fp32)
+constexpr int AB_BYTES = BN * 4;           // 512 s per column (fp32)
+constexpr int X_BYTES = BM * 128;          // digit rows of DG groups (activations)
+constexpr int W_BYTES = BN * 128;          // -z 2^b_j rows (weights): a ring of 4 K slices
+// Block `it` (counted over the CTA's whole run) writes the weights' digits into
+// slice it % 4; block it + 4 reuses it, and its weights are only expanded once
+// the TMA stage it + 4 - STAGES = it is free again, i.e. once block it's MMAs
+// have completed.
+static_assert(STAGES == 4, "the weights' digit slices are recycled through the stage ring");
 constexpr uint32_t STAGE_TX = A_BYTES + P_BYTES + S_BYTES + Z_BYTES;
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
@@ -63,35 +82,45 @@ constexpr int OFF_P = OFF_B + STAGES * B_BYTES;
 constexpr int OFF_S = OFF_P + STAGES * P_BYTES;
 constexpr int OFF_Z = OFF_S + STAGES * S_BYTES;
 constexpr int OFF_AB = OFF_Z + STAGES * 128;  // zero rows at 128-byte slots
-constexpr int OFF_BAR = OFF_AB + STAGES * AB_BYTES;
-constexpr int NUM_BARS = 3 * STAGES + 4;
+constexpr int OFF_XD = (OFF_AB + STAGES * AB_BYTES + 1023) & ~1023;  // swizzled tiles: 1024-aligned
+constexpr int OFF_WD = OFF_XD + 2 * X_BYTES;
+constexpr int OFF_BAR = OFF_WD + W_BYTES;
+constexpr int NUM_BARS = 3 * STAGES + 4 + 4;
 constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
 constexpr int TMEM_COLS = 256;                    // two 128-column fp32 accumulators
 constexpr int AMAX_PARTS = 1024;                  // partial maxima of the first pass
 
+// Digit j of the zero-point term: the activations' factor sign(I) u_j 2^a_j and
+// the weights' factor -z 2^b_j, a_j + b_j = 4j - 18, both exact in e4m3 for
+// u_j, z in 0..15 (exponents within -9..4).
+__host__ __device__ constexpr int f8_digit_a(int j) { return j < 4 ? 4 * j - 9 : 4; }
+__host__ __device__ constexpr int f8_digit_b(int j) { return 4 * j - 18 - f8_digit_a(j); }
+
 struct W4a8Params {
   CUtensorMap tm_a;  // x8 [M][K] bytes, box 128 x 128, 128-byte swizzle
+  CUtensorMap tm_d;  // digit rows [M][ceil(K/128/DG) * 128] bytes, box 128 x 128, 128-byte swizzle
   CUtensorMap tm_p;  // TILE words [N/128][K/64][8][128], box 128 x 8 x 2 x 1
   CUtensorMap tm_s;  // scales [G][N] 16-bit, box 128 x 1
   CUtensorMap tm_z;  // zeros [G][N/8] words, box 16 x 1
   uint16_t* y;
-  const float* xs;     // [M][K / 128] sums of the e4m3 activations per block
   const float* sx;     // the per-tensor activation scale
   int* status;
   int M, N, K, group;
   int m_blocks, n_blocks, num_tiles, k_blocks;
 };
 
-// Workspace: x8 [M][K] bytes, xs [M][K/128] floats, the partial maxima, s_x.
+// Workspace: x8 [M][K] bytes, the digit rows [M][dpitch] bytes (32 per group),
+// the partial maxima, s_x.
 struct W4a8Ws {
-  size_t x8, xs, parts, sx, total;
+  size_t x8, xd, parts, sx, total, dpitch;
 };
 W4a8Ws w4a8_ws(int M, int K) {
   W4a8Ws w;
+  w.dpitch = (size_t)((K / BK + DG - 1) / DG) * 128;
   w.x8 = 0;
-  w.xs = ((size_t)M * K + 255) & ~(size_t)255;
-  w.parts = (w.xs + (size_t)M * (K / BK) * 4 + 255) & ~(size_t)255;
+  w.xd = ((size_t)M * K + 255) & ~(size_t)255;
+  w.parts = (w.xd + (size_t)M * w.dpitch + 255) & ~(size_t)255;
   w.sx = w.parts + AMAX_PARTS * 4;
   w.total = w.sx + 256;
   return w;
@@ -141,6 +170,9 @@ __global__ void __launch_bounds__(256) w4a8_amax_kernel(const uint4* __restrict_
   }
 }
 
+// 2^e for e in [-126, 127] (exact)
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+
 __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
   uint16_t d;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
@@ -153,14 +185,17 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t v) {
                      __half2float(__ushort_as_half((uint16_t)(h >> 16))));
 }
 
-// s_x from the partial maxima, then x8 and the per-(row, 128-column block) sums:
-// one warp per block, four values per lane.
+// s_x from the partial maxima, then x8 and, per (row, 128-column block), the
+// digits of I = 512 * (the block's sum of the codes): one warp per block, four
+// values per lane. I is summed exactly in integers (every code times 512 is an
+// integer of at most 229376 in magnitude; 128 of them stay below 2^25).
 template <bool BF16>
 __global__ void __launch_bounds__(256) w4a8_quant_kernel(const uint16_t* __restrict__ x,
                                                          const float* __restrict__ parts,
                                                          int nparts, int M, int K,
                                                          uint8_t* __restrict__ x8,
-                                                         float* __restrict__ xs,
+                                                         uint8_t* __restrict__ xd,
+                                                         size_t dpitch,
                                                          float* __restrict__ sx_out) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
@@ -198,10 +233,26 @@ __global__ void __launch_bounds__(256) w4a8_quant_kernel(const uint16_t* __restr
     const uint16_t c01 = e4m3x2(f[0], f[1]), c23 = e4m3x2(f[2], f[3]);
     *reinterpret_cast<uint32_t*>(x8 + off) = (uint32_t)c01 | ((uint32_t)c23 << 16);
     const float2 d01 = e4m3x2_to_float2(c01), d23 = e4m3x2_to_float2(c23);
-    float sum = (d01.x + d01.y) + (d23.x + d23.y);
+    int isum = __float2int_rn(d01.x * 512.f) + __float2int_rn(d01.y * 512.f) +
+               __float2int_rn(d23.x * 512.f) + __float2int_rn(d23.y * 512.f);
 #pragma unroll
-    for (int d = 16; d > 0; d >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, d);
-    if (lane == 0) xs[(size_t)row * KB + kb] = sum;
+    for (int d = 16; d > 0; d >>= 1) isum += __shfl_xor_sync(0xffffffffu, isum, d);
+    // lanes 0..1 write the block's 32 digit bytes: sign(I) u_j 2^a_j for j < 7, then zeros
+    if (lane < 2) {
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+      if (lane == 0) {
+        const uint32_t u = (uint32_t)(isum < 0 ? -isum : isum);
+        const float sg = isum < 0 ? -1.f : 1.f;
+        float dv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          dv[j] = j < DIGITS ? sg * (float)((u >> (4 * j)) & 0xFu) * pow2f(f8_digit_a(j)) : 0.f;
+        w[0] = (uint32_t)e4m3x2(dv[0], dv[1]) | ((uint32_t)e4m3x2(dv[2], dv[3]) << 16);
+        w[1] = (uint32_t)e4m3x2(dv[4], dv[5]) | ((uint32_t)e4m3x2(dv[6], dv[7]) << 16);
+      }
+      *reinterpret_cast<uint4*>(xd + (size_t)row * dpitch + 32 * (size_t)kb + 16 * lane) =
+          make_uint4(w[0], w[1], w[2], w[3]);
+    }
   }
 }
 
@@ -213,6 +264,9 @@ struct Bars {
   __device__ uint32_t empty(int s) const { return base + 8 * (2 * STAGES + s); }
   __device__ uint32_t accfull(int b) const { return base + 8 * (3 * STAGES + b); }
   __device__ uint32_t accempty(int b) const { return base + 8 * (3 * STAGES + 2 + b); }
+  // the activations' digit rows: TMA landed / the MMAs reading them completed
+  __device__ uint32_t dfull(int d) const { return base + 8 * (3 * STAGES + 4 + d); }
+  __device__ uint32_t dempty(int d) const { return base + 8 * (3 * STAGES + 6 + d); }
 };
 
 __device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
@@ -253,6 +307,8 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_gemm_kernel(const __grid_cons
     for (int b = 0; b < 2; ++b) {
       mbar_init(bars.accfull(b), 1);
       mbar_init(bars.accempty(b), EPI_WARPS);
+      mbar_init(bars.dfull(b), 1);
+      mbar_init(bars.dempty(b), 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -263,6 +319,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_gemm_kernel(const __grid_cons
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&p.tm_a);
+    prefetch_tmap(&p.tm_d);
     prefetch_tmap(&p.tm_p);
     prefetch_tmap(&p.tm_s);
     prefetch_tmap(&p.tm_z);
@@ -276,14 +333,26 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_gemm_kernel(const __grid_cons
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int it = 0;
-      int last_armed[STAGES];
+      int it = 0, dg = 0;  // blocks, and groups of DG blocks (digit rows), so far
+      int last_armed[STAGES], last_dg[2] = {-1, -1};
       for (int s = 0; s < STAGES; ++s) last_armed[s] = -1;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
         const int m_blk = tile % p.m_blocks, n_blk = tile / p.m_blocks;
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % STAGES;
+          if (kb % DG == 0) {  // the digit rows of blocks kb .. kb + DG - 1
+            const int d = dg & 1;
+            if (!bounded_wait(bars.dempty(d), ((dg >> 1) & 1) ^ 1, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bars.dfull(d), X_BYTES);
+            last_dg[d] = dg;
+            tma_load_2d(sbase + OFF_XD + d * X_BYTES, &p.tm_d, bars.dfull(d), (kb / DG) * 128,
+                        m_blk * BM);
+            ++dg;
+          }
           if (!bounded_wait(bars.empty(s), ((it / STAGES) & 1) ^ 1, abort_flag, p.status)) {
             ok = false;
             break;
@@ -297,23 +366,29 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_gemm_kernel(const __grid_cons
           tma_load_2d(sbase + OFF_Z + s * 128, &p.tm_z, bars.full(s), n_blk * (BN / 8), grow);
         }
       }
-      if (!ok)
+      if (!ok) {
         for (int s = 0; s < STAGES; ++s)
           if (last_armed[s] >= 0) drain_wait(bars.full(s), (last_armed[s] / STAGES) & 1);
+        for (int d = 0; d < 2; ++d)
+          if (last_dg[d] >= 0) drain_wait(bars.dfull(d), (last_dg[d] >> 1) & 1);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ UMMA issuer
     if (lane == 0) {
       constexpr uint32_t IDESC = idesc_f16(0, BM, BN);  // kind::f8f6f4: A, B e4m3 (0), D f32
-      int it = 0;
+      int it = 0, dg = -1;
       bool ok = true, issued = false;
       for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % STAGES, buf = it & 1;
           const uint32_t ph = (it / STAGES) & 1;
+          if (kb % DG == 0) ++dg;
+          const int d = dg & 1;
           if (!bounded_wait(bars.accempty(buf), ((it >> 1) & 1) ^ 1, abort_flag, p.status) ||
               !bounded_wait(bars.full(s), ph, abort_flag, p.status) ||
-              !bounded_wait(bars.bfull(s), ph, abort_flag, p.status)) {
+              !bounded_wait(bars.bfull(s), ph, abort_flag, p.status) ||
+              (kb % DG == 0 && !bounded_wait(bars.dfull(d), (dg >> 1) & 1, abort_flag, p.status))) {
             ok = false;
             break;
           }
@@ -323,9 +398,15 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_gemm_kernel(const __grid_cons
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k)
             umma_f8(tmem + buf * BN, adesc + 2 * k, bdesc + 2 * k, IDESC, k != 0);
+          // the zero point: the block's 32-byte slice of the activations' digit rows
+          // against the weights' (-z 2^b_j rows), into the same accumulator
+          const uint64_t xdesc = smem_desc_k128(sbase + OFF_XD + d * X_BYTES);
+          const uint64_t wdesc = smem_desc_k128(sbase + OFF_WD);
+          umma_f8(tmem + buf * BN, xdesc + 2 * (kb % DG), wdesc + 2 * (it % 4), IDESC, 1);
           issued = true;
           umma_commit(bars.empty(s));
           umma_commit(bars.accfull(buf));
+          if (kb % DG == DG - 1 || kb == KB - 1) umma_commit(bars.dempty(d));
         }
       }
       if (!ok && issued) {
@@ -342,15 +423,11 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_gemm_kernel(const __grid_cons
     for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
       const int m_blk = tile % p.m_blocks, n_blk = tile / p.m_blocks;
       const int row = m_blk * BM + quarter * 32 + lane;
-      const float* xs_row = p.xs + (size_t)min(row, p.M - 1) * KB;
       uint64_t y2[32];  // the 64 columns' running sums, two per register
 #pragma unroll
       for (int c = 0; c < 32; ++c) y2[c] = 0;
-      float xs_next = __ldg(xs_row);
       for (int kb = 0; kb < KB; ++kb, ++it) {
         const int s = it % STAGES, buf = it & 1;
-        const float xs = xs_next;
-        if (kb + 1 < KB) xs_next = __ldg(xs_row + kb + 1);
         if (!bounded_wait(bars.accfull(buf), (it >> 1) & 1, abort_flag, p.status) ||
             !bounded_wait(bars.bfull(s), (it / STAGES) & 1, abort_flag, p.status)) {
           ok = false;
@@ -358,7 +435,6 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_gemm_kernel(const __grid_cons
         }
         tc_fence_after();
         const float* ab = reinterpret_cast<const float*>(smem + OFF_AB + s * AB_BYTES);
-        const uint64_t nxs2 = f32x2_pack(-xs, -xs);
 #pragma unroll
         for (int c0 = 0; c0 < 64; c0 += 32) {
           uint32_t r[32];
@@ -367,12 +443,9 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_gemm_kernel(const __grid_cons
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             const float4 a4 = *reinterpret_cast<const float4*>(ab + 64 * half + c0 + 4 * q);
-            const float4 b4 = *reinterpret_cast<const float4*>(ab + BN + 64 * half + c0 + 4 * q);
-            // y = fma(512 s, acc, fma(-z s, xs, y)), two columns per instruction
-            // (the same two roundings per column as scalar FMAs)
+            // y = fma(512 s, acc, y), two columns per instruction (the same
+            // rounding per column as a scalar FMA); acc already holds the zero point
             const int c = (c0 + 4 * q) / 2;
-            y2[c] = f32x2_fma(f32x2_pack(b4.x, b4.y), nxs2, y2[c]);
-            y2[c + 1] = f32x2_fma(f32x2_pack(b4.z, b4.w), nxs2, y2[c + 1]);
             y2[c] = f32x2_fma(f32x2_pack(a4.x, a4.y),
                               f32x2_pack(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1])),
                               y2[c]);
@@ -448,14 +521,25 @@ __global__ void __launch_bounds__(THREADS, 1) w4a8_gemm_kernel(const __grid_cons
           }
         }
         {
-          // this column's 512 s and z s for the epilogue
+          // this column's 512 s for the epilogue, and its digit row for this block:
+          // -z 2^b_j for j < 7, then zeros (32 bytes at K slice it % 4 of the
+          // swizzled rows: two 16-byte chunks)
           const uint16_t* sS = reinterpret_cast<const uint16_t*>(smem + OFF_S + s * S_BYTES);
           const uint32_t* sZ = reinterpret_cast<const uint32_t*>(smem + OFF_Z + s * 128);
           const float sc = half_bits_to_float<BF16>(sS[dt]);
-          const float z = (float)((sZ[dt >> 3] >> (4 * (dt & 7))) & 0xFu);
+          const float nz = -(float)((sZ[dt >> 3] >> (4 * (dt & 7))) & 0xFu);
           float* ab = reinterpret_cast<float*>(smem + OFF_AB + s * AB_BYTES);
           ab[dt] = 512.f * sc;
-          ab[BN + dt] = z * sc;
+          float dv[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) dv[j] = j < DIGITS ? nz * pow2f(f8_digit_b(j)) : 0.f;
+          const uint4 lo = make_uint4(
+              (uint32_t)e4m3x2(dv[0], dv[1]) | ((uint32_t)e4m3x2(dv[2], dv[3]) << 16),
+              (uint32_t)e4m3x2(dv[4], dv[5]) | ((uint32_t)e4m3x2(dv[6], dv[7]) << 16), 0u, 0u);
+          uint8_t* sW = smem + OFF_WD + (dt >> 3) * 1024 + (dt & 7) * 128;
+          const int c0 = (2 * (it % 4)) ^ (dt & 7), c1 = (2 * (it % 4) + 1) ^ (dt & 7);
+          *reinterpret_cast<uint4*>(sW + c0 * 16) = lo;
+          *reinterpret_cast<uint4*>(sW + c1 * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
         fence_proxy_async_smem();
         mbar_arrive(bars.bfull(s));
@@ -529,7 +613,8 @@ cudaError_t launch_w4a8(const void* x, const uint32_t* qw, const void* scales,
   const W4a8Ws w = w4a8_ws(M, K);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint8_t* x8 = ws + w.x8;
-  float* xs = reinterpret_cast<float*>(ws + w.xs);
+  uint8_t* xd = ws + w.xd;
+  size_t dpitch = w.dpitch;
   float* parts = reinterpret_cast<float*>(ws + w.parts);
   float* sx = reinterpret_cast<float*>(ws + w.sx);
 
@@ -548,7 +633,7 @@ cudaError_t launch_w4a8(const void* x, const uint32_t* qw, const void* scales,
     int np = g1, Mi = M, Ki = K;
     const long long units = (long long)M * (K / BK);
     const int g2 = (int)std::min<long long>((long long)info.sm_count * 8, (units + 7) / 8);
-    void* args[] = {&xh, &parts, &np, &Mi, &Ki, &x8, &xs, &sx};
+    void* args[] = {&xh, &parts, &np, &Mi, &Ki, &x8, &xd, &dpitch, &sx};
     const void* fn = bf16 ? reinterpret_cast<const void*>(&w4a8_quant_kernel<true>)
                           : reinterpret_cast<const void*>(&w4a8_quant_kernel<false>);
     if ((err = launch_pdl(fn, dim3(std::max(1, g2)), dim3(256), 0, stream, args)) != cudaSuccess)
@@ -560,6 +645,8 @@ cudaError_t launch_w4a8(const void* x, const uint32_t* qw, const void* scales,
   const uint64_t NG = ((uint64_t)N + 127) / 128;
   bool ok = encode_2d_map(&p.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, x8, K, M, (uint64_t)K, BK, BM,
                           CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && encode_2d_map(&p.tm_d, CU_TENSOR_MAP_DATA_TYPE_UINT8, xd, dpitch, M, dpitch, 128, BM,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && encode_tile_box(&p.tm_p, qw, K, NG, 8, 2, 1);
   ok = ok && encode_2d_map(&p.tm_s, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, N, G, (uint64_t)N * 2,
                            BN, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -567,7 +654,6 @@ cudaError_t launch_w4a8(const void* x, const uint32_t* qw, const void* scales,
                            (uint64_t)N / 2, BN / 8, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (!ok) return cudaErrorInvalidValue;
   p.y = static_cast<uint16_t*>(y);
-  p.xs = xs;
   p.sx = sx;
   p.status = status;
   p.M = M;
