@@ -101,3 +101,41 @@ def test_w4a8_zero_activations(w4):
     w4.w4a8_gemm(x, layer.qw, layer.scales, layer.zeros, y, M, N, K, 128, torch.bfloat16, ws)
     torch.cuda.synchronize()
     assert torch.count_nonzero(y).item() == 0
+
+
+def test_w4a8_extreme_group_sums(w4):
+    """Activations that drive each 128-value block's code sum to its extremes: the
+    zero point enters the tensor cores as the seven base-16 digits of 512 * (the
+    block's code sum), so a block of 448s (the largest sum, every digit used), a
+    block of -448s (negative), blocks that cancel exactly (sum 0) and blocks of
+    small codes must all match the oracle. K = 640: five blocks, the last of a
+    second digit row."""
+    import torch
+    K, N, M = 640, 256, 6
+    L = synth.make_custom_layer([153, K, N], K, N, group=128, dtype="bf16")
+    layer = w4.repack_awq(to_dev(L.qweight), to_dev(L.qzeros), half_to_dev(L.scales, "bf16"),
+                          K, N, 128, torch.bfloat16)
+    c = 3.5
+    xf = np.zeros((M, K), dtype=np.float64)
+    xf[0, :] = c                                   # every code 448: the largest block sums
+    xf[1, :] = -c                                  # the most negative
+    xf[2, :] = np.where(np.arange(K) % 2 == 0, c, -c)  # every block sums to zero
+    xf[3, :] = c * 2.0 ** -12                      # codes far below 448
+    xf[3, 0] = c                                   # ... with one at 448 setting s_x
+    xf[4, :] = np.where((np.arange(K) // 128) % 2 == 0, c, -c)  # alternate sign per block
+    xf[5, :] = np.linspace(-c, c, K)
+    xb = synth.f32_to_bits(xf.astype(np.float32), "bf16")
+    x = half_to_dev(xb, "bf16")
+    ws = torch.empty(w4.w4a8_gemm_workspace_size(M, K), dtype=torch.uint8, device="cuda")
+    y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    w4.w4a8_gemm(x, layer.qw, layer.scales, layer.zeros, y, M, N, K, 128, torch.bfloat16, ws)
+    torch.cuda.synchronize()
+    codes_ref, _ = f8.quantize_act_per_tensor(oracle.half_bits_to_f64(xb, "bf16"))
+    got_codes = np.where(ws[:M * K].cpu().numpy().reshape(M, K) == 0x80, 0,
+                         ws[:M * K].cpu().numpy().reshape(M, K))
+    assert np.array_equal(got_codes, codes_ref)
+    got = half_from_dev(y)
+    y_ref = f8.reference_y_w4a8(xb, L.qweight, L.qzeros, L.scales, 128, "bf16", "awq")
+    assert oracle.rel_err(oracle.half_bits_to_f64(got, "bf16"), y_ref) <= TOL
+    assert ulp_error(got, y_ref, "bf16") <= 1.0
+    assert w4.w4_device_status() == 0
