@@ -100,10 +100,10 @@ __global__ void __launch_bounds__(BLOCK_THREADS) to_tile_kernel(
 
 
 // ---- vectorised repacks into the TILE layout (no act-order) ---------------------
-// One block per (128-column group, 64-row k-atom): the source block is read with
-// 16-byte loads into shared memory, turned into the group's 1024 TILE words in
-// registers, and leaves as 4 KB of 16-byte stores. Requires N % 32 == 0 (whole
-// 16-byte source pieces); a partial last group gets zero words.
+// One block per (128-column group, KA 64-row k-atoms): the group's 1024 TILE words
+// per k-atom are formed in registers and leave as 4 KB of 16-byte stores staged
+// in shared memory. Requires N % 32 == 0 (whole 16-byte source pieces); a partial
+// last group gets zero words.
 // The permutation {0, 2, 4, 6, 1, 3, 5, 7}: nibble p of an AWQ word holds column
 // sigma(p) of its block, and nibble p of a TILE word holds row sigma(p).
 __host__ __device__ constexpr int sigma(int p) { return p < 4 ? 2 * p : 2 * (p - 4) + 1; }
@@ -114,6 +114,12 @@ __device__ __forceinline__ int tile_word_index(int cl, int r) {
   const int tt = cl >> 4, c16 = cl & 15;
   return tt * 128 + 4 * (4 * (c16 & 7) + (r & 3)) + 2 * (r >> 2) + (c16 >> 3);
 }
+
+// Staged TILE words: word i of an atom sits at i with its 16-byte chunk index
+// (bits 2-4) XORed with its tile (bits 7-9), so that the scatter below, whose
+// warp spans the eight tiles, meets two-way bank conflicts instead of eight-way;
+// a 16-byte chunk stays whole.
+__device__ __forceinline__ int staged_word(int i) { return i ^ (((i >> 7) & 7) << 2); }
 
 // In-register transpose of an 8 x 8 nibble matrix (w[i] nibble p <-> w[p] nibble i).
 __device__ __forceinline__ void transpose8x8_nibbles(uint32_t (&w)[8]) {
@@ -141,49 +147,33 @@ __device__ __forceinline__ void transpose8x8_nibbles(uint32_t (&w)[8]) {
 // nibble p (the order {0,4,1,5,2,6,3,7} read backwards), and a TILE word holds
 // row 8r + sigma(p) at nibble p: taking the eight rows in sigma order makes the
 // repack a plain nibble transpose whose word q is column 8c + sigma(q).
+// Thread t takes column word c = t % 16 of the group and the 8-row run r8 = t / 16
+// (k-atom r8 / 8): eight 4-byte loads, coalesced across the warp (two rows of
+// sixteen words), straight into registers.
 template <int KA>
 __global__ void __launch_bounds__(256) awq_to_tile_vec_kernel(const uint32_t* __restrict__ qweight,
                                                               uint32_t* __restrict__ out, int K,
                                                               int N) {
-  // KA k-atoms per CTA: every thread has KA 16-byte loads in flight
-  __shared__ uint32_t in_s[KA * 64][17];
   __shared__ __align__(16) uint32_t out_s[KA][1024];
   const int cg = blockIdx.x, a0 = blockIdx.y * KA;
   const int C = N / 8, A = K / 64;
   const int ncw = min(16, C - cg * 16);  // column words of this group present (a multiple of 4)
-  {
-    const int row = threadIdx.x >> 2, q4 = threadIdx.x & 3;
-    uint4 v[KA];
-#pragma unroll
-    for (int u = 0; u < KA; ++u) {
-      v[u] = make_uint4(0, 0, 0, 0);
-      if (4 * q4 < ncw)
-        v[u] = *reinterpret_cast<const uint4*>(qweight + (size_t)(64 * (a0 + u) + row) * C +
-                                               16 * cg + 4 * q4);
-    }
-#pragma unroll
-    for (int u = 0; u < KA; ++u) {
-      in_s[64 * u + row][4 * q4] = v[u].x;
-      in_s[64 * u + row][4 * q4 + 1] = v[u].y;
-      in_s[64 * u + row][4 * q4 + 2] = v[u].z;
-      in_s[64 * u + row][4 * q4 + 3] = v[u].w;
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x < 128 * KA) {
-    const int u = threadIdx.x >> 7, c = threadIdx.x & 15, r = (threadIdx.x >> 4) & 7;
+  const int c = threadIdx.x & 15, r8 = threadIdx.x >> 4, u = r8 >> 3, r = r8 & 7;
+  if (u < KA) {
     uint32_t w[8];
 #pragma unroll
-    for (int p = 0; p < 8; ++p) w[p] = in_s[64 * u + 8 * r + sigma(p)][c];
+    for (int p = 0; p < 8; ++p)
+      w[p] = c < ncw ? __ldg(qweight + (size_t)(64 * (a0 + u) + 8 * r + sigma(p)) * C + 16 * cg + c)
+                     : 0u;
     transpose8x8_nibbles(w);
 #pragma unroll
-    for (int q = 0; q < 8; ++q) out_s[u][tile_word_index(8 * c + sigma(q), r)] = w[q];
+    for (int q = 0; q < 8; ++q) out_s[u][staged_word(tile_word_index(8 * c + sigma(q), r))] = w[q];
   }
   __syncthreads();
 #pragma unroll
-  for (int u = 0; u < KA; ++u) {
-    uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)cg * A + a0 + u) * 8 * 128);
-    dst[threadIdx.x] = reinterpret_cast<const uint4*>(out_s[u])[threadIdx.x];
+  for (int v = 0; v < KA; ++v) {
+    uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)cg * A + a0 + v) * 8 * 128);
+    dst[threadIdx.x] = *reinterpret_cast<const uint4*>(&out_s[v][staged_word(4 * threadIdx.x)]);
   }
 }
 
