@@ -199,11 +199,11 @@ __global__ void __launch_bounds__(256) std_to_tile_vec_kernel(const uint32_t* __
     const uint32_t ev2 = ev | (ev >> 4), od2 = od | (od >> 4);
     uint32_t o;
     asm("prmt.b32 %0, %1, %2, 0x6420;" : "=r"(o) : "r"(ev2), "r"(od2));
-    out_s[tile_word_index(c4 + j, r)] = o;
+    out_s[staged_word(tile_word_index(c4 + j, r))] = o;
   }
   __syncthreads();
   uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)cg * A + a) * 8 * 128);
-  dst[threadIdx.x] = reinterpret_cast<const uint4*>(out_s)[threadIdx.x];
+  dst[threadIdx.x] = *reinterpret_cast<const uint4*>(&out_s[staged_word(4 * threadIdx.x)]);
 }
 
 // AWQ qweight [K][N/8] -> standard [K/8][N]: an 8 x 8 nibble transpose per thread.
