@@ -123,6 +123,8 @@ struct SmemLayout {
 // 16 columns as they are stored (one 32-bit word per lane group: columns gg
 // and gg + 8), then per warp and group slot the tile's two zero words.
 // xsum: per group slot, the sum of x over the group's rows for each token.
+// recv: the cluster peers' partial sums of this CTA's output columns, [peer]
+// [token][column] (the reducing threads walk consecutive columns).
 __host__ __device__ inline SmemLayout smem_layout(int MT, int m_rows, int x_stride, int nbuf,
                                                   int ring, int maxg, int S, int slice) {
   SmemLayout L;
@@ -601,7 +603,7 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
   auto push = [&](int col, int m, float v) {
     const int owner = col / SL;
     float* dst = cluster.map_shared_rank(recv, owner);
-    dst[((size_t)srank * SL + (col - owner * SL)) * MR + m] = v;
+    dst[((size_t)srank * MR + m) * SL + (col - owner * SL)] = v;
   };
   if (has_cols) {
 #pragma unroll
@@ -628,7 +630,7 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
       const int n = cgi * NCOL + c_lo + cl;
       if (n >= p.N) continue;
       float sum = 0.f;
-      for (int r = 0; r < S; ++r) sum += recv[((size_t)r * SL + cl) * MR + m];
+      for (int r = 0; r < S; ++r) sum += recv[((size_t)r * MR + m) * SL + cl];
       if (p.bias != nullptr) sum += half_bits_to_float<BF16>(p.bias[n]);  // one rounding below
       yg[(size_t)m * p.N + n] = float_to_half_bits<BF16>(sum);
     }
