@@ -21,11 +21,10 @@
 //  * Dequantisation ("vLLM AWQ 4-bit 量化实践" §5.3: (b - zeros) * scales) is
 //    split: one LOP3 turns a nibble pair into MAGIC + q halves and the
 //    per-(group, column) scale multiplies the fp32 partial sum of each group.
-//    With bf16 and M <= 16 the MMA consumes MAGIC + q = 128 + q directly and
-//    the group sum is corrected by (128 + z) * s * sum(x); the per-group sums
-//    of x are computed once per CTA (MMAs against an all-ones operand) before
-//    the weight loop. Otherwise one packed subtraction per register forms
-//    q - z, exact in both types.
+//    With bf16 one packed subtraction of 128 + z per register forms q - z
+//    exactly (on the FMA pipe, beside the LOP3s on the ALU pipe); with fp16
+//    nibbles of two slots are taken per shift and one packed fma or
+//    subtraction forms q - z, exact as well.
 //  * The CTA stages its slice of x in shared memory (gathering x[:, perm] for
 //    act-order layers), padded so fragment loads are free of bank conflicts;
 //    when it does not fit, x is staged in double-buffered chunks while the
@@ -112,7 +111,7 @@ struct DecodeParams {
 };
 
 struct SmemLayout {
-  int xs, ring, bars, cnt, meta, xsum, recv, total;
+  int xs, ring, bars, cnt, meta, recv, total;
 };
 
 // xs: nbuf buffers of M token rows (the MMA lanes whose token row is beyond M
@@ -122,7 +121,6 @@ struct SmemLayout {
 // and the abort flag. meta: per warp and group slot, the scales of the tile's
 // 16 columns as they are stored (one 32-bit word per lane group: columns gg
 // and gg + 8), then per warp and group slot the tile's two zero words.
-// xsum: per group slot, the sum of x over the group's rows for each token.
 // recv: the cluster peers' partial sums of this CTA's output columns, [peer]
 // [token][column] (the reducing threads walk consecutive columns).
 __host__ __device__ inline SmemLayout smem_layout(int MT, int m_rows, int x_stride, int nbuf,
@@ -133,8 +131,7 @@ __host__ __device__ inline SmemLayout smem_layout(int MT, int m_rows, int x_stri
   L.bars = L.ring + ring * STAGE_BYTES;
   L.cnt = L.bars + (ring + 2) * 8;
   L.meta = (L.cnt + (2 * ring + 2 + 1) * 4 + 15) & ~15;
-  L.xsum = L.meta + DEC_WARPS * maxg * (8 * 4 + 8);
-  L.recv = L.xsum + maxg * 8 * MT * 4;
+  L.recv = L.meta + DEC_WARPS * maxg * (8 * 4 + 8);
   L.total = L.recv + S * slice * 8 * MT * 4;
   return L;
 }
@@ -145,17 +142,12 @@ __host__ __device__ inline SmemLayout smem_layout(int MT, int m_rows, int x_stri
 #endif
 constexpr int decode_min_ctas(int MT) { return MT == 1 ? W4_DECODE_MIN_CTAS : 2; }
 
-// With bf16 activations the MMA consumes the codes as 128 + q (exact in bf16)
-// and each group's sum is corrected by (128 + z) s sum(x); those corrections
-// are summed over the chunk's groups before the weight loop (from per-group
-// sums of x taken with all-ones MMAs), so the loop only adds s * acc per group.
-// With fp16 one packed subtraction per register forms q - z exactly (the zero
-// pairs are built per group from the staged zero words).
+// The MMA consumes q - z, exact in both types (the zero pairs are built per
+// group from the staged zero words), and the loop adds s * acc per group.
 template <int MT, bool BF16, bool G64>
 __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
     w4a16_decode_kernel(const DecodeParams p) {
   constexpr uint32_t MAGIC = Magic<BF16>::pair;  // 128 (bf16) / 1024 (fp16) in both halves
-  constexpr uint32_t ONES = 0x3F803F80u;         // bf16 1.0 in both halves
   extern __shared__ __align__(1024) uint8_t smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -194,7 +186,6 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
     return make_float2(half_bits_to_float<BF16>((uint16_t)(w & 0xFFFFu)),
                        half_bits_to_float<BF16>((uint16_t)(w >> 16)));
   };
-  float* xsum = reinterpret_cast<float*>(smem + L.xsum);  // [maxg][MR] (bf16 only)
   float* recv = reinterpret_cast<float*>(smem + L.recv);
   constexpr int NCOL = 16 * DEC_WARPS;
 
@@ -345,7 +336,7 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = tc[i][j] = 0.f;
   float2 gf = make_float2(0.f, 0.f);  // scales of the open group (columns gg, gg + 8)
-  uint32_t zl = 0, zh = 0;            // fp16: MAGIC + z pairs of the open group
+  uint32_t zl = 0, zh = 0;            // MAGIC + z pairs of the open group
   uint32_t nl = 0, nh = 0;            // fp16: -(64 + z) pairs (the high slot's offset)
   int gslot = -1;                     // its slot in meta (-1: none open)
   uint32_t rslot = 0, rphase = 0;     // ring slot of the next stage, its parity
@@ -366,14 +357,16 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
     if (gslot >= 0) flush();
     ++gslot;
     gf = scale_pair(meta[gslot * 8 + gg]);
-    if constexpr (!BF16) {
+    {
       const uint2 zw = zraw[gslot];
       const uint32_t z0 = (zw.x >> (4 * gg)) & 0xFu, z1 = (zw.y >> (4 * gg)) & 0xFu;
       zl = MAGIC + z0 * 0x00010001u;
       zh = MAGIC + z1 * 0x00010001u;
-      // -(64 + z) in fp16: 64 is 0x5400, whose last mantissa bit is 1/16
-      nl = (0xD400u + 16u * z0) * 0x00010001u;
-      nh = (0xD400u + 16u * z1) * 0x00010001u;
+      if constexpr (!BF16) {
+        // -(64 + z) in fp16: 64 is 0x5400, whose last mantissa bit is 1/16
+        nl = (0xD400u + 16u * z0) * 0x00010001u;
+        nh = (0xD400u + 16u * z1) * 0x00010001u;
+      }
     }
   };
 
@@ -382,8 +375,6 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
     const int c1 = min(ka1, c0 + p.chunk_atoms);
     const int KC = (c1 - c0) * ATOM_K;
     const int b = NB == 2 ? (ci & 1) : 0;
-    const int g_first = (c0 * ATOM_K) >> p.gshift;
-    const int ng = ((c1 * ATOM_K - 1) >> p.gshift) - g_first + 1;
     const bool live = !*abort_flag;
 
     // 1) scales / zeros (the first chunk's were staged before the wait)
@@ -407,59 +398,11 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
         v.w = h[6] | ((uint32_t)h[7] << 16);
         *reinterpret_cast<uint4*>(xb + (size_t)m * p.x_stride + 8 * c) = v;
       }
-      if constexpr (BF16) __syncthreads();  // the sums below read every warp's rows
     } else if (live) {
       bounded_wait(xbar0 + 8 * b, (uint32_t)((NB == 2 ? ci >> 1 : ci) & 1), abort_flag, p.status);
     }
-    // 3) per-group sums of x (bf16): warp w takes group slots w, w + 8, ... and runs
-    //    the group's 32-row halves in this chunk through all-ones MMAs (two chains)
-    if constexpr (BF16) {
-      for (int gl = warp; gl < ng; gl += DEC_WARPS) {
-        const int gi = g_first + gl;
-        const int r0 = max(c0 * ATOM_K, p.gshift >= 31 ? 0 : gi << p.gshift);
-        const int r1 = min(c1 * ATOM_K, p.gshift >= 31 ? p.K : (gi + 1) << p.gshift);
-        for (int mt = 0; mt < MT; ++mt) {
-          const int row = 8 * mt + gg;
-          const uint16_t* xr = xb + (size_t)(row < M ? row : 0) * p.x_stride + 8 * t;
-          float sa[2][4] = {};
-          for (int r = r0; r < r1; r += 64) {
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              if (r + 32 * c < r1) {
-                const uint4 xf =
-                    *reinterpret_cast<const uint4*>(xr + (r + 32 * c - c0 * ATOM_K));
-                mma16816<true>(sa[c], ONES, ONES, ONES, ONES, xf.x, xf.y);
-                mma16816<true>(sa[c], ONES, ONES, ONES, ONES, xf.z, xf.w);
-              }
-            }
-          }
-          if (gg == 0)
-            *reinterpret_cast<float2*>(xsum + gl * MR + 8 * mt + 2 * t) =
-                make_float2(sa[0][0] + sa[1][0], sa[0][1] + sa[1][1]);
-        }
-      }
-    }
-    __syncthreads();  // x, the group sums and every warp's scale / zero stage are ready
-    // 4) bf16: remove every group's (128 + z) s sum(x) from the total up front
-    //    ((128 + z) s is exact in fp32: two 8-bit significands)
-    if (BF16 && has_cols) {
-      for (int gl = 0; gl < ng; ++gl) {
-        const float2 sc = scale_pair(meta[gl * 8 + gg]);
-        const uint2 zw = zraw[gl];
-        const float cl = sc.x * (float)(128 + ((zw.x >> (4 * gg)) & 0xF));
-        const float ch = sc.y * (float)(128 + ((zw.y >> (4 * gg)) & 0xF));
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          const float2 xg = *reinterpret_cast<const float2*>(xsum + gl * MR + 8 * mt + 2 * t);
-          tc[mt][0] = fmaf(-cl, xg.x, tc[mt][0]);
-          tc[mt][1] = fmaf(-cl, xg.y, tc[mt][1]);
-          tc[mt][2] = fmaf(-ch, xg.x, tc[mt][2]);
-          tc[mt][3] = fmaf(-ch, xg.y, tc[mt][3]);
-        }
-      }
-    }
-
-    // 4) consume this chunk's stages. Shared-memory operands are addressed with
+    __syncthreads();  // x and every warp's scale / zero stage are ready
+    // 3) consume this chunk's stages. Shared-memory operands are addressed with
     //    32-bit shared-window addresses with constant offsets inside a stage.
     // this lane's x row at the chunk's first atom, column 8t; lanes whose token
     // row is beyond M read row 0 (their output columns are discarded)
@@ -483,10 +426,11 @@ __global__ void __launch_bounds__(DEC_THREADS, decode_min_ctas(MT))
       for (int step = 0; step < 2; ++step) {
         const int sh = 8 * step;
         if constexpr (BF16) {
-          af[step][0] = lop3_and_or(wlo >> sh, 0x000F000Fu, MAGIC);
-          af[step][2] = lop3_and_or(wlo >> (sh + 4), 0x000F000Fu, MAGIC);
-          af[step][1] = lop3_and_or(whi >> sh, 0x000F000Fu, MAGIC);
-          af[step][3] = lop3_and_or(whi >> (sh + 4), 0x000F000Fu, MAGIC);
+          // 128 + q minus 128 + z: q - z exactly
+          af[step][0] = sub_x2<true>(lop3_and_or(wlo >> sh, 0x000F000Fu, MAGIC), zl);
+          af[step][2] = sub_x2<true>(lop3_and_or(wlo >> (sh + 4), 0x000F000Fu, MAGIC), zl);
+          af[step][1] = sub_x2<true>(lop3_and_or(whi >> sh, 0x000F000Fu, MAGIC), zh);
+          af[step][3] = sub_x2<true>(lop3_and_or(whi >> (sh + 4), 0x000F000Fu, MAGIC), zh);
         } else {
           // fp16 has two 4-bit slots below its 10 mantissa bits: the nibbles
           // at bits 4-7 / 20-23 give 1024 + 16q in place, and one fused

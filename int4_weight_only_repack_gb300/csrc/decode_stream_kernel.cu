@@ -26,12 +26,9 @@
 //    previous kernel, so their DRAM latency overlaps its tail. x is read after
 //    the wait, with 16-byte loads through L1 (every warp of the SM reads it).
 //  * Dequantisation ("vLLM AWQ 4-bit 量化实践" §5.3: (b - zeros) * scales): one
-//    LOP3 turns a nibble pair into MAGIC + q halves. With bf16 the MMA consumes
-//    128 + q (exact) and each group's sum is corrected by (128 + z) * sum(x)
-//    before the scale, the per-group sums of x coming from MMAs against an
-//    all-ones operand on the same x fragments (shared by the slab's two tiles);
-//    with fp16 one packed subtraction forms q - z exactly. The scale multiplies
-//    the group's fp32 partial sum.
+//    LOP3 turns a nibble pair into MAGIC + q halves and one packed subtraction
+//    of MAGIC + z forms q - z, exact in both types. The scale multiplies the
+//    group's fp32 partial sum.
 //  * At the end each warp stores the slabs it covered whole directly and puts
 //    its partial slabs in shared memory; after one CTA barrier the partial
 //    slabs are summed over the warps in a fixed order (deterministic) and
@@ -151,7 +148,6 @@ __device__ __forceinline__ size_t slab_base(int s, int A) {
 template <int MT, bool BF16, bool GATHER>
 __global__ void __launch_bounds__(ST, W4_STREAM_MINB) w4a16_stream_kernel(const __grid_constant__ StreamParams p) {
   constexpr uint32_t MAGIC = Magic<BF16>::pair;  // 128 (bf16) / 1024 (fp16) in both halves
-  constexpr uint32_t ONES = 0x3F803F80u;         // bf16 1.0 in both halves
   constexpr int MR = 8 * MT;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -251,17 +247,13 @@ __global__ void __launch_bounds__(ST, W4_STREAM_MINB) w4a16_stream_kernel(const 
   cp_async_wait_all();
   __syncthreads();  // the scales and zeros are in shared memory
   // ---- the weight loop ------------------------------------------------------------
-  float acc[2][MT][4], tc[2][MT][4], ax[MT][4];
+  float acc[2][MT][4], tc[2][MT][4];
 #pragma unroll
   for (int h = 0; h < 2; ++h)
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
       for (int j = 0; j < 4; ++j) acc[h][mt][j] = tc[h][mt][j] = 0.f;
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) ax[mt][j] = 0.f;
 
   // x of this lane's token rows (gg, gg + 8) at k-atom a: two 16-byte pieces
   // (columns 8t..8t+7 of each 32-row half); rows at or beyond M read as zero.
@@ -308,7 +300,7 @@ __global__ void __launch_bounds__(ST, W4_STREAM_MINB) w4a16_stream_kernel(const 
   // the open group: its index (-1: none), scales and zero terms of this lane's
   // four columns (tile h, column gg + 8 j)
   int gopen = -1;
-  uint32_t zp[2][2];  // fp16: MAGIC + z pairs of the open group (tile h, column gg + 8 j)
+  uint32_t zp[2][2];  // MAGIC + z pairs of the open group (tile h, column gg + 8 j)
 
   auto meta_col = [&](int h, int j) { return 32 * cs + 16 * h + gg + 8 * j; };
   auto zero_of = [&](int gi, int col) {
@@ -316,15 +308,12 @@ __global__ void __launch_bounds__(ST, W4_STREAM_MINB) w4a16_stream_kernel(const 
   };
   auto open_group = [&](int gi) {
     gopen = gi;
-    if constexpr (!BF16) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
+    for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int j = 0; j < 2; ++j) zp[h][j] = MAGIC + zero_of(gi, meta_col(h, j)) * 0x00010001u;
-    }
+      for (int j = 0; j < 2; ++j) zp[h][j] = MAGIC + zero_of(gi, meta_col(h, j)) * 0x00010001u;
   };
-  // tc += s * (acc - (128 + z) sum(x)) (bf16) or s * acc (fp16); acc = 0. The
-  // group's scales and zeros are read from shared memory here.
+  // tc += s * acc; acc = 0. The group's scales are read from shared memory here.
   auto flush = [&]() {
     if (gopen < 0) return;
 #pragma unroll
@@ -333,25 +322,17 @@ __global__ void __launch_bounds__(ST, W4_STREAM_MINB) w4a16_stream_kernel(const 
       for (int jj = 0; jj < 2; ++jj) {
         const int col = meta_col(h, jj);
         const float sc = half_bits_to_float<BF16>(sS[(size_t)gopen * ncols + col]);
-        float zz = 0.f;
-        if constexpr (BF16) zz = (float)(128 + (int)zero_of(gopen, col));
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int j = 2 * jj + e;
-            float d = acc[h][mt][j];
-            if constexpr (BF16) d = fmaf(-zz, ax[mt][j], d);
-            tc[h][mt][j] = fmaf(sc, d, tc[h][mt][j]);
+            tc[h][mt][j] = fmaf(sc, acc[h][mt][j], tc[h][mt][j]);
             acc[h][mt][j] = 0.f;
           }
         }
       }
     }
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) ax[mt][j] = 0.f;
     gopen = -1;
   };
   // one 32-row half of both tiles: words (lo, hi) of tile h come from w[h]
@@ -372,14 +353,12 @@ __global__ void __launch_bounds__(ST, W4_STREAM_MINB) w4a16_stream_kernel(const 
         a[h][1] = lop3_and_or(hi_a, 0x000F000Fu, MAGIC);
         a[h][3] = lop3_and_or(hi_b, 0x000F000Fu, MAGIC);
       }
-      if constexpr (!BF16) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          a[h][0] = sub_x2<false>(a[h][0], zp[h][0]);
-          a[h][2] = sub_x2<false>(a[h][2], zp[h][0]);
-          a[h][1] = sub_x2<false>(a[h][1], zp[h][1]);
-          a[h][3] = sub_x2<false>(a[h][3], zp[h][1]);
-        }
+      for (int h = 0; h < 2; ++h) {
+        a[h][0] = sub_x2<BF16>(a[h][0], zp[h][0]);
+        a[h][2] = sub_x2<BF16>(a[h][2], zp[h][0]);
+        a[h][1] = sub_x2<BF16>(a[h][1], zp[h][1]);
+        a[h][3] = sub_x2<BF16>(a[h][3], zp[h][1]);
       }
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
@@ -387,7 +366,6 @@ __global__ void __launch_bounds__(ST, W4_STREAM_MINB) w4a16_stream_kernel(const 
         const uint32_t b1 = step ? xh[mt].w : xh[mt].y;
         mma_k16<BF16>(acc[0][mt], a[0][0], a[0][1], a[0][2], a[0][3], b0, b1);
         mma_k16<BF16>(acc[1][mt], a[1][0], a[1][1], a[1][2], a[1][3], b0, b1);
-        if constexpr (BF16) mma_k16<true>(ax[mt], ONES, ONES, ONES, ONES, b0, b1);
       }
     }
   };
