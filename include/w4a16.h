@@ -202,8 +202,7 @@ W4_API size_t w4a16_gemm_workspace_size(int M, int N, int K, int group, int dtyp
  *          W4_ERR_WORKSPACE when it lacks the required act-order staging.
  * Accumulation is fp32; the result is rounded once to dtype. Deterministic:
  * the same inputs give the same bits. M <= 16 (any M when N % 32 != 0) runs
- * the small-M kernel (CUDA-core dequantisation into exact operands: q - z for
- * fp16, 128 + q for bf16 with the (128 + z) * s * sum(x) part removed in fp32;
+ * the small-M kernel (CUDA-core dequantisation into exact q - z operands;
  * mma.sync; per-group fp32 scaling); larger M runs the tcgen05 kernel, whose
  * B operand is the dequantised weight rounded once to dtype.
  * Ordering: the kernels are launched with programmatic dependent launch and
