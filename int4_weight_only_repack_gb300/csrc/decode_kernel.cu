@@ -675,23 +675,46 @@ DecodePlan fit_ring(int S, int A, int Mc, int MT, int gshift, int per_sm, void* 
   return d;
 }
 
-// Choose the split-K factor, then the ring. The rule is calibrated on GB300
-// sweeps over S for the Llama-2 7B / 70B decode shapes:
-//  * x of the CTA's K range is staged in one piece when it fits (chunked x costs
-//    a barrier per chunk), so S is at least the smallest split that makes it fit;
-//  * a CTA's K range stays between 16 and 64 k-atoms (shorter runs are
-//    dominated by the fixed prologue / reduction cost, longer ones by the wait
-//    for the slowest CTA);
-//  * CTA counts below count every (column group, expert) pair of a grouped call;
-//  * with one token tile the launch aims at about 2.6 CTAs per SM (enough warps
-//    to hide the loop's latencies, few enough to stay near one wave);
-//  * a split that would take more than three waves is replaced by the longest
-//    CTA ranges (x in chunks) at about one wave.
-// The ring is then as deep as fits with 3 resident CTAs per SM (2 when the
-// register budget allows only 2), at least 2 stages; residency is the runtime's
-// occupancy count for the kernel (a plan that looked like three CTAs by plain
-// byte arithmetic but ran two per SM took a second wave: Llama-2-70B qkv at
-// M = 8 22.9 us against 17.0 us with three).
+// Clusters of the launch (grid gx x S x gz, clusters 1 x S x 1, `smem` bytes of
+// dynamic shared memory) that the device runs at once, as the runtime counts
+// them (residency per SM and the packing of a cluster's CTAs into one GPC); 0
+// on an error.
+int resident_clusters(void* fn, int gx, int S, int gz, int smem) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)gx, (unsigned)S, (unsigned)gz);
+  cfg.blockDim = dim3(DEC_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = (unsigned)S;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) return 0;
+  return n;
+}
+
+// Choose the split-K factor S and the ring. For every S the ring is as deep as
+// keeps 3 CTAs per SM resident (2 when the register budget allows only 2; the
+// runtime's occupancy count), and the runtime says how many clusters of S CTAs
+// run at once: a cluster's CTAs must fit on S SMs of one GPC, so the number of
+// waves of a split depends on how clusters pack into GPCs, not only on CTAs per
+// SM. Then:
+//  * the largest S whose clusters run in one wave with at least two CTAs per SM
+//    on average (the most warps per SM and the shortest K range per CTA);
+//  * failing that, the S with the least waves x (k-atoms per CTA + 8): the
+//    busiest SM's share of the stream plus a fixed cost per wave (prologue,
+//    pipeline fill, cluster reduction) worth about 8 k-atoms; fewer waves on a
+//    tie.
+// Measured on GB300 against the S that each shape ran best with (sweeps over
+// S = 1..16 of the Llama-2 7B / 70B decode calls at M = 1, 4, 16), this picks
+// the best split on every call; the rule it replaced (about 2.6 CTAs per SM
+// from the CTA count alone) ran Llama-2-70B down at 42.5 / 63.5 us against
+// 35.3 / 52.7 us at M = 1 / 16 (its split took a second wave of clusters).
+// CTA and cluster counts include every (column group, expert) pair of a grouped
+// call.
 DecodePlan plan_decode(int N, int K, int Mc, int MT, int gshift, int experts,
                        const DeviceInfo& info, void* fn) {
   const int NG = (N / 16 + DEC_WARPS - 1) / DEC_WARPS, A = K / ATOM_K;
@@ -699,32 +722,33 @@ DecodePlan plan_decode(int N, int K, int Mc, int MT, int gshift, int experts,
   const int nst_all = (A + SA - 1) / SA;
   auto cta_atoms = [&](int S) { return (nst_all + S - 1) / S * SA; };
   const int s_cap = std::min(MAX_SPLIT, nst_all);
-  int s_x = 1;  // x in one piece
-  while (s_x < s_cap && (long long)cta_atoms(s_x) * ATOM_K * Mc * 2 > X_BUDGET) ++s_x;
-  int s_lo = 1;  // at most 64 k-atoms per CTA
-  while (s_lo < s_cap && cta_atoms(s_lo) > 64) ++s_lo;
-  const int s64 = s_lo;
-  s_lo = std::max(s_lo, s_x);
-  int s_hi = s_cap;  // at least 16 k-atoms per CTA
-  while (s_hi > 1 && cta_atoms(s_hi) < 16) --s_hi;
-  s_hi = std::max(s_hi, s_lo);
-  int S = s_lo;
-  if (MT == 1) {
-    const int target = (int)(2.6 * info.sm_count / units + 0.5);
-    S = std::min(std::max(target, s_lo), s_hi);
-  }
-  if (units * S > 3LL * info.sm_count * decode_min_ctas(MT)) {
-    // more than three waves of short CTAs, each paying the prologue and the
-    // cluster reduction again: one wave's worth of the longest CTAs instead,
-    // x staged in chunks (measured on GB300, M = 16: Llama-2-70B gate_up
-    // 135 -> 108 us, down 88 -> 71 us; a grouped Mixtral-shaped w13 at up to
-    // 8 rows per expert 164 -> 160 us; shapes of up to three waves lose)
-    S = std::max(s64, (int)(2.0 * info.sm_count / units + 0.5));
-  }
   const int reg_ctas = decode_min_ctas(MT);
-  DecodePlan d = fit_ring(S, A, Mc, MT, gshift, std::min(3, reg_ctas), fn);
-  if (resident_ctas(fn, d.L.total) < std::min(3, reg_ctas)) d = fit_ring(S, A, Mc, MT, gshift, 2, fn);
-  return d;
+  DecodePlan one_wave{}, best{};
+  bool have_one = false, have_best = false;
+  long long best_cost = 0, best_waves = 0;
+  for (int S = 1; S <= s_cap; ++S) {
+    if (S > 1 && cta_atoms(S) == cta_atoms(S - 1)) continue;  // the same K ranges, more CTAs idle
+    DecodePlan d = fit_ring(S, A, Mc, MT, gshift, std::min(3, reg_ctas), fn);
+    if (resident_ctas(fn, d.L.total) < std::min(3, reg_ctas)) d = fit_ring(S, A, Mc, MT, gshift, 2, fn);
+    const int clusters = resident_clusters(fn, NG, S, experts, d.L.total);
+    if (clusters <= 0) continue;
+    const long long waves = (units + clusters - 1) / clusters;
+    if (waves == 1 && units * S >= 2LL * info.sm_count) {
+      one_wave = d;
+      have_one = true;
+    }
+    const long long cost = waves * (cta_atoms(S) + 8);
+    if (!have_best || cost < best_cost || (cost == best_cost && waves < best_waves)) {
+      best = d;
+      best_cost = cost;
+      best_waves = waves;
+      have_best = true;
+    }
+  }
+  if (have_one) return one_wave;
+  if (have_best) return best;
+  // no occupancy answer: the smallest split, two CTAs per SM
+  return fit_ring(1, A, Mc, MT, gshift, 2, fn);
 }
 
 // Plans are cached per (device, shape): planning costs tens of microseconds of
