@@ -803,7 +803,7 @@ size_t decode_workspace_bytes(int M, int K, bool has_perm) {
 }
 
 cudaError_t launch_decode(const GemmArgs& a, cudaStream_t stream) {
-  // M <= 16 on a small layer (at most 96 KB of packed weights per SM), no
+  // M <= 8 on a small layer (at most 96 KB of packed weights per SM), no
   // experts: the streaming kernel (decode_stream_kernel.cu); otherwise this one
   bool launched = false;
   cudaError_t err = launch_decode_stream(a, stream, &launched);

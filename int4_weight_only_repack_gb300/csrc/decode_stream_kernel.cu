@@ -1,4 +1,4 @@
-// Small-M (decode) W4A16 GEMM, streaming form: y[M][N] = x[M][K] · W, M <= 16.
+// Small-M (decode) W4A16 GEMM, streaming form: y[M][N] = x[M][K] · W, M <= 8.
 //
 // Decode is bound by streaming the packed weights from HBM ("vLLM 学习手册 01.
 // 量化" §1: decode has FLOPs/Bytes ~ 1 and moving the weights dominates). This
@@ -549,13 +549,9 @@ void* stream_kernel_ptr() {
   return reinterpret_cast<void*>(&w4a16_stream_kernel<MT, BF16, GATHER>);
 }
 
-void* pick_stream_kernel(int MT, bool bf16, bool gather) {
-  if (MT == 1) {
-    if (bf16) return gather ? stream_kernel_ptr<1, true, true>() : stream_kernel_ptr<1, true, false>();
-    return gather ? stream_kernel_ptr<1, false, true>() : stream_kernel_ptr<1, false, false>();
-  }
-  if (bf16) return gather ? stream_kernel_ptr<2, true, true>() : stream_kernel_ptr<2, true, false>();
-  return gather ? stream_kernel_ptr<2, false, true>() : stream_kernel_ptr<2, false, false>();
+void* pick_stream_kernel(bool bf16, bool gather) {
+  if (bf16) return gather ? stream_kernel_ptr<1, true, true>() : stream_kernel_ptr<1, true, false>();
+  return gather ? stream_kernel_ptr<1, false, true>() : stream_kernel_ptr<1, false, false>();
 }
 
 // The kernels' dynamic shared-memory limit, raised once per (kernel, device) to
@@ -587,7 +583,10 @@ int log2_of(int v) {
 
 cudaError_t launch_decode_stream(const GemmArgs& a, cudaStream_t stream, bool* launched) {
   *launched = false;
-  if (a.eoff != nullptr || a.test_stall || a.M < 1 || a.M > 16) return cudaSuccess;
+  // At most 8 rows: at 9-16 rows the clustered kernel is faster on these layers
+  // too (measured on GB300, Llama-2-7B o_proj at M = 16: 6.7 against 7.5 us;
+  // at M = 1 / 4 this kernel: 5.2 / 5.5 against 5.9 / 6.3 us)
+  if (a.eoff != nullptr || a.test_stall || a.M < 1 || a.M > 8) return cudaSuccess;
   DeviceInfo info;
   cudaError_t err = device_info(&info);
   if (err != cudaSuccess) return err;
@@ -595,7 +594,7 @@ cudaError_t launch_decode_stream(const GemmArgs& a, cudaStream_t stream, bool* l
   // there the clustered kernel's fixed per-CTA costs (staging x and its group
   // sums, the cluster reduction) dominate its time, and this kernel, which has
   // none of them, is faster (measured on GB300: Llama-2-7B o_proj, 57 KB per
-  // SM, 5.4 / 7.7 us against 7.7 / 10.1 us at M = 1 / 16). On larger layers the
+  // SM, 5.4 against 7.7 us at M = 1). On larger layers the
   // clustered kernel's loop, with three times the warps per SM, is faster
   // (7B down, 154 KB per SM: 13.9 against 11.0 us at M = 1).
   if ((double)a.K * a.N / 2 / info.sm_count > STREAM_MAX_BYTES_PER_SM) return cudaSuccess;
@@ -606,7 +605,7 @@ cudaError_t launch_decode_stream(const GemmArgs& a, cudaStream_t stream, bool* l
   int gshift = log2_of(a.group);
   if (a.group == a.K || gshift < 0) gshift = 31;
   const int G = gshift >= 31 ? 1 : a.K >> gshift;
-  const int MT = a.M <= 8 ? 1 : 2;
+  const int MT = 1;
   const StreamLayout L = stream_layout(G, ns_max, 8 * MT);
   // scales and zeros beyond the budget: the clustered kernel takes the call
   if (L.p_off - L.s_off > META_BUDGET || L.total > info.max_smem_optin) return cudaSuccess;
@@ -620,7 +619,7 @@ cudaError_t launch_decode_stream(const GemmArgs& a, cudaStream_t stream, bool* l
     xsrc = a.workspace;
     perm = nullptr;
   }
-  void* fn = pick_stream_kernel(MT, a.bf16 != 0, perm != nullptr);
+  void* fn = pick_stream_kernel(a.bf16 != 0, perm != nullptr);
   const int which = (MT - 1) + 2 * (a.bf16 ? 1 : 0) + 4 * (perm != nullptr ? 1 : 0);
   if ((err = ensure_stream_smem(which, fn, L.total, info.max_smem_optin)) != cudaSuccess) return err;
   int* status = nullptr;

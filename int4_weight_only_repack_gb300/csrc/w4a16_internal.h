@@ -58,7 +58,7 @@ struct GemmArgs {
 // every CTA gathers its own slice of x.
 constexpr int DECODE_MAX_M = 64;
 cudaError_t launch_decode(const GemmArgs& a, cudaStream_t s);
-// The streaming small-M kernel (M <= 16, layers of at most 96 KB of packed
+// The streaming small-M kernel (M <= 8, layers of at most 96 KB of packed
 // weights per SM, no grouped call): *launched says whether it took the call;
 // when it did not, launch_decode runs the clustered kernel instead.
 cudaError_t launch_decode_stream(const GemmArgs& a, cudaStream_t s, bool* launched);
