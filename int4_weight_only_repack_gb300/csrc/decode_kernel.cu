@@ -657,8 +657,10 @@ DecodePlan shape_plan(int S, int A, int Mc, int MT, int gshift, int ring) {
 int resident_ctas(void* fn, int smem) {
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, DEC_THREADS, (size_t)smem) !=
-      cudaSuccess)
+      cudaSuccess) {
+    (void)cudaGetLastError();  // a failed query must not surface in a later launch's check
     return 0;
+  }
   return n;
 }
 
@@ -692,7 +694,10 @@ int resident_clusters(void* fn, int gx, int S, int gz, int smem) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();  // a failed query must not surface in a later launch's check
+    return 0;
+  }
   return n;
 }
 
