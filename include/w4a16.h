@@ -181,10 +181,12 @@ W4_API w4_status w4_repack_gptq(const int32_t* qweight, const int32_t* qzeros, c
  *     large-M kernel; optional for the small-M kernel, whose CTAs otherwise
  *     each gather the columns they need (slower at larger M: every column
  *     group's CTAs read the same columns).
- *   - After that, large-M calls whose 128 x 256 output tiles cannot fill the
- *     GPU keep fp32 partial tiles of a split-K run there (optional: with a
- *     smaller workspace the kernel splits K less, or not at all; the sum
- *     order, and so the result bits, follow the split chosen).
+ *   - After that, large-M calls keep fp32 partial tiles there: calls whose
+ *     output tiles cannot fill the GPU, of a split-K run; calls whose tiles
+ *     take whole waves plus a few, of the few tiles beyond the last whole wave,
+ *     which run as K slices over the otherwise idle SMs (both optional: with a
+ *     smaller workspace the kernel splits less, or not at all; the sum order,
+ *     and so the result bits of the affected tiles, follow the split chosen).
  */
 W4_API size_t w4a16_gemm_workspace_size(int M, int N, int K, int group, int dtype, int has_perm);
 
@@ -297,14 +299,15 @@ W4_API w4_status w4_test_stalled_gemm(const void* x, const int32_t* qw, const vo
  *
  * Same arguments, layouts, results and error statuses as w4a16_gemm, minus
  * workspace / workspace_bytes. Where w4a16_gemm would use a workspace
- * (act-order staging of x[:, perm]; split-K partials of the large-M kernel),
+ * (act-order staging of x[:, perm]; split-K partials of the large-M kernel,
+ * including those of a split last wave),
  * this call uses one static device array of W4_NOALLOC_SCRATCH_BYTES that the
  * library holds on every GPU that loads it, until the process exits. Large-M
  * calls whose act-order staging would exceed it (M * K * 2 bytes) return
  * W4_ERR_WORKSPACE and launch nothing (small-M ones gather in the kernel
  * instead), and split-K partials that do not fit after the staging make the
- * kernel split K less (then the result bits can differ from a w4a16_gemm call
- * given the full workspace).
+ * kernel split K less, or not split its last wave (then the result bits can
+ * differ from a w4a16_gemm call given the full workspace).
  * It never allocates or frees device memory.
  *   - Set-up: the first call with M > 0 on each device (whatever its shape,
  *     once its arguments pass validation) looks up the array's device address

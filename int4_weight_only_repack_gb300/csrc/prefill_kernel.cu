@@ -141,6 +141,12 @@ struct PrefillParams {
   float* part;  // split-K partial tiles [ksplit][M][N] fp32 (ksplit > 1)
   int M, N, K, group;
   int m_blocks, n_blocks, num_tiles, k_blocks, ksplit;
+  // Split last wave (ungrouped, ksplit == 1): the tiles from tail_start on (the
+  // tail_tiles that would leave most SMs idle in a last wave of their own) run
+  // as tail_split K slices each, whose fp32 partial tiles go to tail_part
+  // [tail_split][tail_tiles][BM][BN] (slice-major) for tail_reduce_kernel.
+  float* tail_part;
+  int tail_start, tail_tiles, tail_split;
   // Grouped (MoE) calls: eoff != nullptr. x and y hold the rows of all experts,
   // sorted by expert ([eoff[e], eoff[e+1]) for expert e); tm_p spans the
   // experts' TILE buffers one after another (ng128 column groups each), tm_s
@@ -176,18 +182,32 @@ static_assert(Cfg<1, false, false>::SMEM_BYTES <= 227 * 1024 &&
 // within the expert, then N (no K split).
 struct Unit {
   int e, m_blk, n_blk, ks, kb0, kb1, row0, row_end;
+  int slot;  // partial-tile slot of a split last-wave unit in tail_part, else -1
 };
 template <bool GROUPED>
 __device__ __forceinline__ Unit unit_of(const PrefillParams& p, const int* tab, int BM, int tile) {
   Unit u;
   if (!GROUPED) {
     u.e = 0;
-    u.m_blk = tile % p.m_blocks;
-    const int rest = tile / p.m_blocks;
-    u.n_blk = rest % p.n_blocks;
-    u.ks = rest / p.n_blocks;
-    u.kb0 = (int)((long long)u.ks * p.k_blocks / p.ksplit);
-    u.kb1 = (int)((long long)(u.ks + 1) * p.k_blocks / p.ksplit);
+    u.slot = -1;
+    if (p.tail_split > 1 && tile >= p.tail_start) {
+      // a split last-wave unit: slice v / tail_tiles of tile tail_start + v % tail_tiles
+      const int v = tile - p.tail_start;
+      const int tt = p.tail_start + v % p.tail_tiles;
+      u.m_blk = tt % p.m_blocks;
+      u.n_blk = tt / p.m_blocks;
+      u.ks = v / p.tail_tiles;
+      u.kb0 = (int)((long long)u.ks * p.k_blocks / p.tail_split);
+      u.kb1 = (int)((long long)(u.ks + 1) * p.k_blocks / p.tail_split);
+      u.slot = v;
+    } else {
+      u.m_blk = tile % p.m_blocks;
+      const int rest = tile / p.m_blocks;
+      u.n_blk = rest % p.n_blocks;
+      u.ks = rest / p.n_blocks;
+      u.kb0 = (int)((long long)u.ks * p.k_blocks / p.ksplit);
+      u.kb1 = (int)((long long)(u.ks + 1) * p.k_blocks / p.ksplit);
+    }
     u.row0 = u.m_blk * BM;
     u.row_end = p.M;
     return u;
@@ -206,6 +226,7 @@ __device__ __forceinline__ Unit unit_of(const PrefillParams& p, const int* tab, 
   const int local = tile - tab[lo];
   const int mb = (r1[lo] - r0[lo] + BM - 1) / BM;
   u.e = lo;
+  u.slot = -1;
   u.m_blk = local % mb;
   u.n_blk = local / mb;
   u.ks = 0;
@@ -510,6 +531,17 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
                 dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
                                      __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
             }
+          } else if (u.slot >= 0) {
+            // split last wave: this slice's fp32 partial of the tile (rows beyond
+            // M are never read back)
+            if (m < u.row_end && n < p.N) {
+              float4* dst = reinterpret_cast<float4*>(
+                  p.tail_part + ((size_t)u.slot * BM + (m - u.row0)) * BN + c0);
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                     __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+            }
           } else if (m < u.row_end) {
             if (p.bias != nullptr) {
               // y = RN(acc + bias): the bias joins the fp32 sum before the one rounding
@@ -687,6 +719,45 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4* __rest
   }
 }
 
+// ---- split last wave: y = RN(sum over the slices + bias) for the tail tiles -------
+// One thread per four consecutive outputs of a tail tile; the slices are summed
+// in order (deterministic).
+template <bool BF16>
+__global__ void __launch_bounds__(256) tail_reduce_kernel(const float4* __restrict__ part,
+                                                          uint16_t* __restrict__ y,
+                                                          const uint16_t* __restrict__ bias,
+                                                          int M, int N, int BM, int m_blocks,
+                                                          int tail_start, int tail_tiles,
+                                                          int tail_split) {
+  const size_t per_tile = (size_t)BM * (BN / 4);
+  const size_t total = (size_t)tail_tiles * per_tile;
+  for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < total; i += (size_t)gridDim.x * 256) {
+    const int ti = (int)(i / per_tile);
+    const int rr = (int)((i - (size_t)ti * per_tile) / (BN / 4));
+    const int c4 = (int)(i % (BN / 4));
+    const int tt = tail_start + ti;
+    const int m = (tt % m_blocks) * BM + rr;
+    const int n = (tt / m_blocks) * BN + 4 * c4;
+    if (m >= M || n >= N) continue;
+    float4 a = part[i];
+    for (int sl = 1; sl < tail_split; ++sl) {
+      const float4 b = part[(size_t)sl * total + i];
+      a.x += b.x;
+      a.y += b.y;
+      a.z += b.z;
+      a.w += b.w;
+    }
+    if (bias != nullptr) {
+      a.x += half_bits_to_float<BF16>(bias[n]);
+      a.y += half_bits_to_float<BF16>(bias[n + 1]);
+      a.z += half_bits_to_float<BF16>(bias[n + 2]);
+      a.w += half_bits_to_float<BF16>(bias[n + 3]);
+    }
+    *reinterpret_cast<uint2*>(y + (size_t)m * N + n) =
+        make_uint2(pack_half2(a.x, a.y, BF16), pack_half2(a.z, a.w, BF16));
+  }
+}
+
 // ---- host side ------------------------------------------------------------------
 bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
                uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
@@ -726,9 +797,11 @@ cudaError_t ensure_prefill_smem(void* fn, int which, int bytes) {
 // that takes fewer estimated wave-times: a 256-row tile does the MMA work of
 // two 128-row tiles in ~1.25x the time (it dequantises each B tile once for
 // both). When the output tiles cannot fill the SMs, K is split into slices of
-// at least 8 k-blocks so that tiles x slices still fit in one wave.
+// at least 8 k-blocks so that tiles x slices still fit in one wave; when they
+// take whole waves plus a few, only those few are split (the split last wave).
 struct PrefillPlan {
   int nacc, m_blocks, n_blocks, ksplit;
+  int tail_tiles, tail_split;  // split last wave (tail_split > 1): its tiles and slices
 };
 PrefillPlan prefill_plan(int M, int N, int K, int sm_count) {
   PrefillPlan pl;
@@ -741,6 +814,8 @@ PrefillPlan prefill_plan(int M, int N, int K, int sm_count) {
   pl.m_blocks = (M + 128 * pl.nacc - 1) / (128 * pl.nacc);
   const long long tiles = (long long)pl.m_blocks * pl.n_blocks;
   pl.ksplit = 1;
+  pl.tail_tiles = 0;
+  pl.tail_split = 1;
   if (tiles < sm_count || M <= 128) {
     // Split K in slices of at least 8 k-blocks. First choice: as many slices as
     // one wave holds (none when the tiles alone fill the SMs). Another split
@@ -772,8 +847,39 @@ PrefillPlan prefill_plan(int M, int N, int K, int sm_count) {
     for (int ks = 1; ks <= kmax; ++ks)
       if (cost(ks) < cost(best)) best = ks;
     pl.ksplit = cost(best) < 0.9 * cost(one_wave) ? best : one_wave;
+  } else if (tiles % sm_count != 0) {
+    // Split last wave: the rem tiles beyond whole waves would run as one more
+    // wave of full tiles on rem SMs while the rest idle. Split each of them
+    // into ks K slices (at least 8 k-blocks each) over the SMs instead, when the
+    // same cost model (units of one unsplit tile's time T1) predicts the tail at
+    // least 10 % faster: ceil(rem*ks / SMs) waves of 1/ks of T1 plus the
+    // pipeline fill, plus writing and reading the rem*ks fp32 partial tiles and
+    // the reduce launch. Measured on GB300: Llama-2-70B qkv at M = 1024 (160
+    // tiles) 211 -> 133 us, 7B gate_up at M = 512 (172) 116 -> 85 us, 70B down at
+    // M = 4096 (512) 1410 -> 1257 us, 7B qkv at M = 4096 (768) 335 -> 304 us.
+    const long long rem = tiles % sm_count;
+    const int kmax = std::max(1, K / BK / 8);
+    const int kb_total = K / BK;
+    const double t1 = 2.0 * 128 * pl.nacc * BN * (double)K / 8e12;
+    const double slice = 8.0 * (double)rem * 128 * pl.nacc * BN / 6.6e12 / t1;
+    const double launch = 3e-6 / t1;
+    auto cost = [&](int ks) {
+      const double waves = (double)((rem * ks + sm_count - 1) / sm_count);
+      return waves * (1.0 / ks + 4.0 / kb_total) + (ks > 1 ? slice * ks + launch : 0.0);
+    };
+    int best = 1;
+    for (int ks = 2; ks <= kmax; ++ks)
+      if (cost(ks) < cost(best)) best = ks;
+    if (best > 1 && cost(best) < 0.9 * cost(1)) {
+      pl.tail_tiles = (int)rem;
+      pl.tail_split = best;
+    }
   }
   return pl;
+}
+
+size_t tail_bytes(const PrefillPlan& pl) {
+  return pl.tail_split > 1 ? (size_t)pl.tail_split * pl.tail_tiles * 128 * pl.nacc * BN * 4 : 0;
 }
 
 size_t split_bytes(int M, int N, int ksplit) {
@@ -807,7 +913,8 @@ size_t prefill_workspace_bytes(int M, int K, bool has_perm) {
 size_t prefill_split_workspace_bytes(int M, int N, int K) {
   DeviceInfo info;
   if (device_info(&info) != cudaSuccess) return 0;
-  return split_bytes(M, N, prefill_plan(M, N, K, info.sm_count).ksplit);
+  const PrefillPlan pl = prefill_plan(M, N, K, info.sm_count);
+  return std::max(split_bytes(M, N, pl.ksplit), tail_bytes(pl));
 }
 
 bool prefill_supported(int M, int N, int K) {
@@ -850,6 +957,8 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
     pl.n_blocks = (a.N + BN - 1) / BN;
     pl.m_blocks = 0;
     pl.ksplit = 1;
+    pl.tail_tiles = 0;
+    pl.tail_split = 1;
   } else {
     pl = prefill_plan(a.M, a.N, a.K, info.sm_count);
   }
@@ -859,6 +968,7 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
   const size_t room = a.workspace_bytes > staged ? a.workspace_bytes - staged : 0;
   while (pl.ksplit > 1 && (a.workspace == nullptr || split_bytes(a.M, a.N, pl.ksplit) > room))
     --pl.ksplit;
+  if (pl.tail_split > 1 && (a.workspace == nullptr || tail_bytes(pl) > room)) pl.tail_split = 1;
   const int nacc = pl.nacc;
   const int BM = 128 * nacc;
   // 64-row x tiles (and a deeper TMA ring) for ungrouped calls of at most 64 rows
@@ -884,6 +994,9 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
   p.bias = static_cast<const uint16_t*>(a.bias);
   p.part = pl.ksplit > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + staged)
                          : nullptr;
+  p.tail_part = pl.tail_split > 1
+                    ? reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + staged)
+                    : nullptr;
   p.M = a.M;
   p.N = a.N;
   p.K = a.K;
@@ -892,6 +1005,10 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
   p.n_blocks = n_blocks;
   p.ksplit = pl.ksplit;
   p.num_tiles = p.m_blocks * n_blocks * pl.ksplit;
+  p.tail_split = pl.tail_split;
+  p.tail_tiles = pl.tail_split > 1 ? pl.tail_tiles : 0;
+  p.tail_start = p.num_tiles - p.tail_tiles;
+  if (pl.tail_split > 1) p.num_tiles = p.tail_start + pl.tail_tiles * pl.tail_split;
   p.k_blocks = a.K / BK;
   p.eoff = a.eoff;
   p.num_experts = E;
@@ -953,6 +1070,20 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
       splitk_reduce_kernel<false><<<g, 256, 0, stream>>>(reinterpret_cast<const float4*>(p.part),
                                                           static_cast<uint2*>(a.y), n4, pl.ksplit,
                                                           bias, (size_t)a.N / 4);
+    err = cudaGetLastError();
+  }
+  if (pl.tail_split > 1) {
+    const size_t total = (size_t)pl.tail_tiles * BM * (BN / 4);
+    const unsigned g = (unsigned)std::min<size_t>((total + 255) / 256, (size_t)info.sm_count * 8);
+    const float4* part = reinterpret_cast<const float4*>(p.tail_part);
+    uint16_t* yy = static_cast<uint16_t*>(a.y);
+    const uint16_t* bias = static_cast<const uint16_t*>(a.bias);
+    if (a.bf16)
+      tail_reduce_kernel<true><<<g, 256, 0, stream>>>(part, yy, bias, a.M, a.N, BM, p.m_blocks,
+                                                      p.tail_start, pl.tail_tiles, pl.tail_split);
+    else
+      tail_reduce_kernel<false><<<g, 256, 0, stream>>>(part, yy, bias, a.M, a.N, BM, p.m_blocks,
+                                                       p.tail_start, pl.tail_tiles, pl.tail_split);
     err = cudaGetLastError();
   }
   return err;

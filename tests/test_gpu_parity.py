@@ -434,6 +434,40 @@ def test_gemm_bias(w4, K, N, dtype, fmt, act_order, Ms):
     assert w4.w4_device_status() == 0
 
 
+def test_prefill_split_last_wave(w4):
+    """A call whose 256-row tiles take one wave plus a few (1024 x 10240: 160
+    tiles on 152 SMs): with a workspace the tiles beyond the last whole wave run
+    as K slices whose fp32 partials a second kernel sums (bias added there);
+    without one they run whole. Both against the oracle, and within one output
+    ulp of the rounded-W result."""
+    import torch
+    K, N, M, dtype = 1024, 10240, 1024, "bf16"
+    L = synth.make_custom_layer([131, K, N], K, N, group=128, dtype=dtype, fmt="awq")
+    qw, zeros, scales, perm, _ = repack(w4, L, w4.W4_LAYOUT_TILE)
+    b = synth.f32_to_bits(np.random.default_rng(132).standard_normal(N).astype(np.float32), dtype)
+    bias = half_to_dev(b, dtype)
+    xb = synth.make_custom_x([133, K, M], M, K, dtype)
+    y_ref = oracle.reference_y(xb, L.qweight, L.qzeros, L.scales, 128, dtype, "awq", bias_bits=b)
+    y_rw = rounded_w_reference(xb, L, 128) + oracle.half_bits_to_f64(b, dtype)
+    need = w4.w4a16_gemm_workspace_size(M, N, K, 128, dtype, False)
+    assert need > 0  # the split last wave needs room for its partial tiles
+    outs = []
+    for ws in (torch.empty(need, dtype=torch.uint8, device="cuda"), None):
+        raw, y = guarded(M * N, hdt(dtype))
+        w4.w4a16_gemm_bias(half_to_dev(xb, dtype), qw, scales, zeros, perm, bias, y, M, N, K, 128,
+                           dtype, ws)
+        torch.cuda.synchronize()
+        check_guards(raw, M * N, 2)
+        yb = half_from_dev(y).reshape(M, N)
+        assert oracle.rel_err(oracle.half_bits_to_f64(yb, dtype), y_ref) <= TOL
+        assert ulp_error(yb, y_rw, dtype) <= 1.0, ulp_error(yb, y_rw, dtype)
+        outs.append(yb)
+    # the whole tiles (all but the last 8; M blocks run fastest, so columns below 9728)
+    # take the same path either way
+    assert np.array_equal(outs[0][:, :9728], outs[1][:, :9728])
+    assert w4.w4_device_status() == 0
+
+
 @pytest.mark.parametrize("K,N,group,dtype,Ms", [
     (64, 1 << 20, 64, "bf16", (1, 3, 33)),      # N at the API limit: 8192 column groups
     (1 << 20, 32, 128, "fp16", (1, 17)),        # K at the API limit: 8192 groups, x in chunks
