@@ -79,8 +79,8 @@ using namespace sm100;
 // overlaps the next tile); NACC = 2 fills TMEM with the two accumulators and
 // halves the dequantisation work per MMA.
 constexpr int BN = 256, BK = 64;
-constexpr int THREADS = 512;
-constexpr int DEQ_THREADS = 256;  // warps 8-15
+// warps 0-3: TMA, MMA issue, TMEM allocation, second TMA issuer; 4-7: epilogue;
+// 8 onward: dequantisation (Cfg::DEQ_WARPS of them)
 constexpr int EPI_THREADS = 128;  // warps 4-7
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int P_BYTES = BN * BK / 2;
@@ -107,6 +107,11 @@ struct Cfg {
   static constexpr int A_BYTES = A_ROWS * BK * 2;
   static constexpr int ST_T = NACC == 2 ? 3 : GROUPED ? 3 : HALF_A ? 6 : 4;
   static constexpr int ST_B = 3;
+  // Dequantising warps (8 onward), one or two of a B tile's 16 atoms each. The
+  // 64-row x tiles (M <= 64) are bound by the dequantisation alone (the MMA
+  // does little per block), so they get sixteen, one atom each.
+  static constexpr int DEQ_WARPS = HALF_A ? 16 : 8;
+  static constexpr int NTHREADS = 256 + 32 * DEQ_WARPS;
   // Threads that issue the TMA ring's loads. One issuing thread starts the
   // loads of a 256-row stage (x tile of 256 rows, packed block, scale and zero
   // rows) more slowly than the MMAs consume them (measured on GB300: 0.9 us a
@@ -291,8 +296,11 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi, bool bf16) {
 // GROUPED: a grouped (MoE) call, p.eoff != nullptr (its own instantiation, so
 // that ungrouped calls carry none of its per-tile work).
 template <bool BF16, int NACC, bool GROUPED, bool HALF_A>
-__global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_constant__ PrefillParams p) {
+__global__ void __launch_bounds__(Cfg<NACC, GROUPED, HALF_A>::NTHREADS, 1)
+    w4a16_prefill_kernel(const __grid_constant__ PrefillParams p) {
   using C = Cfg<NACC, GROUPED, HALF_A>;
+  constexpr int DEQ_WARPS = C::DEQ_WARPS, NTHREADS = C::NTHREADS;
+  constexpr int ATOMS_PER_WARP = 16 / DEQ_WARPS;
   constexpr int BM = C::BM, NBUF = C::NBUF, A_BYTES = C::A_BYTES;
   constexpr int ST_T = C::ST_T, ST_B = C::ST_B, ISSUERS = C::ISSUERS;
   constexpr int OFF_A = C::OFF_A, OFF_B = C::OFF_B, OFF_P = C::OFF_P, OFF_S = C::OFF_S;
@@ -318,7 +326,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
       mbar_init(bars.empty(s), 1);
     }
     for (int b = 0; b < ST_B; ++b) {
-      mbar_init(bars.bready(b), DEQ_THREADS);
+      mbar_init(bars.bready(b), 32 * DEQ_WARPS);
       mbar_init(bars.bfree(b), 1);
     }
     for (int b = 0; b < NBUF; ++b) {
@@ -337,7 +345,7 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
   if (GROUPED) {
     // grouped call: the experts' row offsets (they may come from the kernel
     // before this one), staged in tile0[] by all threads in one pass
-    for (int e = tid; e <= p.num_experts; e += THREADS)
+    for (int e = tid; e <= p.num_experts; e += NTHREADS)
       tab[e] = *reinterpret_cast<const volatile int32_t*>(p.eoff + e);
   }
   if (warp == 0 && lane == 0) {
@@ -599,14 +607,14 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
         const uint8_t* sP = smem + OFF_P + s * P_BYTES;
         uint8_t* sB = smem + OFF_B + b * B_BYTES;
         // the scale pairs (s | s << 16) and MAGIC + z pairs of this lane's four
-        // columns (atoms wd and wd + 8, rows gg and gg + 8), per K half when the
+        // columns (atoms wd + DEQ_WARPS r, rows gg and gg + 8), per K half when the
         // block holds two groups: read once per block, not per word
-        uint32_t ss[2][2][2], zz[2][2][2];
+        uint32_t ss[ATOMS_PER_WARP][2][2], zz[ATOMS_PER_WARP][2][2];
 #pragma unroll
-        for (int r = 0; r < 2; ++r)
+        for (int r = 0; r < ATOMS_PER_WARP; ++r)
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
-            const int n_loc = (wd + 8 * r) * 16 + gg + 8 * c;
+            const int n_loc = (wd + DEQ_WARPS * r) * 16 + gg + 8 * c;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               if (h == 1 && !two_groups) {
@@ -621,8 +629,8 @@ __global__ void __launch_bounds__(THREADS, 1) w4a16_prefill_kernel(const __grid_
             }
           }
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int at = wd + 8 * r;  // atom (16-column tile) inside the block
+        for (int r = 0; r < ATOMS_PER_WARP; ++r) {
+          const int at = wd + DEQ_WARPS * r;  // atom (16-column tile) inside the block
           const uint4 w = *reinterpret_cast<const uint4*>(sP + (at * 128 + 4 * lane) * 4);
           const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -1048,7 +1056,10 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
   if ((err = ensure_prefill_smem(fn, which, smem_max)) != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)std::min<long long>(max_units, info.sm_count), 1, 1);
-  cfg.blockDim = dim3(THREADS, 1, 1);
+  static const int cfg_threads[5] = {Cfg<1, false, false>::NTHREADS, Cfg<1, false, true>::NTHREADS,
+                                     Cfg<2, false, false>::NTHREADS, Cfg<1, true, false>::NTHREADS,
+                                     Cfg<2, true, false>::NTHREADS};
+  cfg.blockDim = dim3((unsigned)cfg_threads[variant], 1, 1);
   cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
