@@ -434,25 +434,35 @@ def test_gemm_bias(w4, K, N, dtype, fmt, act_order, Ms):
     assert w4.w4_device_status() == 0
 
 
-def test_prefill_split_last_wave(w4):
+@pytest.mark.parametrize("dtype,fmt,act_order", [
+    ("bf16", "awq", False),
+    ("fp16", "gptq", True),   # the partials sit after the staged x[:, perm] in the workspace
+])
+def test_prefill_split_last_wave(w4, dtype, fmt, act_order):
     """A call whose 256-row tiles take one wave plus a few (1024 x 10240: 160
     tiles on 152 SMs): with a workspace the tiles beyond the last whole wave run
     as K slices whose fp32 partials a second kernel sums (bias added there);
     without one they run whole. Both against the oracle, and within one output
     ulp of the rounded-W result."""
     import torch
-    K, N, M, dtype = 1024, 10240, 1024, "bf16"
-    L = synth.make_custom_layer([131, K, N], K, N, group=128, dtype=dtype, fmt="awq")
+    K, N, M = 1024, 10240, 1024
+    L = synth.make_custom_layer([131, K, N], K, N, group=128, dtype=dtype, fmt=fmt,
+                                act_order=act_order)
     qw, zeros, scales, perm, _ = repack(w4, L, w4.W4_LAYOUT_TILE)
     b = synth.f32_to_bits(np.random.default_rng(132).standard_normal(N).astype(np.float32), dtype)
     bias = half_to_dev(b, dtype)
     xb = synth.make_custom_x([133, K, M], M, K, dtype)
-    y_ref = oracle.reference_y(xb, L.qweight, L.qzeros, L.scales, 128, dtype, "awq", bias_bits=b)
-    y_rw = rounded_w_reference(xb, L, 128) + oracle.half_bits_to_f64(b, dtype)
-    need = w4.w4a16_gemm_workspace_size(M, N, K, 128, dtype, False)
-    assert need > 0  # the split last wave needs room for its partial tiles
+    y_ref = oracle.reference_y(xb, L.qweight, L.qzeros, L.scales, 128, dtype, fmt,
+                               g_idx=L.g_idx, bias_bits=b)
+    y_rw = rounded_w_reference(xb, L, 128, fmt=fmt) + oracle.half_bits_to_f64(b, dtype)
+    need = w4.w4a16_gemm_workspace_size(M, N, K, 128, dtype, perm is not None)
+    staged = M * K * 2 if perm is not None else 0
+    assert need > staged  # the split last wave needs room for its partial tiles
     outs = []
-    for ws in (torch.empty(need, dtype=torch.uint8, device="cuda"), None):
+    # with the whole workspace; with only the act-order staging (no room for
+    # the partials: the last wave runs whole)
+    for ws_bytes in (need, staged):
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda") if ws_bytes else None
         raw, y = guarded(M * N, hdt(dtype))
         w4.w4a16_gemm_bias(half_to_dev(xb, dtype), qw, scales, zeros, perm, bias, y, M, N, K, 128,
                            dtype, ws)
