@@ -631,22 +631,67 @@ def ours(args):
     traffic = TRAFFIC_RECORDS.get(kernel_source_hash())
 
     # ---- end to end through the public API, host buffers ------------------------
+    # Every step copies its inputs in from pinned host memory and its results
+    # out to pinned host memory. The copies run on a copy stream with two sets
+    # of device buffers, so that a step's copies overlap the neighbouring steps'
+    # GEMMs, as a serving loop would arrange them; events order every copy
+    # against the GEMMs that read or write its buffers.
     e2e_steps = min(args.steps, 200)
-
-    def e2e_step(s):
-        x_all.copy_(hx_all, non_blocking=True)
+    comp = torch.cuda.current_stream()
+    cps = torch.cuda.Stream(device=device)
+    xsets = [x_all, torch.empty_like(x_all)]
+    ysets = [y_all, torch.empty_like(y_all)]
+    hys = [hy_all, torch.empty(y_elems, dtype=torch.bfloat16).pin_memory()]
+    views = []
+    for b in range(2):
+        xo = yo = 0
+        vs = []
         for c in calls:
-            layer = c["pool"].copies[(c["mi"] + len(WORKLOAD.ms) * s) % len(c["pool"].copies)]
-            w4.linear(c["x"], layer, y=c["y"])
-        hy_all.copy_(y_all, non_blocking=True)
+            K, N, M = c["pool"].K, c["pool"].N, c["M"]
+            vs.append((xsets[b][xo:xo + M * K].view(M, K), ysets[b][yo:yo + M * N].view(M, N)))
+            xo += M * K
+            yo += M * N
+        views.append(vs)
+    h2d_done = [torch.cuda.Event(), torch.cuda.Event()]
+    comp_done = [torch.cuda.Event(), torch.cuda.Event()]
+    d2h_done = [torch.cuda.Event(), torch.cuda.Event()]
 
-    for s in range(2 * nsets):
-        e2e_step(s % nsets)
+    def issue_h2d(s):
+        b = s % 2
+        with torch.cuda.stream(cps):
+            if s >= 2:
+                cps.wait_event(comp_done[b])  # the GEMMs of step s - 2 have read set b
+            xsets[b].copy_(hx_all, non_blocking=True)
+            h2d_done[b].record(cps)
+
+    def e2e_step(s, last):
+        b = s % 2
+        comp.wait_event(h2d_done[b])
+        if s >= 2:
+            comp.wait_event(d2h_done[b])  # step s - 2's results have left set b
+        for c, (xv, yv) in zip(calls, views[b]):
+            layer = c["pool"].copies[(c["mi"] + len(WORKLOAD.ms) * (s % nsets)) % len(c["pool"].copies)]
+            w4.linear(xv, layer, y=yv)
+        comp_done[b].record(comp)
+        with torch.cuda.stream(cps):
+            cps.wait_event(comp_done[b])
+            hys[b].copy_(ysets[b], non_blocking=True)
+            d2h_done[b].record(cps)
+        if s + 2 < last:
+            issue_h2d(s + 2)
+
+    def e2e_run(n):
+        issue_h2d(0)
+        if n > 1:
+            issue_h2d(1)
+        for s in range(n):
+            e2e_step(s, n)
+
+    e2e_run(2 * nsets)
     torch.cuda.synchronize()
     barrier(world)
     t0 = time.perf_counter()
-    for s in range(e2e_steps):
-        e2e_step(s % nsets)
+    e2e_run(e2e_steps)
     torch.cuda.synchronize()
     e2e_el = max_over_ranks(time.perf_counter() - t0, world, device)
 
@@ -727,8 +772,10 @@ def ours(args):
             "e2e": {"value": round(step_bytes * e2e_steps * world / e2e_el / 1e9, 2),
                     "unit": "GB/s", "h2d_bytes_per_step": x_elems * 2,
                     "d2h_bytes_per_step": y_elems * 2, "steps": e2e_steps,
-                    "how": "linear() per call; each step's x in one pinned-host -> device "
-                           "copy and its y in one device -> pinned-host copy, eager"},
+                    "how": "linear() per call, eager; each step's x in one pinned-host -> "
+                           "device copy and its y in one device -> pinned-host copy, on a "
+                           "copy stream with two sets of device buffers, so that a step's "
+                           "copies overlap the neighbouring steps' GEMMs"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
                          "unit": "GB/s", "frac": round(achieved / hbm, 4),
                          "traffic": traffic, "peak_source": hbm_src,
