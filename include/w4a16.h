@@ -181,12 +181,13 @@ W4_API w4_status w4_repack_gptq(const int32_t* qweight, const int32_t* qzeros, c
  *     large-M kernel; optional for the small-M kernel, whose CTAs otherwise
  *     each gather the columns they need (slower at larger M: every column
  *     group's CTAs read the same columns).
- *   - After that, large-M calls keep fp32 partial tiles there: calls whose
- *     output tiles cannot fill the GPU, of a split-K run; calls whose tiles
- *     take whole waves plus a few, of the few tiles beyond the last whole wave,
- *     which run as K slices over the otherwise idle SMs (both optional: with a
- *     smaller workspace the kernel splits less, or not at all; the sum order,
- *     and so the result bits of the affected tiles, follow the split chosen).
+ *   - After that, large-M calls keep fp32 partial tiles there, min(M, tile
+ *     rows) x 256 floats a tile and K slice: of every output tile when the
+ *     tiles cannot fill the GPU, of the few tiles beyond the last whole wave
+ *     when they take whole waves plus a few; those tiles run as K slices over
+ *     the otherwise idle SMs (optional: with a smaller workspace the kernel
+ *     splits less, or not at all; the sum order, and so the result bits of
+ *     the affected tiles, follow the split chosen).
  */
 W4_API size_t w4a16_gemm_workspace_size(int M, int N, int K, int group, int dtype, int has_perm);
 
@@ -306,8 +307,8 @@ W4_API w4_status w4_test_stalled_gemm(const void* x, const int32_t* qw, const vo
  * calls whose act-order staging would exceed it (M * K * 2 bytes) return
  * W4_ERR_WORKSPACE and launch nothing (small-M ones gather in the kernel
  * instead), and split-K partials that do not fit after the staging make the
- * kernel split K less, or not split its last wave (then the result bits can
- * differ from a w4a16_gemm call given the full workspace).
+ * kernel split K less, or not at all (then the result bits can differ from a
+ * w4a16_gemm call given the full workspace).
  * It never allocates or frees device memory.
  *   - Set-up: the first call with M > 0 on each device (whatever its shape,
  *     once its arguments pass validation) looks up the array's device address

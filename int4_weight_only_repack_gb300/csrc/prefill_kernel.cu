@@ -107,10 +107,13 @@ struct Cfg {
   static constexpr int A_BYTES = A_ROWS * BK * 2;
   static constexpr int ST_T = NACC == 2 ? 3 : GROUPED ? 3 : HALF_A ? 6 : 4;
   static constexpr int ST_B = 3;
-  // Dequantising warps (8 onward), one or two of a B tile's 16 atoms each. The
-  // 64-row x tiles (M <= 64) are bound by the dequantisation alone (the MMA
-  // does little per block), so they get sixteen, one atom each.
-  static constexpr int DEQ_WARPS = HALF_A ? 16 : 8;
+  // Dequantising warps (8 onward), one or two of a B tile's 16 atoms each.
+  // Ungrouped 128-row tiles get sixteen, one atom each: the MMA does half a
+  // 256-row tile's work per dequantised B tile, so the dequantisation sets
+  // their pace (measured on GB300: Llama-2-70B layers at M = 32 / 64 2-4 %
+  // faster, at M = 128 gate_up 183 -> 175 us and down 90 -> 86 us, Llama-2-7B
+  // o_proj / down at M = 512 2 %; 72-76 registers at 768 threads, no spills).
+  static constexpr int DEQ_WARPS = (HALF_A || (NACC == 1 && !GROUPED)) ? 16 : 8;
   static constexpr int NTHREADS = 256 + 32 * DEQ_WARPS;
   // Threads that issue the TMA ring's loads. One issuing thread starts the
   // loads of a 256-row stage (x tile of 256 rows, packed block, scale and zero
@@ -143,15 +146,16 @@ struct PrefillParams {
   CUtensorMap tm_z;  // zeros [G][N/8], box 32 x 2
   uint16_t* y;
   const uint16_t* bias;  // [N] in the activation dtype, or nullptr
-  float* part;  // split-K partial tiles [ksplit][M][N] fp32 (ksplit > 1)
   int M, N, K, group;
-  int m_blocks, n_blocks, num_tiles, k_blocks, ksplit;
-  // Split last wave (ungrouped, ksplit == 1): the tiles from tail_start on (the
-  // tail_tiles that would leave most SMs idle in a last wave of their own) run
-  // as tail_split K slices each, whose fp32 partial tiles go to tail_part
-  // [tail_split][tail_tiles][BM][BN] (slice-major) for tail_reduce_kernel.
+  int m_blocks, n_blocks, num_tiles, k_blocks;
+  // Split K (ungrouped): the tiles from tail_start on run as tail_split K
+  // slices each, whose fp32 partial tiles go to tail_part
+  // [tail_split][tail_tiles][tail_rows][BN] (slice-major; tail_rows = min(M, BM),
+  // rows at or beyond M are not stored) for tail_reduce_kernel. Either every
+  // tile (tail_start = 0: the tiles cannot fill the SMs) or the few beyond
+  // whole waves that would leave most SMs idle in a last wave of their own.
   float* tail_part;
-  int tail_start, tail_tiles, tail_split;
+  int tail_start, tail_tiles, tail_split, tail_rows;
   // Grouped (MoE) calls: eoff != nullptr. x and y hold the rows of all experts,
   // sorted by expert ([eoff[e], eoff[e+1]) for expert e); tm_p spans the
   // experts' TILE buffers one after another (ng128 column groups each), tm_s
@@ -183,11 +187,12 @@ static_assert(Cfg<1, false, false>::SMEM_BYTES <= 227 * 1024 &&
 
 // Work unit `tile` -> (expert, M block, N block, K slice [kb0, kb1) of
 // k-blocks, first row and end row of the unit's rows). Ungrouped units run M
-// fastest, then N, then the K slice; grouped ones expert by expert, M fastest
-// within the expert, then N (no K split).
+// fastest, then N; the split tiles' units after the whole tiles, slice by
+// slice. Grouped ones run expert by expert, M fastest within the expert, then
+// N (no K split).
 struct Unit {
   int e, m_blk, n_blk, ks, kb0, kb1, row0, row_end;
-  int slot;  // partial-tile slot of a split last-wave unit in tail_part, else -1
+  int slot;  // partial-tile slot of a split unit in tail_part, else -1
 };
 template <bool GROUPED>
 __device__ __forceinline__ Unit unit_of(const PrefillParams& p, const int* tab, int BM, int tile) {
@@ -196,7 +201,7 @@ __device__ __forceinline__ Unit unit_of(const PrefillParams& p, const int* tab, 
     u.e = 0;
     u.slot = -1;
     if (p.tail_split > 1 && tile >= p.tail_start) {
-      // a split last-wave unit: slice v / tail_tiles of tile tail_start + v % tail_tiles
+      // a split unit: slice v / tail_tiles of tile tail_start + v % tail_tiles
       const int v = tile - p.tail_start;
       const int tt = p.tail_start + v % p.tail_tiles;
       u.m_blk = tt % p.m_blocks;
@@ -207,11 +212,10 @@ __device__ __forceinline__ Unit unit_of(const PrefillParams& p, const int* tab, 
       u.slot = v;
     } else {
       u.m_blk = tile % p.m_blocks;
-      const int rest = tile / p.m_blocks;
-      u.n_blk = rest % p.n_blocks;
-      u.ks = rest / p.n_blocks;
-      u.kb0 = (int)((long long)u.ks * p.k_blocks / p.ksplit);
-      u.kb1 = (int)((long long)(u.ks + 1) * p.k_blocks / p.ksplit);
+      u.n_blk = tile / p.m_blocks;
+      u.ks = 0;
+      u.kb0 = 0;
+      u.kb1 = p.k_blocks;
     }
     u.row0 = u.m_blk * BM;
     u.row_end = p.M;
@@ -530,21 +534,12 @@ __global__ void __launch_bounds__(Cfg<NACC, GROUPED, HALF_A>::NTHREADS, 1)
           tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + buf * (BN * NACC) + i * BN + c0, r);
           tmem_ld_wait();
           const int n = n_blk * BN + c0;
-          if (p.ksplit > 1) {
-            // split K: this slice's fp32 partial tile (N % 32 == 0: whole 32-column chunks)
-            if (m < u.row_end && n < p.N) {
-              float4* dst = reinterpret_cast<float4*>(p.part + ((size_t)u.ks * p.M + m) * p.N + n);
-#pragma unroll
-              for (int q = 0; q < 8; ++q)
-                dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                     __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
-            }
-          } else if (u.slot >= 0) {
-            // split last wave: this slice's fp32 partial of the tile (rows beyond
-            // M are never read back)
+          if (u.slot >= 0) {
+            // split K: this slice's fp32 partial of the tile (N % 32 == 0: whole
+            // 32-column chunks; m - row0 < tail_rows for every stored row)
             if (m < u.row_end && n < p.N) {
               float4* dst = reinterpret_cast<float4*>(
-                  p.tail_part + ((size_t)u.slot * BM + (m - u.row0)) * BN + c0);
+                  p.tail_part + ((size_t)u.slot * p.tail_rows + (m - u.row0)) * BN + c0);
 #pragma unroll
               for (int q = 0; q < 8; ++q)
                 dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
@@ -699,45 +694,17 @@ __global__ void __launch_bounds__(256) gather_columns_kernel(const uint16_t* __r
   }
 }
 
-// ---- split K: y = RN(sum over the K slices of the fp32 partials), in slice order --
-// With a bias, y = RN(sum + bias[n]) (n4_row: float4 groups per row, N / 4).
-template <bool BF16>
-__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4* __restrict__ part,
-                                                            uint2* __restrict__ y, size_t n4,
-                                                            int ksplit,
-                                                            const uint2* __restrict__ bias,
-                                                            size_t n4_row) {
-  for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < n4; i += (size_t)gridDim.x * 256) {
-    float4 a = part[i];
-    for (int s = 1; s < ksplit; ++s) {
-      const float4 b = part[(size_t)s * n4 + i];
-      a.x += b.x;
-      a.y += b.y;
-      a.z += b.z;
-      a.w += b.w;
-    }
-    if (bias != nullptr) {
-      const uint2 b = __ldg(bias + i % n4_row);
-      a.x += half_bits_to_float<BF16>((uint16_t)b.x);
-      a.y += half_bits_to_float<BF16>((uint16_t)(b.x >> 16));
-      a.z += half_bits_to_float<BF16>((uint16_t)b.y);
-      a.w += half_bits_to_float<BF16>((uint16_t)(b.y >> 16));
-    }
-    y[i] = make_uint2(pack_half2(a.x, a.y, BF16), pack_half2(a.z, a.w, BF16));
-  }
-}
-
-// ---- split last wave: y = RN(sum over the slices + bias) for the tail tiles -------
-// One thread per four consecutive outputs of a tail tile; the slices are summed
-// in order (deterministic).
+// ---- split K: y = RN(sum over the slices + bias) for the split tiles --------------
+// One thread per four consecutive outputs of a split tile (R = tail_rows rows of
+// partials a tile); the slices are summed in order (deterministic).
 template <bool BF16>
 __global__ void __launch_bounds__(256) tail_reduce_kernel(const float4* __restrict__ part,
                                                           uint16_t* __restrict__ y,
                                                           const uint16_t* __restrict__ bias,
-                                                          int M, int N, int BM, int m_blocks,
-                                                          int tail_start, int tail_tiles,
-                                                          int tail_split) {
-  const size_t per_tile = (size_t)BM * (BN / 4);
+                                                          int M, int N, int BM, int R,
+                                                          int m_blocks, int tail_start,
+                                                          int tail_tiles, int tail_split) {
+  const size_t per_tile = (size_t)R * (BN / 4);
   const size_t total = (size_t)tail_tiles * per_tile;
   for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < total; i += (size_t)gridDim.x * 256) {
     const int ti = (int)(i / per_tile);
@@ -801,97 +768,79 @@ cudaError_t ensure_prefill_smem(void* fn, int which, int bytes) {
   return e;
 }
 
-// Tiling and K split of a call. Two accumulators per CTA (256-row tiles) when
-// that takes fewer estimated wave-times: a 256-row tile does the MMA work of
-// two 128-row tiles in ~1.25x the time (it dequantises each B tile once for
-// both). When the output tiles cannot fill the SMs, K is split into slices of
-// at least 8 k-blocks so that tiles x slices still fit in one wave; when they
-// take whole waves plus a few, only those few are split (the split last wave).
+// Tiling and K split of a call, chosen by an estimate of its time. A CTA
+// computes one 128 x 256 tile (NACC = 1) or one 256 x 256 tile (NACC = 2: it
+// dequantises each B tile once for both accumulators). One SM's measured rate
+// on GB300 is about 5.8 TFLOP/s with 128-row tiles and 8.7 with 256-row ones,
+// over a long K. Tiles beyond whole waves (all of them when they cannot fill
+// the SMs) may be split into K slices of at least 8 k-blocks, each slice's
+// fp32 partial tile written out and summed by tail_reduce_kernel. The estimate
+// of a split: ceil(split tiles * slices / SMs) waves of 1/slices of a tile's
+// time, every wave plus about 4 k-blocks of pipeline fill and drain, plus
+// writing and reading the partials (8 bytes an output a slice at about
+// 6.6 TB/s) and the reduce launch (about 3 us). Among the splits, one wave's
+// worth (as many slices as the SMs hold, when the tiles cannot fill them) or
+// none (for the tiles of a last wave) is kept unless another is estimated at
+// least 10 % faster. Measured on GB300 against the former fixed choices:
+// Llama-2-70B gate_up at M = 128 175 -> 142 us (its last wave split), 7B down
+// at M = 512 70 -> 62 us (256-row tiles split 3-4 ways), 70B qkv at M = 1024
+// 211 -> 133 us and 7B gate_up at M = 512 116 -> 85 us (the last wave split).
 struct PrefillPlan {
-  int nacc, m_blocks, n_blocks, ksplit;
-  int tail_tiles, tail_split;  // split last wave (tail_split > 1): its tiles and slices
+  int nacc, m_blocks, n_blocks;
+  int tail_tiles, tail_split;  // split K (tail_split > 1): the last tail_tiles tiles and their slices
+  double seconds;              // the estimate
 };
-PrefillPlan prefill_plan(int M, int N, int K, int sm_count) {
+
+PrefillPlan plan_tiles(int M, int N, int K, int sm_count, int nacc) {
   PrefillPlan pl;
+  pl.nacc = nacc;
   pl.n_blocks = (N + BN - 1) / BN;
-  const long long t128 = (long long)((M + 127) / 128) * pl.n_blocks;
-  const long long t256 = (long long)((M + 255) / 256) * pl.n_blocks;
-  const double w128 = (double)((t128 + sm_count - 1) / sm_count);
-  const double w256 = 1.25 * (double)((t256 + sm_count - 1) / sm_count);
-  pl.nacc = w256 < w128 ? 2 : 1;
-  pl.m_blocks = (M + 128 * pl.nacc - 1) / (128 * pl.nacc);
-  const long long tiles = (long long)pl.m_blocks * pl.n_blocks;
-  pl.ksplit = 1;
+  pl.m_blocks = (M + 128 * nacc - 1) / (128 * nacc);
   pl.tail_tiles = 0;
   pl.tail_split = 1;
-  if (tiles < sm_count || M <= 128) {
-    // Split K in slices of at least 8 k-blocks. First choice: as many slices as
-    // one wave holds (none when the tiles alone fill the SMs). Another split
-    // replaces it when a cost model, in units of one unsplit tile's time T1,
-    // predicts it at least 10 % faster: ceil(tiles*ks / SMs) waves of units that
-    // take 1/ks of T1 plus about 4 k-blocks of pipeline fill and drain, plus
-    // writing and reading ks fp32 partial tiles (8*M*N*ks bytes at about
-    // 6.6 TB/s) and the reduce launch (about 3 us). T1 = 2 * rows * 256 * K /
-    // 8 TFLOP/s (one SM's measured tcgen05 rate). It moves the shapes whose
-    // tiles fill more than half the SMs but not all of them (one wave with no
-    // split leaves the rest idle): measured on GB300, Llama-2-70B qkv at
-    // M = 256 98.7 -> 86.3 us and Llama-2-13B down at M = 1024 232 -> 199 us;
-    // and, at M <= 128 (small fp32 partials), those whose tiles take one and a
-    // half waves: Llama-2-70B gate_up at M = 32 / 64, 224 tiles, where half the
-    // SMs would run two tiles and the rest one: 192 -> 141 / 194 -> 148 us.
-    // (Above M = 128 the partials cost more than the model charges: 70B qkv at
-    // M = 1024, 160 tiles, measured no faster split three ways.)
-    const int kmax = std::max(1, K / BK / 8);
-    const int kb_total = K / BK;
-    const double t1 = 2.0 * 128 * pl.nacc * BN * (double)K / 8e12;
-    const double part = 8.0 * M * (double)N / 6.6e12 / t1;
-    const double launch = 3e-6 / t1;
-    auto cost = [&](int ks) {
-      const double waves = (double)((tiles * ks + sm_count - 1) / sm_count);
-      return waves * (1.0 / ks + 4.0 / kb_total) + (ks > 1 ? part * ks + launch : 0.0);
-    };
-    const int one_wave = (int)std::max(1LL, std::min<long long>(kmax, sm_count / tiles));
-    int best = one_wave;
-    for (int ks = 1; ks <= kmax; ++ks)
-      if (cost(ks) < cost(best)) best = ks;
-    pl.ksplit = cost(best) < 0.9 * cost(one_wave) ? best : one_wave;
-  } else if (tiles % sm_count != 0) {
-    // Split last wave: the rem tiles beyond whole waves would run as one more
-    // wave of full tiles on rem SMs while the rest idle. Split each of them
-    // into ks K slices (at least 8 k-blocks each) over the SMs instead, when the
-    // same cost model (units of one unsplit tile's time T1) predicts the tail at
-    // least 10 % faster: ceil(rem*ks / SMs) waves of 1/ks of T1 plus the
-    // pipeline fill, plus writing and reading the rem*ks fp32 partial tiles and
-    // the reduce launch. Measured on GB300: Llama-2-70B qkv at M = 1024 (160
-    // tiles) 211 -> 133 us, 7B gate_up at M = 512 (172) 116 -> 85 us, 70B down at
-    // M = 4096 (512) 1410 -> 1257 us, 7B qkv at M = 4096 (768) 335 -> 304 us.
-    const long long rem = tiles % sm_count;
-    const int kmax = std::max(1, K / BK / 8);
-    const int kb_total = K / BK;
-    const double t1 = 2.0 * 128 * pl.nacc * BN * (double)K / 8e12;
-    const double slice = 8.0 * (double)rem * 128 * pl.nacc * BN / 6.6e12 / t1;
-    const double launch = 3e-6 / t1;
-    auto cost = [&](int ks) {
-      const double waves = (double)((rem * ks + sm_count - 1) / sm_count);
-      return waves * (1.0 / ks + 4.0 / kb_total) + (ks > 1 ? slice * ks + launch : 0.0);
-    };
-    int best = 1;
-    for (int ks = 2; ks <= kmax; ++ks)
-      if (cost(ks) < cost(best)) best = ks;
-    if (best > 1 && cost(best) < 0.9 * cost(1)) {
-      pl.tail_tiles = (int)rem;
-      pl.tail_split = best;
-    }
+  const long long tiles = (long long)pl.m_blocks * pl.n_blocks;
+  const int kb_total = K / BK;
+  const int kmax = std::max(1, kb_total / 8);
+  const double tile_s = 2.0 * 128 * nacc * BN * (double)K / (nacc == 2 ? 8.7e12 : 5.8e12);
+  const double fill = 4.0 / kb_total;
+  const long long full = tiles / sm_count;
+  const long long rem = tiles - full * sm_count;
+  const double whole = (double)full * tile_s * (1.0 + fill);
+  pl.seconds = whole;
+  if (rem == 0) return pl;
+  // partial bytes of one slice of the rem tiles: their stored rows x BN x 8
+  const double rows = (double)std::min<long long>(M, 128LL * nacc * pl.m_blocks) / pl.m_blocks;
+  const double slice_s = 8.0 * (double)rem * rows * BN / 6.6e12;
+  auto cost = [&](int ks) {
+    const double waves = (double)((rem * ks + sm_count - 1) / sm_count);
+    return waves * tile_s * (1.0 / ks + fill) + (ks > 1 ? slice_s * ks + 3e-6 : 0.0);
+  };
+  const int base = full == 0 ? (int)std::max(1LL, std::min<long long>(kmax, sm_count / rem)) : 1;
+  int best = base;
+  for (int ks = 1; ks <= kmax; ++ks)
+    if (cost(ks) < cost(best)) best = ks;
+  const int ks = cost(best) < 0.9 * cost(base) ? best : base;
+  if (ks > 1) {
+    pl.tail_tiles = (int)rem;
+    pl.tail_split = ks;
+  }
+  pl.seconds = whole + cost(ks);
+  return pl;
+}
+
+PrefillPlan prefill_plan(int M, int N, int K, int sm_count) {
+  PrefillPlan pl = plan_tiles(M, N, K, sm_count, 1);
+  if (M > 128) {
+    const PrefillPlan p2 = plan_tiles(M, N, K, sm_count, 2);
+    if (p2.seconds < pl.seconds) pl = p2;
   }
   return pl;
 }
 
-size_t tail_bytes(const PrefillPlan& pl) {
-  return pl.tail_split > 1 ? (size_t)pl.tail_split * pl.tail_tiles * 128 * pl.nacc * BN * 4 : 0;
-}
-
-size_t split_bytes(int M, int N, int ksplit) {
-  return ksplit > 1 ? (size_t)ksplit * M * N * 4 : 0;
+// fp32 partials of a plan's split tiles (rows at or beyond M are not stored)
+size_t tail_bytes(const PrefillPlan& pl, int M) {
+  const size_t rows = (size_t)std::min(M, 128 * pl.nacc);
+  return pl.tail_split > 1 ? (size_t)pl.tail_split * pl.tail_tiles * rows * BN * 4 : 0;
 }
 
 }  // namespace
@@ -921,8 +870,7 @@ size_t prefill_workspace_bytes(int M, int K, bool has_perm) {
 size_t prefill_split_workspace_bytes(int M, int N, int K) {
   DeviceInfo info;
   if (device_info(&info) != cudaSuccess) return 0;
-  const PrefillPlan pl = prefill_plan(M, N, K, info.sm_count);
-  return std::max(split_bytes(M, N, pl.ksplit), tail_bytes(pl));
+  return tail_bytes(prefill_plan(M, N, K, info.sm_count), M);
 }
 
 bool prefill_supported(int M, int N, int K) {
@@ -964,9 +912,9 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
     pl.nacc = (a.M > 128 && a.num_experts <= GROUPED_MAX_EXPERTS_256) ? 2 : 1;
     pl.n_blocks = (a.N + BN - 1) / BN;
     pl.m_blocks = 0;
-    pl.ksplit = 1;
     pl.tail_tiles = 0;
     pl.tail_split = 1;
+    pl.seconds = 0.0;
   } else {
     pl = prefill_plan(a.M, a.N, a.K, info.sm_count);
   }
@@ -974,9 +922,8 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
   // has room for them; with less room the split shrinks (down to none)
   const size_t staged = prefill_workspace_bytes(a.M, a.K, a.perm != nullptr);
   const size_t room = a.workspace_bytes > staged ? a.workspace_bytes - staged : 0;
-  while (pl.ksplit > 1 && (a.workspace == nullptr || split_bytes(a.M, a.N, pl.ksplit) > room))
-    --pl.ksplit;
-  if (pl.tail_split > 1 && (a.workspace == nullptr || tail_bytes(pl) > room)) pl.tail_split = 1;
+  while (pl.tail_split > 1 && (a.workspace == nullptr || tail_bytes(pl, a.M) > room))
+    --pl.tail_split;
   const int nacc = pl.nacc;
   const int BM = 128 * nacc;
   // 64-row x tiles (and a deeper TMA ring) for ungrouped calls of at most 64 rows
@@ -1000,8 +947,6 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
   if (!ok) return cudaErrorInvalidValue;
   p.y = static_cast<uint16_t*>(a.y);
   p.bias = static_cast<const uint16_t*>(a.bias);
-  p.part = pl.ksplit > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + staged)
-                         : nullptr;
   p.tail_part = pl.tail_split > 1
                     ? reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + staged)
                     : nullptr;
@@ -1011,11 +956,11 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
   p.group = a.group;
   p.m_blocks = (a.M + BM - 1) / BM;
   p.n_blocks = n_blocks;
-  p.ksplit = pl.ksplit;
-  p.num_tiles = p.m_blocks * n_blocks * pl.ksplit;
+  p.num_tiles = p.m_blocks * n_blocks;
   p.tail_split = pl.tail_split;
   p.tail_tiles = pl.tail_split > 1 ? pl.tail_tiles : 0;
   p.tail_start = p.num_tiles - p.tail_tiles;
+  p.tail_rows = std::min(a.M, BM);
   if (pl.tail_split > 1) p.num_tiles = p.tail_start + pl.tail_tiles * pl.tail_split;
   p.k_blocks = a.K / BK;
   p.eoff = a.eoff;
@@ -1069,32 +1014,20 @@ cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t stream) {
   cfg.numAttrs = 1;
   void* args[] = {&p};
   if ((err = cudaLaunchKernelExC(&cfg, fn, args)) != cudaSuccess) return err;
-  if (pl.ksplit > 1) {
-    const size_t n4 = (size_t)a.M * a.N / 4;
-    const unsigned g = (unsigned)std::min<size_t>((n4 + 255) / 256, (size_t)info.sm_count * 8);
-    const uint2* bias = static_cast<const uint2*>(a.bias);
-    if (a.bf16)
-      splitk_reduce_kernel<true><<<g, 256, 0, stream>>>(reinterpret_cast<const float4*>(p.part),
-                                                         static_cast<uint2*>(a.y), n4, pl.ksplit,
-                                                         bias, (size_t)a.N / 4);
-    else
-      splitk_reduce_kernel<false><<<g, 256, 0, stream>>>(reinterpret_cast<const float4*>(p.part),
-                                                          static_cast<uint2*>(a.y), n4, pl.ksplit,
-                                                          bias, (size_t)a.N / 4);
-    err = cudaGetLastError();
-  }
   if (pl.tail_split > 1) {
-    const size_t total = (size_t)pl.tail_tiles * BM * (BN / 4);
+    const size_t total = (size_t)pl.tail_tiles * p.tail_rows * (BN / 4);
     const unsigned g = (unsigned)std::min<size_t>((total + 255) / 256, (size_t)info.sm_count * 8);
     const float4* part = reinterpret_cast<const float4*>(p.tail_part);
     uint16_t* yy = static_cast<uint16_t*>(a.y);
     const uint16_t* bias = static_cast<const uint16_t*>(a.bias);
     if (a.bf16)
-      tail_reduce_kernel<true><<<g, 256, 0, stream>>>(part, yy, bias, a.M, a.N, BM, p.m_blocks,
-                                                      p.tail_start, pl.tail_tiles, pl.tail_split);
+      tail_reduce_kernel<true><<<g, 256, 0, stream>>>(part, yy, bias, a.M, a.N, BM, p.tail_rows,
+                                                      p.m_blocks, p.tail_start, pl.tail_tiles,
+                                                      pl.tail_split);
     else
-      tail_reduce_kernel<false><<<g, 256, 0, stream>>>(part, yy, bias, a.M, a.N, BM, p.m_blocks,
-                                                       p.tail_start, pl.tail_tiles, pl.tail_split);
+      tail_reduce_kernel<false><<<g, 256, 0, stream>>>(part, yy, bias, a.M, a.N, BM, p.tail_rows,
+                                                       p.m_blocks, p.tail_start, pl.tail_tiles,
+                                                       pl.tail_split);
     err = cudaGetLastError();
   }
   return err;
