@@ -286,6 +286,18 @@ W4_API w4_status w4_test_stalled_gemm(const void* x, const int32_t* qw, const vo
                                       int group, int dtype, void* stream);
 
 /*
+ * Test hook for the large-M kernel's planner (no counterpart in the pages; host
+ * only, needs no device). For an ungrouped call of M x N x K (M > 16,
+ * N % 32 == 0, K % 64 == 0) on a GPU with sm_count SMs, writes the plan that
+ * w4a16_gemm would take with the whole workspace: out[0] = rows per output
+ * tile (128 or 256), out[1] = output tiles, out[2] = tiles split along K (the
+ * last ones; 0 when none), out[3] = K slices of each split tile (1 when none).
+ * out must hold 4 ints. Errors: W4_ERR_NULL for out == NULL, W4_ERR_SHAPE for
+ * a shape the kernel does not take or sm_count < 1.
+ */
+W4_API w4_status w4_test_prefill_plan(int M, int N, int K, int sm_count, int* out);
+
+/*
  * Size of the static device scratch array that w4a16_gemm_noalloc uses (32 MiB).
  */
 #define W4_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)

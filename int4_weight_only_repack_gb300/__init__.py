@@ -21,7 +21,7 @@ __all__ = [
     "w4_repack_gptq", "w4a16_gemm_workspace_size", "w4a16_gemm", "w4a16_gemm_bias",
     "w4a16_gemm_noalloc", "w4a8_gemm_workspace_size", "w4a8_gemm", "linear_fp8",
     "w4_dequant", "gemm_workspace",
-    "w4_device_status", "w4_test_stalled_gemm",
+    "w4_device_status", "w4_test_stalled_gemm", "w4_test_prefill_plan",
     "RepackedLayer", "repack_awq", "repack_gptq", "linear", "w4a16_moe_gemm", "RepackedExperts",
     "repack_awq_experts", "moe_linear",
 ]
@@ -57,6 +57,7 @@ _SIGNATURES = {
                                 _c_void_p]),
     "w4_test_stalled_gemm": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                                       _c_int, _c_int, _c_int, _c_int, _c_int, _c_void_p]),
+    "w4_test_prefill_plan": (_c_int, [_c_int, _c_int, _c_int, _c_int, ctypes.POINTER(_c_int)]),
     "w4a16_gemm_bias": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                                  _c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int,
                                  _c_void_p, _c_size, _c_void_p]),
@@ -249,6 +250,14 @@ def w4_test_stalled_gemm(x, qw, scales, zeros, y, M, N, K, group, dtype, stream=
     """The small-M GEMM with its weight copies withheld (the timeout test hook)."""
     _check(lib().w4_test_stalled_gemm(_ptr(x), _ptr(qw), _ptr(scales), _ptr(zeros), _ptr(y), M, N,
                                       K, group, dtype_code(dtype), _stream(stream)))
+
+
+def w4_test_prefill_plan(M, N, K, sm_count):
+    """The large-M kernel's plan for an M x N x K call on sm_count SMs (host
+    only): (rows per tile, output tiles, split tiles, K slices of each)."""
+    out = (_c_int * 4)()
+    _check(lib().w4_test_prefill_plan(M, N, K, sm_count, out))
+    return tuple(out)
 
 
 def w4a16_gemm_noalloc(x, qw, scales, zeros, perm, y, M, N, K, group, dtype, stream=None):

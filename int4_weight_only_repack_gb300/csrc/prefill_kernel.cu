@@ -867,6 +867,14 @@ size_t prefill_workspace_bytes(int M, int K, bool has_perm) {
   return ((size_t)M * K * 2 + 255) & ~(size_t)255;
 }
 
+void prefill_plan_query(int M, int N, int K, int sm_count, int* out) {
+  const PrefillPlan pl = prefill_plan(M, N, K, sm_count);
+  out[0] = 128 * pl.nacc;
+  out[1] = pl.m_blocks * pl.n_blocks;
+  out[2] = pl.tail_split > 1 ? pl.tail_tiles : 0;
+  out[3] = pl.tail_split;
+}
+
 size_t prefill_split_workspace_bytes(int M, int N, int K) {
   DeviceInfo info;
   if (device_info(&info) != cudaSuccess) return 0;

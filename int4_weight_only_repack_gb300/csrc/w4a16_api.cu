@@ -338,6 +338,15 @@ w4_status w4_test_stalled_gemm(const void* x, const int32_t* qw, const void* sca
                    stream, 1);
 }
 
+w4_status w4_test_prefill_plan(int M, int N, int K, int sm_count, int* out) {
+  if (!out) return W4_ERR_NULL;
+  if (M <= 16 || M > MAX_DIM || N < 1 || N > MAX_DIM || K < 1 || K > MAX_DIM || sm_count < 1 ||
+      !prefill_supported(M, N, K))
+    return W4_ERR_SHAPE;
+  prefill_plan_query(M, N, K, sm_count, out);
+  return W4_OK;
+}
+
 }  // extern "C"
 
 namespace w4 {

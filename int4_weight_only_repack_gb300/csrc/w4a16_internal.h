@@ -84,10 +84,13 @@ bool prefill_supported(int M, int N, int K);
 // Whether the large-M kernel takes a grouped (MoE) call of this shape.
 bool grouped_prefill_supported(int N, int K, int num_experts);
 size_t prefill_workspace_bytes(int M, int K, bool has_perm);
-// Further workspace bytes the tcgen05 kernel uses, when given, for a split-K
-// run of a call whose output tiles cannot fill the GPU (0 when it would not
-// split, or when no device is current).
+// Further workspace bytes the tcgen05 kernel uses, when given, for the fp32
+// partials of its split tiles (0 when it would not split, or when no device
+// is current).
 size_t prefill_split_workspace_bytes(int M, int N, int K);
+// The planner's choice for an ungrouped call on sm_count SMs: rows per tile,
+// output tiles, split tiles and K slices of each (out[4]).
+void prefill_plan_query(int M, int N, int K, int sm_count, int* out);
 cudaError_t launch_prefill(const GemmArgs& a, cudaStream_t s);
 
 // INT4 weights x FP8 activations (w4a8_gemm): workspace bytes for M x K
