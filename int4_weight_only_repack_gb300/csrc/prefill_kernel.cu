@@ -113,6 +113,9 @@ struct Cfg {
   // their pace (measured on GB300: Llama-2-70B layers at M = 32 / 64 2-4 %
   // faster, at M = 128 gate_up 183 -> 175 us and down 90 -> 86 us, Llama-2-7B
   // o_proj / down at M = 512 2 %; 72-76 registers at 768 threads, no spills).
+  // Grouped (MoE) 128-row tiles keep eight: with sixteen, a Mixtral-8x7B-shaped
+  // layer at 41-109 rows an expert ran about 6 % slower (w13 298 -> 316 us,
+  // w2 176 -> 187 us).
   static constexpr int DEQ_WARPS = (HALF_A || (NACC == 1 && !GROUPED)) ? 16 : 8;
   static constexpr int NTHREADS = 256 + 32 * DEQ_WARPS;
   // Threads that issue the TMA ring's loads. One issuing thread starts the
